@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark: the 7B-shaped q4_K_M prefill GEMM stack on GB300.
+
+One step = one pass of the whole hot path over one prompt of M = 3314 tokens:
+for every GEMM of the stack (32 layers x {q, k, o, gate, up: q4_K; v, down:
+q6_K} + lm_head q6_K, 225 GEMMs) the activation quantize prepass and the MMQ
+GEMM, through the C ABI.  Weights are random (seeded, the pages' block
+distributions), repacked once at registration (outside the timed region).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded token sample of the same workload instead.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
+the prefill (independent prompts, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "q4_K/q6_K MMQ GEMM int8 TOPS and prefill-GEMM tok/s; % of GB300 int8 peak"
+WORKLOAD = ("7B-shaped q4_K_M prefill GEMM stack: 32 layers x (q,k,o 4096x4096 q4_K; v 4096x4096 q6_K; "
+            "gate,up 11008x4096 q4_K; down 4096x11008 q6_K) + lm_head 32000x4096 q6_K; "
+            "quantize prepass per GEMM")
+FALLBACK_TFLOPS_SUSTAINED = 1700.0
+FALLBACK_TFLOPS_BURST = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=synth.STACK_LAYERS, help="fewer layers: a quick look only")
+    p.add_argument("--tokens", type=int, default=synth.STACK_M)
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU baseline)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def stack_list(layers):
+    out = []
+    for name, typ, od, id_, seed in synth.stack_gemms():
+        if name[0] == "l" and name[1].isdigit() and int(name[1:].split(".")[0]) >= layers:
+            continue
+        out.append((name, typ, od, id_, seed))
+    return out
+
+
+def config(args, extra=None):
+    c = {"workload": WORKLOAD, "tokens": args.tokens, "layers": args.layers, "gemms_per_step": len(stack_list(args.layers)),
+         "prepass_per_gemm": True,
+         "l2": "inputs larger than L2: every step streams ~14.9 GB of repacked weights (129 MB L2)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ----------------------------------------------------------------------------- peaks
+def _find_key(obj, names):
+    if isinstance(obj, dict):
+        for k, v in obj.items():
+            if k in names and isinstance(v, (int, float)):
+                return float(v)
+        for v in obj.values():
+            r = _find_key(v, names)
+            if r is not None:
+                return r
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    out = {"source": "fallback", "bf16_tflops_sustained": FALLBACK_TFLOPS_SUSTAINED,
+           "bf16_tflops": FALLBACK_TFLOPS_BURST, "hbm_gbs": FALLBACK_HBM_GBS}
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            sus = _find_key(d, {"bf16_tflops_sustained"})
+            burst = _find_key(d, {"bf16_tflops"})
+            hbm = _find_key(d, {"hbm_gbs"})
+            if sus or burst:
+                out["source"] = "measured"
+                out["bf16_tflops_sustained"] = sus or burst
+                out["bf16_tflops"] = burst or sus
+            if hbm:
+                out["hbm_gbs"] = hbm
+        except Exception:
+            pass
+    probe = os.path.join(ROOT, "profiles", "peaks_gb300.json")
+    if os.path.exists(probe):
+        try:
+            out["probe"] = json.load(open(probe))
+        except Exception:
+            pass
+    return out
+
+
+def kernel_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, valid only for the unchanged source."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        src = open(os.path.join(ROOT, "quant_int8_mmq_gb300", "csrc", "gemm.cu"), "rb").read()
+        if d.get("gemm_cu_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return d.get("per_launch_dram_bytes", {}).get(kernel_key)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader",
+                                          "-lms", "200", "-i", self.gpu_id],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                mx.append(float(f[2].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle stack
+def oracle_stack_tokens(raws, xh, xf, n_tokens, threads):
+    """Run the CPU oracle over the first n_tokens of the prompt through every GEMM."""
+    import oracle
+    for (name, typ, od, id_, seed), raw in raws:
+        x = xh if id_ == 4096 else xf
+        q, d, s = oracle.quantize_act(x[:n_tokens])
+        fn = oracle.gemm_q6k if typ == "q6_K" else oracle.gemm_q4k
+        fn(raw, q, d, s, nthreads=threads)
+
+
+def host_weights(gemms):
+    return [((name, typ, od, id_, seed), synth.blocks(typ, od, id_, seed)) for name, typ, od, id_, seed in gemms]
+
+
+def host_acts(tokens):
+    return (synth.activations(tokens, 4096, synth.STACK_SEED * 1000 + 900),
+            synth.activations(tokens, 11008, synth.STACK_SEED * 1000 + 901))
+
+
+def cpu_sample_run(raws, xh, xf, seconds, threads):
+    t0 = time.perf_counter()
+    oracle_stack_tokens(raws, xh, xf, 1, threads)
+    t1 = time.perf_counter() - t0
+    n = max(1, min(xh.shape[0], int(seconds / max(t1, 1e-6))))
+    t0 = time.perf_counter()
+    oracle_stack_tokens(raws, xh, xf, n, threads)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    threads = oracle.cpu_threads()
+    gemms = stack_list(args.layers)
+    raws = host_weights(gemms)
+    xh, xf = host_acts(args.tokens)
+    # size one step's token sample so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    oracle_stack_tokens(raws, xh, xf, 1, threads)
+    t_tok = time.perf_counter() - t0
+    per_step = max(1, int(8.0 / max(t_tok, 1e-6) / max(1, args.steps + args.warmup) * 3))
+    per_step = min(per_step, args.tokens)
+    for _ in range(args.warmup):
+        oracle_stack_tokens(raws, xh, xf, per_step, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_stack_tokens(raws, xh, xf, per_step, threads)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    sample = (f"{per_step} token(s) of the {args.tokens}-token prompt per step through all {len(gemms)} GEMMs "
+              f"(prepass + f64 oracle GEMM, all output columns)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+            "data": "synthetic", "config": config(args),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    import quant_int8_mmq_gb300 as mmq
+    from quant_int8_mmq_gb300 import build as mmq_build
+
+    if rank == 0 or world == 1:
+        mmq_build.build()
+    barrier(world)
+    lib = mmq.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    M = args.tokens
+    gemms = stack_list(args.layers)
+
+    # ---- registration (untimed): generate raw blocks, upload, repack, keep the packed planes
+    want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
+    host_raws = []
+    packed = []
+    for g in gemms:
+        name, typ, od, id_, seed = g
+        raw = synth.blocks(typ, od, id_, seed)
+        if want_cpu:
+            host_raws.append((g, raw))
+        rt = torch.from_numpy(raw.reshape(-1)).to(dev)
+        pk = mmq.pack_weights(typ, rt, od, id_)
+        packed.append((typ, od, id_, pk))
+        del rt
+    xh_np, xf_np = host_acts(M)
+    xh = torch.from_numpy(xh_np).to(dev)
+    xf = torch.from_numpy(xf_np).to(dev)
+    qa_b, sc_b = mmq.mmq_act_plane_bytes(M, 11008)
+    qa = torch.empty(qa_b, dtype=torch.uint8, device=dev)
+    sc = torch.empty(sc_b, dtype=torch.uint8, device=dev)
+    ys = {od: torch.empty((M, od), dtype=torch.float32, device=dev) for od in sorted({g[2] for g in gemms})}
+    torch.cuda.synchronize()
+    assert mmq.mmq_get_device_error() == 0
+
+    calls = []
+    for typ, od, id_, pk in packed:
+        x = xh if id_ == 4096 else xf
+        gemm_fn = lib.mmq_gemm_q6k if typ == "q6_K" else lib.mmq_gemm_q4k
+        calls.append((typ, od, id_, x.data_ptr(), pk.data_ptr(), ys[od].data_ptr(), gemm_fn))
+    qa_p, sc_p = qa.data_ptr(), sc.data_ptr()
+    quant = lib.mmq_quantize_act
+
+    def step(events=None):
+        for i, (typ, od, id_, xp, pkp, yp, gemm_fn) in enumerate(calls):
+            st = quant(xp, M, id_, id_, qa_p, sc_p, sptr)
+            if events is not None:
+                events[i][0].record(stream)
+            st |= gemm_fn(pkp, od, id_, qa_p, sc_p, M, yp, od, sptr)
+            if events is not None:
+                events[i][1].record(stream)
+            if st:
+                raise RuntimeError(f"launch failed with status {st}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if mmq.mmq_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+          for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        gpu_id = str(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clocks:
+        e0.record(stream)
+        for k in range(args.steps):
+            step(ev[k])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    t = e0.elapsed_time(e1) * 1e-3
+    if mmq.mmq_get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    t_max = max_over_ranks(world, t, dev if world > 1 else None)
+    value = world * M * args.steps / t_max
+
+    # per-kernel-class time (events on the launching stream, inside the timed region)
+    cls_time, cls_flops, cls_n = {}, {}, {}
+    for k in range(args.steps):
+        for (typ, od, id_, *_), (a, b) in zip(calls, ev[k]):
+            key = f"gemm_{typ}"
+            cls_time[key] = cls_time.get(key, 0.0) + a.elapsed_time(b) * 1e-3
+            cls_flops[key] = cls_flops.get(key, 0.0) + 2.0 * M * od * id_
+            cls_n[key] = cls_n.get(key, 0) + 1
+    dom = max(cls_time, key=cls_time.get)
+    gemm_time = sum(cls_time.values())
+    total_flops = sum(cls_flops.values())
+    peaks = measured_peaks()
+    achieved = cls_flops[dom] / cls_time[dom] / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": kernel_traffic(dom),
+            "achieved_def": "2*M*od*id per launch (int8-equivalent MACs x2) / mean launch time, CUDA events",
+            "peak_source": f"{peaks['source']} dense bf16 sustained (f16 operands run at the bf16 rate)"}
+
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16-held int8/int6/int4 codes -> f32 (exact), f32 scales",
+            "data": "synthetic (seeded random k-quant blocks, N(0,1) activations)",
+            "config": config(args, {"parallelism": f"replicas x{world}"}),
+            "tops_int8_equiv": world * total_flops / args.steps / (t_max / args.steps) / 1e12,
+            "gemm_only_tops": total_flops / gemm_time / 1e12,
+            "gemm_share_of_step": gemm_time / t,
+            "roofline": roof,
+            "gpu_launches": 2 * len(calls) * args.steps,
+            "path": mmq.mmq_last_path()}
+    probe = peaks.get("probe") or {}
+    if probe.get("int8_mma_sync_tops"):
+        line["int8_peak_tops"] = probe["int8_mma_sync_tops"]
+        line["frac_of_int8_peak"] = line["gemm_only_tops"] / probe["int8_mma_sync_tops"]
+    line["clocks"] = clocks.summary()
+
+    # ---- end to end through the public API: pinned host inputs in, logits out, every step
+    if not args.no_e2e:
+        xh_host = torch.from_numpy(xh_np).pin_memory()
+        xf_host = torch.from_numpy(xf_np).pin_memory()
+        y_last = ys[calls[-1][1]]
+        y_host = torch.empty(y_last.shape, dtype=torch.float32).pin_memory()
+        h2d = xh_host.numel() * 4 + xf_host.numel() * 4
+        d2h = y_host.numel() * 4
+        barrier(world)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            xh.copy_(xh_host, non_blocking=True)
+            xf.copy_(xf_host, non_blocking=True)
+            step()
+            y_host.copy_(y_last, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        te = max_over_ranks(world, a.elapsed_time(b) * 1e-3, dev if world > 1 else None)
+        line["e2e"] = {"value": world * M * args.steps / te, "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+        line["gpu_launches_e2e"] = 2 * len(calls) * args.steps
+
+    if want_cpu:
+        import oracle
+        oracle.build()
+        threads = oracle.cpu_threads()
+        v, n, dt = cpu_sample_run(host_raws, xh_np, xf_np, args.cpu_seconds, threads)
+        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {n} token(s) of the prompt through all {len(gemms)} GEMMs "
+                                          f"(oracle quantize + f64 GEMM, all columns), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_init()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,162 @@
+/*
+ * mmq.h -- C ABI of the GB300 (sm_103a) prefill quantized matrix multiply (MMQ):
+ * k-quant weight super-blocks (q6_K 210 B, q4_K 144 B, 256 values each) times
+ * per-32 q8 activations,
+ *
+ *     q6_K: Y[t,j] = sum_c sum_h d_a[t,c] * (d*sc[2(c%8)+h]) * I[t,j,c,h]
+ *     q4_K: Y[t,j] = sum_c d_a[t,c] * ((d*sc_c) * I[t,j,c] - (dmin*m_c) * ssum[t,c])
+ *
+ * with I the integer dot of a 16-value (q6_K) or 32-value (q4_K) sub-block.
+ *
+ * Sources (page title, section):
+ *   [r45] "r45 - cp.async for the q6_K A-side staging: mechanism confirmed,
+ *          wall-neutral (REVERTED)"
+ *   [r56] "r56 - q6_K A-side bundle: A cp.async + W_dsc f32 plane (LANDED)"
+ *   [r58] "r58 - q4_K BT spec + cp.async-db2 transplant (REVERTED)"
+ * The pages show the registration step, the activation prepass and the GEMM
+ * launch ([r56] §3.1: registration gates and planes; [r45] §1.1: the
+ * quantize-transpose prepass; [r58] §2.2: the GEMM's staging); this ABI exposes
+ * those three steps as calls.
+ *
+ * Conventions (all calls):
+ *  - Every buffer pointer is a DEVICE pointer owned by the caller.  The library
+ *    never allocates or frees device memory; sizes come from the *_bytes queries.
+ *  - Calls are asynchronous on stream `s` (NULL = legacy default stream).
+ *    Argument, shape and alignment errors are returned synchronously, before
+ *    anything is launched; a failed launch returns MMQ_ERR_CUDA.
+ *  - K = id must be a multiple of 256 (one super-block); od >= 1 may be odd; M >= 1.
+ *  - Buffers read by bulk copies (qa, scales, packed) must be 16-byte aligned,
+ *    else MMQ_ERR_ALIGN.  x and Y need 4-byte alignment.
+ *  - Every bounded wait inside a kernel gives up after about two seconds, sets a
+ *    sticky device error word and lets the kernel exit; mmq_get_device_error()
+ *    reports (and clears) it.  Results of a launch that timed out are undefined.
+ *  - Calls may come from several host threads; the one piece of shared host
+ *    state is the label mmq_last_path() returns (the most recent GEMM launch
+ *    of the process).
+ */
+#ifndef MMQ_GB300_H
+#define MMQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (the runtime's stream handle). */
+typedef struct CUstream_st* mmq_stream_t;
+
+typedef enum {
+    MMQ_OK = 0,
+    MMQ_ERR_ARG = 1,         /* null pointer, bad type id, ldx < K, ldy < od */
+    MMQ_ERR_SHAPE = 2,       /* K/id not a multiple of 256, M/od < 1, sizes over the limits */
+    MMQ_ERR_ALIGN = 3,       /* a pointer is not aligned as stated above */
+    MMQ_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    MMQ_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait expired (see mmq_get_device_error) */
+    MMQ_ERR_UNSUPPORTED = 6  /* no sm_103 device is current */
+} mmq_status;
+
+typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
+
+/* Size limits (checked; MMQ_ERR_SHAPE beyond them). */
+#define MMQ_MAX_M (1 << 22)
+#define MMQ_MAX_OD (1 << 22)
+#define MMQ_MAX_ID (1 << 20)
+
+/* --------------------------------------------------------------------------
+ * Activation planes ([r45] §2.3 and [r56] §1: the prepass writes a
+ * pre-transposed q8 code plane and a d/ssum scale pair per (chunk, token),
+ * padded token rows zero-filled).
+ *
+ * Layout (fixed, documented so a caller can read it back):
+ *   Mp = 128 * ceil(M/128) padded tokens; nkb = K/64; nchunk = K/32.
+ *   qa:     Mp*K f16 values, the q8 codes held as exact binary16 integers.
+ *           Tile (mt, kb) = tokens 128*mt.. and values 64*kb.. is a 16384-byte
+ *           block at byte (mt*nkb + kb)*16384.  Inside it token r (0..127) and
+ *           value k (0..63) sit at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2
+ *           (the 128-byte swizzle of the tensor-core operand tile).
+ *   scales: Mp*nchunk entries of 8 bytes {float d, int32 ssum}; entry (t, c)
+ *           at index ((t/128)*nchunk + c)*128 + t%128.
+ *   Rows t >= M hold code 0, d 0, ssum 0.
+ * -------------------------------------------------------------------------- */
+mmq_status mmq_act_plane_bytes(int M, int K, size_t* qa_bytes, size_t* scale_bytes);
+
+/* Quantize x [M][ldx] f32 (row-major, first K values of each row used) per
+ * 32-value chunk: d = amax/127 (IEEE f32 division), q = round(x/d) (IEEE f32
+ * division, ties away from zero, clamped to [-127,127]; d == 0 gives q = 0),
+ * ssum = sum q.  Writes qa and scales in the layout above.  x must be finite. */
+mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
+                            void* qa, void* scales, mmq_stream_t s);
+
+/* --------------------------------------------------------------------------
+ * Registration-time weight repack ([r56] §2.2-§2.3 W_dsc plane: exact f16->f32
+ * and int->f32 conversions, one f32 multiply, no FMA contraction; chunk-major
+ * so one tile's window is contiguous; [r58] §5 names the same plane for q4_K).
+ *
+ * raw_blocks: od rows x id/256 super-blocks, row-major, 210 B (q6_K: ql[128]@0,
+ *   qh[64]@128, int8 scales[16]@192, f16 d@208) or 144 B (q4_K: f16 d@0,
+ *   f16 dmin@2, scales[12]@4 = 16 six-bit fields little-endian, fields 0..7 the
+ *   scales sc_c and 8..15 the mins m_c, qs[128]@16).  Code of value e:
+ *   q6_K ((ql[e/2] >> 4*(e%2)) & 15 | ((qh[e/4] >> 2*(e%4)) & 3) << 4) - 32,
+ *   q4_K (qs[e/2] >> 4*(e%2)) & 15.  Value e of a q6_K block uses scales[e/16].
+ *
+ * packed (caller-owned, mmq_packed_weight_bytes() bytes):
+ *   Np = 128 * ceil(od/128); nkb = id/64; nchunk = id/32.
+ *   code plane at byte 0, Np*id f16 values (q6_K: code in [-32,31]; q4_K: code
+ *     in [0,15]), tile (nt, kb) a 16384-byte block at byte (nt*nkb + kb)*16384
+ *     with row r, value k at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2.
+ *   scale plane at byte Np*id*2, Np*nchunk entries of two floats, entry (j, c)
+ *     at index ((j/128)*nchunk + c)*128 + j%128:
+ *       q6_K {d*scales[2*(c%8)], d*scales[2*(c%8)+1]}
+ *       q4_K {d*sc_(c%8), dmin*m_(c%8)}
+ *   Rows j >= od are zero.
+ * -------------------------------------------------------------------------- */
+mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes);
+mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id,
+                                    size_t* code_offset, size_t* code_bytes,
+                                    size_t* scale_offset, size_t* scale_bytes);
+mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
+                            void* packed, mmq_stream_t s);
+
+/* --------------------------------------------------------------------------
+ * The GEMM: Y[t][j] (t < M, j < od, row stride ldy floats) is overwritten with
+ * the formula at the top of this file.  packed comes from mmq_pack_weights of
+ * the same (type, od, id); qa/scales from mmq_quantize_act with K = id and the
+ * same M.  The integer dots run exactly on the tensor cores (codes held as f16
+ * integers, every partial sum an integer below 2^24 in the f32 accumulator);
+ * the scales are applied in f32.  Rows t >= M and columns j >= od are never
+ * written.  ldy >= od.
+ * -------------------------------------------------------------------------- */
+mmq_status mmq_gemm_q6k(const void* packed, int od, int id, const void* qa, const void* scales,
+                        int M, float* Y, int ldy, mmq_stream_t s);
+mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, const void* scales,
+                        int M, float* Y, int ldy, mmq_stream_t s);
+
+/* Debug/verification: the same GEMM kernel (same staging, same tensor-core
+ * contraction) writes the raw per-sub-block dots instead of Y:
+ * dots[(t*od + j)*nsub + s] as f32 holding the exact integer, nsub = id/16
+ * (q6_K, one per 16-value sub-block) or id/32 (q4_K, one per chunk). */
+mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa,
+                               const void* scales, int M, float* dots, mmq_stream_t s);
+
+/* Synchronizes `s`, then reports and clears the sticky device error word:
+ * MMQ_ERR_TIMEOUT if a bounded wait expired since the last call, MMQ_ERR_CUDA
+ * if the synchronization failed, else MMQ_OK. */
+mmq_status mmq_get_device_error(mmq_stream_t s);
+
+const char* mmq_status_string(mmq_status st);
+
+/* Label of the path the most recent GEMM launch took (liveness check,
+ * [r56] §3.2 and §4: a fast path needs a visible label because parity alone
+ * cannot show it ran). */
+const char* mmq_last_path(void);
+
+/* Library version string. */
+const char* mmq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMQ_GB300_H */

@@ -64,10 +64,12 @@ def _load():
         lib.oracle_gemm_q4k.argtypes = [P, I, I, P, P, P, I, P, P, I]
         lib.oracle_dequant_q6k.argtypes = [P, I, I, P]
         lib.oracle_dequant_q4k.argtypes = [P, I, I, P]
+        lib.oracle_codes_q6k.argtypes = [P, I, I, P]
+        lib.oracle_codes_q4k.argtypes = [P, I, I, P]
         for name in ("oracle_f16_to_f32_array", "oracle_quantize_act", "oracle_decode_q6k",
                      "oracle_decode_q4k", "oracle_scale_planes_q6k", "oracle_scale_planes_q4k",
                      "oracle_dots_q6k", "oracle_dots_q4k", "oracle_gemm_q6k", "oracle_gemm_q4k",
-                     "oracle_dequant_q6k", "oracle_dequant_q4k"):
+                     "oracle_dequant_q6k", "oracle_dequant_q4k", "oracle_codes_q6k", "oracle_codes_q4k"):
             getattr(lib, name).restype = None
         _lib = lib
         return lib
@@ -201,6 +203,22 @@ def dequant_q4k(raw: np.ndarray) -> np.ndarray:
     W = np.empty((od, id_), np.float64)
     _load().oracle_dequant_q4k(_p(raw), od, id_, _p(W))
     return W
+
+
+def codes_q6k(raw: np.ndarray) -> np.ndarray:
+    """Decoded codes [od, id] int8 in [-32, 31]."""
+    raw, od, id_ = _raw(raw, Q6K_BYTES)
+    out = np.empty((od, id_), np.int8)
+    _load().oracle_codes_q6k(_p(raw), od, id_, _p(out))
+    return out
+
+
+def codes_q4k(raw: np.ndarray) -> np.ndarray:
+    """Decoded codes [od, id] uint8 in [0, 15]."""
+    raw, od, id_ = _raw(raw, Q4K_BYTES)
+    out = np.empty((od, id_), np.uint8)
+    _load().oracle_codes_q4k(_p(raw), od, id_, _p(out))
+    return out
 
 
 def cpu_threads() -> int:

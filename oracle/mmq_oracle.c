@@ -430,3 +430,29 @@ void oracle_dequant_q4k(const uint8_t* raw, int od, int id, double* W)
                     (double)d * (double)sc[e / 32] * (double)q[e] - (double)dmin * (double)m[e / 32];
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Decoded integer codes of a whole weight matrix, row-major [od][id]       */
+/* (q6_K: centred codes in [-32,31]; q4_K: nibbles in [0,15]).              */
+/* ------------------------------------------------------------------------ */
+void oracle_codes_q6k(const uint8_t* raw, int od, int id, int8_t* codes)
+{
+    const int nsb = id / QK_K;
+    float d;
+    int8_t sc[16];
+    for (int j = 0; j < od; ++j)
+        for (int sb = 0; sb < nsb; ++sb)
+            oracle_decode_q6k(raw + ((size_t)j * nsb + sb) * Q6K_BYTES, &d, sc,
+                              codes + (size_t)j * id + (size_t)sb * QK_K);
+}
+
+void oracle_codes_q4k(const uint8_t* raw, int od, int id, uint8_t* codes)
+{
+    const int nsb = id / QK_K;
+    float d, dmin;
+    uint8_t sc[8], m[8];
+    for (int j = 0; j < od; ++j)
+        for (int sb = 0; sb < nsb; ++sb)
+            oracle_decode_q4k(raw + ((size_t)j * nsb + sb) * Q4K_BYTES, &d, &dmin, sc, m,
+                              codes + (size_t)j * id + (size_t)sb * QK_K);
+}

@@ -1,0 +1,216 @@
+"""GB300 (sm_103a) prefill MMQ: q6_K / q4_K weight super-blocks x per-32 q8 activations.
+
+Thin ctypes binding over the C ABI in ``include/mmq.h`` (``libmmq_gb300.so``, built
+in-tree by ``quant_int8_mmq_gb300.build``).  The functions named like the C entry
+points take raw device pointers and a stream handle and only marshal arguments;
+every step of the computation runs in the library's CUDA kernels.  The tensor
+helpers below them use PyTorch for device memory and streams only.
+
+There is no fallback: if the library is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+__all__ = [
+    "MMQError", "MMQ_Q4_K", "MMQ_Q6_K", "load", "lib_path",
+    "mmq_act_plane_bytes", "mmq_quantize_act", "mmq_packed_weight_bytes", "mmq_packed_weight_layout",
+    "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_get_device_error",
+    "mmq_status_string", "mmq_last_path", "mmq_version",
+    "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
+]
+
+MMQ_Q4_K = 12
+MMQ_Q6_K = 14
+TYPES = {"q4_K": MMQ_Q4_K, "q6_K": MMQ_Q6_K}
+BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}
+
+STATUS = {0: "MMQ_OK", 1: "MMQ_ERR_ARG", 2: "MMQ_ERR_SHAPE", 3: "MMQ_ERR_ALIGN", 4: "MMQ_ERR_CUDA",
+          5: "MMQ_ERR_TIMEOUT", 6: "MMQ_ERR_UNSUPPORTED"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MMQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+def lib_path() -> str:
+    return LIB_PATH
+
+
+def load():
+    """Load libmmq_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run quant_int8_mmq_gb300.build.build() "
+                               "(or __graft_entry__.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
+        sig = {
+            "mmq_act_plane_bytes": [I, I, S, S],
+            "mmq_quantize_act": [P, I, I, I, P, P, P],
+            "mmq_packed_weight_bytes": [I, I, I, S],
+            "mmq_packed_weight_layout": [I, I, I, S, S, S, S],
+            "mmq_pack_weights": [I, P, I, I, P, P],
+            "mmq_gemm_q6k": [P, I, I, P, P, I, P, I, P],
+            "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
+            "mmq_debug_gemm_dots": [I, P, I, I, P, P, I, P, P],
+            "mmq_get_device_error": [P],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        for name in ("mmq_status_string",):
+            getattr(lib, name).argtypes = [ctypes.c_int]
+            getattr(lib, name).restype = ctypes.c_char_p
+        for name in ("mmq_last_path", "mmq_version"):
+            getattr(lib, name).argtypes = []
+            getattr(lib, name).restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise MMQError(st, what)
+
+
+# ----------------------------------------------------------------------------
+# Same names as the C entry points (pointers and streams as Python ints).
+# ----------------------------------------------------------------------------
+def mmq_act_plane_bytes(M: int, K: int):
+    qa, sc = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().mmq_act_plane_bytes(M, K, ctypes.byref(qa), ctypes.byref(sc)), "mmq_act_plane_bytes")
+    return qa.value, sc.value
+
+
+def mmq_quantize_act(x, M, K, ldx, qa, scales, stream=0):
+    _check(load().mmq_quantize_act(x, M, K, ldx, qa, scales, stream or None), "mmq_quantize_act")
+
+
+def mmq_packed_weight_bytes(t, od, id_):
+    b = ctypes.c_size_t()
+    _check(load().mmq_packed_weight_bytes(t, od, id_, ctypes.byref(b)), "mmq_packed_weight_bytes")
+    return b.value
+
+
+def mmq_packed_weight_layout(t, od, id_):
+    v = [ctypes.c_size_t() for _ in range(4)]
+    _check(load().mmq_packed_weight_layout(t, od, id_, *[ctypes.byref(x) for x in v]), "mmq_packed_weight_layout")
+    return tuple(x.value for x in v)
+
+
+def mmq_pack_weights(t, raw, od, id_, packed, stream=0):
+    _check(load().mmq_pack_weights(t, raw, od, id_, packed, stream or None), "mmq_pack_weights")
+
+
+def mmq_gemm_q6k(packed, od, id_, qa, scales, M, Y, ldy, stream=0):
+    _check(load().mmq_gemm_q6k(packed, od, id_, qa, scales, M, Y, ldy, stream or None), "mmq_gemm_q6k")
+
+
+def mmq_gemm_q4k(packed, od, id_, qa, scales, M, Y, ldy, stream=0):
+    _check(load().mmq_gemm_q4k(packed, od, id_, qa, scales, M, Y, ldy, stream or None), "mmq_gemm_q4k")
+
+
+def mmq_debug_gemm_dots(t, packed, od, id_, qa, scales, M, dots, stream=0):
+    _check(load().mmq_debug_gemm_dots(t, packed, od, id_, qa, scales, M, dots, stream or None),
+           "mmq_debug_gemm_dots")
+
+
+def mmq_get_device_error(stream=0) -> int:
+    """Returns the raw status (0 ok, 5 timeout, 4 CUDA error)."""
+    return load().mmq_get_device_error(stream or None)
+
+
+def mmq_status_string(st: int) -> str:
+    return load().mmq_status_string(st).decode()
+
+
+def mmq_last_path() -> str:
+    return load().mmq_last_path().decode()
+
+
+def mmq_version() -> str:
+    return load().mmq_version().decode()
+
+
+# ----------------------------------------------------------------------------
+# Tensor helpers: PyTorch provides device memory and the current stream only.
+# ----------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _type_id(t) -> int:
+    return TYPES[t] if isinstance(t, str) else int(t)
+
+
+def quantize_act(x, qa=None, scales=None, stream=None):
+    """x: float32 CUDA tensor [M, K] (row stride >= K).  Returns (qa, scales) uint8 buffers."""
+    torch = _torch()
+    assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    qb, sb = mmq_act_plane_bytes(M, K)
+    if qa is None:
+        qa = torch.empty(qb, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(sb, dtype=torch.uint8, device=x.device)
+    assert qa.numel() * qa.element_size() >= qb and scales.numel() * scales.element_size() >= sb
+    mmq_quantize_act(x.data_ptr(), M, K, x.stride(0), qa.data_ptr(), scales.data_ptr(), _stream(stream))
+    return qa, scales
+
+
+def pack_weights(t, raw, od, id_, packed=None, stream=None):
+    """raw: uint8 CUDA tensor holding od * id/256 super-blocks.  Returns the packed buffer."""
+    torch = _torch()
+    tid = _type_id(t)
+    assert raw.is_cuda and raw.dtype == torch.uint8 and raw.is_contiguous()
+    assert raw.numel() == od * (id_ // 256) * BLOCK_BYTES[tid]
+    nb = mmq_packed_weight_bytes(tid, od, id_)
+    if packed is None:
+        packed = torch.empty(nb, dtype=torch.uint8, device=raw.device)
+    mmq_pack_weights(tid, raw.data_ptr(), od, id_, packed.data_ptr(), _stream(stream))
+    return packed
+
+
+def gemm(t, packed, od, id_, qa, scales, M, Y=None, stream=None):
+    """Y [M, od] float32 (allocated if not given; a given Y may have row stride >= od)."""
+    torch = _torch()
+    tid = _type_id(t)
+    if Y is None:
+        Y = torch.empty((M, od), dtype=torch.float32, device=packed.device)
+    assert Y.dtype == torch.float32 and Y.stride(1) == 1 and Y.shape[0] >= M
+    fn = mmq_gemm_q6k if tid == MMQ_Q6_K else mmq_gemm_q4k
+    fn(packed.data_ptr(), od, id_, qa.data_ptr(), scales.data_ptr(), M, Y.data_ptr(), Y.stride(0), _stream(stream))
+    return Y
+
+
+def gemm_dots(t, packed, od, id_, qa, scales, M, stream=None):
+    """Per-sub-block dots [M, od, nsub] (f32 holding exact integers), from the GEMM kernel."""
+    torch = _torch()
+    tid = _type_id(t)
+    nsub = id_ // 16 if tid == MMQ_Q6_K else id_ // 32
+    dots = torch.empty((M, od, nsub), dtype=torch.float32, device=packed.device)
+    mmq_debug_gemm_dots(tid, packed.data_ptr(), od, id_, qa.data_ptr(), scales.data_ptr(), M, dots.data_ptr(),
+                        _stream(stream))
+    return dots

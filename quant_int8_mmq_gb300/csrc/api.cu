@@ -1,0 +1,196 @@
+// api.cu -- the extern "C" entry points declared in include/mmq.h.
+//
+// Every call validates its arguments on the host first (no CUDA call before an
+// argument error is returned), then checks that the current device is an sm_103
+// part, then launches on the caller's stream.  Nothing here allocates device
+// memory.
+#include <atomic>
+#include <cstdint>
+
+#include "mmq.h"
+#include "mmq_internal.h"
+
+namespace {
+
+std::atomic<const char*> g_last_path{"none"};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_k(int K) { return K >= mmq::QK_K && K <= MMQ_MAX_ID && (K % mmq::QK_K) == 0; }
+
+mmq_status check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_UNSUPPORTED;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_UNSUPPORTED;
+    }
+    return (major == 10 && minor == 3) ? MMQ_OK : MMQ_ERR_UNSUPPORTED;
+}
+
+mmq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MMQ_OK : MMQ_ERR_CUDA; }
+
+mmq_status check_weight_shape(mmq_type t, int od, int id)
+{
+    if (t != MMQ_Q4_K && t != MMQ_Q6_K)
+        return MMQ_ERR_ARG;
+    if (od < 1 || od > MMQ_MAX_OD || !valid_k(id))
+        return MMQ_ERR_SHAPE;
+    return MMQ_OK;
+}
+
+mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int od, int id, const void* qa,
+                       const void* scales, int M, float* out, int ldy, mmq_stream_t s)
+{
+    mmq_status st = check_weight_shape(t, od, id);
+    if (st != MMQ_OK)
+        return st;
+    if (!packed || !qa || !scales || !out)
+        return MMQ_ERR_ARG;
+    if (M < 1 || M > MMQ_MAX_M)
+        return MMQ_ERR_SHAPE;
+    if (mode == mmq::GEMM_Y && ldy < od)
+        return MMQ_ERR_ARG;
+    if (!aligned(packed, 16) || !aligned(qa, 16) || !aligned(scales, 16) || !aligned(out, 4))
+        return MMQ_ERR_ALIGN;
+    st = check_device();
+    if (st != MMQ_OK)
+        return st;
+    const char* label = nullptr;
+    const cudaError_t e = mmq::launch_gemm(static_cast<int>(t), mode, packed, od, id, qa, scales, M, out, ldy,
+                                           reinterpret_cast<cudaStream_t>(s), &label);
+    if (label)
+        g_last_path.store(label);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+mmq_status mmq_act_plane_bytes(int M, int K, size_t* qa_bytes, size_t* scale_bytes)
+{
+    if (!qa_bytes || !scale_bytes)
+        return MMQ_ERR_ARG;
+    if (M < 1 || M > MMQ_MAX_M || !valid_k(K))
+        return MMQ_ERR_SHAPE;
+    const mmq::ActPlanes p = mmq::act_planes(M, K);
+    *qa_bytes = p.qa_bytes;
+    *scale_bytes = p.scale_bytes;
+    return MMQ_OK;
+}
+
+mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales, mmq_stream_t s)
+{
+    if (!x || !qa || !scales)
+        return MMQ_ERR_ARG;
+    if (M < 1 || M > MMQ_MAX_M || !valid_k(K))
+        return MMQ_ERR_SHAPE;
+    if (ldx < K)
+        return MMQ_ERR_ARG;
+    if (!aligned(x, 4) || !aligned(qa, 16) || !aligned(scales, 16))
+        return MMQ_ERR_ALIGN;
+    const mmq_status st = check_device();
+    if (st != MMQ_OK)
+        return st;
+    return from_cuda(mmq::launch_quantize_act(x, M, K, ldx, qa, scales, reinterpret_cast<cudaStream_t>(s)));
+}
+
+mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes)
+{
+    if (!bytes)
+        return MMQ_ERR_ARG;
+    const mmq_status st = check_weight_shape(t, od, id);
+    if (st != MMQ_OK)
+        return st;
+    *bytes = mmq::weight_planes(od, id).total;
+    return MMQ_OK;
+}
+
+mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t* code_offset, size_t* code_bytes,
+                                    size_t* scale_offset, size_t* scale_bytes)
+{
+    if (!code_offset || !code_bytes || !scale_offset || !scale_bytes)
+        return MMQ_ERR_ARG;
+    const mmq_status st = check_weight_shape(t, od, id);
+    if (st != MMQ_OK)
+        return st;
+    const mmq::WeightPlanes w = mmq::weight_planes(od, id);
+    *code_offset = w.code_off;
+    *code_bytes = w.code_bytes;
+    *scale_offset = w.scale_off;
+    *scale_bytes = w.scale_bytes;
+    return MMQ_OK;
+}
+
+mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id, void* packed, mmq_stream_t s)
+{
+    mmq_status st = check_weight_shape(t, od, id);
+    if (st != MMQ_OK)
+        return st;
+    if (!raw_blocks || !packed)
+        return MMQ_ERR_ARG;
+    if (!aligned(packed, 16))
+        return MMQ_ERR_ALIGN;
+    st = check_device();
+    if (st != MMQ_OK)
+        return st;
+    return from_cuda(mmq::launch_pack(static_cast<int>(t), raw_blocks, od, id, packed,
+                                      reinterpret_cast<cudaStream_t>(s)));
+}
+
+mmq_status mmq_gemm_q6k(const void* packed, int od, int id, const void* qa, const void* scales, int M, float* Y,
+                        int ldy, mmq_stream_t s)
+{
+    return gemm_common(MMQ_Q6_K, mmq::GEMM_Y, packed, od, id, qa, scales, M, Y, ldy, s);
+}
+
+mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, const void* scales, int M, float* Y,
+                        int ldy, mmq_stream_t s)
+{
+    return gemm_common(MMQ_Q4_K, mmq::GEMM_Y, packed, od, id, qa, scales, M, Y, ldy, s);
+}
+
+mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa, const void* scales,
+                               int M, float* dots, mmq_stream_t s)
+{
+    return gemm_common(t, mmq::GEMM_DOTS, packed, od, id, qa, scales, M, dots, od, s);
+}
+
+mmq_status mmq_get_device_error(mmq_stream_t s)
+{
+    const mmq_status st = check_device();
+    if (st != MMQ_OK)
+        return st;
+    unsigned int word = 0;
+    const cudaError_t e = mmq::gemm_read_and_clear_error(reinterpret_cast<cudaStream_t>(s), &word);
+    if (e != cudaSuccess)
+        return MMQ_ERR_CUDA;
+    return word ? MMQ_ERR_TIMEOUT : MMQ_OK;
+}
+
+const char* mmq_status_string(mmq_status st)
+{
+    switch (st) {
+    case MMQ_OK: return "MMQ_OK";
+    case MMQ_ERR_ARG: return "MMQ_ERR_ARG: invalid argument";
+    case MMQ_ERR_SHAPE: return "MMQ_ERR_SHAPE: unsupported shape";
+    case MMQ_ERR_ALIGN: return "MMQ_ERR_ALIGN: misaligned pointer";
+    case MMQ_ERR_CUDA: return "MMQ_ERR_CUDA: CUDA runtime error";
+    case MMQ_ERR_TIMEOUT: return "MMQ_ERR_TIMEOUT: in-kernel wait expired";
+    case MMQ_ERR_UNSUPPORTED: return "MMQ_ERR_UNSUPPORTED: no sm_103 device current";
+    }
+    return "MMQ_ERR_UNKNOWN";
+}
+
+const char* mmq_last_path(void) { return g_last_path.load(); }
+
+const char* mmq_version(void) { return "mmq_gb300 0.1.0 (sm_103a, tcgen05 kind::f16 exact-integer MMQ)"; }
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+"""Read the library's tile-major planes back into row-major numpy arrays.
+
+Implements the layouts documented in include/mmq.h (test helper; no method
+arithmetic): 16384-byte operand tiles of 128 rows x 64 values of binary16 with
+the 128-byte swizzle, and tile-major 8-byte scale entries.
+"""
+import numpy as np
+
+TILE_ROWS = 128
+TILE_K = 64
+
+
+def _tile_index():
+    r = np.arange(TILE_ROWS)[:, None]
+    k = np.arange(TILE_K)[None, :]
+    byte = r * 128 + (((k >> 3) ^ (r & 7)) << 4) + ((k & 7) << 1)
+    return byte // 2  # index in binary16 units
+
+
+_IDX = _tile_index()
+
+
+def untile_codes(buf: np.ndarray, rows_padded: int, K: int) -> np.ndarray:
+    """Code plane (uint8 bytes) -> int64 codes [rows_padded, K]."""
+    nt, nkb = rows_padded // TILE_ROWS, K // TILE_K
+    u16 = np.ascontiguousarray(buf[: rows_padded * K * 2]).view(np.uint16).reshape(nt, nkb, TILE_ROWS * TILE_K)
+    tiles = u16[:, :, _IDX]                         # [nt, nkb, 128, 64]
+    vals = tiles.view(np.float16).astype(np.float64)
+    out = vals.transpose(0, 2, 1, 3).reshape(rows_padded, K)
+    assert np.all(out == np.round(out)), "codes must be exact integers"
+    return out.astype(np.int64)
+
+
+def untile_pairs(buf: np.ndarray, rows_padded: int, nchunk: int, dtype0, dtype1):
+    """Scale plane (uint8 bytes) -> two arrays [rows_padded, nchunk]."""
+    nt = rows_padded // TILE_ROWS
+    raw = np.ascontiguousarray(buf[: rows_padded * nchunk * 8]).view(np.uint32).reshape(nt, nchunk, TILE_ROWS, 2)
+    raw = raw.transpose(0, 2, 1, 3).reshape(rows_padded, nchunk, 2)
+    return raw[..., 0].copy().view(dtype0), raw[..., 1].copy().view(dtype1)
+
+
+def padded(n: int) -> int:
+    return (n + TILE_ROWS - 1) // TILE_ROWS * TILE_ROWS

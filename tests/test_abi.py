@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads, exports every symbol include/mmq.h declares,
+and validates arguments on the host before touching CUDA (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quant_int8_mmq_gb300 as mmq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mmq.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mmq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("mmq_quantize_act", "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k",
+                 "mmq_act_plane_bytes", "mmq_packed_weight_bytes", "mmq_get_device_error",
+                 "mmq_status_string", "mmq_last_path", "mmq_debug_gemm_dots"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(mmq_lib):
+    lib = ctypes.CDLL(mmq.lib_path())
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_python_binding_has_same_names(mmq_lib):
+    for name in _declared_functions():
+        assert callable(getattr(mmq, name)), name
+
+
+def test_size_queries_follow_the_documented_layout(mmq_lib):
+    qa, sc = mmq.mmq_act_plane_bytes(130, 512)
+    assert (qa, sc) == (256 * 512 * 2, 256 * 16 * 8)
+    for t in (mmq.MMQ_Q4_K, mmq.MMQ_Q6_K):
+        code_off, code_bytes, scale_off, scale_bytes = mmq.mmq_packed_weight_layout(t, 4097, 1024)
+        assert code_off == 0 and code_bytes == 4224 * 1024 * 2
+        assert scale_off == code_bytes and scale_bytes == 4224 * 32 * 8
+        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == code_bytes + scale_bytes
+
+
+@pytest.mark.parametrize("M,K,err", [(0, 256, 2), (1, 255, 2), (1, 0, 2), (5, 300, 2), (1 << 23, 256, 2)])
+def test_shape_errors(mmq_lib, M, K, err):
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_act_plane_bytes(M, K)
+    assert e.value.status == err
+
+
+def test_argument_errors_are_synchronous_and_cuda_free(mmq_lib):
+    lib = mmq.load()
+    p16 = 0x10000          # aligned fake pointers: never dereferenced on the error paths
+    # null pointers
+    assert lib.mmq_quantize_act(None, 4, 256, 256, p16, p16, None) == 1
+    assert lib.mmq_gemm_q4k(None, 8, 256, p16, p16, 4, p16, 8, None) == 1
+    # ldx < K, ldy < od
+    assert lib.mmq_quantize_act(p16, 4, 256, 200, p16, p16, None) == 1
+    assert lib.mmq_gemm_q6k(p16, 8, 256, p16, p16, 4, p16, 7, None) == 1
+    # shapes
+    assert lib.mmq_gemm_q4k(p16, 0, 256, p16, p16, 4, p16, 8, None) == 2
+    assert lib.mmq_gemm_q4k(p16, 8, 320, p16, p16, 4, p16, 8, None) == 2
+    assert lib.mmq_gemm_q4k(p16, 8, 256, p16, p16, 0, p16, 8, None) == 2
+    # alignment
+    assert lib.mmq_gemm_q4k(p16 + 8, 8, 256, p16, p16, 4, p16, 8, None) == 3
+    assert lib.mmq_gemm_q4k(p16, 8, 256, p16 + 4, p16, 4, p16, 8, None) == 3
+    assert lib.mmq_gemm_q4k(p16, 8, 256, p16, p16, 4, p16 + 2, 8, None) == 3
+    assert lib.mmq_quantize_act(p16 + 2, 4, 256, 256, p16, p16, None) == 3
+    assert lib.mmq_pack_weights(14, p16, 8, 256, p16 + 8, None) == 3
+    # bad type id
+    assert lib.mmq_pack_weights(7, p16, 8, 256, p16, None) == 1
+    assert lib.mmq_debug_gemm_dots(7, p16, 8, 256, p16, p16, 4, p16, None) == 1
+
+
+def test_valid_calls_without_a_gpu_report_unsupported(mmq_lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = mmq.load()
+    p16 = 0x10000
+    assert lib.mmq_quantize_act(p16, 4, 256, 256, p16, p16, None) == 6
+    assert lib.mmq_gemm_q4k(p16, 8, 256, p16, p16, 4, p16, 8, None) == 6
+
+
+def test_status_strings_and_labels(mmq_lib):
+    for st in range(7):
+        assert mmq.mmq_status_string(st).startswith(mmq.STATUS[st])
+    assert "sm_103a" in mmq.mmq_version()
+    assert isinstance(mmq.mmq_last_path(), str)

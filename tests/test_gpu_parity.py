@@ -1,0 +1,286 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (the workload's stated targets):
+  * prepass planes (q8 codes, d, ssum) and repacked planes: bit-exact;
+  * per-sub-block integer dots from the GEMM kernel: bit-exact;
+  * Y: normwise max|Y - Y_o| / max|Y_o| <= 1e-5 and, per element,
+    |Y - Y_o| <= 1e-5 * S (S = sum of |terms| of that output, from the oracle).
+Sizes span several tiles and ragged tails; the full-size configurations are
+checked on sampled tokens against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import quant_int8_mmq_gb300 as mmq
+from tests.planes import padded, untile_codes, untile_pairs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = 1e-5
+NTHREADS = oracle.cpu_threads()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(mmq_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+
+
+def _sync():
+    torch.cuda.synchronize()
+    assert mmq.mmq_get_device_error() == 0
+
+
+def _raw(typ, od, id_, seed, **kw):
+    if typ == "q6_K":
+        return synth.q6k_blocks(od, id_, seed, **kw)
+    return synth.q4k_blocks(od, id_, seed, **kw)
+
+
+def _to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def gpu_quantize(x: np.ndarray, ldx: int | None = None):
+    M, K = x.shape
+    if ldx is None:
+        xt = _to_dev(x)
+    else:
+        buf = torch.full((M, ldx), float("nan"), dtype=torch.float32, device=DEV)
+        buf[:, :K] = _to_dev(x)
+        xt = buf[:, :K]
+    qa, sc = mmq.quantize_act(xt)
+    return qa, sc
+
+
+def gpu_pack(typ, raw):
+    od, nsb = raw.shape[:2]
+    return mmq.pack_weights(typ, _to_dev(raw.reshape(-1)), od, nsb * 256)
+
+
+def oracle_gemm(typ, raw, x, nthreads=NTHREADS):
+    q, d, s = oracle.quantize_act(x)
+    fn = oracle.gemm_q6k if typ == "q6_K" else oracle.gemm_q4k
+    return fn(raw, q, d, s, nthreads=nthreads, with_abs=True)
+
+
+def assert_y_close(Y, Yo, S, tol=TOL):
+    Y = Y.astype(np.float64)
+    err = np.abs(Y - Yo)
+    scale = np.max(np.abs(Yo))
+    assert np.all(np.isfinite(Y))
+    assert err.max() <= tol * scale, f"normwise rel err {err.max() / scale:.3e}"
+    bad = err > tol * S + 1e-30
+    assert not bad.any(), f"{bad.sum()} elements over the condition-aware bound"
+
+
+# --------------------------------------------------------------------------- prepass
+def _check_prepass(x, ldx=None):
+    M, K = x.shape
+    qa, sc = gpu_quantize(x, ldx)
+    _sync()
+    q, d, s = oracle.quantize_act(x)
+    Mp = padded(M)
+    codes = untile_codes(qa.cpu().numpy(), Mp, K)
+    dd, ss = untile_pairs(sc.cpu().numpy(), Mp, K // 32, np.float32, np.int32)
+    assert np.array_equal(codes[:M], q.astype(np.int64))
+    assert np.array_equal(dd[:M].view(np.uint32), d.view(np.uint32))
+    assert np.array_equal(ss[:M], s)
+    assert not codes[M:].any() and not dd[M:].view(np.uint32).any() and not ss[M:].any()
+
+
+@pytest.mark.parametrize("M,K,seed", [(16, 512, 0), (512, 4096, 1), (130, 768, 5), (1, 256, 6), (2047, 1024, 7)])
+def test_prepass_bit_exact(M, K, seed):
+    _check_prepass(synth.activations(M, K, seed))
+
+
+def test_prepass_row_stride_and_special_values():
+    x = synth.activations(37, 512, 9)
+    x[0, :32] = 0.0                                  # all-zero chunk -> d = 0
+    x[1, 32:64] = 0.0
+    x[1, 40] = -3.0                                  # one-hot chunk -> -127
+    x[2, :32] = 0.0
+    x[2, 0] = 127.0
+    x[2, 1:7] = [0.5, 1.5, 2.5, -0.5, -1.5, -2.5]    # exact ties, away from zero
+    x[3] *= 1e-30                                    # tiny (subnormal d)
+    x[4] *= 3e30                                     # huge
+    _check_prepass(x, ldx=515)                       # odd row stride (scalar loads)
+    _check_prepass(x, ldx=520)
+
+
+# --------------------------------------------------------------------------- pack
+@pytest.mark.parametrize("typ", ["q6_K", "q4_K"])
+@pytest.mark.parametrize("od,id_", [(64, 512), (4097, 1024), (3, 256), (130, 768)])
+def test_pack_planes_byte_exact(typ, od, id_):
+    raw = _raw(typ, od, id_, seed=od + id_)
+    if typ == "q6_K":
+        raw = synth.q6k_blocks(od, id_, od + id_, sc_lo=-128, sc_hi=127)   # full int8 scale range
+    packed = gpu_pack(typ, raw)
+    _sync()
+    pk = packed.cpu().numpy()
+    tid = mmq.TYPES[typ]
+    code_off, code_bytes, scale_off, scale_bytes = mmq.mmq_packed_weight_layout(tid, od, id_)
+    assert pk.size == code_bytes + scale_bytes
+    Np = padded(od)
+    codes = untile_codes(pk[code_off:code_off + code_bytes], Np, id_)
+    a, b = untile_pairs(pk[scale_off:scale_off + scale_bytes], Np, id_ // 32, np.float32, np.float32)
+    if typ == "q6_K":
+        want = oracle.codes_q6k(raw).astype(np.int64)
+        dsc = oracle.scale_planes_q6k(raw)
+        wa, wb = dsc[..., 0], dsc[..., 1]
+    else:
+        want = oracle.codes_q4k(raw).astype(np.int64)
+        wa, wb = oracle.scale_planes_q4k(raw)
+    assert np.array_equal(codes[:od], want)
+    assert np.array_equal(a[:od].view(np.uint32), wa.view(np.uint32))
+    assert np.array_equal(b[:od].view(np.uint32), wb.view(np.uint32))
+    assert not codes[od:].any() and not a[od:].view(np.uint32).any() and not b[od:].view(np.uint32).any()
+
+
+# --------------------------------------------------------------------------- dots
+@pytest.mark.parametrize("typ", ["q6_K", "q4_K"])
+@pytest.mark.parametrize("M,od,id_", [(200, 300, 768), (1, 129, 256), (130, 64, 512), (257, 131, 2048)])
+def test_gemm_dots_bit_exact(typ, M, od, id_):
+    kw = dict(sc_lo=-128, sc_hi=127) if typ == "q6_K" else {}
+    raw = _raw(typ, od, id_, seed=3 * od + M, **kw)
+    x = synth.activations(M, id_, seed=M + 17)
+    qa, sc = gpu_quantize(x)
+    packed = gpu_pack(typ, raw)
+    dots = mmq.gemm_dots(typ, packed, od, id_, qa, sc, M)
+    _sync()
+    assert "tcgen05" in mmq.mmq_last_path()
+    q, _, _ = oracle.quantize_act(x)
+    ref = oracle.dots_q6k(raw, q) if typ == "q6_K" else oracle.dots_q4k(raw, q)
+    got = dots.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, ref.astype(np.float64))
+
+
+# --------------------------------------------------------------------------- Y
+def _run_gemm(typ, raw, x, Y=None):
+    M = x.shape[0]
+    od, nsb = raw.shape[:2]
+    qa, sc = gpu_quantize(x)
+    packed = gpu_pack(typ, raw)
+    Y = mmq.gemm(typ, packed, od, nsb * 256, qa, sc, M, Y=Y)
+    _sync()
+    return Y
+
+
+@pytest.mark.parametrize("typ,M,od,id_", [
+    ("q6_K", 16, 64, 512),        # the oracle-sized configuration
+    ("q4_K", 200, 300, 768),
+    ("q6_K", 200, 300, 768),
+    ("q4_K", 1, 1, 256),
+    ("q6_K", 129, 129, 512),
+    ("q4_K", 257, 385, 1280),
+])
+def test_gemm_small_full_parity(typ, M, od, id_):
+    raw = _raw(typ, od, id_, seed=od * 7 + M)
+    x = synth.activations(M, id_, seed=M * 3 + 1)
+    Y = _run_gemm(typ, raw, x).cpu().numpy()
+    Yo, S = oracle_gemm(typ, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+def test_gemm_q6k_full_int8_scale_range():
+    raw = synth.q6k_blocks(200, 1024, 77, sc_lo=-128, sc_hi=127)
+    x = synth.activations(150, 1024, 78)
+    Y = _run_gemm("q6_K", raw, x).cpu().numpy()
+    Yo, S = oracle_gemm("q6_K", raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+def test_gemm_cfg2_attention_projection_full():
+    cfg = synth.CONFIGS["cfg2_q4k_4096x4096_m512"]
+    raw = synth.q4k_blocks(cfg["od"], cfg["id"], cfg["seed"])
+    x = synth.activations(cfg["M"], cfg["id"], cfg["seed"] + 100)
+    Y = _run_gemm("q4_K", raw, x).cpu().numpy()
+    Yo, S = oracle_gemm("q4_K", raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+def _sampled_check(typ, raw, x, Y, rows):
+    Yo, S = oracle_gemm(typ, raw, x[rows])
+    assert_y_close(Y[rows], Yo, S)
+
+
+@pytest.mark.parametrize("M", [2048, 2047])
+def test_gemm_cfg3_ffn_gate_up_sampled(M):
+    cfg = synth.CONFIGS["cfg3_q4k_11008x4096_m2048"]
+    raw = synth.q4k_blocks(cfg["od"], cfg["id"], cfg["seed"])
+    x = synth.activations(M, cfg["id"], cfg["seed"] + 100)
+    Y = _run_gemm("q4_K", raw, x).cpu().numpy()
+    rows = np.unique(np.r_[0, 1, 127, 128, 129, 1023, M - 2, M - 1, np.random.default_rng(M).integers(0, M, 8)])
+    _sampled_check("q4_K", raw, x, Y, rows)
+
+
+def test_gemm_cfg4_ffn_down_sampled():
+    cfg = synth.CONFIGS["cfg4_q6k_4096x11008_m2048"]
+    raw = synth.q6k_blocks(cfg["od"], cfg["id"], cfg["seed"])
+    x = synth.activations(cfg["M"], cfg["id"], cfg["seed"] + 100)
+    Y = _run_gemm("q6_K", raw, x).cpu().numpy()
+    rows = np.unique(np.r_[0, 127, 128, 2047, np.random.default_rng(4).integers(0, 2048, 8)])
+    _sampled_check("q6_K", raw, x, Y, rows)
+
+
+@pytest.mark.parametrize("M", [1, 31])
+def test_gemm_cfg4_odd_od_tails_full(M):
+    cfg = synth.CONFIGS["cfg4_q6k_4096x11008_m2048"]
+    raw = synth.q6k_blocks(4097, cfg["id"], cfg["seed"])
+    x = synth.activations(M, cfg["id"], cfg["seed"] + 200 + M)
+    Y = _run_gemm("q6_K", raw, x).cpu().numpy()
+    Yo, S = oracle_gemm("q6_K", raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+@pytest.mark.parametrize("name,typ,od,id_", [("q", "q4_K", 4096, 4096), ("down", "q6_K", 4096, 11008),
+                                             ("lm_head", "q6_K", 32000, 4096)])
+def test_gemm_stack_shapes_at_prompt_length_sampled(name, typ, od, id_):
+    """The 7B-stack GEMM shapes at M = 3314 tokens, in the launch configuration the bench times."""
+    M = synth.STACK_M
+    raw = synth.blocks(typ, od, id_, synth.stack_seed(0, 0) + od)
+    x = synth.activations(M, id_, 1234 + od)
+    Y = _run_gemm(typ, raw, x).cpu().numpy()
+    rows = np.unique(np.r_[0, 3199, 3200, M - 1, np.random.default_rng(od).integers(0, M, 4)])
+    _sampled_check(typ, raw, x, Y, rows)
+
+
+def test_gemm_row_stride_and_unaligned_output():
+    typ, M, od, id_ = "q4_K", 100, 203, 512
+    raw = _raw(typ, od, id_, seed=5)
+    x = synth.activations(M, id_, 6)
+    Yo, S = oracle_gemm(typ, raw, x)
+    for ldy, off in ((211, 0), (208, 1), (256, 0)):
+        buf = torch.full((M * ldy + 8,), -7.0, dtype=torch.float32, device=DEV)
+        Yv = buf[off:off + M * ldy].view(M, ldy)
+        _run_gemm(typ, raw, x, Y=Yv)
+        host = Yv.cpu().numpy()
+        assert_y_close(host[:, :od], Yo, S)
+        assert np.all(host[:, od:] == -7.0)           # columns >= od never written
+        assert np.all(buf[:off].cpu().numpy() == -7.0)
+
+
+def test_gemm_deterministic():
+    typ = "q6_K"
+    raw = _raw(typ, 300, 1024, seed=1)
+    x = synth.activations(333, 1024, 2)
+    a = _run_gemm(typ, raw, x).cpu().numpy()
+    b = _run_gemm(typ, raw, x).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_status_codes_on_device():
+    raw = _raw("q4_K", 64, 256, seed=1)
+    packed = gpu_pack("q4_K", raw)
+    qa, sc = gpu_quantize(synth.activations(8, 256, 1))
+    Y = torch.empty((8, 64), dtype=torch.float32, device=DEV)
+    lib = mmq.load()
+    assert lib.mmq_gemm_q4k(packed.data_ptr() + 8, 64, 256, qa.data_ptr(), sc.data_ptr(), 8, Y.data_ptr(), 64,
+                            None) == 3
+    assert lib.mmq_gemm_q4k(packed.data_ptr(), 64, 256, qa.data_ptr(), sc.data_ptr(), 8, Y.data_ptr(), 64,
+                            None) == 0
+    assert mmq.mmq_last_path().startswith("q4_K")
+    _sync()

@@ -373,3 +373,22 @@ def test_gemm_token_permutation_and_threads(oracle_lib, kind):
     assert np.array_equal(Yp, Y[perm])
     Yt = fn(raw, q, d, s, nthreads=4)
     assert np.array_equal(Yt, Y)
+
+
+def test_whole_matrix_codes_match_encoder(oracle_lib):
+    rng = np.random.default_rng(81)
+    od, id_ = 5, 512
+    raw6 = np.zeros((od, 2, 210), np.uint8)
+    raw4 = np.zeros((od, 2, 144), np.uint8)
+    want6 = np.zeros((od, id_), np.int64)
+    want4 = np.zeros((od, id_), np.int64)
+    for j in range(od):
+        for b in range(2):
+            d, sc, q = random_q6k_fields(rng)
+            raw6[j, b] = encode_q6k(f16_bits(d), sc, q)
+            want6[j, 256 * b: 256 * b + 256] = q
+            d, dmin, sc, m, q = random_q4k_fields(rng)
+            raw4[j, b] = encode_q4k(f16_bits(d), f16_bits(dmin), sc, m, q)
+            want4[j, 256 * b: 256 * b + 256] = q
+    assert np.array_equal(oracle.codes_q6k(raw6), want6)
+    assert np.array_equal(oracle.codes_q4k(raw4), want4)
