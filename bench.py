@@ -52,6 +52,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (CPU baseline)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--peaks", action="store_true", help="run the throughput probes and print their JSON")
     return p.parse_args()
 
 
@@ -233,10 +234,12 @@ def host_acts(tokens):
 
 
 def cpu_sample_run(raws, xh, xf, seconds, threads):
+    # calibrate on a few tokens (per-GEMM thread start-up dominates a 1-token pass)
+    n0 = 4
     t0 = time.perf_counter()
-    oracle_stack_tokens(raws, xh, xf, 1, threads)
-    t1 = time.perf_counter() - t0
-    n = max(1, min(xh.shape[0], int(seconds / max(t1, 1e-6))))
+    oracle_stack_tokens(raws, xh, xf, n0, threads)
+    per_tok = (time.perf_counter() - t0) / n0
+    n = max(1, min(xh.shape[0], int(seconds / max(per_tok, 1e-6))))
     t0 = time.perf_counter()
     oracle_stack_tokens(raws, xh, xf, n, threads)
     dt = time.perf_counter() - t0
@@ -255,9 +258,10 @@ def run_reference(args, world, rank):
     xh, xf = host_acts(args.tokens)
     # size one step's token sample so the whole run stays within a few minutes
     t0 = time.perf_counter()
-    oracle_stack_tokens(raws, xh, xf, 1, threads)
-    t_tok = time.perf_counter() - t0
-    per_step = max(1, int(8.0 / max(t_tok, 1e-6) / max(1, args.steps + args.warmup) * 3))
+    oracle_stack_tokens(raws, xh, xf, 4, threads)
+    t_tok = (time.perf_counter() - t0) / 4
+    # whole run (warm-up + timed steps) sized to about two minutes of CPU work
+    per_step = max(1, int(120.0 / max(t_tok, 1e-6) / max(1, args.steps + args.warmup)))
     per_step = min(per_step, args.tokens)
     for _ in range(args.warmup):
         oracle_stack_tokens(raws, xh, xf, per_step, threads)
@@ -441,8 +445,19 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_peaks():
+    from quant_int8_mmq_gb300 import build as mmq_build
+    exe = mmq_build.build_peaks()
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
+    sys.stderr.write(r.stderr)
+    print(r.stdout.strip(), flush=True)
+    return r.returncode
+
+
 def main():
     args = parse_args()
+    if args.peaks:
+        return run_peaks()
     world, rank, local = dist_init()
     try:
         if args.impl == "reference":

@@ -6,6 +6,9 @@
  *     q6_K: Y[t,j] = sum_c sum_h d_a[t,c] * (d*sc[2(c%8)+h]) * I[t,j,c,h]
  *     q4_K: Y[t,j] = sum_c d_a[t,c] * ((d*sc_c) * I[t,j,c] - (dmin*m_c) * ssum[t,c])
  *
+ * (d, sc, dmin, m from the weight super-block; d_a, ssum the activation chunk's
+ * scale and code sum)
+ *
  * with I the integer dot of a 16-value (q6_K) or 32-value (q4_K) sub-block.
  *
  * Sources (page title, section):
@@ -70,17 +73,26 @@ typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
  * padded token rows zero-filled).
  *
  * Layout (fixed, documented so a caller can read it back):
- *   Mp = 128 * ceil(M/128) padded tokens; nkb = K/64; nchunk = K/32.
+ *   Mp = 128 * ceil(M/128) padded tokens; nkb = K/64; nchunk = K/32; nsb = K/256.
  *   qa:     Mp*K f16 values, the q8 codes held as exact binary16 integers.
  *           Tile (mt, kb) = tokens 128*mt.. and values 64*kb.. is a 16384-byte
  *           block at byte (mt*nkb + kb)*16384.  Inside it token r (0..127) and
  *           value k (0..63) sit at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2
  *           (the 128-byte swizzle of the tensor-core operand tile).
- *   scales: Mp*nchunk entries of 8 bytes {float d, int32 ssum}; entry (t, c)
- *           at index ((t/128)*nchunk + c)*128 + t%128.
- *   Rows t >= M hold code 0, d 0, ssum 0.
+ *   scales: two planes (offsets from mmq_act_scale_layout):
+ *     pairs  Mp*nchunk entries of 8 bytes {float d, int32 ssum}; entry (t, c) at
+ *            index ((t/128)*nchunk + c)*128 + t%128.
+ *     am     the q4_K min-term operand ma = d*ssum (one f32 multiply) split into
+ *            tf32 hi = round-to-nearest(ma) and lo = round-to-nearest(ma - hi):
+ *            per (token tile mt, super-block sb) an 8192-byte block at
+ *            (mt*nsb + sb)*8192 holding the hi tile then the lo tile, each
+ *            128 rows x 8 chunks of 4-byte values, row r / chunk k at byte
+ *            (r/8)*256 + (k/4)*128 + (r%8)*16 + (k%4)*4.
+ *   Rows t >= M hold code 0, d 0, ssum 0, ma 0.
  * -------------------------------------------------------------------------- */
 mmq_status mmq_act_plane_bytes(int M, int K, size_t* qa_bytes, size_t* scale_bytes);
+mmq_status mmq_act_scale_layout(int M, int K, size_t* pair_offset, size_t* pair_bytes,
+                                size_t* am_offset, size_t* am_bytes);
 
 /* Quantize x [M][ldx] f32 (row-major, first K values of each row used) per
  * 32-value chunk: d = amax/127 (IEEE f32 division), q = round(x/d) (IEEE f32
@@ -92,7 +104,8 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
 /* --------------------------------------------------------------------------
  * Registration-time weight repack ([r56] §2.2-§2.3 W_dsc plane: exact f16->f32
  * and int->f32 conversions, one f32 multiply, no FMA contraction; chunk-major
- * so one tile's window is contiguous; [r58] §5 names the same plane for q4_K).
+ * so one tile's window is contiguous; [r58] §5 names the same plane for q4_K;
+ * [r56] §1 and [r58] §3.2: codes unpacked once at registration).
  *
  * raw_blocks: od rows x id/256 super-blocks, row-major, 210 B (q6_K: ql[128]@0,
  *   qh[64]@128, int8 scales[16]@192, f16 d@208) or 144 B (q4_K: f16 d@0,
@@ -101,21 +114,37 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *   q6_K ((ql[e/2] >> 4*(e%2)) & 15 | ((qh[e/4] >> 2*(e%4)) & 3) << 4) - 32,
  *   q4_K (qs[e/2] >> 4*(e%2)) & 15.  Value e of a q6_K block uses scales[e/16].
  *
- * packed (caller-owned, mmq_packed_weight_bytes() bytes):
- *   Np = 128 * ceil(od/128); nkb = id/64; nchunk = id/32.
- *   code plane at byte 0, Np*id f16 values (q6_K: code in [-32,31]; q4_K: code
- *     in [0,15]), tile (nt, kb) a 16384-byte block at byte (nt*nkb + kb)*16384
- *     with row r, value k at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2.
- *   scale plane at byte Np*id*2, Np*nchunk entries of two floats, entry (j, c)
- *     at index ((j/128)*nchunk + c)*128 + j%128:
- *       q6_K {d*scales[2*(c%8)], d*scales[2*(c%8)+1]}
- *       q4_K {d*sc_(c%8), dmin*m_(c%8)}
- *   Rows j >= od are zero.
+ * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds five planes at
+ * the offsets mmq_packed_weight_layout() returns; Np = 128*ceil(od/128),
+ * nkb = id/64, nchunk = id/32, nsb = id/256; rows j >= od are zero:
+ *   CODES  Np*id f16 integers in 16384-byte tiles (nt, kb) at (nt*nkb + kb)*16384,
+ *          row r / value k at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2.
+ *          The integer sub-block scale is folded into the code where the product
+ *          is an exact f16 integer: q4_K sc_c*q (|.| <= 945); q6_K sc*q when every
+ *          |scales[i]| of the tensor is <= 64 (|.| <= 2048), else the plain code q.
+ *   PAIRS  Np*nchunk entries of two floats, entry (j, c) at index
+ *          ((j/128)*nchunk + c)*128 + j%128:
+ *            q6_K {d*scales[2*(c%8)], d*scales[2*(c%8)+1]}
+ *            q4_K {d*sc_(c%8), dmin*m_(c%8)}
+ *   SBD    f32 d per (row, super-block) at index ((j/128)*nsb + sb)*128 + j%128.
+ *   AUX    per (row tile nt, super-block sb) an 8192-byte block at (nt*nsb + sb)*8192:
+ *            q4_K: dmn = dmin*m_c split exactly into tf32 hi + lo; the hi tile then
+ *                  the lo tile, row r / chunk k at (r/8)*256 + (k/4)*128 + (r%8)*16 + (k%4)*4;
+ *            q6_K: the 16 scales as f32, scale s of row r at byte (s*128 + r)*4.
+ *   FLAG   q6_K: uint32 word 0 = 1 if CODES are folded, word 1 = max |scales[i]|.
  * -------------------------------------------------------------------------- */
+typedef enum {
+    MMQ_PLANE_CODES = 0,
+    MMQ_PLANE_PAIRS = 1,
+    MMQ_PLANE_SBD = 2,
+    MMQ_PLANE_AUX = 3,
+    MMQ_PLANE_FLAG = 4,
+    MMQ_NUM_WEIGHT_PLANES = 5
+} mmq_weight_plane;
+
 mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes);
-mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id,
-                                    size_t* code_offset, size_t* code_bytes,
-                                    size_t* scale_offset, size_t* scale_bytes);
+mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[MMQ_NUM_WEIGHT_PLANES],
+                                    size_t sizes[MMQ_NUM_WEIGHT_PLANES]);
 mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
                             void* packed, mmq_stream_t s);
 
@@ -125,8 +154,10 @@ mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
  * the same (type, od, id); qa/scales from mmq_quantize_act with K = id and the
  * same M.  The integer dots run exactly on the tensor cores (codes held as f16
  * integers, every partial sum an integer below 2^24 in the f32 accumulator);
- * the scales are applied in f32.  Rows t >= M and columns j >= od are never
- * written.  ldy >= od.
+ * the f32 scales are applied per chunk (d_a) and per super-block (d); the q4_K
+ * min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo tensor-core
+ * contraction (relative error about 2^-21 per product).  Rows t >= M and
+ * columns j >= od are never written.  ldy >= od.
  * -------------------------------------------------------------------------- */
 mmq_status mmq_gemm_q6k(const void* packed, int od, int id, const void* qa, const void* scales,
                         int M, float* Y, int ldy, mmq_stream_t s);
@@ -134,9 +165,12 @@ mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, cons
                         int M, float* Y, int ldy, mmq_stream_t s);
 
 /* Debug/verification: the same GEMM kernel (same staging, same tensor-core
- * contraction) writes the raw per-sub-block dots instead of Y:
- * dots[(t*od + j)*nsub + s] as f32 holding the exact integer, nsub = id/16
- * (q6_K, one per 16-value sub-block) or id/32 (q4_K, one per chunk). */
+ * contraction) writes the raw integer dots it accumulates instead of Y, as f32
+ * values holding the exact integers, at dots[(t*od + j)*nsub + s]:
+ *   q4_K: nsub = id/32, s = chunk c: sc_c * sum(q * q_a)
+ *   q6_K folded codes: nsub = id/32, s = chunk c: sc0*I_0 + sc1*I_1
+ *   q6_K plain codes:  nsub = id/16, s = 16-value sub-block: I_s = sum(q * q_a)
+ * (I_s the per-sub-block dot).  Size the buffer for id/16 per (t, j) for q6_K. */
 mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa,
                                const void* scales, int M, float* dots, mmq_stream_t s);
 

@@ -66,10 +66,13 @@ def _load():
         lib.oracle_dequant_q4k.argtypes = [P, I, I, P]
         lib.oracle_codes_q6k.argtypes = [P, I, I, P]
         lib.oracle_codes_q4k.argtypes = [P, I, I, P]
+        lib.oracle_fields_q6k.argtypes = [P, I, I, P, P]
+        lib.oracle_fields_q4k.argtypes = [P, I, I, P, P, P, P]
         for name in ("oracle_f16_to_f32_array", "oracle_quantize_act", "oracle_decode_q6k",
                      "oracle_decode_q4k", "oracle_scale_planes_q6k", "oracle_scale_planes_q4k",
                      "oracle_dots_q6k", "oracle_dots_q4k", "oracle_gemm_q6k", "oracle_gemm_q4k",
-                     "oracle_dequant_q6k", "oracle_dequant_q4k", "oracle_codes_q6k", "oracle_codes_q4k"):
+                     "oracle_dequant_q6k", "oracle_dequant_q4k", "oracle_codes_q6k", "oracle_codes_q4k", "oracle_fields_q6k",
+                     "oracle_fields_q4k"):
             getattr(lib, name).restype = None
         _lib = lib
         return lib
@@ -219,6 +222,28 @@ def codes_q4k(raw: np.ndarray) -> np.ndarray:
     out = np.empty((od, id_), np.uint8)
     _load().oracle_codes_q4k(_p(raw), od, id_, _p(out))
     return out
+
+
+def fields_q6k(raw: np.ndarray):
+    """(d [od, nsb] f32, scales [od, nsb, 16] int8) of every super-block."""
+    raw, od, id_ = _raw(raw, Q6K_BYTES)
+    nsb = id_ // QK_K
+    d = np.empty((od, nsb), np.float32)
+    sc = np.empty((od, nsb, 16), np.int8)
+    _load().oracle_fields_q6k(_p(raw), od, id_, _p(d), _p(sc))
+    return d, sc
+
+
+def fields_q4k(raw: np.ndarray):
+    """(d, dmin [od, nsb] f32, sc, m [od, nsb, 8] uint8) of every super-block."""
+    raw, od, id_ = _raw(raw, Q4K_BYTES)
+    nsb = id_ // QK_K
+    d = np.empty((od, nsb), np.float32)
+    dmin = np.empty((od, nsb), np.float32)
+    sc = np.empty((od, nsb, 8), np.uint8)
+    m = np.empty((od, nsb, 8), np.uint8)
+    _load().oracle_fields_q4k(_p(raw), od, id_, _p(d), _p(dmin), _p(sc), _p(m))
+    return d, dmin, sc, m
 
 
 def cpu_threads() -> int:

@@ -456,3 +456,29 @@ void oracle_codes_q4k(const uint8_t* raw, int od, int id, uint8_t* codes)
             oracle_decode_q4k(raw + ((size_t)j * nsb + sb) * Q4K_BYTES, &d, &dmin, sc, m,
                               codes + (size_t)j * id + (size_t)sb * QK_K);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Decoded per-super-block fields of a whole weight matrix, [od][id/256]:   */
+/*   q6_K: d, scales[16];  q4_K: d, dmin, sc[8], m[8].                       */
+/* ------------------------------------------------------------------------ */
+void oracle_fields_q6k(const uint8_t* raw, int od, int id, float* d, int8_t* sc)
+{
+    const int nsb = id / QK_K;
+    int8_t q[QK_K];
+    for (int j = 0; j < od; ++j)
+        for (int sb = 0; sb < nsb; ++sb) {
+            const size_t b = (size_t)j * nsb + sb;
+            oracle_decode_q6k(raw + b * Q6K_BYTES, d + b, sc + b * 16, q);
+        }
+}
+
+void oracle_fields_q4k(const uint8_t* raw, int od, int id, float* d, float* dmin, uint8_t* sc, uint8_t* m)
+{
+    const int nsb = id / QK_K;
+    uint8_t q[QK_K];
+    for (int j = 0; j < od; ++j)
+        for (int sb = 0; sb < nsb; ++sb) {
+            const size_t b = (size_t)j * nsb + sb;
+            oracle_decode_q4k(raw + b * Q4K_BYTES, d + b, dmin + b, sc + b * 8, m + b * 8, q);
+        }
+}

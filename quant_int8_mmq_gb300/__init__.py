@@ -19,7 +19,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "MMQError", "MMQ_Q4_K", "MMQ_Q6_K", "load", "lib_path",
-    "mmq_act_plane_bytes", "mmq_quantize_act", "mmq_packed_weight_bytes", "mmq_packed_weight_layout",
+    "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_quantize_act", "mmq_packed_weight_bytes",
+    "mmq_packed_weight_layout",
     "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_get_device_error",
     "mmq_status_string", "mmq_last_path", "mmq_version",
     "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
@@ -62,7 +63,8 @@ def load():
             "mmq_act_plane_bytes": [I, I, S, S],
             "mmq_quantize_act": [P, I, I, I, P, P, P],
             "mmq_packed_weight_bytes": [I, I, I, S],
-            "mmq_packed_weight_layout": [I, I, I, S, S, S, S],
+            "mmq_packed_weight_layout": [I, I, I, S, S],
+            "mmq_act_scale_layout": [I, I, S, S, S, S],
             "mmq_pack_weights": [I, P, I, I, P, P],
             "mmq_gemm_q6k": [P, I, I, P, P, I, P, I, P],
             "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
@@ -107,10 +109,22 @@ def mmq_packed_weight_bytes(t, od, id_):
     return b.value
 
 
+PLANES = ("codes", "pairs", "sbd", "aux", "flag")
+
+
 def mmq_packed_weight_layout(t, od, id_):
+    """{plane name: (offset, size)} of a packed weight buffer."""
+    off = (ctypes.c_size_t * 5)()
+    size = (ctypes.c_size_t * 5)()
+    _check(load().mmq_packed_weight_layout(t, od, id_, off, size), "mmq_packed_weight_layout")
+    return {name: (off[i], size[i]) for i, name in enumerate(PLANES)}
+
+
+def mmq_act_scale_layout(M, K):
+    """{"pairs": (offset, size), "am": (offset, size)} of the activation scale buffer."""
     v = [ctypes.c_size_t() for _ in range(4)]
-    _check(load().mmq_packed_weight_layout(t, od, id_, *[ctypes.byref(x) for x in v]), "mmq_packed_weight_layout")
-    return tuple(x.value for x in v)
+    _check(load().mmq_act_scale_layout(M, K, *[ctypes.byref(x) for x in v]), "mmq_act_scale_layout")
+    return {"pairs": (v[0].value, v[1].value), "am": (v[2].value, v[3].value)}
 
 
 def mmq_pack_weights(t, raw, od, id_, packed, stream=0):
@@ -206,11 +220,12 @@ def gemm(t, packed, od, id_, qa, scales, M, Y=None, stream=None):
 
 
 def gemm_dots(t, packed, od, id_, qa, scales, M, stream=None):
-    """Per-sub-block dots [M, od, nsub] (f32 holding exact integers), from the GEMM kernel."""
+    """Raw integer dots from the GEMM kernel as a flat f32 buffer of M*od*nsub values
+    (nsub = id/32, or id/16 for q6_K tensors with plain codes; see include/mmq.h)."""
     torch = _torch()
     tid = _type_id(t)
     nsub = id_ // 16 if tid == MMQ_Q6_K else id_ // 32
-    dots = torch.empty((M, od, nsub), dtype=torch.float32, device=packed.device)
+    dots = torch.full((M * od * nsub,), float("nan"), dtype=torch.float32, device=packed.device)
     mmq_debug_gemm_dots(tid, packed.data_ptr(), od, id_, qa.data_ptr(), scales.data_ptr(), M, dots.data_ptr(),
                         _stream(stream))
     return dots

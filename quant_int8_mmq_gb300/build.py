@@ -15,6 +15,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmmq_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["api.cu", "prepass.cu", "pack.cu", "gemm.cu"]
+PEAKS_SRC = "peaks.cu"
+PEAKS_EXE = os.path.join(BUILD_DIR, "mmq_peaks")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,7 +32,8 @@ def nvcc_path() -> str:
 
 
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "mmq.h"), __file__]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f != PEAKS_SRC]
+    files += [os.path.join(INCLUDE, "mmq.h"), __file__]
     return [f for f in files if os.path.isfile(f)]
 
 
@@ -77,6 +80,19 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+def build_peaks() -> str:
+    """The throughput-probe program (roofline denominators), built on demand."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    src = os.path.join(CSRC, PEAKS_SRC)
+    if os.path.exists(PEAKS_EXE) and os.path.getmtime(PEAKS_EXE) >= os.path.getmtime(src):
+        return PEAKS_EXE
+    cmd = [nvcc_path()] + compile_flags() + [src, "-o", PEAKS_EXE]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {PEAKS_SRC}:\n{r.stdout}\n{r.stderr}")
+    return PEAKS_EXE
 
 
 if __name__ == "__main__":

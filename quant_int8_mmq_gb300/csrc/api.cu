@@ -113,19 +113,40 @@ mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes)
     return MMQ_OK;
 }
 
-mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t* code_offset, size_t* code_bytes,
-                                    size_t* scale_offset, size_t* scale_bytes)
+mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[MMQ_NUM_WEIGHT_PLANES],
+                                    size_t sizes[MMQ_NUM_WEIGHT_PLANES])
 {
-    if (!code_offset || !code_bytes || !scale_offset || !scale_bytes)
+    if (!offsets || !sizes)
         return MMQ_ERR_ARG;
     const mmq_status st = check_weight_shape(t, od, id);
     if (st != MMQ_OK)
         return st;
     const mmq::WeightPlanes w = mmq::weight_planes(od, id);
-    *code_offset = w.code_off;
-    *code_bytes = w.code_bytes;
-    *scale_offset = w.scale_off;
-    *scale_bytes = w.scale_bytes;
+    offsets[MMQ_PLANE_CODES] = w.code_off;
+    sizes[MMQ_PLANE_CODES] = w.code_bytes;
+    offsets[MMQ_PLANE_PAIRS] = w.pair_off;
+    sizes[MMQ_PLANE_PAIRS] = w.pair_bytes;
+    offsets[MMQ_PLANE_SBD] = w.sbd_off;
+    sizes[MMQ_PLANE_SBD] = w.sbd_bytes;
+    offsets[MMQ_PLANE_AUX] = w.aux_off;
+    sizes[MMQ_PLANE_AUX] = w.aux_bytes;
+    offsets[MMQ_PLANE_FLAG] = w.flag_off;
+    sizes[MMQ_PLANE_FLAG] = w.flag_bytes;
+    return MMQ_OK;
+}
+
+mmq_status mmq_act_scale_layout(int M, int K, size_t* pair_offset, size_t* pair_bytes, size_t* am_offset,
+                                size_t* am_bytes)
+{
+    if (!pair_offset || !pair_bytes || !am_offset || !am_bytes)
+        return MMQ_ERR_ARG;
+    if (M < 1 || M > MMQ_MAX_M || !valid_k(K))
+        return MMQ_ERR_SHAPE;
+    const mmq::ActPlanes p = mmq::act_planes(M, K);
+    *pair_offset = p.pair_off;
+    *pair_bytes = p.pair_bytes;
+    *am_offset = p.am_off;
+    *am_bytes = p.am_bytes;
     return MMQ_OK;
 }
 

@@ -27,27 +27,59 @@ __host__ __device__ constexpr int tile_byte(int r, int k)
     return r * 128 + (((k >> 3) ^ (r & 7)) << 4) + ((k & 7) << 1);
 }
 
+// Byte offset of value k (0..7) of row r (0..127) inside one 128 x 8 tf32 operand
+// tile: K-major, no swizzle, 8-row x 16-byte core matrices; the two core matrices
+// of an 8-row group are adjacent (K-direction stride 128 B), 8-row groups are
+// 256 B apart.
+__host__ __device__ constexpr int tf32_tile_byte(int r, int k)
+{
+    return (r >> 3) * 256 + (k >> 2) * 128 + (r & 7) * 16 + (k & 3) * 4;
+}
+constexpr int TF32_TILE_BYTES = 128 * 8 * 4;
+
 struct ActPlanes {       // layout of mmq_quantize_act's outputs
-    size_t qa_bytes, scale_bytes;
+    size_t qa_bytes;     // f16 code tiles
+    size_t pair_off, pair_bytes;   // {f32 d, i32 ssum} per (token, chunk)
+    size_t am_off, am_bytes;       // tf32 hi/lo tiles of d*ssum per (token tile, super-block)
+    size_t scale_bytes;            // pairs + am
 };
 inline ActPlanes act_planes(int M, int K)
 {
     const size_t Mp = static_cast<size_t>(ceil_div(M, TILE_ROWS)) * TILE_ROWS;
-    return {Mp * static_cast<size_t>(K) * 2, Mp * static_cast<size_t>(K / CHUNK) * 8};
+    ActPlanes a;
+    a.qa_bytes = Mp * static_cast<size_t>(K) * 2;
+    a.pair_off = 0;
+    a.pair_bytes = Mp * static_cast<size_t>(K / CHUNK) * 8;
+    a.am_off = a.pair_bytes;
+    a.am_bytes = Mp / TILE_ROWS * static_cast<size_t>(K / QK_K) * 2 * TF32_TILE_BYTES;
+    a.scale_bytes = a.am_off + a.am_bytes;
+    return a;
 }
 
 struct WeightPlanes {    // layout of mmq_pack_weights' output
-    size_t code_off, code_bytes, scale_off, scale_bytes, total;
+    size_t code_off, code_bytes;   // f16 code tiles (scale-folded where exact)
+    size_t pair_off, pair_bytes;   // f32 scale pairs per (row, chunk)
+    size_t sbd_off, sbd_bytes;     // f32 d per (row, super-block)
+    size_t aux_off, aux_bytes;     // q4_K: tf32 hi/lo tiles of dmin*m; q6_K: f32 scales per sub-block
+    size_t flag_off, flag_bytes;   // q6_K: word 0 = 1 if codes hold sc*q, word 1 = max |sc|
+    size_t total;
 };
 inline WeightPlanes weight_planes(int od, int id)
 {
     const size_t Np = static_cast<size_t>(ceil_div(od, TILE_ROWS)) * TILE_ROWS;
+    const size_t nsb = static_cast<size_t>(id / QK_K);
     WeightPlanes w;
     w.code_off = 0;
     w.code_bytes = Np * static_cast<size_t>(id) * 2;
-    w.scale_off = w.code_bytes;
-    w.scale_bytes = Np * static_cast<size_t>(id / CHUNK) * 8;
-    w.total = w.scale_off + w.scale_bytes;
+    w.pair_off = w.code_off + w.code_bytes;
+    w.pair_bytes = Np * static_cast<size_t>(id / CHUNK) * 8;
+    w.sbd_off = w.pair_off + w.pair_bytes;
+    w.sbd_bytes = Np * nsb * 4;
+    w.aux_off = w.sbd_off + w.sbd_bytes;
+    w.aux_bytes = Np * nsb * 64;   // q4_K: 2 x 8 tf32; q6_K: 16 f32
+    w.flag_off = w.aux_off + w.aux_bytes;
+    w.flag_bytes = 256;
+    w.total = w.flag_off + w.flag_bytes;
     return w;
 }
 

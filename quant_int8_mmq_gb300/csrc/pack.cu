@@ -1,20 +1,32 @@
 // pack.cu -- registration-time weight repack.
 //
-// Raw q6_K / q4_K super-blocks -> (1) a code plane of exact f16 integer codes in
-// the tensor-core operand tile layout (128 weight rows x 64 values, 128-byte
-// swizzle) and (2) a tile-major f32 scale-pair plane, rows >= od zero-filled.
-//
-// Scale planes are built the way the W_dsc plane is ("r56 - q6_K A-side
-// bundle ...", §2.2 and §2.3): exact f16 -> f32 and int -> f32 conversions and
-// exactly one f32 multiply (__fmul_rn, never contracted into an FMA), so each
-// entry is bit-identical to the scalar product.  The pair per (chunk, row) is
-//   q6_K: {d * scales[2(c%8)], d * scales[2(c%8)+1]}   (the r56 float2 pair)
-//   q4_K: {d * sc_c, dmin * m_c}                      (the q4_K plane named as the
-//          next step in "r58 - q4_K BT spec ...", §5)
-// The layout follows the GEMM's consumption window: one tile's 128 rows of one
-// chunk are 1 KiB contiguous (the chunk-major principle of r56 §2.2).  Codes are
-// unpacked once here instead of in the GEMM's staging (the registration-time
-// expansion of r56 §1 / r58 §3.2).
+// Raw q6_K / q4_K super-blocks -> the planes the GEMM streams (rows >= od zero):
+//  codes  f16 integer codes in the tensor-core operand tile layout (128 weight
+//         rows x 64 values, 128-byte swizzle) with the integer sub-block scale
+//         folded in where the product stays an exact f16 integer:
+//           q4_K: sc_c * q  (|.| <= 63 * 15 = 945, always folded)
+//           q6_K: sc * q    when every |sc| of the tensor is <= 64 (|.| <= 2048),
+//                 else the plain code q (the GEMM then keeps one accumulator per
+//                 16-value sub-block)
+//  pairs  tile-major f32 scale pairs per (row, chunk), built the way the W_dsc
+//         plane is ("r56 - q6_K A-side bundle ...", §2.2 and §2.3): exact f16 -> f32
+//         and int -> f32 conversions and exactly one f32 multiply (__fmul_rn, never
+//         contracted into an FMA):
+//           q6_K {d * scales[2(c%8)], d * scales[2(c%8)+1]}   (the r56 float2 pair)
+//           q4_K {d * sc_c, dmin * m_c}     (the q4_K plane "r58 - q4_K BT spec ...",
+//                                           §5 names as the next step)
+//  sbd    f32 d per (row, super-block): the factor applied once per super-block
+//         when the codes carry the integer scale.
+//  aux    q4_K: the min-term operand dmn = dmin * m (exact f32, <= 17 significant
+//               bits) split exactly into tf32 hi + lo, in 128 x 8 tf32 tiles per
+//               (row tile, super-block);
+//         q6_K: the 16 int8 sub-block scales as f32 per (row, super-block), used
+//               when the codes are not folded.
+//  flag   q6_K: word 0 = 1 if the codes are folded, word 1 = max |sc|.
+// The layout follows the GEMM's consumption window: one tile's rows of one chunk
+// or super-block are contiguous (the chunk-major principle of r56 §2.2), and the
+// codes are unpacked once here instead of in the GEMM's staging (the
+// registration-time expansion of r56 §1 and r58 §3.2).
 //
 // Bit mapping inside ql/qh/qs and the scales[12] packing: the documented reading
 // (see include/mmq.h).  One thread per (padded row j, chunk c).
@@ -37,6 +49,13 @@ __device__ __forceinline__ uint32_t half2_bits(int a, int b)
            (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(b))) << 16);
 }
 
+__device__ __forceinline__ float tf32_rna(float v)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+
 // Six-bit field f (0..15) of the 12 scale bytes read as one little-endian 96-bit word.
 __device__ __forceinline__ int q4k_field(const uint8_t* sc12, int f)
 {
@@ -48,66 +67,123 @@ __device__ __forceinline__ int q4k_field(const uint8_t* sc12, int f)
     return static_cast<int>(v & 63u);
 }
 
+// q6_K: max |sc| over the tensor -> flag word 1 (atomicMax); word 0 is set later.
+__global__ void q6k_scale_scan(const uint8_t* __restrict__ raw, long long nblocks, unsigned int* flag)
+{
+    unsigned int mx = 0;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks * 16;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int v = static_cast<int8_t>(raw[(i >> 4) * Q6K_BYTES + 192 + (i & 15)]);
+        const unsigned int a = static_cast<unsigned int>(v < 0 ? -v : v);
+        mx = a > mx ? a : mx;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0 && mx)
+        atomicMax(flag + 1, mx);
+}
+
 template <int TYPE>
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ raw, int od, int id, int Np,
-                                                   uint8_t* __restrict__ codes, float2* __restrict__ wscale)
+                                                   uint8_t* __restrict__ codes, float2* __restrict__ pairs,
+                                                   float* __restrict__ sbd, uint8_t* __restrict__ aux,
+                                                   unsigned int* __restrict__ flag)
 {
     const int nchunk = id / CHUNK;
     const int nkb = id / TILE_K;
     const int nsb = id / QK_K;
+    const bool fold = (TYPE == 12) || (flag[1] <= 64u);
+    if (TYPE == 14 && blockIdx.x == 0 && threadIdx.x == 0)
+        flag[0] = fold ? 1u : 0u;
     const long long total = static_cast<long long>(Np) * nchunk;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int c = static_cast<int>(i % nchunk);
         const int j = static_cast<int>(i / nchunk);
-        const int cc = c & 7;  // chunk within its super-block
-        uint32_t h2[16];       // 32 codes as 16 f16 pairs
+        const int cc = c & 7;       // chunk within its super-block
+        const int sb = c >> 3;
+        const int nt = j / TILE_ROWS, r = j % TILE_ROWS;
+        uint32_t h2[16];            // 32 codes as 16 f16 pairs
         float2 w = make_float2(0.0f, 0.0f);
         if (j < od) {
             if (TYPE == 14) {  // q6_K
-                const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + (c >> 3)) * Q6K_BYTES;
+                const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + sb) * Q6K_BYTES;
                 const uint8_t* ql = b + 16 * cc;   // values 32cc.. use ql bytes 16cc..16cc+15
                 const uint8_t* qh = b + 128 + 8 * cc;
+                const int s0 = static_cast<int8_t>(b[192 + 2 * cc]);
+                const int s1 = static_cast<int8_t>(b[192 + 2 * cc + 1]);
 #pragma unroll
                 for (int p = 0; p < 16; ++p) {
-                    const int e0 = 2 * p, e1 = 2 * p + 1;  // values 32cc+e0, 32cc+e1 (e0 even)
+                    const int e0 = 2 * p, e1 = 2 * p + 1;  // values 32cc+e0, 32cc+e1
                     const unsigned lo = ql[p];
                     const unsigned hb = qh[p >> 1];
-                    const int u0 = static_cast<int>((lo & 15u) | (((hb >> (2 * (e0 & 3))) & 3u) << 4));
-                    const int u1 = static_cast<int>((lo >> 4) | (((hb >> (2 * (e1 & 3))) & 3u) << 4));
-                    h2[p] = half2_bits(u0 - 32, u1 - 32);
+                    int u0 = static_cast<int>((lo & 15u) | (((hb >> (2 * (e0 & 3))) & 3u) << 4)) - 32;
+                    int u1 = static_cast<int>((lo >> 4) | (((hb >> (2 * (e1 & 3))) & 3u) << 4)) - 32;
+                    if (fold) {
+                        const int sc = p < 8 ? s0 : s1;  // values 0..15 of the chunk use s0
+                        u0 *= sc;
+                        u1 *= sc;
+                    }
+                    h2[p] = half2_bits(u0, u1);
                 }
                 const float d = load_f16_bytes(b + 208);
-                const float s0 = static_cast<float>(static_cast<int8_t>(b[192 + 2 * cc]));
-                const float s1 = static_cast<float>(static_cast<int8_t>(b[192 + 2 * cc + 1]));
-                w = make_float2(__fmul_rn(d, s0), __fmul_rn(d, s1));
+                w = make_float2(__fmul_rn(d, static_cast<float>(s0)), __fmul_rn(d, static_cast<float>(s1)));
+                if (cc == 0) {
+                    sbd[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = d;
+                    float* scp = reinterpret_cast<float*>(aux + (static_cast<size_t>(nt) * nsb + sb) * 8192);
+#pragma unroll
+                    for (int s = 0; s < 16; ++s)
+                        scp[s * TILE_ROWS + r] = static_cast<float>(static_cast<int8_t>(b[192 + s]));
+                }
             } else {  // q4_K
-                const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + (c >> 3)) * Q4K_BYTES;
+                const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + sb) * Q4K_BYTES;
                 const uint8_t* qs = b + 16 + 16 * cc;
+                const int sc = q4k_field(b + 4, cc);
+                const int m = q4k_field(b + 4, 8 + cc);
 #pragma unroll
                 for (int p = 0; p < 16; ++p) {
                     const unsigned v = qs[p];
-                    h2[p] = half2_bits(static_cast<int>(v & 15u), static_cast<int>(v >> 4));
+                    h2[p] = half2_bits(sc * static_cast<int>(v & 15u), sc * static_cast<int>(v >> 4));
                 }
                 const float d = load_f16_bytes(b + 0);
                 const float dmin = load_f16_bytes(b + 2);
-                const float sc = static_cast<float>(q4k_field(b + 4, cc));
-                const float m = static_cast<float>(q4k_field(b + 4, 8 + cc));
-                w = make_float2(__fmul_rn(d, sc), __fmul_rn(dmin, m));
+                const float dmn = __fmul_rn(dmin, static_cast<float>(m));
+                w = make_float2(__fmul_rn(d, static_cast<float>(sc)), dmn);
+                if (cc == 0)
+                    sbd[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = d;
+                const float hi = tf32_rna(dmn);
+                const float lo = __fsub_rn(dmn, hi);  // <= 6 significant bits: exact in tf32
+                uint8_t* t0 = aux + (static_cast<size_t>(nt) * nsb + sb) * (2 * TF32_TILE_BYTES);
+                *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, cc)) = hi;
+                *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, cc)) = lo;
             }
         } else {
 #pragma unroll
             for (int p = 0; p < 16; ++p)
                 h2[p] = 0u;
+            if (cc == 0)
+                sbd[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = 0.0f;
+            if (TYPE == 14) {
+                if (cc == 0) {
+                    float* scp = reinterpret_cast<float*>(aux + (static_cast<size_t>(nt) * nsb + sb) * 8192);
+#pragma unroll
+                    for (int s = 0; s < 16; ++s)
+                        scp[s * TILE_ROWS + r] = 0.0f;
+                }
+            } else {
+                uint8_t* t0 = aux + (static_cast<size_t>(nt) * nsb + sb) * (2 * TF32_TILE_BYTES);
+                *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, cc)) = 0.0f;
+                *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, cc)) = 0.0f;
+            }
         }
-        const int nt = j / TILE_ROWS, r = j % TILE_ROWS;
         const int kb = c >> 1, k0 = (c & 1) * CHUNK;
         uint8_t* tile = codes + (static_cast<size_t>(nt) * nkb + kb) * TILE_BYTES;
 #pragma unroll
         for (int u = 0; u < 4; ++u)  // four 16-byte units of 8 codes each
             *reinterpret_cast<uint4*>(tile + tile_byte(r, k0 + 8 * u)) =
                 make_uint4(h2[4 * u], h2[4 * u + 1], h2[4 * u + 2], h2[4 * u + 3]);
-        wscale[(static_cast<size_t>(nt) * nchunk + c) * TILE_ROWS + r] = w;
+        pairs[(static_cast<size_t>(nt) * nchunk + c) * TILE_ROWS + r] = w;
     }
 }
 
@@ -122,13 +198,25 @@ cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed,
     if (blocks > 65535LL * 8)
         blocks = 65535LL * 8;
     uint8_t* base = static_cast<uint8_t*>(packed);
-    float2* ws = reinterpret_cast<float2*>(base + wp.scale_off);
-    if (type == 14)
-        pack_kernel<14><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint8_t*>(raw), od, id,
-                                                                        Np, base + wp.code_off, ws);
-    else
-        pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint8_t*>(raw), od, id,
-                                                                        Np, base + wp.code_off, ws);
+    const uint8_t* rb = static_cast<const uint8_t*>(raw);
+    unsigned int* flag = reinterpret_cast<unsigned int*>(base + wp.flag_off);
+    cudaError_t e = cudaMemsetAsync(flag, 0, wp.flag_bytes, s);
+    if (e != cudaSuccess)
+        return e;
+    float2* pairs = reinterpret_cast<float2*>(base + wp.pair_off);
+    float* sbd = reinterpret_cast<float*>(base + wp.sbd_off);
+    if (type == 14) {
+        const long long nblocks = static_cast<long long>(od) * (id / QK_K);
+        long long sblocks = (nblocks * 16 + 255) / 256;
+        if (sblocks > 4096)
+            sblocks = 4096;
+        q6k_scale_scan<<<static_cast<unsigned>(sblocks), 256, 0, s>>>(rb, nblocks, flag);
+        pack_kernel<14><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
+                                                                        sbd, base + wp.aux_off, flag);
+    } else {
+        pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
+                                                                        sbd, base + wp.aux_off, flag);
+    }
     return cudaGetLastError();
 }
 

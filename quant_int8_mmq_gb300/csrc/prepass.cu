@@ -5,8 +5,11 @@
 // [-127,127]), ssum = sum q; d == 0 gives q = 0.  The codes are written as exact
 // f16 integers straight into the tensor-core operand tile layout (128 tokens x 64
 // values, 128-byte swizzle), so the GEMM stages them with one bulk copy and no
-// conversion; the (d, ssum) pairs go to a tile-major scale plane.  Padded token
-// rows (t >= M) are zero-filled.
+// conversion; the (d, ssum) pairs go to a tile-major scale plane.  It also writes
+// the operand of the q4_K min-term side contraction: ma = d*ssum (one f32
+// multiply) split exactly-enough into tf32 hi = rna(ma) and lo = rna(ma - hi),
+// in 128 x 8 tf32 tiles per (token tile, super-block).  Padded token rows
+// (t >= M) are zero-filled.
 //
 // Sources: the prepass that moved activation quantization and transposition
 // out of the GEMM and writes pre-transposed qa8 and d/ssum planes with padded
@@ -31,9 +34,16 @@ __device__ __forceinline__ int quant_one(float x, float d)
     return static_cast<int>(r);
 }
 
+__device__ __forceinline__ float tf32_rna(float v)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int M, int K, int ldx,
                                                            int Mp, int vec2, uint16_t* __restrict__ qa,
-                                                           uint2* __restrict__ scales)
+                                                           uint2* __restrict__ scales, uint8_t* __restrict__ am)
 {
     const int lane = threadIdx.x & 31;
     const int nkb = K / TILE_K;
@@ -80,6 +90,12 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
             const int c = 2 * kb + (lane >> 4);
             scales[(static_cast<size_t>(mt) * nchunk + c) * TILE_ROWS + r] =
                 make_uint2(__float_as_uint(d), static_cast<uint32_t>(s));
+            const float ma = __fmul_rn(d, static_cast<float>(s));
+            const float hi = tf32_rna(ma);
+            const float lo = tf32_rna(__fsub_rn(ma, hi));
+            uint8_t* t0 = am + (static_cast<size_t>(mt) * (K / QK_K) + c / 8) * (2 * TF32_TILE_BYTES);
+            *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = hi;
+            *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = lo;
         }
     }
 }
@@ -101,8 +117,11 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
     if (blocks > cap)
         blocks = cap;
     const int vec2 = ((ldx % 2) == 0 && (reinterpret_cast<uintptr_t>(x) % 8) == 0) ? 1 : 0;
+    const ActPlanes ap = act_planes(M, K);
+    uint8_t* sc = static_cast<uint8_t*>(scales);
     quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, M, K, ldx, Mp, vec2, static_cast<uint16_t*>(qa), static_cast<uint2*>(scales));
+        x, M, K, ldx, Mp, vec2, static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off),
+        sc + ap.am_off);
     return cudaGetLastError();
 }
 

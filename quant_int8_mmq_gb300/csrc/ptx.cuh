@@ -294,6 +294,25 @@ __device__ __forceinline__ void tmem_ld16x2_wait(uint32_t taddr0, uint32_t taddr
     }
 }
 
+// Two 8-column loads (columns taddr0.. and taddr1..) with a single wait.
+__device__ __forceinline__ void tmem_ld8x2_wait(uint32_t taddr0, uint32_t taddr1, float (&v0)[8], float (&v1)[8])
+{
+    uint32_t r[8], s[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : MMQ_R32(0), MMQ_R32(1), MMQ_R32(2), MMQ_R32(3), MMQ_R32(4), MMQ_R32(5), MMQ_R32(6), MMQ_R32(7),
+          "=r"(s[0]), "=r"(s[1]), "=r"(s[2]), "=r"(s[3]), "=r"(s[4]), "=r"(s[5]), "=r"(s[6]), "=r"(s[7])
+        : "r"(taddr0), "r"(taddr1)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v0[i] = __uint_as_float(r[i]);
+        v1[i] = __uint_as_float(s[i]);
+    }
+}
+
 #undef MMQ_R32
 
 }  // namespace mmq

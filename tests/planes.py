@@ -41,3 +41,34 @@ def untile_pairs(buf: np.ndarray, rows_padded: int, nchunk: int, dtype0, dtype1)
 
 def padded(n: int) -> int:
     return (n + TILE_ROWS - 1) // TILE_ROWS * TILE_ROWS
+
+
+def _tf32_index():
+    r = np.arange(TILE_ROWS)[:, None]
+    k = np.arange(8)[None, :]
+    return ((r >> 3) * 256 + (k >> 2) * 128 + (r & 7) * 16 + (k & 3) * 4) // 4
+
+
+_TF32_IDX = _tf32_index()
+
+
+def untile_tf32_pair(buf: np.ndarray, rows_padded: int, nsb: int):
+    """hi/lo tf32 tile plane (8192-byte blocks per (row tile, super-block)) -> two
+    float32 arrays [rows_padded, nsb*8]."""
+    nt = rows_padded // TILE_ROWS
+    f = np.ascontiguousarray(buf[: nt * nsb * 8192]).view(np.float32).reshape(nt, nsb, 2, 1024)
+    tiles = f[:, :, :, _TF32_IDX]                       # [nt, nsb, 2, 128, 8]
+    hi = tiles[:, :, 0].transpose(0, 2, 1, 3).reshape(rows_padded, nsb * 8)
+    lo = tiles[:, :, 1].transpose(0, 2, 1, 3).reshape(rows_padded, nsb * 8)
+    return hi, lo
+
+
+def untile_rows(buf: np.ndarray, rows_padded: int, n: int, dtype=np.float32):
+    """[row tile][n][128] plane -> [rows_padded, n]."""
+    nt = rows_padded // TILE_ROWS
+    a = np.ascontiguousarray(buf[: nt * n * TILE_ROWS * 4]).view(dtype).reshape(nt, n, TILE_ROWS)
+    return a.transpose(0, 2, 1).reshape(rows_padded, n)
+
+
+def is_tf32(a: np.ndarray) -> bool:
+    return bool(np.all((a.view(np.uint32) & 0x1FFF) == 0))

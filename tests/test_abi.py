@@ -39,12 +39,21 @@ def test_python_binding_has_same_names(mmq_lib):
 
 def test_size_queries_follow_the_documented_layout(mmq_lib):
     qa, sc = mmq.mmq_act_plane_bytes(130, 512)
-    assert (qa, sc) == (256 * 512 * 2, 256 * 16 * 8)
+    lay = mmq.mmq_act_scale_layout(130, 512)
+    assert qa == 256 * 512 * 2
+    assert lay["pairs"] == (0, 256 * 16 * 8)
+    assert lay["am"] == (256 * 16 * 8, 2 * 2 * 8192)            # 2 token tiles x 2 super-blocks
+    assert sc == lay["am"][0] + lay["am"][1]
     for t in (mmq.MMQ_Q4_K, mmq.MMQ_Q6_K):
-        code_off, code_bytes, scale_off, scale_bytes = mmq.mmq_packed_weight_layout(t, 4097, 1024)
-        assert code_off == 0 and code_bytes == 4224 * 1024 * 2
-        assert scale_off == code_bytes and scale_bytes == 4224 * 32 * 8
-        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == code_bytes + scale_bytes
+        L = mmq.mmq_packed_weight_layout(t, 4097, 1024)
+        Np, nsb = 4224, 4
+        assert L["codes"] == (0, Np * 1024 * 2)
+        assert L["pairs"] == (Np * 1024 * 2, Np * 32 * 8)
+        assert L["sbd"] == (sum(L["pairs"]), Np * nsb * 4)
+        assert L["aux"] == (sum(L["sbd"]), Np * nsb * 64)
+        assert L["flag"][0] == sum(L["aux"])
+        assert all(off % 16 == 0 for off, _ in L.values())
+        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["flag"])
 
 
 @pytest.mark.parametrize("M,K,err", [(0, 256, 2), (1, 255, 2), (1, 0, 2), (5, 300, 2), (1 << 23, 256, 2)])

@@ -15,7 +15,7 @@ import torch
 import oracle
 import synth
 import quant_int8_mmq_gb300 as mmq
-from tests.planes import padded, untile_codes, untile_pairs
+from tests.planes import is_tf32, padded, untile_codes, untile_pairs, untile_rows, untile_tf32_pair
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -84,12 +84,24 @@ def _check_prepass(x, ldx=None):
     _sync()
     q, d, s = oracle.quantize_act(x)
     Mp = padded(M)
+    scb = sc.cpu().numpy()
+    lay = mmq.mmq_act_scale_layout(M, K)
     codes = untile_codes(qa.cpu().numpy(), Mp, K)
-    dd, ss = untile_pairs(sc.cpu().numpy(), Mp, K // 32, np.float32, np.int32)
+    po, pb = lay["pairs"]
+    dd, ss = untile_pairs(scb[po:po + pb], Mp, K // 32, np.float32, np.int32)
     assert np.array_equal(codes[:M], q.astype(np.int64))
     assert np.array_equal(dd[:M].view(np.uint32), d.view(np.uint32))
     assert np.array_equal(ss[:M], s)
     assert not codes[M:].any() and not dd[M:].view(np.uint32).any() and not ss[M:].any()
+    # min-term operand: tf32 hi + lo of the f32 product d * ssum
+    ao, ab = lay["am"]
+    hi, lo = untile_tf32_pair(scb[ao:ao + ab], Mp, K // 256)
+    assert is_tf32(hi) and is_tf32(lo)
+    ma = (d * s.astype(np.float32)).astype(np.float64)
+    err = np.abs(hi[:M].astype(np.float64) + lo[:M].astype(np.float64) - ma)
+    assert np.all(err <= np.abs(ma) * 2.0 ** -21)
+    assert np.all(np.abs(lo[:M]) <= np.abs(hi[:M]) * 2.0 ** -10 + 1e-38)
+    assert not hi[M:].any() and not lo[M:].any()
 
 
 @pytest.mark.parametrize("M,K,seed", [(16, 512, 0), (512, 4096, 1), (130, 768, 5), (1, 256, 6), (2047, 1024, 7)])
@@ -112,50 +124,98 @@ def test_prepass_row_stride_and_special_values():
 
 
 # --------------------------------------------------------------------------- pack
-@pytest.mark.parametrize("typ", ["q6_K", "q4_K"])
+def _q6_raw(od, id_, seed, full_range):
+    lo, hi = (-128, 127) if full_range else (-32, 31)
+    return synth.q6k_blocks(od, id_, seed, sc_lo=lo, sc_hi=hi)
+
+
+@pytest.mark.parametrize("typ", ["q6_K", "q6_K_full", "q4_K"])
 @pytest.mark.parametrize("od,id_", [(64, 512), (4097, 1024), (3, 256), (130, 768)])
 def test_pack_planes_byte_exact(typ, od, id_):
-    raw = _raw(typ, od, id_, seed=od + id_)
-    if typ == "q6_K":
-        raw = synth.q6k_blocks(od, id_, od + id_, sc_lo=-128, sc_hi=127)   # full int8 scale range
-    packed = gpu_pack(typ, raw)
+    seed = od + id_
+    if typ.startswith("q6_K"):
+        raw = _q6_raw(od, id_, seed, typ == "q6_K_full")
+        t = "q6_K"
+    else:
+        raw = synth.q4k_blocks(od, id_, seed)
+        t = typ
+    packed = gpu_pack(t, raw)
     _sync()
     pk = packed.cpu().numpy()
-    tid = mmq.TYPES[typ]
-    code_off, code_bytes, scale_off, scale_bytes = mmq.mmq_packed_weight_layout(tid, od, id_)
-    assert pk.size == code_bytes + scale_bytes
-    Np = padded(od)
-    codes = untile_codes(pk[code_off:code_off + code_bytes], Np, id_)
-    a, b = untile_pairs(pk[scale_off:scale_off + scale_bytes], Np, id_ // 32, np.float32, np.float32)
-    if typ == "q6_K":
-        want = oracle.codes_q6k(raw).astype(np.int64)
+    tid = mmq.TYPES[t]
+    L = mmq.mmq_packed_weight_layout(tid, od, id_)
+    assert pk.size == sum(L["flag"])
+    Np, nsb, nchunk = padded(od), id_ // 256, id_ // 32
+    part = {k: pk[o:o + n] for k, (o, n) in L.items()}
+    codes = untile_codes(part["codes"], Np, id_)
+    a, b = untile_pairs(part["pairs"], Np, nchunk, np.float32, np.float32)
+    sbd = untile_rows(part["sbd"], Np, nsb)
+    if t == "q6_K":
+        d, sc = oracle.fields_q6k(raw)
+        q = oracle.codes_q6k(raw).astype(np.int64)
+        scale_e = np.repeat(sc.reshape(od, -1).astype(np.int64), 16, axis=1)     # scales[e/16]
+        maxsc = int(np.abs(sc.astype(np.int64)).max())
+        folded = maxsc <= 64
+        flag = part["flag"].view(np.uint32)
+        assert flag[0] == int(folded) and flag[1] == maxsc
+        assert folded == (typ == "q6_K")
+        want_codes = q * scale_e if folded else q
         dsc = oracle.scale_planes_q6k(raw)
         wa, wb = dsc[..., 0], dsc[..., 1]
+        # sub-block scales as f32, [row tile][sb][16][128]
+        aux = np.ascontiguousarray(part["aux"]).view(np.float32).reshape(Np // 128, nsb, 16, 128)
+        aux = aux.transpose(0, 3, 1, 2).reshape(Np, nsb, 16)
+        assert np.array_equal(aux[:od], sc.astype(np.float32)) and not aux[od:].any()
     else:
-        want = oracle.codes_q4k(raw).astype(np.int64)
+        d, dmin, sc, m = oracle.fields_q4k(raw)
+        q = oracle.codes_q4k(raw).astype(np.int64)
+        want_codes = q * np.repeat(sc.reshape(od, -1).astype(np.int64), 32, axis=1)   # sc_c * q
         wa, wb = oracle.scale_planes_q4k(raw)
-    assert np.array_equal(codes[:od], want)
+        hi, lo = untile_tf32_pair(part["aux"], Np, nsb)
+        assert is_tf32(hi) and is_tf32(lo)
+        # hi + lo reproduces dmn = dmin * m_c exactly (f64 sum of two tf32 values)
+        assert np.array_equal(hi[:od].astype(np.float64) + lo[:od].astype(np.float64), wb.astype(np.float64))
+        assert not hi[od:].any() and not lo[od:].any()
+    assert np.array_equal(codes[:od], want_codes)
     assert np.array_equal(a[:od].view(np.uint32), wa.view(np.uint32))
     assert np.array_equal(b[:od].view(np.uint32), wb.view(np.uint32))
+    assert np.array_equal(sbd[:od].view(np.uint32), d.view(np.uint32))
     assert not codes[od:].any() and not a[od:].view(np.uint32).any() and not b[od:].view(np.uint32).any()
+    assert not sbd[od:].view(np.uint32).any()
 
 
 # --------------------------------------------------------------------------- dots
-@pytest.mark.parametrize("typ", ["q6_K", "q4_K"])
+@pytest.mark.parametrize("typ", ["q6_K", "q6_K_full", "q4_K"])
 @pytest.mark.parametrize("M,od,id_", [(200, 300, 768), (1, 129, 256), (130, 64, 512), (257, 131, 2048)])
 def test_gemm_dots_bit_exact(typ, M, od, id_):
-    kw = dict(sc_lo=-128, sc_hi=127) if typ == "q6_K" else {}
-    raw = _raw(typ, od, id_, seed=3 * od + M, **kw)
+    seed = 3 * od + M
+    t = "q6_K" if typ.startswith("q6_K") else "q4_K"
+    raw = _q6_raw(od, id_, seed, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, seed)
     x = synth.activations(M, id_, seed=M + 17)
     qa, sc = gpu_quantize(x)
-    packed = gpu_pack(typ, raw)
-    dots = mmq.gemm_dots(typ, packed, od, id_, qa, sc, M)
+    packed = gpu_pack(t, raw)
+    dots = mmq.gemm_dots(t, packed, od, id_, qa, sc, M)
     _sync()
     assert "tcgen05" in mmq.mmq_last_path()
     q, _, _ = oracle.quantize_act(x)
-    ref = oracle.dots_q6k(raw, q) if typ == "q6_K" else oracle.dots_q4k(raw, q)
     got = dots.cpu().numpy().astype(np.float64)
-    assert np.array_equal(got, ref.astype(np.float64))
+    nchunk = id_ // 32
+    if t == "q4_K":
+        I = oracle.dots_q4k(raw, q).astype(np.int64)                       # [M, od, nchunk]
+        _, _, scf, _ = oracle.fields_q4k(raw)
+        want = I * scf.reshape(od, nchunk).astype(np.int64)[None]
+        got = got[: M * od * nchunk].reshape(M, od, nchunk)
+    else:
+        I = oracle.dots_q6k(raw, q).astype(np.int64)                       # [M, od, 2*nchunk]
+        _, scf = oracle.fields_q6k(raw)
+        if typ == "q6_K":                                                  # folded: sc0*I0 + sc1*I1
+            s16 = scf.reshape(od, 2 * nchunk).astype(np.int64)[None]
+            want = (I * s16).reshape(M, od, nchunk, 2).sum(-1)
+            got = got[: M * od * nchunk].reshape(M, od, nchunk)
+        else:                                                              # plain codes: per sub-block
+            want = I
+            got = got.reshape(M, od, 2 * nchunk)
+    assert np.array_equal(got, want.astype(np.float64))
 
 
 # --------------------------------------------------------------------------- Y

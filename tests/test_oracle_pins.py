@@ -392,3 +392,25 @@ def test_whole_matrix_codes_match_encoder(oracle_lib):
             want4[j, 256 * b: 256 * b + 256] = q
     assert np.array_equal(oracle.codes_q6k(raw6), want6)
     assert np.array_equal(oracle.codes_q4k(raw4), want4)
+
+
+def test_block_fields_match_encoder(oracle_lib):
+    rng = np.random.default_rng(91)
+    raw6 = np.zeros((3, 2, 210), np.uint8)
+    raw4 = np.zeros((3, 2, 144), np.uint8)
+    want6, want4 = [], []
+    for j in range(3):
+        for b in range(2):
+            d, sc, q = random_q6k_fields(rng, (-128, 127))
+            raw6[j, b] = encode_q6k(f16_bits(d), sc, q)
+            want6.append((np.float32(np.float16(d)), sc))
+            d, dmin, sc, m, q = random_q4k_fields(rng)
+            raw4[j, b] = encode_q4k(f16_bits(d), f16_bits(dmin), sc, m, q)
+            want4.append((np.float32(np.float16(d)), np.float32(np.float16(dmin)), sc, m))
+    d6, sc6 = oracle.fields_q6k(raw6)
+    d4, dm4, sc4, m4 = oracle.fields_q4k(raw4)
+    for i, (d, sc) in enumerate(want6):
+        assert d6.reshape(-1)[i] == d and np.array_equal(sc6.reshape(-1, 16)[i], sc)
+    for i, (d, dmin, sc, m) in enumerate(want4):
+        assert d4.reshape(-1)[i] == d and dm4.reshape(-1)[i] == dmin
+        assert np.array_equal(sc4.reshape(-1, 8)[i], sc) and np.array_equal(m4.reshape(-1, 8)[i], m)
