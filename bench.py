@@ -234,16 +234,15 @@ def host_acts(tokens):
 
 
 def cpu_sample_run(raws, xh, xf, seconds, threads):
-    # calibrate on a few tokens (per-GEMM thread start-up dominates a 1-token pass)
-    n0 = 4
-    t0 = time.perf_counter()
-    oracle_stack_tokens(raws, xh, xf, n0, threads)
-    per_tok = (time.perf_counter() - t0) / n0
-    n = max(1, min(xh.shape[0], int(seconds / max(per_tok, 1e-6))))
-    t0 = time.perf_counter()
-    oracle_stack_tokens(raws, xh, xf, n, threads)
-    dt = time.perf_counter() - t0
-    return n / dt, n, dt
+    """Time the oracle on the first n tokens, growing n until one pass takes about `seconds`."""
+    n = 4
+    while True:
+        t0 = time.perf_counter()
+        oracle_stack_tokens(raws, xh, xf, n, threads)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * seconds or n >= xh.shape[0]:
+            return n / dt, n, dt
+        n = min(xh.shape[0], max(n + 1, int(n * seconds / max(dt, 1e-3))))
 
 
 # ----------------------------------------------------------------------------- reference arm

@@ -13,18 +13,25 @@
 // chunks (K = id/32); it runs on the tensor cores in tf32 with both operands split
 // hi + lo (hi*hi + hi*lo + lo*hi, relative error ~2^-21 per product).
 //
-// One CTA per SM, persistent over 128-token x 128-row tiles; 18 warps:
+// One CTA per SM, persistent over 128-token x 128-row tiles; 10 warps:
 //   warp 0      producer: cp.async.bulk copies (no multicast) of the pre-swizzled
 //               f16 operand tiles into a STAGES-deep ring, token scale pairs into an
 //               SSTAGES ring, and per-super-block data (d, min-term operands, q6_K
 //               sub-block scales) into an SBR ring; completion on mbarriers.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 (f16-held
-//               integer codes, f32 accumulate) into rotating per-chunk TMEM slots,
-//               and (q4_K) kind::tf32 into a per-tile min-term accumulator.
-//   warps 2-17  promotion: tcgen05.ld of a finished chunk slot, release it,
-//               inner += d_a * I'; per super-block acc += d * inner; at tile end
-//               (q4_K) acc -= min term; store Y.  Each warp owns one TMEM lane
-//               quarter (warp % 4) and 32 of the 128 columns.
+//               integer codes, f32 accumulate) into four rotating 128-column chunk
+//               slots (plain-code q6_K: two 256-column slots) and, for q4_K after each
+//               super-block, three kind::tf32 MMAs of the min term into the next slot.
+//   warps 2-9   promotion: tcgen05.ld of a finished slot (64 columns per thread),
+//               release it, inner += d_a * I' (packed f32x2 FMAs); per super-block
+//               acc += d * inner (- the min-term slot for q4_K), with acc kept in
+//               shared memory; store Y per tile.  Each warp owns one TMEM lane
+//               quarter (warp % 4) and 64 of the 128 columns.
+// Per-chunk scaling forces one TMEM round trip per 32-value chunk, and TMEM holds
+// at most four 128-column chunks; the design keeps that round trip short: slot and
+// stage positions advance without division, slot counts are compile-time, the
+// issuing thread does nothing else, and the promotion spends one packed FMA per two
+// outputs per chunk.
 // The multi-stage rings replace the pages' one-deep double buffer and group-count
 // waits ("r45 ...", §2.2; "r58 ...", §2.2 and §6 lesson 2: one tile of lookahead
 // cannot cover the global-to-shared latency); registration-time planes remove the
@@ -48,16 +55,15 @@ namespace {
 constexpr int BM = 128;             // tokens per tile (TMEM lanes)
 constexpr int BN = 128;             // weight rows per tile (MMA N)
 constexpr int BK = TILE_K;          // values per stage: two 32-value chunks
-constexpr int STAGES = 5;           // operand ring depth
+constexpr int STAGES = 3;           // operand ring depth
 constexpr int SSTAGES = 8;          // token-scale ring depth (entries of one stage)
 constexpr int SBR = 2;              // super-block ring depth
-constexpr int NUM_WARPS = 18;
+constexpr int NUM_WARPS = 10;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int PROMO_WARP0 = 2;
-constexpr int NUM_PROMO_WARPS = 16;
-constexpr int COLS_PER_WARP = BN / 4;   // 32
+constexpr int NUM_PROMO_WARPS = 8;
+constexpr int COLS_PER_WARP = BN / 2;   // 64
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t MIN_COL = 384;   // q4_K min-term accumulator columns [384, 512)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 constexpr int SCALE_STAGE_BYTES = 2 * BM * 8;      // {d, ssum} for two chunks x 128 tokens
@@ -67,12 +73,14 @@ constexpr int SB_BM_BYTES = 2 * TF32_TILE_BYTES;   // q4_K: weight min-term oper
 constexpr int SB_SC_BYTES = 16 * BN * 4;           // q6_K: sub-block scales
 constexpr int SB_BYTES = SB_AM_BYTES + SB_BM_BYTES + SB_SBD_BYTES;
 static_assert(SB_BYTES >= SB_SBD_BYTES + SB_SC_BYTES, "super-block entry");
+constexpr int ACC_BYTES = BM * BN * 4;             // f32 tile accumulator (shared memory)
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * TILE_BYTES;
 constexpr int SMEM_AS = SMEM_B + STAGES * TILE_BYTES;
 constexpr int SMEM_SB = SMEM_AS + SSTAGES * SCALE_STAGE_BYTES;
-constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
+constexpr int SMEM_ACC = SMEM_SB + SBR * SB_BYTES;
+constexpr int SMEM_BAR = SMEM_ACC + ACC_BYTES;
 constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = BAR_FULL + STAGES;
 constexpr int BAR_SFULL = BAR_EMPTY + STAGES;
@@ -81,15 +89,15 @@ constexpr int BAR_SBFULL = BAR_SEMPTY + SSTAGES;
 constexpr int BAR_SBEMPTY = BAR_SBFULL + SBR;
 constexpr int BAR_TFULL = BAR_SBEMPTY + SBR;
 constexpr int BAR_TEMPTY = BAR_TFULL + 4;
-constexpr int BAR_MINFULL = BAR_TEMPTY + 4;
-constexpr int BAR_MINEMPTY = BAR_MINFULL + 1;
-constexpr int BAR_DRAIN = BAR_MINEMPTY + 1;
+constexpr int BAR_DRAIN = BAR_TEMPTY + 4;
 constexpr int NUM_BARS = BAR_DRAIN + 1;
 constexpr int SMEM_TMEMPTR = SMEM_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_TMEMPTR + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;    // slack for 1024-byte alignment
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-static_assert(SMEM_B % 1024 == 0 && SMEM_AS % 16 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0, "alignment");
+static_assert(SMEM_B % 1024 == 0 && SMEM_AS % 16 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 &&
+                  SMEM_ACC % 16 == 0 && SMEM_BAR % 8 == 0,
+              "alignment");
 
 struct GemmArgs {
     const uint8_t* A;     // activation code tiles      [num_m][nkb][16 KiB]
@@ -149,68 +157,43 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
-// TYPE 12 = q4_K, 14 = q6_K; MODE GEMM_Y or GEMM_DOTS (raw per-chunk dots).
-template <int TYPE, int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
+// Position in a ring of N entries: entry index and the phase parity of its barriers.
+template <uint32_t N>
+struct RingPos {
+    uint32_t i = 0, ph = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++i == N) {
+            i = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// The three roles of one CTA.  TYPE 12 = q4_K, 14 = q6_K; MODE GEMM_Y or GEMM_DOTS;
+// FOLDED = the codes carry the integer sub-block scale (one accumulator per chunk).
+template <int TYPE, int MODE, bool FOLDED>
+__device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
+                                           int warp, int lane)
 {
     constexpr bool Q4 = (TYPE == 12);
-
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
-    uint8_t* smem = smem_raw + pad;
-    const uint32_t sbase = raw_addr + pad;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    constexpr uint32_t NSLOT = FOLDED ? 4u : 2u;             // TMEM chunk slots
+    constexpr uint32_t SLOT_COLS = FOLDED ? BN : 2 * BN;     // plain q6_K codes: two sub-block accumulators
     const int nkb = g.id / BK;
     const int nchunk = g.id / CHUNK;
     const int nsb = g.id / QK_K;
     const int num_tiles = g.num_m * g.num_n;
-    // q6_K codes hold sc*q (one accumulator per chunk) unless some |sc| > 64.
-    const bool folded = Q4 || (__ldg(g.FLAG) != 0u);
-    const uint32_t nslot = Q4 ? 3u : (folded ? 4u : 2u);       // TMEM chunk slots
-    const uint32_t slot_cols = (Q4 || folded) ? BN : 2 * BN;
     auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(BAR_FULL + s), 1);
-            mbar_init(bar(BAR_EMPTY + s), 1);
-        }
-        for (int s = 0; s < SSTAGES; ++s) {
-            mbar_init(bar(BAR_SFULL + s), 1);
-            mbar_init(bar(BAR_SEMPTY + s), NUM_PROMO_WARPS);
-        }
-        for (int s = 0; s < SBR; ++s) {
-            mbar_init(bar(BAR_SBFULL + s), 1);
-            mbar_init(bar(BAR_SBEMPTY + s), NUM_PROMO_WARPS + (Q4 ? 1 : 0));
-        }
-        for (int k = 0; k < 4; ++k) {
-            mbar_init(bar(BAR_TFULL + k), 1);
-            mbar_init(bar(BAR_TEMPTY + k), NUM_PROMO_WARPS);
-        }
-        mbar_init(bar(BAR_MINFULL), 1);
-        mbar_init(bar(BAR_MINEMPTY), NUM_PROMO_WARPS);
-        mbar_init(bar(BAR_DRAIN), 1);
-        fence_barrier_init();
-        fence_proxy_async_smem();
-    }
-    if (warp == 1) {
-        tmem_alloc(sbase + SMEM_TMEMPTR, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + SMEM_TMEMPTR);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            RingPos<STAGES> op;
+            RingPos<SSTAGES> sc;
+            RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sc = 0, n_sb = 0;  // fills issued on each ring
-            const uint32_t sb_tx = Q4 ? (SB_AM_BYTES + SB_BM_BYTES + SB_SBD_BYTES)
-                                      : (SB_SBD_BYTES + (folded ? 0 : SB_SC_BYTES));
+            constexpr uint32_t sb_tx = Q4 ? (SB_AM_BYTES + SB_BM_BYTES + SB_SBD_BYTES)
+                                          : (SB_SBD_BYTES + (FOLDED ? 0 : SB_SC_BYTES));
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int m = tile % g.num_m, n = tile / g.num_m;
@@ -219,52 +202,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
                 const uint8_t* ASb = g.AS + static_cast<size_t>(m) * nchunk * BM * 8;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if ((kb & 3) == 0) {  // a new super-block
-                        const int sb = kb >> 2;
-                        const uint32_t e = n_sb % SBR;
-                        if (!mbar_wait(bar(BAR_SBEMPTY + e), ((n_sb / SBR) & 1u) ^ 1u, WAIT_LIMIT_NS)) {
+                        const int s = kb >> 2;
+                        if (!mbar_wait(bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u, WAIT_LIMIT_NS)) {
                             ok = false;
                             break;
                         }
                         // The promotion warps read this entry with ordinary loads before
                         // releasing it; order those reads before the bulk copy's writes.
                         fence_proxy_async_smem();
-                        const uint32_t dst = sbase + SMEM_SB + e * SB_BYTES;
-                        mbar_arrive_expect_tx(bar(BAR_SBFULL + e), sb_tx);
-                        bulk_g2s(dst, g.SBD + (static_cast<size_t>(n) * nsb + sb) * SB_SBD_BYTES, SB_SBD_BYTES,
-                                 bar(BAR_SBFULL + e));
+                        const uint32_t dst = sbase + SMEM_SB + sb.i * SB_BYTES;
+                        const uint32_t fb = bar(BAR_SBFULL + sb.i);
+                        mbar_arrive_expect_tx(fb, sb_tx);
+                        bulk_g2s(dst, g.SBD + (static_cast<size_t>(n) * nsb + s) * SB_SBD_BYTES, SB_SBD_BYTES, fb);
                         if (Q4) {
-                            bulk_g2s(dst + SB_SBD_BYTES, g.AM + (static_cast<size_t>(m) * nsb + sb) * SB_AM_BYTES,
-                                     SB_AM_BYTES, bar(BAR_SBFULL + e));
+                            bulk_g2s(dst + SB_SBD_BYTES, g.AM + (static_cast<size_t>(m) * nsb + s) * SB_AM_BYTES,
+                                     SB_AM_BYTES, fb);
                             bulk_g2s(dst + SB_SBD_BYTES + SB_AM_BYTES,
-                                     g.AUX + (static_cast<size_t>(n) * nsb + sb) * SB_BM_BYTES, SB_BM_BYTES,
-                                     bar(BAR_SBFULL + e));
-                        } else if (!folded) {
-                            bulk_g2s(dst + SB_SBD_BYTES, g.AUX + (static_cast<size_t>(n) * nsb + sb) * SB_SC_BYTES,
-                                     SB_SC_BYTES, bar(BAR_SBFULL + e));
+                                     g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_BM_BYTES, SB_BM_BYTES, fb);
+                        } else if (!FOLDED) {
+                            bulk_g2s(dst + SB_SBD_BYTES, g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_SC_BYTES,
+                                     SB_SC_BYTES, fb);
                         }
+                        sb.next();
                         ++n_sb;
                     }
-                    const uint32_t s = n_ops % STAGES;
-                    if (!mbar_wait(bar(BAR_EMPTY + s), ((n_ops / STAGES) & 1u) ^ 1u, WAIT_LIMIT_NS)) {
+                    if (!mbar_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(BAR_FULL + s), 2 * TILE_BYTES);
-                    bulk_g2s(sbase + SMEM_A + s * TILE_BYTES, Ab + static_cast<size_t>(kb) * TILE_BYTES,
-                             TILE_BYTES, bar(BAR_FULL + s));
-                    bulk_g2s(sbase + SMEM_B + s * TILE_BYTES, Bb + static_cast<size_t>(kb) * TILE_BYTES,
-                             TILE_BYTES, bar(BAR_FULL + s));
+                    const uint32_t fo = bar(BAR_FULL + op.i);
+                    mbar_arrive_expect_tx(fo, 2 * TILE_BYTES);
+                    bulk_g2s(sbase + SMEM_A + op.i * TILE_BYTES, Ab + static_cast<size_t>(kb) * TILE_BYTES,
+                             TILE_BYTES, fo);
+                    bulk_g2s(sbase + SMEM_B + op.i * TILE_BYTES, Bb + static_cast<size_t>(kb) * TILE_BYTES,
+                             TILE_BYTES, fo);
+                    op.next();
                     ++n_ops;
-                    const uint32_t ss = n_sc % SSTAGES;
-                    if (!mbar_wait(bar(BAR_SEMPTY + ss), ((n_sc / SSTAGES) & 1u) ^ 1u, WAIT_LIMIT_NS)) {
+                    if (!mbar_wait(bar(BAR_SEMPTY + sc.i), sc.ph ^ 1u, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
                     }
                     fence_proxy_async_smem();  // same ordering for the token-scale ring
-                    mbar_arrive_expect_tx(bar(BAR_SFULL + ss), SCALE_STAGE_BYTES);
-                    bulk_g2s(sbase + SMEM_AS + ss * SCALE_STAGE_BYTES,
-                             ASb + static_cast<size_t>(kb) * SCALE_STAGE_BYTES, SCALE_STAGE_BYTES,
-                             bar(BAR_SFULL + ss));
+                    const uint32_t fs = bar(BAR_SFULL + sc.i);
+                    mbar_arrive_expect_tx(fs, SCALE_STAGE_BYTES);
+                    bulk_g2s(sbase + SMEM_AS + sc.i * SCALE_STAGE_BYTES,
+                             ASb + static_cast<size_t>(kb) * SCALE_STAGE_BYTES, SCALE_STAGE_BYTES, fs);
+                    sc.next();
                     ++n_sc;
                 }
             }
@@ -281,70 +264,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_t = idesc_tf32_f32(BM, BN);
-            uint32_t it = 0, ch = 0, n_sb = 0, tiles = 0;
+            RingPos<STAGES> op;
+            RingPos<NSLOT> slot;
+            RingPos<SBR> sb;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb) {
-                    const uint32_t s = it % STAGES;
-                    if (!mbar_wait(bar(BAR_FULL + s), (it / STAGES) & 1u, WAIT_LIMIT_NS)) {
+                    if (!mbar_wait(bar(BAR_FULL + op.i), op.ph, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a0 = sdesc_k_sw128(sbase + SMEM_A + s * TILE_BYTES);
-                    const uint64_t b0 = sdesc_k_sw128(sbase + SMEM_B + s * TILE_BYTES);
+                    const uint64_t a0 = sdesc_k_sw128(sbase + SMEM_A + op.i * TILE_BYTES);
+                    const uint64_t b0 = sdesc_k_sw128(sbase + SMEM_B + op.i * TILE_BYTES);
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
-                        const uint32_t slot = ch % nslot;
-                        if (!mbar_wait(bar(BAR_TEMPTY + slot), ((ch / nslot) & 1u) ^ 1u, WAIT_LIMIT_NS)) {
+                        if (!mbar_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u, WAIT_LIMIT_NS)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d = tmem_base + slot * slot_cols;
+                        const uint32_t d = tmem_base + slot.i * SLOT_COLS;
                         // K advance inside the 128-byte swizzled rows: 32 bytes per 16 values
                         // (the descriptor's address field counts 16-byte units).
                         const uint64_t ak = a0 + static_cast<uint64_t>(4 * cc);
                         const uint64_t bk = b0 + static_cast<uint64_t>(4 * cc);
                         umma_f16(d, ak, bk, idesc, 0u);
-                        if (folded)
+                        if (FOLDED)
                             umma_f16(d, ak + 2, bk + 2, idesc, 1u);
                         else
                             umma_f16(d + BN, ak + 2, bk + 2, idesc, 0u);
-                        umma_commit(bar(BAR_TFULL + slot));
-                        ++ch;
+                        umma_commit(bar(BAR_TFULL + slot.i));
+                        slot.next();
                     }
                     if (!ok)
                         break;
-                    umma_commit(bar(BAR_EMPTY + s));  // operand stage free once these MMAs finish
-                    ++it;
+                    umma_commit(bar(BAR_EMPTY + op.i));  // operand stage free once these MMAs finish
+                    op.next();
                     if (Q4 && (kb & 3) == 3) {
-                        // min-term contraction of this super-block: 8 chunks, hi/lo split
-                        const uint32_t e = n_sb % SBR;
-                        if (!mbar_wait(bar(BAR_SBFULL + e), (n_sb / SBR) & 1u, WAIT_LIMIT_NS)) {
-                            ok = false;
-                            break;
-                        }
-                        if (kb == 3 && !mbar_wait(bar(BAR_MINEMPTY), (tiles & 1u) ^ 1u, WAIT_LIMIT_NS)) {
+                        // Min-term contraction of this super-block (8 chunks, hi/lo split) into
+                        // the next chunk slot, consumed by the promotion like a chunk.
+                        if (!mbar_wait(bar(BAR_SBFULL + sb.i), sb.ph, WAIT_LIMIT_NS) ||
+                            !mbar_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u, WAIT_LIMIT_NS)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t am = sbase + SMEM_SB + e * SB_BYTES + SB_SBD_BYTES;
+                        const uint32_t am = sbase + SMEM_SB + sb.i * SB_BYTES + SB_SBD_BYTES;
                         const uint32_t bm = am + SB_AM_BYTES;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
-                        const uint32_t dmin_acc = tmem_base + MIN_COL;
-                        umma_tf32(dmin_acc, ahi, bhi, idesc_t, kb == 3 ? 0u : 1u);
-                        umma_tf32(dmin_acc, ahi, blo, idesc_t, 1u);
-                        umma_tf32(dmin_acc, alo, bhi, idesc_t, 1u);
-                        umma_commit(bar(BAR_SBEMPTY + e));
-                        ++n_sb;
+                        const uint32_t d = tmem_base + slot.i * SLOT_COLS;
+                        umma_tf32(d, ahi, bhi, idesc_t, 0u);
+                        umma_tf32(d, ahi, blo, idesc_t, 1u);
+                        umma_tf32(d, alo, bhi, idesc_t, 1u);
+                        umma_commit(bar(BAR_TFULL + slot.i));
+                        umma_commit(bar(BAR_SBEMPTY + sb.i));
+                        slot.next();
+                        sb.next();
                     }
                 }
-                if (ok && Q4)
-                    umma_commit(bar(BAR_MINFULL));
-                ++tiles;
             }
             umma_commit(bar(BAR_DRAIN));  // every MMA issued so far has completed
             drain_wait(bar(BAR_DRAIN), 0u);
@@ -352,75 +331,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ promotion
-        const int pw = warp - PROMO_WARP0;              // 0..15
+        const int pw = warp - PROMO_WARP0;              // 0..7
         const int q = warp & 3;                          // TMEM lane quarter this warp may read
-        const int cg = pw >> 2;                          // which 32 of the 128 columns
+        const int hc = pw >> 2;                          // which 64 of the 128 columns
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        uint32_t it = 0, ch = 0, n_sb = 0, tiles = 0;
+        // This thread's accumulator pairs in shared memory: pair i (columns 2i, 2i+1 of
+        // its 64) at accs[i * BM]; consecutive lanes hit consecutive 8-byte words.
+        float2* accs = reinterpret_cast<float2*>(smem + SMEM_ACC) + (hc * (COLS_PER_WARP / 2)) * BM + row_in_tile;
+        RingPos<SSTAGES> sc;
+        RingPos<NSLOT> slot;
+        RingPos<SBR> sb;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             const int m = tile % g.num_m, n = tile / g.num_m;
             const int row = m * BM + row_in_tile;
-            const int jb = n * BN + cg * COLS_PER_WARP;
-            float acc[COLS_PER_WARP], inner[COLS_PER_WARP];
+            const int jb = n * BN + hc * COLS_PER_WARP;
+            float2 inner[COLS_PER_WARP / 2];
 #pragma unroll
-            for (int i = 0; i < COLS_PER_WARP; ++i) {
-                acc[i] = 0.0f;
-                inner[i] = 0.0f;
-            }
+            for (int i = 0; i < COLS_PER_WARP / 2; ++i)
+                inner[i] = make_float2(0.0f, 0.0f);
             for (int kb = 0; kb < nkb; ++kb) {
-                const uint32_t e = n_sb % SBR;
-                const uint8_t* sbe = smem + SMEM_SB + e * SB_BYTES;
+                const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
                 if ((kb & 3) == 0) {
-                    if (!mbar_wait(bar(BAR_SBFULL + e), (n_sb / SBR) & 1u, WAIT_LIMIT_NS)) {
+                    if (!mbar_wait(bar(BAR_SBFULL + sb.i), sb.ph, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
                     }
 #pragma unroll
-                    for (int i = 0; i < COLS_PER_WARP; ++i)
-                        inner[i] = 0.0f;
+                    for (int i = 0; i < COLS_PER_WARP / 2; ++i)
+                        inner[i] = make_float2(0.0f, 0.0f);
                 }
-                const uint32_t ss = it % SSTAGES;
-                if (!mbar_wait(bar(BAR_SFULL + ss), (it / SSTAGES) & 1u, WAIT_LIMIT_NS)) {
+                if (!mbar_wait(bar(BAR_SFULL + sc.i), sc.ph, WAIT_LIMIT_NS)) {
                     ok = false;
                     break;
                 }
-                const uint2* tsc = reinterpret_cast<const uint2*>(smem + SMEM_AS + ss * SCALE_STAGE_BYTES);
+                const uint2* tsc = reinterpret_cast<const uint2*>(smem + SMEM_AS + sc.i * SCALE_STAGE_BYTES);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    const uint32_t slot = ch % nslot;
-                    if (!mbar_wait(bar(BAR_TFULL + slot), (ch / nslot) & 1u, WAIT_LIMIT_NS)) {
+                    if (!mbar_wait(bar(BAR_TFULL + slot.i), slot.ph, WAIT_LIMIT_NS)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const float da = __uint_as_float(tsc[cc * BM + row_in_tile].x);
+                    const float2 da2 = make_float2(da, da);
                     const int c = 2 * kb + cc;                  // chunk index along id
-                    const uint32_t col0 = lane_addr + slot * slot_cols + cg * COLS_PER_WARP;
-                    if (folded) {
-                        float I0[16], I1[16];
-                        tmem_ld16x2_wait(col0, col0 + 16, I0, I1);
+                    const uint32_t col0 = lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP;
+                    if (FOLDED) {
+                        float I[COLS_PER_WARP];
+                        tmem_ld64_wait(col0, I);
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
-                            mbar_arrive(bar(BAR_TEMPTY + slot));
+                            mbar_arrive(bar(BAR_TEMPTY + slot.i));
                         if (MODE == GEMM_DOTS) {
                             if (row < g.M) {
 #pragma unroll
                                 for (int i = 0; i < COLS_PER_WARP; ++i) {
                                     const int j = jb + i;
                                     if (j < g.od)
-                                        g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] =
-                                            i < 16 ? I0[i] : I1[i - 16];
+                                        g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] = I[i];
                                 }
                             }
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                inner[i] = fmaf(da, I0[i], inner[i]);
-                                inner[16 + i] = fmaf(da, I1[i], inner[16 + i]);
-                            }
+                            for (int i = 0; i < COLS_PER_WARP / 2; ++i)
+                                inner[i] = ffma2(da2, make_float2(I[2 * i], I[2 * i + 1]), inner[i]);
                         }
                     } else {
                         // q6_K with plain codes: one accumulator per 16-value sub-block,
@@ -428,14 +405,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
                         const float* scp = reinterpret_cast<const float*>(sbe + SB_SBD_BYTES);
                         const int s0 = 2 * (c & 7);
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) {
+                        for (int p = 0; p < COLS_PER_WARP / 8; ++p) {
                             float h0[8], h1[8];
                             tmem_ld8x2_wait(col0 + p * 8, col0 + BN + p * 8, h0, h1);
-                            if (p == 3) {
+                            if (p == COLS_PER_WARP / 8 - 1) {
                                 tc_fence_before();
                                 __syncwarp();
                                 if (lane == 0)
-                                    mbar_arrive(bar(BAR_TEMPTY + slot));
+                                    mbar_arrive(bar(BAR_TEMPTY + slot.i));
                             }
                             if (MODE == GEMM_DOTS) {
                                 if (row < g.M) {
@@ -451,77 +428,144 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
                                 }
                             } else {
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const int col = cg * COLS_PER_WARP + p * 8 + i;
-                                    const float u = fmaf(h1[i], scp[(s0 + 1) * BN + col], h0[i] * scp[s0 * BN + col]);
-                                    inner[p * 8 + i] = fmaf(da, u, inner[p * 8 + i]);
+                                for (int i = 0; i < 8; i += 2) {
+                                    const int col = hc * COLS_PER_WARP + p * 8 + i;
+                                    const float u0 = fmaf(h1[i], scp[(s0 + 1) * BN + col], h0[i] * scp[s0 * BN + col]);
+                                    const float u1 =
+                                        fmaf(h1[i + 1], scp[(s0 + 1) * BN + col + 1], h0[i + 1] * scp[s0 * BN + col + 1]);
+                                    inner[p * 4 + i / 2] = ffma2(da2, make_float2(u0, u1), inner[p * 4 + i / 2]);
                                 }
                             }
                         }
                     }
-                    ++ch;
+                    slot.next();
                 }
                 if (!ok)
                     break;
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(BAR_SEMPTY + ss));
-                ++it;
+                    mbar_arrive(bar(BAR_SEMPTY + sc.i));
+                sc.next();
                 if ((kb & 3) == 3) {
-                    // acc += d * inner  (d per weight row of this super-block)
-                    const float4* d4 = reinterpret_cast<const float4*>(sbe) + cg * (COLS_PER_WARP / 4);
+                    // acc += d * inner  (d per weight row of this super-block); q4_K also
+                    // subtracts the super-block's min term, delivered through the next slot.
+                    const float4* d4 = reinterpret_cast<const float4*>(sbe) + hc * (COLS_PER_WARP / 4);
+                    const bool first = (kb == 3);
+                    if (Q4) {
+                        if (!mbar_wait(bar(BAR_TFULL + slot.i), slot.ph, WAIT_LIMIT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        float mn[COLS_PER_WARP];
+                        tmem_ld64_wait(lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP, mn);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar(BAR_TEMPTY + slot.i));
+                        slot.next();
+                        if (MODE == GEMM_Y) {
 #pragma unroll
-                    for (int i = 0; i < COLS_PER_WARP; i += 4) {
-                        const float4 dv = d4[i / 4];
-                        acc[i] = fmaf(dv.x, inner[i], acc[i]);
-                        acc[i + 1] = fmaf(dv.y, inner[i + 1], acc[i + 1]);
-                        acc[i + 2] = fmaf(dv.z, inner[i + 2], acc[i + 2]);
-                        acc[i + 3] = fmaf(dv.w, inner[i + 3], acc[i + 3]);
+                            for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
+                                const float4 dv = d4[i];
+                                float2 a0 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i) * BM];
+                                float2 a1 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i + 1) * BM];
+                                a0 = ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i], mn[4 * i + 1]), a0);
+                                a1 = ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i + 2], mn[4 * i + 3]), a1);
+                                accs[(2 * i) * BM] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
+                                accs[(2 * i + 1) * BM] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
+                            }
+                        }
+                    } else if (MODE == GEMM_Y) {
+#pragma unroll
+                        for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
+                            const float4 dv = d4[i];
+                            const float2 a0 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i) * BM];
+                            const float2 a1 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i + 1) * BM];
+                            accs[(2 * i) * BM] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
+                            accs[(2 * i + 1) * BM] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
+                        }
                     }
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(bar(BAR_SBEMPTY + e));
-                    ++n_sb;
+                        mbar_arrive(bar(BAR_SBEMPTY + sb.i));
+                    sb.next();
                 }
             }
             if (!ok)
                 break;
-            if (Q4) {
-                if (!mbar_wait(bar(BAR_MINFULL), tiles & 1u, WAIT_LIMIT_NS)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float m0[16], m1[16];
-                const uint32_t mc = lane_addr + MIN_COL + cg * COLS_PER_WARP;
-                tmem_ld16x2_wait(mc, mc + 16, m0, m1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(BAR_MINEMPTY));
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    acc[i] -= m0[i];
-                    acc[16 + i] -= m1[i];
-                }
-            }
-            ++tiles;
             if (MODE == GEMM_Y && row < g.M) {
                 float* yrow = g.out + static_cast<size_t>(row) * g.ldy;
 #pragma unroll
                 for (int i = 0; i < COLS_PER_WARP; i += 4) {
                     const int j = jb + i;
+                    const float2 lo = accs[(i / 2) * BM], hi = accs[(i / 2 + 1) * BM];
                     if (g.vec_store && j + 3 < g.od) {
-                        *reinterpret_cast<float4*>(yrow + j) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                        *reinterpret_cast<float4*>(yrow + j) = make_float4(lo.x, lo.y, hi.x, hi.y);
                     } else {
+                        const float v[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             if (j + k < g.od)
-                                yrow[j + k] = acc[i + k];
+                                yrow[j + k] = v[k];
                     }
                 }
             }
         }
+    }
+}
+
+template <int TYPE, int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(BAR_FULL + s), 1);
+            mbar_init(bar(BAR_EMPTY + s), 1);
+        }
+        for (int s = 0; s < SSTAGES; ++s) {
+            mbar_init(bar(BAR_SFULL + s), 1);
+            mbar_init(bar(BAR_SEMPTY + s), NUM_PROMO_WARPS);
+        }
+        for (int s = 0; s < SBR; ++s) {
+            mbar_init(bar(BAR_SBFULL + s), 1);
+            mbar_init(bar(BAR_SBEMPTY + s), NUM_PROMO_WARPS + (TYPE == 12 ? 1 : 0));
+        }
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(bar(BAR_TFULL + k), 1);
+            mbar_init(bar(BAR_TEMPTY + k), NUM_PROMO_WARPS);
+        }
+        mbar_init(bar(BAR_DRAIN), 1);
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + SMEM_TMEMPTR, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + SMEM_TMEMPTR);
+
+    if constexpr (TYPE == 14) {
+        // q6_K codes hold sc*q (one accumulator per chunk) unless some |sc| > 64;
+        // the repack recorded which in the flag word (uniform for the launch).
+        if (__ldg(g.FLAG) != 0u)
+            gemm_roles<14, MODE, true>(g, smem, sbase, tmem_base, warp, lane);
+        else
+            gemm_roles<14, MODE, false>(g, smem, sbase, tmem_base, warp, lane);
+    } else {
+        gemm_roles<12, MODE, true>(g, smem, sbase, tmem_base, warp, lane);
     }
 
     tc_fence_before();
@@ -589,15 +633,15 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
 
     if (type == 14) {
         if (path_label)
-            *path_label = "q6_K: persistent tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes "
+            *path_label = "q6_K: persistent tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes, 4 TMEM chunk slots "
                           "(plain codes + per-sub-block slots when |sc| > 64), cp.async.bulk rings, "
                           "f32 d_a per chunk / d per super-block";
         return mode == GEMM_Y ? launch_typed<14, GEMM_Y>(a, grid, s) : launch_typed<14, GEMM_DOTS>(a, grid, s);
     }
     if (path_label)
         *path_label = "q4_K: persistent tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes, "
-                      "tf32 hi/lo min-term side contraction in TMEM, cp.async.bulk rings, "
-                      "f32 d_a per chunk / d per super-block";
+                      "4 TMEM chunk slots, tf32 hi/lo min-term contraction per super-block through the slots, "
+                      "cp.async.bulk rings, f32 d_a per chunk / d per super-block";
     return mode == GEMM_Y ? launch_typed<12, GEMM_Y>(a, grid, s) : launch_typed<12, GEMM_DOTS>(a, grid, s);
 }
 

@@ -66,24 +66,40 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Wait until the phase with the given parity has completed.  Gives up (returns
 // false) once the sticky error word is set by anyone, or after limit_ns of
-// global time, in which case it sets the error word itself.
+// global time, in which case it sets the error word itself.  The global timer is
+// first read only after 64 unsuccessful polls, so short waits cost one or a few
+// try_wait round trips.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    const uint64_t t0 = globaltimer_ns();
+    uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 127u) == 0) {
+        if ((i & 63u) == 0) {
             if (*reinterpret_cast<volatile unsigned int*>(&g_error_word) != 0u)
                 return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
+            const uint64_t now = globaltimer_ns();
+            if (i == 64u)
+                t0 = now;
+            else if (now - t0 > limit_ns) {
                 atomicOr(&g_error_word, 1u);
                 return false;
             }
         }
     }
+}
+
+// Packed f32x2 fused multiply-add: {a.x*b.x + c.x, a.y*b.y + c.y}, one rounding each.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+          "l"(*reinterpret_cast<uint64_t*>(&c)));
+    return *reinterpret_cast<float2*>(&d);
 }
 
 // ---------------------------------------------------------------- bulk copy
@@ -311,6 +327,37 @@ __device__ __forceinline__ void tmem_ld8x2_wait(uint32_t taddr0, uint32_t taddr1
         v0[i] = __uint_as_float(r[i]);
         v1[i] = __uint_as_float(s[i]);
     }
+}
+
+// Four 16-column loads (columns taddr, +16, +32, +48) with a single wait: the 64
+// consecutive columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, float (&v)[64])
+{
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%67];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : MMQ_R32(0), MMQ_R32(1), MMQ_R32(2), MMQ_R32(3), MMQ_R32(4), MMQ_R32(5), MMQ_R32(6), MMQ_R32(7),
+          MMQ_R32(8), MMQ_R32(9), MMQ_R32(10), MMQ_R32(11), MMQ_R32(12), MMQ_R32(13), MMQ_R32(14),
+          MMQ_R32(15), MMQ_R32(16), MMQ_R32(17), MMQ_R32(18), MMQ_R32(19), MMQ_R32(20), MMQ_R32(21),
+          MMQ_R32(22), MMQ_R32(23), MMQ_R32(24), MMQ_R32(25), MMQ_R32(26), MMQ_R32(27), MMQ_R32(28),
+          MMQ_R32(29), MMQ_R32(30), MMQ_R32(31), MMQ_R32(32), MMQ_R32(33), MMQ_R32(34), MMQ_R32(35),
+          MMQ_R32(36), MMQ_R32(37), MMQ_R32(38), MMQ_R32(39), MMQ_R32(40), MMQ_R32(41), MMQ_R32(42),
+          MMQ_R32(43), MMQ_R32(44), MMQ_R32(45), MMQ_R32(46), MMQ_R32(47), MMQ_R32(48), MMQ_R32(49),
+          MMQ_R32(50), MMQ_R32(51), MMQ_R32(52), MMQ_R32(53), MMQ_R32(54), MMQ_R32(55), MMQ_R32(56),
+          MMQ_R32(57), MMQ_R32(58), MMQ_R32(59), MMQ_R32(60), MMQ_R32(61), MMQ_R32(62), MMQ_R32(63)
+        : "r"(taddr), "r"(taddr + 16), "r"(taddr + 32), "r"(taddr + 48)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+        v[i] = __uint_as_float(r[i]);
 }
 
 #undef MMQ_R32
