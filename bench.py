@@ -53,22 +53,30 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--peaks", action="store_true", help="run the throughput probes and print their JSON")
+    p.add_argument("--only", default="", help="comma-separated GEMM names of the stack (e.g. l0.gate): "
+                   "a small case for profiling, not a bench line")
     return p.parse_args()
 
 
-def stack_list(layers):
+def stack_list(layers, only=""):
+    keep = {x for x in only.split(",") if x}
     out = []
     for name, typ, od, id_, seed in synth.stack_gemms():
         if name[0] == "l" and name[1].isdigit() and int(name[1:].split(".")[0]) >= layers:
+            continue
+        if keep and name not in keep:
             continue
         out.append((name, typ, od, id_, seed))
     return out
 
 
 def config(args, extra=None):
-    c = {"workload": WORKLOAD, "tokens": args.tokens, "layers": args.layers, "gemms_per_step": len(stack_list(args.layers)),
+    c = {"workload": WORKLOAD, "tokens": args.tokens, "layers": args.layers,
+         "gemms_per_step": len(stack_list(args.layers, getattr(args, "only", ""))),
          "prepass_per_gemm": True,
          "l2": "inputs larger than L2: every step streams ~14.9 GB of repacked weights (129 MB L2)"}
+    if getattr(args, "only", ""):
+        c["only"] = args.only
     if extra:
         c.update(extra)
     return c
@@ -297,7 +305,9 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     M = args.tokens
-    gemms = stack_list(args.layers)
+    gemms = stack_list(args.layers, args.only)
+    if not gemms:
+        raise SystemExit(f"--only {args.only!r} matches no GEMM of the stack")
 
     # ---- registration (untimed): generate raw blocks, upload, repack, keep the packed planes
     want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
@@ -370,11 +380,11 @@ def run_ours(args, world, rank, local):
     t_max = max_over_ranks(world, t, dev if world > 1 else None)
     value = world * M * args.steps / t_max
 
-    # per-kernel-class time (events on the launching stream, inside the timed region)
+    # per-kernel time by GEMM shape (events on the launching stream, inside the timed region)
     cls_time, cls_flops, cls_n = {}, {}, {}
     for k in range(args.steps):
         for (typ, od, id_, *_), (a, b) in zip(calls, ev[k]):
-            key = f"gemm_{typ}"
+            key = f"gemm_{typ}_{od}x{id_}"
             cls_time[key] = cls_time.get(key, 0.0) + a.elapsed_time(b) * 1e-3
             cls_flops[key] = cls_flops.get(key, 0.0) + 2.0 * M * od * id_
             cls_n[key] = cls_n.get(key, 0) + 1
@@ -386,6 +396,7 @@ def run_ours(args, world, rank, local):
     peak = peaks["bf16_tflops_sustained"]
     roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": kernel_traffic(dom),
+            "launches": cls_n[dom], "time_share": cls_time[dom] / t,
             "achieved_def": "2*M*od*id per launch (int8-equivalent MACs x2) / mean launch time, CUDA events",
             "peak_source": f"{peaks['source']} dense bf16 sustained (f16 operands run at the bf16 rate)"}
 

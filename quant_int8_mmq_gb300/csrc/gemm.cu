@@ -13,25 +13,35 @@
 // chunks (K = id/32); it runs on the tensor cores in tf32 with both operands split
 // hi + lo (hi*hi + hi*lo + lo*hi, relative error ~2^-21 per product).
 //
-// One CTA per SM, persistent over 128-token x 128-row tiles; 10 warps:
+// One CTA per SM, persistent over 128-token x 128-row tiles; 12 warps in three
+// warpgroups.  The control warpgroup gives up registers (setmaxnreg) so that each
+// promotion thread can keep its 64 tile accumulators and 64 super-block partial
+// sums in registers:
 //   warp 0      producer: cp.async.bulk copies (no multicast) of the pre-swizzled
-//               f16 operand tiles into a STAGES-deep ring, token scale pairs into an
-//               SSTAGES ring, and per-super-block data (d, min-term operands, q6_K
-//               sub-block scales) into an SBR ring; completion on mbarriers.
+//               f16 operand tiles into a STAGES-deep ring, and once per super-block
+//               the token scales of its 8 chunks, the weight d, and the min-term
+//               operands (q4_K) or sub-block scales (plain-code q6_K) into an SBR
+//               ring; completion on mbarriers.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 (f16-held
 //               integer codes, f32 accumulate) into four rotating 128-column chunk
 //               slots (plain-code q6_K: two 256-column slots) and, for q4_K after each
 //               super-block, three kind::tf32 MMAs of the min term into the next slot.
-//   warps 2-9   promotion: tcgen05.ld of a finished slot (64 columns per thread),
+//   warps 2-3   idle (they only lend their registers).
+//   warps 4-11  promotion: tcgen05.ld of a finished slot (64 columns per thread),
 //               release it, inner += d_a * I' (packed f32x2 FMAs); per super-block
-//               acc += d * inner (- the min-term slot for q4_K), with acc kept in
-//               shared memory; store Y per tile.  Each warp owns one TMEM lane
-//               quarter (warp % 4) and 64 of the 128 columns.
+//               acc += d * inner (- the min-term slot for q4_K); store Y per tile.
+//               Each warp owns one TMEM lane quarter (warp % 4) and 64 of the 128
+//               columns.
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk, and TMEM holds
 // at most four 128-column chunks; the design keeps that round trip short: slot and
 // stage positions advance without division, slot counts are compile-time, the
 // issuing thread does nothing else, and the promotion spends one packed FMA per two
-// outputs per chunk.
+// outputs per chunk with no shared-memory traffic besides one scale per chunk.
+// Measured on GB300, the promotion's per-chunk chain (slot wait, TMEM load, release,
+// FMAs) rather than the tensor pipe sets the pace: about 700 SM cycles per chunk
+// against 128 for the chunk's two MMAs.  Variants that moved the MMA issue into the
+// promotion warps, doubled the promotion warps at half the columns, or pipelined the
+// TMEM loads against the FMAs all measured slower.
 // The multi-stage rings replace the pages' one-deep double buffer and group-count
 // waits ("r45 ...", §2.2; "r58 ...", §2.2 and §6 lesson 2: one tile of lookahead
 // cannot cover the global-to-shared latency); registration-time planes remove the
@@ -55,37 +65,43 @@ namespace {
 constexpr int BM = 128;             // tokens per tile (TMEM lanes)
 constexpr int BN = 128;             // weight rows per tile (MMA N)
 constexpr int BK = TILE_K;          // values per stage: two 32-value chunks
-constexpr int STAGES = 3;           // operand ring depth
-constexpr int SSTAGES = 8;          // token-scale ring depth (entries of one stage)
-constexpr int SBR = 2;              // super-block ring depth
-constexpr int NUM_WARPS = 10;
+constexpr int STAGES = 4;           // operand ring depth
+constexpr int SBR = 3;              // super-block ring depth
+constexpr int NUM_WARPS = 12;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
-constexpr int PROMO_WARP0 = 2;
+constexpr int PROMO_WARP0 = 4;
 constexpr int NUM_PROMO_WARPS = 8;
 constexpr int COLS_PER_WARP = BN / 2;   // 64
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+// Register split: the launch gives every thread LAUNCH_REGS; the control warpgroup
+// drops to CTRL_REGS and the two promotion warpgroups grow to PROMO_REGS out of the
+// same pool (the host checks the compiled count before launching).
+constexpr int LAUNCH_REGS = 168;
+constexpr int CTRL_REGS = 56;
+constexpr int PROMO_REGS = 224;
+static_assert(CTRL_REGS * 128 + PROMO_REGS * 256 <= LAUNCH_REGS * NUM_THREADS, "register split");
 
-constexpr int SCALE_STAGE_BYTES = 2 * BM * 8;      // {d, ssum} for two chunks x 128 tokens
-constexpr int SB_SBD_BYTES = BN * 4;               // d per row
+// One super-block ring entry: weight d per row, the token scale pairs of the
+// super-block's 8 chunks, then q4_K min-term operands or plain-code q6_K scales.
+constexpr int SB_SBD_OFF = 0;
+constexpr int SB_SBD_BYTES = BN * 4;
+constexpr int SB_AS_OFF = SB_SBD_OFF + SB_SBD_BYTES;
+constexpr int SB_AS_BYTES = 8 * BM * 8;            // {d, ssum} x 8 chunks x 128 tokens
+constexpr int SB_X_OFF = SB_AS_OFF + SB_AS_BYTES;
 constexpr int SB_AM_BYTES = 2 * TF32_TILE_BYTES;   // q4_K: token min-term operand hi, lo
 constexpr int SB_BM_BYTES = 2 * TF32_TILE_BYTES;   // q4_K: weight min-term operand hi, lo
 constexpr int SB_SC_BYTES = 16 * BN * 4;           // q6_K: sub-block scales
-constexpr int SB_BYTES = SB_AM_BYTES + SB_BM_BYTES + SB_SBD_BYTES;
-static_assert(SB_BYTES >= SB_SBD_BYTES + SB_SC_BYTES, "super-block entry");
-constexpr int ACC_BYTES = BM * BN * 4;             // f32 tile accumulator (shared memory)
+constexpr int SB_BYTES = SB_X_OFF + SB_AM_BYTES + SB_BM_BYTES;
+static_assert(SB_BYTES >= SB_X_OFF + SB_SC_BYTES, "super-block entry");
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * TILE_BYTES;
-constexpr int SMEM_AS = SMEM_B + STAGES * TILE_BYTES;
-constexpr int SMEM_SB = SMEM_AS + SSTAGES * SCALE_STAGE_BYTES;
-constexpr int SMEM_ACC = SMEM_SB + SBR * SB_BYTES;
-constexpr int SMEM_BAR = SMEM_ACC + ACC_BYTES;
+constexpr int SMEM_SB = SMEM_B + STAGES * TILE_BYTES;
+constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
 constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = BAR_FULL + STAGES;
-constexpr int BAR_SFULL = BAR_EMPTY + STAGES;
-constexpr int BAR_SEMPTY = BAR_SFULL + SSTAGES;
-constexpr int BAR_SBFULL = BAR_SEMPTY + SSTAGES;
+constexpr int BAR_SBFULL = BAR_EMPTY + STAGES;
 constexpr int BAR_SBEMPTY = BAR_SBFULL + SBR;
 constexpr int BAR_TFULL = BAR_SBEMPTY + SBR;
 constexpr int BAR_TEMPTY = BAR_TFULL + 4;
@@ -95,8 +111,8 @@ constexpr int SMEM_TMEMPTR = SMEM_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_TMEMPTR + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;    // slack for 1024-byte alignment
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-static_assert(SMEM_B % 1024 == 0 && SMEM_AS % 16 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 &&
-                  SMEM_ACC % 16 == 0 && SMEM_BAR % 8 == 0,
+static_assert(SMEM_B % 1024 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && SB_X_OFF % 16 == 0 &&
+                  SMEM_BAR % 8 == 0,
               "alignment");
 
 struct GemmArgs {
@@ -119,12 +135,25 @@ struct GemmArgs {
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
         if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
             atomicOr(&g_error_word, 1u);
             return;
         }
     }
+}
+
+// Bounded wait of the single producer / MMA thread.
+__device__ __forceinline__ bool ctl_wait(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait(bar, parity, WAIT_LIMIT_NS);
+}
+
+// Bounded wait by a whole warp; the verdict is made warp-uniform so that every lane
+// takes the same branch after it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, WAIT_LIMIT_NS));
 }
 
 // Shared-memory descriptor of a 128 x 8 tf32 tile in the no-swizzle K-major
@@ -157,6 +186,17 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+template <int R>
+__device__ __forceinline__ void regs_grow()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_shrink()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+
 // Position in a ring of N entries: entry index and the phase parity of its barriers.
 template <uint32_t N>
 struct RingPos {
@@ -185,15 +225,17 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
     const int num_tiles = g.num_m * g.num_n;
     auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp < PROMO_WARP0) {
+        regs_shrink<CTRL_REGS>();
+        // One thread of warp 0 produces and one thread of warp 1 issues MMAs; the other
+        // lanes of the control warpgroup wait at the CTA's final barrier.
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- producer
             RingPos<STAGES> op;
-            RingPos<SSTAGES> sc;
             RingPos<SBR> sb;
-            uint32_t n_ops = 0, n_sc = 0, n_sb = 0;  // fills issued on each ring
-            constexpr uint32_t sb_tx = Q4 ? (SB_AM_BYTES + SB_BM_BYTES + SB_SBD_BYTES)
-                                          : (SB_SBD_BYTES + (FOLDED ? 0 : SB_SC_BYTES));
+            uint32_t n_ops = 0, n_sb = 0;  // fills issued on each ring
+            constexpr uint32_t sb_tx =
+                SB_SBD_BYTES + SB_AS_BYTES + (Q4 ? (SB_AM_BYTES + SB_BM_BYTES) : (FOLDED ? 0 : SB_SC_BYTES));
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int m = tile % g.num_m, n = tile / g.num_m;
@@ -203,7 +245,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 for (int kb = 0; kb < nkb; ++kb) {
                     if ((kb & 3) == 0) {  // a new super-block
                         const int s = kb >> 2;
-                        if (!mbar_wait(bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u, WAIT_LIMIT_NS)) {
+                        if (!ctl_wait(bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -213,20 +255,22 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         const uint32_t dst = sbase + SMEM_SB + sb.i * SB_BYTES;
                         const uint32_t fb = bar(BAR_SBFULL + sb.i);
                         mbar_arrive_expect_tx(fb, sb_tx);
-                        bulk_g2s(dst, g.SBD + (static_cast<size_t>(n) * nsb + s) * SB_SBD_BYTES, SB_SBD_BYTES, fb);
+                        bulk_g2s(dst + SB_SBD_OFF, g.SBD + (static_cast<size_t>(n) * nsb + s) * SB_SBD_BYTES,
+                                 SB_SBD_BYTES, fb);
+                        bulk_g2s(dst + SB_AS_OFF, ASb + static_cast<size_t>(s) * SB_AS_BYTES, SB_AS_BYTES, fb);
                         if (Q4) {
-                            bulk_g2s(dst + SB_SBD_BYTES, g.AM + (static_cast<size_t>(m) * nsb + s) * SB_AM_BYTES,
+                            bulk_g2s(dst + SB_X_OFF, g.AM + (static_cast<size_t>(m) * nsb + s) * SB_AM_BYTES,
                                      SB_AM_BYTES, fb);
-                            bulk_g2s(dst + SB_SBD_BYTES + SB_AM_BYTES,
+                            bulk_g2s(dst + SB_X_OFF + SB_AM_BYTES,
                                      g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_BM_BYTES, SB_BM_BYTES, fb);
                         } else if (!FOLDED) {
-                            bulk_g2s(dst + SB_SBD_BYTES, g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_SC_BYTES,
+                            bulk_g2s(dst + SB_X_OFF, g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_SC_BYTES,
                                      SB_SC_BYTES, fb);
                         }
                         sb.next();
                         ++n_sb;
                     }
-                    if (!mbar_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u, WAIT_LIMIT_NS)) {
+                    if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
@@ -238,30 +282,15 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                              TILE_BYTES, fo);
                     op.next();
                     ++n_ops;
-                    if (!mbar_wait(bar(BAR_SEMPTY + sc.i), sc.ph ^ 1u, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_smem();  // same ordering for the token-scale ring
-                    const uint32_t fs = bar(BAR_SFULL + sc.i);
-                    mbar_arrive_expect_tx(fs, SCALE_STAGE_BYTES);
-                    bulk_g2s(sbase + SMEM_AS + sc.i * SCALE_STAGE_BYTES,
-                             ASb + static_cast<size_t>(kb) * SCALE_STAGE_BYTES, SCALE_STAGE_BYTES, fs);
-                    sc.next();
-                    ++n_sc;
                 }
             }
             // Our copies must have landed before the CTA may exit.
             for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i)
                 drain_wait(bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
-            for (uint32_t i = (n_sc > SSTAGES ? n_sc - SSTAGES : 0); i < n_sc; ++i)
-                drain_wait(bar(BAR_SFULL + i % SSTAGES), (i / SSTAGES) & 1u);
             for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
                 drain_wait(bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_t = idesc_tf32_f32(BM, BN);
             RingPos<STAGES> op;
@@ -270,7 +299,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(bar(BAR_FULL + op.i), op.ph, WAIT_LIMIT_NS)) {
+                    if (!ctl_wait(bar(BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -279,7 +308,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     const uint64_t b0 = sdesc_k_sw128(sbase + SMEM_B + op.i * TILE_BYTES);
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
-                        if (!mbar_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u, WAIT_LIMIT_NS)) {
+                        if (!ctl_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -304,13 +333,13 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     if (Q4 && (kb & 3) == 3) {
                         // Min-term contraction of this super-block (8 chunks, hi/lo split) into
                         // the next chunk slot, consumed by the promotion like a chunk.
-                        if (!mbar_wait(bar(BAR_SBFULL + sb.i), sb.ph, WAIT_LIMIT_NS) ||
-                            !mbar_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u, WAIT_LIMIT_NS)) {
+                        if (!ctl_wait(bar(BAR_SBFULL + sb.i), sb.ph) ||
+                            !ctl_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t am = sbase + SMEM_SB + sb.i * SB_BYTES + SB_SBD_BYTES;
+                        const uint32_t am = sbase + SMEM_SB + sb.i * SB_BYTES + SB_X_OFF;
                         const uint32_t bm = am + SB_AM_BYTES;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
@@ -329,54 +358,48 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             drain_wait(bar(BAR_DRAIN), 0u);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ promotion
-        const int pw = warp - PROMO_WARP0;              // 0..7
-        const int q = warp & 3;                          // TMEM lane quarter this warp may read
-        const int hc = pw >> 2;                          // which 64 of the 128 columns
-        const int row_in_tile = q * 32 + lane;
-        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        // This thread's accumulator pairs in shared memory: pair i (columns 2i, 2i+1 of
-        // its 64) at accs[i * BM]; consecutive lanes hit consecutive 8-byte words.
-        float2* accs = reinterpret_cast<float2*>(smem + SMEM_ACC) + (hc * (COLS_PER_WARP / 2)) * BM + row_in_tile;
-        RingPos<SSTAGES> sc;
-        RingPos<NSLOT> slot;
-        RingPos<SBR> sb;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const int m = tile % g.num_m, n = tile / g.num_m;
-            const int row = m * BM + row_in_tile;
-            const int jb = n * BN + hc * COLS_PER_WARP;
+        return;
+    }
+
+    // ---------------------------------------------------------------- promotion
+    regs_grow<PROMO_REGS>();
+    const int pw = warp - PROMO_WARP0;              // 0..7
+    const int q = warp & 3;                          // TMEM lane quarter this warp may read
+    const int hc = pw >> 2;                          // which 64 of the 128 columns
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    RingPos<NSLOT> slot;
+    RingPos<SBR> sb;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m = tile % g.num_m, n = tile / g.num_m;
+        const int row = m * BM + row_in_tile;
+        const int jb = n * BN + hc * COLS_PER_WARP;
+        float2 acc[COLS_PER_WARP / 2];
+#pragma unroll
+        for (int i = 0; i < COLS_PER_WARP / 2; ++i)
+            acc[i] = make_float2(0.0f, 0.0f);
+        for (int s = 0; s < nsb; ++s) {
+            const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
+            if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph)) {
+                ok = false;
+                break;
+            }
+            const uint2* tsc = reinterpret_cast<const uint2*>(sbe + SB_AS_OFF);
             float2 inner[COLS_PER_WARP / 2];
 #pragma unroll
             for (int i = 0; i < COLS_PER_WARP / 2; ++i)
                 inner[i] = make_float2(0.0f, 0.0f);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
-                if ((kb & 3) == 0) {
-                    if (!mbar_wait(bar(BAR_SBFULL + sb.i), sb.ph, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int i = 0; i < COLS_PER_WARP / 2; ++i)
-                        inner[i] = make_float2(0.0f, 0.0f);
-                }
-                if (!mbar_wait(bar(BAR_SFULL + sc.i), sc.ph, WAIT_LIMIT_NS)) {
-                    ok = false;
-                    break;
-                }
-                const uint2* tsc = reinterpret_cast<const uint2*>(smem + SMEM_AS + sc.i * SCALE_STAGE_BYTES);
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    if (!mbar_wait(bar(BAR_TFULL + slot.i), slot.ph, WAIT_LIMIT_NS)) {
+            {
+                for (int k = 0; k < 8; ++k) {
+                    const int c = 8 * s + k;                    // chunk index along id
+                    const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
+                    const float2 da2 = make_float2(da, da);
+                    if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const float da = __uint_as_float(tsc[cc * BM + row_in_tile].x);
-                    const float2 da2 = make_float2(da, da);
-                    const int c = 2 * kb + cc;                  // chunk index along id
                     const uint32_t col0 = lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP;
                     if (FOLDED) {
                         float I[COLS_PER_WARP];
@@ -385,25 +408,23 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         __syncwarp();
                         if (lane == 0)
                             mbar_arrive(bar(BAR_TEMPTY + slot.i));
-                        if (MODE == GEMM_DOTS) {
-                            if (row < g.M) {
-#pragma unroll
-                                for (int i = 0; i < COLS_PER_WARP; ++i) {
-                                    const int j = jb + i;
-                                    if (j < g.od)
-                                        g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] = I[i];
-                                }
-                            }
-                        } else {
+                        if (MODE == GEMM_Y) {
 #pragma unroll
                             for (int i = 0; i < COLS_PER_WARP / 2; ++i)
                                 inner[i] = ffma2(da2, make_float2(I[2 * i], I[2 * i + 1]), inner[i]);
+                        } else if (row < g.M) {
+#pragma unroll
+                            for (int i = 0; i < COLS_PER_WARP; ++i) {
+                                const int j = jb + i;
+                                if (j < g.od)
+                                    g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] = I[i];
+                            }
                         }
                     } else {
                         // q6_K with plain codes: one accumulator per 16-value sub-block,
                         // I' = sc0 * I_0 + sc1 * I_1 (exact: |I'| < 2^24).
-                        const float* scp = reinterpret_cast<const float*>(sbe + SB_SBD_BYTES);
-                        const int s0 = 2 * (c & 7);
+                        const float* scp = reinterpret_cast<const float*>(sbe + SB_X_OFF);
+                        const int s0 = 2 * k;
 #pragma unroll
                         for (int p = 0; p < COLS_PER_WARP / 8; ++p) {
                             float h0[8], h1[8];
@@ -442,73 +463,64 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 }
                 if (!ok)
                     break;
+            }
+            // acc += d * inner  (d per weight row of this super-block); q4_K also
+            // subtracts the super-block's min term, delivered through the next slot.
+            const float4* d4 = reinterpret_cast<const float4*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 4);
+            if (Q4) {
+                if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float mn[COLS_PER_WARP];
+                tmem_ld64_wait(lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP, mn);
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(BAR_SEMPTY + sc.i));
-                sc.next();
-                if ((kb & 3) == 3) {
-                    // acc += d * inner  (d per weight row of this super-block); q4_K also
-                    // subtracts the super-block's min term, delivered through the next slot.
-                    const float4* d4 = reinterpret_cast<const float4*>(sbe) + hc * (COLS_PER_WARP / 4);
-                    const bool first = (kb == 3);
-                    if (Q4) {
-                        if (!mbar_wait(bar(BAR_TFULL + slot.i), slot.ph, WAIT_LIMIT_NS)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        float mn[COLS_PER_WARP];
-                        tmem_ld64_wait(lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP, mn);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar(BAR_TEMPTY + slot.i));
-                        slot.next();
-                        if (MODE == GEMM_Y) {
+                    mbar_arrive(bar(BAR_TEMPTY + slot.i));
+                slot.next();
+                if (MODE == GEMM_Y) {
 #pragma unroll
-                            for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
-                                const float4 dv = d4[i];
-                                float2 a0 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i) * BM];
-                                float2 a1 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i + 1) * BM];
-                                a0 = ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i], mn[4 * i + 1]), a0);
-                                a1 = ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i + 2], mn[4 * i + 3]), a1);
-                                accs[(2 * i) * BM] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
-                                accs[(2 * i + 1) * BM] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
-                            }
-                        }
-                    } else if (MODE == GEMM_Y) {
-#pragma unroll
-                        for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
-                            const float4 dv = d4[i];
-                            const float2 a0 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i) * BM];
-                            const float2 a1 = first ? make_float2(0.0f, 0.0f) : accs[(2 * i + 1) * BM];
-                            accs[(2 * i) * BM] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
-                            accs[(2 * i + 1) * BM] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
-                        }
+                    for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
+                        const float4 dv = d4[i];
+                        const float2 a0 =
+                            ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i], mn[4 * i + 1]), acc[2 * i]);
+                        const float2 a1 =
+                            ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i + 2], mn[4 * i + 3]), acc[2 * i + 1]);
+                        acc[2 * i] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
+                        acc[2 * i + 1] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
                     }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar(BAR_SBEMPTY + sb.i));
-                    sb.next();
+                }
+            } else if (MODE == GEMM_Y) {
+#pragma unroll
+                for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
+                    const float4 dv = d4[i];
+                    acc[2 * i] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], acc[2 * i]);
+                    acc[2 * i + 1] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], acc[2 * i + 1]);
                 }
             }
-            if (!ok)
-                break;
-            if (MODE == GEMM_Y && row < g.M) {
-                float* yrow = g.out + static_cast<size_t>(row) * g.ldy;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(BAR_SBEMPTY + sb.i));
+            sb.next();
+        }
+        if (!ok)
+            break;
+        if (MODE == GEMM_Y && row < g.M) {
+            float* yrow = g.out + static_cast<size_t>(row) * g.ldy;
 #pragma unroll
-                for (int i = 0; i < COLS_PER_WARP; i += 4) {
-                    const int j = jb + i;
-                    const float2 lo = accs[(i / 2) * BM], hi = accs[(i / 2 + 1) * BM];
-                    if (g.vec_store && j + 3 < g.od) {
-                        *reinterpret_cast<float4*>(yrow + j) = make_float4(lo.x, lo.y, hi.x, hi.y);
-                    } else {
-                        const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+            for (int i = 0; i < COLS_PER_WARP; i += 4) {
+                const int j = jb + i;
+                const float2 lo = acc[i / 2], hi = acc[i / 2 + 1];
+                if (g.vec_store && j + 3 < g.od) {
+                    *reinterpret_cast<float4*>(yrow + j) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                } else {
+                    const float v[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            if (j + k < g.od)
-                                yrow[j + k] = v[k];
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        if (j + k < g.od)
+                            yrow[j + k] = v[k];
                 }
             }
         }
@@ -531,10 +543,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(BAR_FULL + s), 1);
             mbar_init(bar(BAR_EMPTY + s), 1);
-        }
-        for (int s = 0; s < SSTAGES; ++s) {
-            mbar_init(bar(BAR_SFULL + s), 1);
-            mbar_init(bar(BAR_SEMPTY + s), NUM_PROMO_WARPS);
         }
         for (int s = 0; s < SBR; ++s) {
             mbar_init(bar(BAR_SBFULL + s), 1);
@@ -586,6 +594,14 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
         return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_set_mask.load() & bit)) {
+        // The setmaxnreg split draws on the registers the launch reserved; a build
+        // that compiled to fewer per thread would make the promotion wait forever.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, gemm_kernel<TYPE, MODE>);
+        if (e != cudaSuccess)
+            return e;
+        if (fa.numRegs < LAUNCH_REGS)
+            return cudaErrorInvalidKernelImage;
         e = cudaFuncSetAttribute(gemm_kernel<TYPE, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess)
             return e;

@@ -64,11 +64,28 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps
+// until the phase completes or about hint_ns pass, instead of returning at once.
+// A sleeping thread issues nothing, so waiting warps leave the issue slots of
+// their scheduler to the warps that share it.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok;
+}
+
 // Wait until the phase with the given parity has completed.  Gives up (returns
 // false) once the sticky error word is set by anyone, or after limit_ns of
-// global time, in which case it sets the error word itself.  The global timer is
-// first read only after 64 unsuccessful polls, so short waits cost one or a few
-// try_wait round trips.
+// global time, in which case it sets the error word itself.  The error word and
+// the global timer are first read after 64 unsuccessful polls, so short waits
+// cost one or a few try_wait round trips.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity))
