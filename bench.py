@@ -253,6 +253,40 @@ def cpu_sample_run(raws, xh, xf, seconds, threads):
         n = min(xh.shape[0], max(n + 1, int(n * seconds / max(dt, 1e-3))))
 
 
+# ----------------------------------------------------------------------------- small M
+def small_m_case(lib, dev, stream, sptr, peaks, typ="q6_K", od=4097, id_=11008, M=1, copies=4, reps=40):
+    """FFN-down q6_K 4097x11008 at M = 1 token: the weight-streaming path against HBM.
+
+    Algorithmic bytes = the raw k-quant blocks (210 B per 256 values); `copies` packed
+    weight buffers are rotated so the raw plane (~37 MB each) cannot stay in L2."""
+    import torch
+    import quant_int8_mmq_gb300 as mmq
+    raw = torch.from_numpy(synth.blocks(typ, od, id_, 77).reshape(-1)).to(dev)
+    pks = [mmq.pack_weights(typ, raw, od, id_) for _ in range(copies)]
+    x = torch.from_numpy(synth.activations(M, id_, 78)).to(dev)
+    qa, sc = mmq.quantize_act(x)
+    Y = torch.empty((M, od), dtype=torch.float32, device=dev)
+    fn = lib.mmq_gemm_q6k if typ == "q6_K" else lib.mmq_gemm_q4k
+    args = [(pk.data_ptr(), od, id_, qa.data_ptr(), sc.data_ptr(), M, Y.data_ptr(), od, sptr) for pk in pks]
+    for i in range(8):
+        fn(*args[i % copies])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(reps):
+        fn(*args[i % copies])
+    b.record(stream)
+    torch.cuda.synchronize()
+    if mmq.mmq_get_device_error() != 0:
+        raise RuntimeError("device error in the small-M case")
+    t = a.elapsed_time(b) * 1e-3 / reps
+    alg = od * (id_ // 256) * (210 if typ == "q6_K" else 144)
+    return {"workload": f"{typ} {od}x{id_} (FFN down, odd od), M={M}", "us": t * 1e6,
+            "achieved_gbs": alg / t / 1e9, "peak_gbs": peaks["hbm_gbs"],
+            "frac_hbm": alg / t / 1e9 / peaks["hbm_gbs"], "bytes_def": "raw block bytes od*id/256*210 per launch",
+            "path": mmq.mmq_last_path(), "l2": f"{copies} rotated weight copies (raw plane 37 MB each)"}
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     if rank != 0:
@@ -416,6 +450,10 @@ def run_ours(args, world, rank, local):
         line["int8_peak_tops"] = probe["int8_mma_sync_tops"]
         line["frac_of_int8_peak"] = line["gemm_only_tops"] / probe["int8_mma_sync_tops"]
     line["clocks"] = clocks.summary()
+
+    # ---- the small-M case (decode / tail): HBM-bound weight streaming, not part of the step
+    if rank == 0 and not args.only:
+        line["small_m"] = small_m_case(lib, dev, stream, sptr, peaks)
 
     # ---- end to end through the public API: pinned host inputs in, logits out, every step
     if not args.no_e2e:

@@ -89,7 +89,13 @@ typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
  *            128 rows x 8 chunks of 4-byte values, row r / chunk k at byte
  *            (r/8)*256 + (k/4)*128 + (r%8)*16 + (k%4)*4.
  *   Rows t >= M hold code 0, d 0, ssum 0, ma 0.
+ *   qa, M <= MMQ_SMALL_M only: after the Mp*K*2 bytes of tiles, the same codes
+ *     as int8, M rows of K bytes, each group of 8 values stored in the order
+ *     (0,2,4,6,1,3,5,7): value k of token t at byte t*K + (k & ~7) +
+ *     ((k & 7) >> 1) + 4*(k & 1).  The weight-streaming GEMM reads this plane.
+ *     mmq_act_plane_bytes includes it in qa_bytes.
  * -------------------------------------------------------------------------- */
+#define MMQ_SMALL_M 8
 mmq_status mmq_act_plane_bytes(int M, int K, size_t* qa_bytes, size_t* scale_bytes);
 mmq_status mmq_act_scale_layout(int M, int K, size_t* pair_offset, size_t* pair_bytes,
                                 size_t* am_offset, size_t* am_bytes);
@@ -114,7 +120,7 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *   q6_K ((ql[e/2] >> 4*(e%2)) & 15 | ((qh[e/4] >> 2*(e%4)) & 3) << 4) - 32,
  *   q4_K (qs[e/2] >> 4*(e%2)) & 15.  Value e of a q6_K block uses scales[e/16].
  *
- * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds five planes at
+ * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds six planes at
  * the offsets mmq_packed_weight_layout() returns; Np = 128*ceil(od/128),
  * nkb = id/64, nchunk = id/32, nsb = id/256; rows j >= od are zero:
  *   CODES  Np*id f16 integers in 16384-byte tiles (nt, kb) at (nt*nkb + kb)*16384,
@@ -132,6 +138,9 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *                  the lo tile, row r / chunk k at (r/8)*256 + (k/4)*128 + (r%8)*16 + (k%4)*4;
  *            q6_K: the 16 scales as f32, scale s of row r at byte (s*128 + r)*4.
  *   FLAG   q6_K: uint32 word 0 = 1 if CODES are folded, word 1 = max |scales[i]|.
+ *   RAW    the raw blocks re-laid for the weight-streaming GEMM, od rows x nsb
+ *          blocks, row-major: q4_K 144 B [qs[128] | d | dmin | scales[12]],
+ *          q6_K 224 B [ql[128] | qh[64] | scales[16] | d | 14 zero bytes].
  * -------------------------------------------------------------------------- */
 typedef enum {
     MMQ_PLANE_CODES = 0,
@@ -139,7 +148,8 @@ typedef enum {
     MMQ_PLANE_SBD = 2,
     MMQ_PLANE_AUX = 3,
     MMQ_PLANE_FLAG = 4,
-    MMQ_NUM_WEIGHT_PLANES = 5
+    MMQ_PLANE_RAW = 5,
+    MMQ_NUM_WEIGHT_PLANES = 6
 } mmq_weight_plane;
 
 mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes);
@@ -158,6 +168,11 @@ mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
  * min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo tensor-core
  * contraction (relative error about 2^-21 per product).  Rows t >= M and
  * columns j >= od are never written.  ldy >= od.
+ * M <= MMQ_SMALL_M (decode and tail shapes) takes the weight-streaming path
+ * instead: the RAW plane and the int8 activation plane, exact integer dots on
+ * the CUDA cores (dp4a), and the scales applied per chunk in the formula's own
+ * order (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=
+ * d_a*(d*sc0*I_0 + d*sc1*I_1)), with a fixed reduction order.
  * -------------------------------------------------------------------------- */
 mmq_status mmq_gemm_q6k(const void* packed, int od, int id, const void* qa, const void* scales,
                         int M, float* Y, int ldy, mmq_stream_t s);

@@ -109,13 +109,14 @@ def mmq_packed_weight_bytes(t, od, id_):
     return b.value
 
 
-PLANES = ("codes", "pairs", "sbd", "aux", "flag")
+PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw")
+SMALL_M = 8          # token counts up to this take the weight-streaming path
 
 
 def mmq_packed_weight_layout(t, od, id_):
     """{plane name: (offset, size)} of a packed weight buffer."""
-    off = (ctypes.c_size_t * 5)()
-    size = (ctypes.c_size_t * 5)()
+    off = (ctypes.c_size_t * len(PLANES))()
+    size = (ctypes.c_size_t * len(PLANES))()
     _check(load().mmq_packed_weight_layout(t, od, id_, off, size), "mmq_packed_weight_layout")
     return {name: (off[i], size[i]) for i, name in enumerate(PLANES)}
 

@@ -18,6 +18,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool valid_k(int K) { return K >= mmq::QK_K && K <= MMQ_MAX_ID && (K % mmq::QK_K) == 0; }
 
+// The verdict per device ordinal is cached (0 unknown, 1 sm_103, 2 other): a
+// device's compute capability does not change while the process runs.
+std::atomic<unsigned char> g_dev_ok[64];
+
 mmq_status check_device()
 {
     int dev = 0;
@@ -25,13 +29,21 @@ mmq_status check_device()
         cudaGetLastError();
         return MMQ_ERR_UNSUPPORTED;
     }
+    if (dev >= 0 && dev < 64) {
+        const unsigned char v = g_dev_ok[dev].load(std::memory_order_relaxed);
+        if (v != 0)
+            return v == 1 ? MMQ_OK : MMQ_ERR_UNSUPPORTED;
+    }
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
         cudaGetLastError();
         return MMQ_ERR_UNSUPPORTED;
     }
-    return (major == 10 && minor == 3) ? MMQ_OK : MMQ_ERR_UNSUPPORTED;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < 64)
+        g_dev_ok[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
+    return ok ? MMQ_OK : MMQ_ERR_UNSUPPORTED;
 }
 
 mmq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MMQ_OK : MMQ_ERR_CUDA; }
@@ -63,8 +75,12 @@ mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int o
     if (st != MMQ_OK)
         return st;
     const char* label = nullptr;
-    const cudaError_t e = mmq::launch_gemm(static_cast<int>(t), mode, packed, od, id, qa, scales, M, out, ldy,
-                                           reinterpret_cast<cudaStream_t>(s), &label);
+    const cudaError_t e =
+        (mode == mmq::GEMM_Y && M <= mmq::SMALL_M)
+            ? mmq::launch_gemm_small(static_cast<int>(t), packed, od, id, qa, scales, M, out, ldy,
+                                     reinterpret_cast<cudaStream_t>(s), &label)
+            : mmq::launch_gemm(static_cast<int>(t), mode, packed, od, id, qa, scales, M, out, ldy,
+                               reinterpret_cast<cudaStream_t>(s), &label);
     if (label)
         g_last_path.store(label);
     return from_cuda(e);
@@ -109,7 +125,7 @@ mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes)
     const mmq_status st = check_weight_shape(t, od, id);
     if (st != MMQ_OK)
         return st;
-    *bytes = mmq::weight_planes(od, id).total;
+    *bytes = mmq::weight_planes(static_cast<int>(t), od, id).total;
     return MMQ_OK;
 }
 
@@ -121,7 +137,7 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
     const mmq_status st = check_weight_shape(t, od, id);
     if (st != MMQ_OK)
         return st;
-    const mmq::WeightPlanes w = mmq::weight_planes(od, id);
+    const mmq::WeightPlanes w = mmq::weight_planes(static_cast<int>(t), od, id);
     offsets[MMQ_PLANE_CODES] = w.code_off;
     sizes[MMQ_PLANE_CODES] = w.code_bytes;
     offsets[MMQ_PLANE_PAIRS] = w.pair_off;
@@ -132,6 +148,8 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
     sizes[MMQ_PLANE_AUX] = w.aux_bytes;
     offsets[MMQ_PLANE_FLAG] = w.flag_off;
     sizes[MMQ_PLANE_FLAG] = w.flag_bytes;
+    offsets[MMQ_PLANE_RAW] = w.raw_off;
+    sizes[MMQ_PLANE_RAW] = w.raw_bytes;
     return MMQ_OK;
 }
 

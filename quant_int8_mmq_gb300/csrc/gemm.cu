@@ -768,7 +768,7 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
 cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int id, const void* qa,
                         const void* scales, int M, float* out, int ldy, cudaStream_t s, const char** path_label)
 {
-    const WeightPlanes wp = weight_planes(od, id);
+    const WeightPlanes wp = weight_planes(type, od, id);
     const ActPlanes ap = act_planes(M, id);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
     const uint8_t* sc = static_cast<const uint8_t*>(scales);

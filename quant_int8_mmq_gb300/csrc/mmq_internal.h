@@ -37,8 +37,20 @@ __host__ __device__ constexpr int tf32_tile_byte(int r, int k)
 }
 constexpr int TF32_TILE_BYTES = 128 * 8 * 4;
 
+// Token counts up to SMALL_M take the weight-streaming path; for them the prepass
+// also writes int8 codes, row-major, each group of 8 values stored in the order
+// (0,2,4,6,1,3,5,7) so that a word of low (or high) weight nibbles meets the four
+// activation codes it multiplies.
+constexpr int SMALL_M = 8;
+__host__ __device__ constexpr int small_pos(int k)   // byte position of value k in its row
+{
+    return (k & ~7) + ((k & 7) >> 1) + 4 * (k & 1);
+}
+
 struct ActPlanes {       // layout of mmq_quantize_act's outputs
-    size_t qa_bytes;     // f16 code tiles
+    size_t tile_bytes;   // f16 code tiles (start of the qa buffer)
+    size_t i8_off, i8_bytes;       // M <= SMALL_M: int8 codes [M][K] (small_pos order), else 0
+    size_t qa_bytes;     // tiles + int8 plane
     size_t pair_off, pair_bytes;   // {f32 d, i32 ssum} per (token, chunk)
     size_t am_off, am_bytes;       // tf32 hi/lo tiles of d*ssum per (token tile, super-block)
     size_t scale_bytes;            // pairs + am
@@ -47,7 +59,10 @@ inline ActPlanes act_planes(int M, int K)
 {
     const size_t Mp = static_cast<size_t>(ceil_div(M, TILE_ROWS)) * TILE_ROWS;
     ActPlanes a;
-    a.qa_bytes = Mp * static_cast<size_t>(K) * 2;
+    a.tile_bytes = Mp * static_cast<size_t>(K) * 2;
+    a.i8_off = a.tile_bytes;
+    a.i8_bytes = (M <= SMALL_M) ? static_cast<size_t>(M) * static_cast<size_t>(K) : 0;
+    a.qa_bytes = a.i8_off + a.i8_bytes;
     a.pair_off = 0;
     a.pair_bytes = Mp * static_cast<size_t>(K / CHUNK) * 8;
     a.am_off = a.pair_bytes;
@@ -56,15 +71,23 @@ inline ActPlanes act_planes(int M, int K)
     return a;
 }
 
+// Raw blocks re-laid for 16-byte loads (the weight-streaming path): per row, per
+// super-block, q4_K [qs 128 | d 2 | dmin 2 | scales 12] = 144 B, q6_K
+// [ql 128 | qh 64 | scales 16 | d 2 | zero 14] = 224 B.
+constexpr int RAW4_BYTES = 144;
+constexpr int RAW6_BYTES = 224;
+__host__ __device__ constexpr int raw_block_bytes(int type) { return type == 12 ? RAW4_BYTES : RAW6_BYTES; }
+
 struct WeightPlanes {    // layout of mmq_pack_weights' output
     size_t code_off, code_bytes;   // f16 code tiles (scale-folded where exact)
     size_t pair_off, pair_bytes;   // f32 scale pairs per (row, chunk)
     size_t sbd_off, sbd_bytes;     // f32 d per (row, super-block)
     size_t aux_off, aux_bytes;     // q4_K: tf32 hi/lo tiles of dmin*m; q6_K: f32 scales per sub-block
     size_t flag_off, flag_bytes;   // q6_K: word 0 = 1 if codes hold sc*q, word 1 = max |sc|
+    size_t raw_off, raw_bytes;     // re-laid raw blocks [od][id/256]
     size_t total;
 };
-inline WeightPlanes weight_planes(int od, int id)
+inline WeightPlanes weight_planes(int type, int od, int id)
 {
     const size_t Np = static_cast<size_t>(ceil_div(od, TILE_ROWS)) * TILE_ROWS;
     const size_t nsb = static_cast<size_t>(id / QK_K);
@@ -79,7 +102,9 @@ inline WeightPlanes weight_planes(int od, int id)
     w.aux_bytes = Np * nsb * 64;   // q4_K: 2 x 8 tf32; q6_K: 16 f32
     w.flag_off = w.aux_off + w.aux_bytes;
     w.flag_bytes = 256;
-    w.total = w.flag_off + w.flag_bytes;
+    w.raw_off = w.flag_off + w.flag_bytes;
+    w.raw_bytes = static_cast<size_t>(od) * nsb * static_cast<size_t>(raw_block_bytes(type));
+    w.total = w.raw_off + ((w.raw_bytes + 255) / 256) * 256;
     return w;
 }
 
@@ -90,6 +115,9 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
 cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed, cudaStream_t s);
 
 enum GemmMode { GEMM_Y = 0, GEMM_DOTS = 1 };
+// Weight-streaming GEMM for M <= SMALL_M (raw blocks x int8 codes, dp4a).
+cudaError_t launch_gemm_small(int type, const void* packed, int od, int id, const void* qa, const void* scales,
+                              int M, float* Y, int ldy, cudaStream_t s, const char** path_label);
 cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int id, const void* qa,
                         const void* scales, int M, float* out, int ldy, cudaStream_t s,
                         const char** path_label);

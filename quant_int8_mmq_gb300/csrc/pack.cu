@@ -23,6 +23,9 @@
 //         q6_K: the 16 int8 sub-block scales as f32 per (row, super-block), used
 //               when the codes are not folded.
 //  flag   q6_K: word 0 = 1 if the codes are folded, word 1 = max |sc|.
+//  raw    the raw blocks re-laid for 16-byte loads by the weight-streaming path
+//         (few tokens): codes first, then the scale bytes; q4_K keeps 144 bytes,
+//         q6_K is padded with zeros to 224.
 // The layout follows the GEMM's consumption window: one tile's rows of one chunk
 // or super-block are contiguous (the chunk-major principle of r56 §2.2), and the
 // codes are unpacked once here instead of in the GEMM's staging (the
@@ -187,11 +190,42 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ r
     }
 }
 
+// Raw blocks -> the re-laid raw plane, one 32-bit output word per thread.
+//   q4_K in [d 2 | dmin 2 | scales 12 | qs 128]  -> out [qs 128 | d, dmin, scales 16]
+//   q6_K in [ql 128 | qh 64 | scales 16 | d 2]   -> out [the same 210 | zeros 14]
+template <int TYPE>
+__global__ void __launch_bounds__(256) raw_relayout_kernel(const uint8_t* __restrict__ raw, long long nblocks,
+                                                           uint32_t* __restrict__ out)
+{
+    constexpr int IN = (TYPE == 12) ? Q4K_BYTES : Q6K_BYTES;
+    constexpr int OUTW = raw_block_bytes(TYPE) / 4;
+    const long long words = nblocks * OUTW;
+    for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < words;
+         w += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long b = w / OUTW;
+        const int o = static_cast<int>(w - b * OUTW) * 4;
+        const uint8_t* src = raw + b * IN;
+        uint32_t v = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int ob = o + k;
+            int sb;
+            if (TYPE == 12)
+                sb = ob < 128 ? ob + 16 : ob - 128;
+            else
+                sb = ob < Q6K_BYTES ? ob : -1;
+            const uint32_t byte = sb >= 0 ? static_cast<uint32_t>(src[sb]) : 0u;
+            v |= byte << (8 * k);
+        }
+        out[w] = v;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed, cudaStream_t s)
 {
-    const WeightPlanes wp = weight_planes(od, id);
+    const WeightPlanes wp = weight_planes(type, od, id);
     const int Np = ceil_div(od, TILE_ROWS) * TILE_ROWS;
     const long long total = static_cast<long long>(Np) * (id / CHUNK);
     long long blocks = (total + 255) / 256;
@@ -217,6 +251,19 @@ cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed,
         pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
                                                                         sbd, base + wp.aux_off, flag);
     }
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const long long nblocks = static_cast<long long>(od) * (id / QK_K);
+    const long long rwords = nblocks * (raw_block_bytes(type) / 4);
+    long long rblocks = (rwords + 255) / 256;
+    if (rblocks > 65535LL * 8)
+        rblocks = 65535LL * 8;
+    uint32_t* rout = reinterpret_cast<uint32_t*>(base + wp.raw_off);
+    if (type == 14)
+        raw_relayout_kernel<14><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(rb, nblocks, rout);
+    else
+        raw_relayout_kernel<12><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(rb, nblocks, rout);
     return cudaGetLastError();
 }
 

@@ -9,7 +9,8 @@
 // the operand of the q4_K min-term side contraction: ma = d*ssum (one f32
 // multiply) split exactly-enough into tf32 hi = rna(ma) and lo = rna(ma - hi),
 // in 128 x 8 tf32 tiles per (token tile, super-block).  Padded token rows
-// (t >= M) are zero-filled.
+// (t >= M) are zero-filled.  For M <= SMALL_M it also writes the codes as int8,
+// row-major, in the small_pos order the weight-streaming GEMM consumes.
 //
 // Sources: the prepass that moved activation quantization and transposition
 // out of the GEMM and writes pre-transposed qa8 and d/ssum planes with padded
@@ -43,7 +44,8 @@ __device__ __forceinline__ float tf32_rna(float v)
 
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int M, int K, int ldx,
                                                            int Mp, int vec2, uint16_t* __restrict__ qa,
-                                                           uint2* __restrict__ scales, uint8_t* __restrict__ am)
+                                                           uint2* __restrict__ scales, uint8_t* __restrict__ am,
+                                                           int8_t* __restrict__ qa8)
 {
     const int lane = threadIdx.x & 31;
     const int nkb = K / TILE_K;
@@ -86,6 +88,12 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
         const uint32_t packed = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q0))) |
                                 (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q1))) << 16);
         *reinterpret_cast<uint32_t*>(tile + tile_byte(r, 2 * lane)) = packed;
+        if (qa8 != nullptr && t < M) {
+            int8_t* row8 = qa8 + static_cast<size_t>(t) * K;
+            const int k0 = kb * TILE_K + 2 * lane;
+            row8[small_pos(k0)] = static_cast<int8_t>(q0);
+            row8[small_pos(k0 + 1)] = static_cast<int8_t>(q1);
+        }
         if ((lane & 15) == 0) {
             const int c = 2 * kb + (lane >> 4);
             scales[(static_cast<size_t>(mt) * nchunk + c) * TILE_ROWS + r] =
@@ -121,7 +129,7 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
     uint8_t* sc = static_cast<uint8_t*>(scales);
     quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         x, M, K, ldx, Mp, vec2, static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off),
-        sc + ap.am_off);
+        sc + ap.am_off, ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr);
     return cudaGetLastError();
 }
 

@@ -44,6 +44,10 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
     assert lay["pairs"] == (0, 256 * 16 * 8)
     assert lay["am"] == (256 * 16 * 8, 2 * 2 * 8192)            # 2 token tiles x 2 super-blocks
     assert sc == lay["am"][0] + lay["am"][1]
+    # token counts up to 8 add the int8 code plane after the tiles
+    assert mmq.mmq_act_plane_bytes(5, 512)[0] == 128 * 512 * 2 + 5 * 512
+    assert mmq.mmq_act_plane_bytes(8, 512)[0] == 128 * 512 * 2 + 8 * 512
+    assert mmq.mmq_act_plane_bytes(9, 512)[0] == 128 * 512 * 2
     for t in (mmq.MMQ_Q4_K, mmq.MMQ_Q6_K):
         L = mmq.mmq_packed_weight_layout(t, 4097, 1024)
         Np, nsb = 4224, 4
@@ -52,8 +56,9 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
         assert L["sbd"] == (sum(L["pairs"]), Np * nsb * 4)
         assert L["aux"] == (sum(L["sbd"]), Np * nsb * 64)
         assert L["flag"][0] == sum(L["aux"])
+        assert L["raw"] == (sum(L["flag"]), 4097 * 4 * (144 if t == mmq.MMQ_Q4_K else 224))
         assert all(off % 16 == 0 for off, _ in L.values())
-        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["flag"])
+        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == -(-sum(L["raw"]) // 256) * 256
 
 
 @pytest.mark.parametrize("M,K,err", [(0, 256, 2), (1, 255, 2), (1, 0, 2), (5, 300, 2), (1 << 23, 256, 2)])

@@ -102,9 +102,21 @@ def _check_prepass(x, ldx=None):
     assert np.all(err <= np.abs(ma) * 2.0 ** -21)
     assert np.all(np.abs(lo[:M]) <= np.abs(hi[:M]) * 2.0 ** -10 + 1e-38)
     assert not hi[M:].any() and not lo[M:].any()
+    # M <= 8: the int8 codes after the tiles, each 8-value group in the order (0,2,4,6,1,3,5,7)
+    qab = qa.cpu().numpy()
+    if M <= mmq.SMALL_M:
+        assert qab.size == Mp * K * 2 + M * K
+        i8 = qab[Mp * K * 2:].view(np.int8).reshape(M, K // 8, 8)
+        order = np.array([0, 2, 4, 6, 1, 3, 5, 7])
+        back = np.empty_like(i8)
+        back[:, :, order] = i8
+        assert np.array_equal(back.reshape(M, K).astype(np.int64), q.astype(np.int64))
+    else:
+        assert qab.size == Mp * K * 2
 
 
-@pytest.mark.parametrize("M,K,seed", [(16, 512, 0), (512, 4096, 1), (130, 768, 5), (1, 256, 6), (2047, 1024, 7)])
+@pytest.mark.parametrize("M,K,seed", [(16, 512, 0), (512, 4096, 1), (130, 768, 5), (1, 256, 6), (2047, 1024, 7),
+                                      (5, 768, 8), (8, 512, 9)])
 def test_prepass_bit_exact(M, K, seed):
     _check_prepass(synth.activations(M, K, seed))
 
@@ -144,7 +156,7 @@ def test_pack_planes_byte_exact(typ, od, id_):
     pk = packed.cpu().numpy()
     tid = mmq.TYPES[t]
     L = mmq.mmq_packed_weight_layout(tid, od, id_)
-    assert pk.size == sum(L["flag"])
+    assert pk.size == -(-sum(L["raw"]) // 256) * 256
     Np, nsb, nchunk = padded(od), id_ // 256, id_ // 32
     part = {k: pk[o:o + n] for k, (o, n) in L.items()}
     codes = untile_codes(part["codes"], Np, id_)
@@ -182,6 +194,13 @@ def test_pack_planes_byte_exact(typ, od, id_):
     assert np.array_equal(sbd[:od].view(np.uint32), d.view(np.uint32))
     assert not codes[od:].any() and not a[od:].view(np.uint32).any() and not b[od:].view(np.uint32).any()
     assert not sbd[od:].view(np.uint32).any()
+    # raw blocks re-laid for the weight-streaming path (the header's byte map)
+    rawp = part["raw"].reshape(od, nsb, -1)
+    if t == "q6_K":
+        want = np.concatenate([raw, np.zeros((od, nsb, 14), np.uint8)], axis=2)
+    else:
+        want = np.concatenate([raw[..., 16:], raw[..., :16]], axis=2)
+    assert np.array_equal(rawp, want)
 
 
 # --------------------------------------------------------------------------- dots
@@ -330,6 +349,49 @@ def test_gemm_deterministic():
     a = _run_gemm(typ, raw, x).cpu().numpy()
     b = _run_gemm(typ, raw, x).cpu().numpy()
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# --------------------------------------------------------------------------- weight-streaming path (M <= 8)
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("od,id_", [(1, 256), (130, 768), (4097, 1024)])
+def test_gemm_streaming_parity(typ, M, od, id_):
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    raw = _q6_raw(od, id_, od + M, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, od + M)
+    x = synth.activations(M, id_, 10 * M + od)
+    Y = _run_gemm(t, raw, x).cpu().numpy()
+    assert "weight-streaming" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+@pytest.mark.parametrize("M", [8, 9])
+def test_gemm_streaming_boundary(M):
+    """M = 8 streams the weights, M = 9 takes the tile GEMM: both match the oracle."""
+    raw = synth.q4k_blocks(257, 2048, 31)
+    x = synth.activations(M, 2048, 32)
+    Y = _run_gemm("q4_K", raw, x).cpu().numpy()
+    assert ("weight-streaming" in mmq.mmq_last_path()) == (M <= mmq.SMALL_M)
+    Yo, S = oracle_gemm("q4_K", raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+def test_gemm_streaming_row_stride_unaligned_and_deterministic():
+    typ, M, od, id_ = "q6_K", 5, 203, 512
+    raw = _raw(typ, od, id_, seed=15)
+    x = synth.activations(M, id_, 16)
+    Yo, S = oracle_gemm(typ, raw, x)
+    outs = []
+    for ldy, off in ((211, 0), (208, 1), (256, 0), (211, 0)):
+        buf = torch.full((M * ldy + 8,), -7.0, dtype=torch.float32, device=DEV)
+        Yv = buf[off:off + M * ldy].view(M, ldy)
+        _run_gemm(typ, raw, x, Y=Yv)
+        host = Yv.cpu().numpy()
+        assert_y_close(host[:, :od], Yo, S)
+        assert np.all(host[:, od:] == -7.0)
+        assert np.all(buf[:off].cpu().numpy() == -7.0)
+        outs.append(host[:, :od].copy())
+    assert np.array_equal(outs[0].view(np.uint32), outs[3].view(np.uint32))
 
 
 def test_status_codes_on_device():
