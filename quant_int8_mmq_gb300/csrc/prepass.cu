@@ -17,10 +17,12 @@
 // rows zeroed ("r45 - cp.async for the q6_K A-side staging ...", §1.1 and §2.3;
 // "r56 - q6_K A-side bundle ...", §1).
 //
-// Mapping: one warp per (token row, 64-value block); lane l owns values 2l, 2l+1,
-// so lanes 0-15 hold chunk 2kb and lanes 16-31 chunk 2kb+1.  Consecutive warps
-// take consecutive token rows of one 64-value block, so the 128-byte code rows and
-// the 8-byte scale entries they write are contiguous in HBM.
+// Mapping: one warp per (token row, 256-value super-block); lane l owns values
+// 8l..8l+7 (two 16-byte loads), so four lanes share a 32-value chunk and the amax
+// and ssum reductions run over those four.  A lane's 8 codes are one 16-byte
+// segment of the swizzled operand tile (one store).  Consecutive warps take
+// consecutive token rows of one super-block, so the tile rows and the scale
+// entries they write are contiguous in HBM.
 #include <cuda_fp16.h>
 
 #include "mmq_internal.h"
@@ -43,67 +45,96 @@ __device__ __forceinline__ float tf32_rna(float v)
 }
 
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int M, int K, int ldx,
-                                                           int Mp, int vec2, uint16_t* __restrict__ qa,
+                                                           int Mp, int vec4, uint16_t* __restrict__ qa,
                                                            uint2* __restrict__ scales, uint8_t* __restrict__ am,
                                                            int8_t* __restrict__ qa8)
 {
     const int lane = threadIdx.x & 31;
     const int nkb = K / TILE_K;
     const int nchunk = K / CHUNK;
-    const long long total = static_cast<long long>(Mp) * nkb;
+    const int nsb = K / QK_K;
+    const long long total = static_cast<long long>(Mp) * nsb;
     const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    // Two items per pass: both loads are in flight before either is reduced.
     for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
-         w += stride) {
-        const int t = static_cast<int>(w % Mp);
-        const int kb = static_cast<int>(w / Mp);
-        float x0 = 0.0f, x1 = 0.0f;
-        if (t < M) {
-            const float* p = x + static_cast<size_t>(t) * ldx + static_cast<size_t>(kb) * TILE_K + 2 * lane;
-            if (vec2) {
-                const float2 v = __ldcs(reinterpret_cast<const float2*>(p));
-                x0 = v.x;
-                x1 = v.y;
-            } else {
-                x0 = __ldcs(p);
-                x1 = __ldcs(p + 1);
+         w += 2 * stride) {
+        float vv[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const long long wi = w + u * stride;
+            const int t = static_cast<int>(wi % Mp);
+            const int k0 = static_cast<int>(wi / Mp) * QK_K + 8 * lane;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                vv[u][i] = 0.0f;
+            if (wi < total && t < M) {
+                const float* p = x + static_cast<size_t>(t) * ldx + k0;
+                if (vec4) {
+                    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+                    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+                    vv[u][0] = a.x; vv[u][1] = a.y; vv[u][2] = a.z; vv[u][3] = a.w;
+                    vv[u][4] = b.x; vv[u][5] = b.y; vv[u][6] = b.z; vv[u][7] = b.w;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        vv[u][i] = __ldcs(p + i);
+                }
             }
         }
-        float a = fmaxf(fabsf(x0), fabsf(x1));
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        const float d = __fdiv_rn(a, 127.0f);
-        int q0 = 0, q1 = 0;
-        if (d != 0.0f) {
-            q0 = quant_one(x0, d);
-            q1 = quant_one(x1, d);
-        }
-        int s = q0 + q1;
+        for (int u = 0; u < 2; ++u) {
+            const long long wi = w + u * stride;
+            if (wi >= total)
+                break;
+            const int t = static_cast<int>(wi % Mp);
+            const int sb = static_cast<int>(wi / Mp);
+            const int k0 = sb * QK_K + 8 * lane;
+            const float(&v)[8] = vv[u];
+            float a = 0.0f;
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-            s += __shfl_xor_sync(0xffffffffu, s, o);
+            for (int i = 0; i < 8; ++i)
+                a = fmaxf(a, fabsf(v[i]));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const float d = __fdiv_rn(a, 127.0f);
+            int q[8];
+            int s = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                q[i] = (d != 0.0f) ? quant_one(v[i], d) : 0;
+                s += q[i];
+            }
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
 
-        const int mt = t / TILE_ROWS, r = t % TILE_ROWS;
-        uint8_t* tile = reinterpret_cast<uint8_t*>(qa) + (static_cast<size_t>(mt) * nkb + kb) * TILE_BYTES;
-        const uint32_t packed = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q0))) |
-                                (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q1))) << 16);
-        *reinterpret_cast<uint32_t*>(tile + tile_byte(r, 2 * lane)) = packed;
-        if (qa8 != nullptr && t < M) {
-            int8_t* row8 = qa8 + static_cast<size_t>(t) * K;
-            const int k0 = kb * TILE_K + 2 * lane;
-            row8[small_pos(k0)] = static_cast<int8_t>(q0);
-            row8[small_pos(k0 + 1)] = static_cast<int8_t>(q1);
-        }
-        if ((lane & 15) == 0) {
-            const int c = 2 * kb + (lane >> 4);
-            scales[(static_cast<size_t>(mt) * nchunk + c) * TILE_ROWS + r] =
-                make_uint2(__float_as_uint(d), static_cast<uint32_t>(s));
-            const float ma = __fmul_rn(d, static_cast<float>(s));
-            const float hi = tf32_rna(ma);
-            const float lo = tf32_rna(__fsub_rn(ma, hi));
-            uint8_t* t0 = am + (static_cast<size_t>(mt) * (K / QK_K) + c / 8) * (2 * TF32_TILE_BYTES);
-            *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = hi;
-            *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = lo;
+            const int mt = t / TILE_ROWS, r = t % TILE_ROWS;
+            const int kb = k0 / TILE_K;
+            uint8_t* tile = reinterpret_cast<uint8_t*>(qa) + (static_cast<size_t>(mt) * nkb + kb) * TILE_BYTES;
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                h[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2 * i]))) |
+                       (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2 * i + 1]))) << 16);
+            *reinterpret_cast<uint4*>(tile + tile_byte(r, k0 % TILE_K)) = make_uint4(h[0], h[1], h[2], h[3]);
+            if (qa8 != nullptr && t < M) {
+                // small_pos order inside the 8-value group: values (0,2,4,6) then (1,3,5,7)
+                const uint32_t lo = (q[0] & 0xFF) | ((q[2] & 0xFF) << 8) | ((q[4] & 0xFF) << 16) |
+                                    (static_cast<uint32_t>(q[6] & 0xFF) << 24);
+                const uint32_t hi = (q[1] & 0xFF) | ((q[3] & 0xFF) << 8) | ((q[5] & 0xFF) << 16) |
+                                    (static_cast<uint32_t>(q[7] & 0xFF) << 24);
+                *reinterpret_cast<uint2*>(qa8 + static_cast<size_t>(t) * K + k0) = make_uint2(lo, hi);
+            }
+            if ((lane & 3) == 0) {
+                const int c = k0 / CHUNK;
+                scales[(static_cast<size_t>(mt) * nchunk + c) * TILE_ROWS + r] =
+                    make_uint2(__float_as_uint(d), static_cast<uint32_t>(s));
+                const float ma = __fmul_rn(d, static_cast<float>(s));
+                const float hi = tf32_rna(ma);
+                const float lo = tf32_rna(__fsub_rn(ma, hi));
+                uint8_t* t0 = am + (static_cast<size_t>(mt) * nsb + sb) * (2 * TF32_TILE_BYTES);
+                *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = hi;
+                *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = lo;
+            }
         }
     }
 }
@@ -113,7 +144,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
 cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales, cudaStream_t s)
 {
     const int Mp = ceil_div(M, TILE_ROWS) * TILE_ROWS;
-    const long long warps = static_cast<long long>(Mp) * (K / TILE_K);
+    const long long warps = static_cast<long long>(Mp) * (K / QK_K);
     int dev = 0, nsm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -121,14 +152,14 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
         nsm = 148;
     // 8 warps per block; up to 8 resident blocks per SM worth of grid, grid-stride beyond.
     long long blocks = (warps + 7) / 8;
-    const long long cap = static_cast<long long>(nsm) * 16;
+    const long long cap = static_cast<long long>(nsm) * 8;
     if (blocks > cap)
         blocks = cap;
-    const int vec2 = ((ldx % 2) == 0 && (reinterpret_cast<uintptr_t>(x) % 8) == 0) ? 1 : 0;
+    const int vec4 = ((ldx % 4) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0) ? 1 : 0;
     const ActPlanes ap = act_planes(M, K);
     uint8_t* sc = static_cast<uint8_t*>(scales);
     quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, M, K, ldx, Mp, vec2, static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off),
+        x, M, K, ldx, Mp, vec4, static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off),
         sc + ap.am_off, ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr);
     return cudaGetLastError();
 }
