@@ -14,36 +14,33 @@
 // hi + lo (hi*hi + hi*lo + lo*hi, relative error ~2^-21 per product).
 //
 // One CTA per SM, persistent over 128-token x 128-row tiles; 12 warps in three
-// warpgroups.  The control warpgroup gives up registers (setmaxnreg) to the two
-// promotion warpgroups:
+// warpgroups.  The control warpgroup gives up registers (setmaxnreg) so that each
+// promotion thread can keep its 64 tile accumulators, 64 super-block partial sums
+// and one 64-column chunk load in registers:
 //   warp 0      producer: cp.async.bulk copies (no multicast) of the pre-swizzled
 //               f16 operand tiles into a STAGES-deep ring, and once per super-block
 //               the token scales of its 8 chunks, the weight d, and the min-term
 //               operands (q4_K) or sub-block scales (plain-code q6_K) into an SBR
 //               ring; completion on mbarriers.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 (f16-held
-//               integer codes, f32 accumulate) into rotating 128-column chunk slots
-//               (folded codes: three slots, TMEM columns 384-511 hold the tile
-//               accumulators; plain-code q6_K: two 256-column slots) and, for q4_K
-//               after each super-block, three kind::tf32 MMAs of the min term into
-//               the next slot.
+//               integer codes, f32 accumulate) into two 256-column TMEM items that are
+//               synchronised as units: with folded codes an item is one 64-value
+//               k-block (its two chunks' accumulators side by side), so the issuing
+//               thread waits, fences and commits once per two chunks; with plain
+//               q6_K codes an item is one chunk (two 16-value sub-block
+//               accumulators).  q4_K: after each super-block, three kind::tf32 MMAs of
+//               the min term into the next item.
 //   warps 2-3   idle (they only lend their registers).
 //   warps 4-11  promotion: each owns one TMEM lane quarter (warp % 4) and 64 of the
-//               128 columns.  Folded codes: a chunk's columns are loaded into one of
-//               two register buffers while the previous chunk's FMAs run (inner +=
-//               d_a * I', packed f32x2), the slot is released as soon as its load has
-//               landed, and per super-block acc += d * inner (- the q4_K min-term
-//               slot) is read-modified-written in TMEM; store Y per tile.
-// Per-chunk scaling forces one TMEM round trip per 32-value chunk; the design keeps
-// that round trip short: slot and stage positions advance without division, slot
-// counts are compile-time, the issuing thread does nothing else, and the promotion
-// spends one packed FMA per two outputs per chunk with no shared-memory traffic
-// besides one scale per chunk.
-// Measured on GB300, the promotion's per-chunk chain (slot wait, TMEM load, release,
-// FMAs) rather than the tensor pipe sets the pace: about 650-700 SM cycles per chunk
-// against 128 for the chunk's two MMAs.  Variants that moved the MMA issue into the
-// promotion warps, or doubled the promotion warps at half the columns, measured
-// slower.
+//               128 columns; per item: wait, tcgen05.ld of its chunks, one release,
+//               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner
+//               (- the q4_K min-term item); store Y per tile.
+// Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
+// set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing
+// thread's wait + fence + commit cost about 80 cycles on top of a chunk's 128 cycles
+// of MMA even when the wait is already satisfied, so the items are made as large as
+// TMEM allows while still double-buffered (two items of 256 columns); that took the
+// q4_K 11008x4096 GEMM from about 700 to about 600 SM cycles per chunk.
 // The multi-stage rings replace the pages' one-deep double buffer and group-count
 // waits ("r45 ...", §2.2; "r58 ...", §2.2 and §6 lesson 2: one tile of lookahead
 // cannot cover the global-to-shared latency); registration-time planes remove the
@@ -75,8 +72,6 @@ constexpr int PROMO_WARP0 = 4;
 constexpr int NUM_PROMO_WARPS = 8;
 constexpr int COLS_PER_WARP = BN / 2;   // 64
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t FOLDED_SLOTS = 3;               // folded codes: 3 chunk slots of BN columns ...
-constexpr uint32_t ACC_COL = FOLDED_SLOTS * BN;    // ... and the tile accumulators in columns [384, 512)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // Register split: the launch gives every thread LAUNCH_REGS; the control warpgroup
 // drops to CTRL_REGS and the two promotion warpgroups grow to PROMO_REGS out of the
@@ -214,150 +209,6 @@ struct RingPos {
     }
 };
 
-// Promotion of folded codes into Y.  Per super-block: each chunk's 64 columns are
-// loaded from their TMEM slot into one of two register buffers while the FMAs of
-// the previous chunk run (inner += d_a * I'), the slot is released as soon as its
-// load has landed, and at the end acc += d * inner (- the q4_K min-term slot) is
-// read, updated and written back in TMEM columns [ACC_COL, 512) of this thread's
-// lane: the tile accumulators live in TMEM so that the registers can hold two
-// chunk buffers.
-template <int TYPE>
-__device__ __forceinline__ void promote_folded(const GemmArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
-                                               int warp, int lane)
-{
-    constexpr bool Q4 = (TYPE == 12);
-    constexpr uint32_t SLOT_COLS = BN;
-    const int nsb = g.id / QK_K;
-    const int num_tiles = g.num_m * g.num_n;
-    auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
-    const int pw = warp - PROMO_WARP0;              // 0..7
-    const int q = warp & 3;                          // TMEM lane quarter this warp may read
-    const int hc = pw >> 2;                          // which 64 of the 128 columns
-    const int row_in_tile = q * 32 + lane;
-    const uint32_t col_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + hc * COLS_PER_WARP;
-    const uint32_t acc_t = col_base + ACC_COL;
-    RingPos<FOLDED_SLOTS> slot;
-    RingPos<SBR> sb;
-    auto release = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(bar(BAR_TEMPTY + slot.i));
-        slot.next();
-    };
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m = tile % g.num_m, n = tile / g.num_m;
-        const int row = m * BM + row_in_tile;
-        const int jb = n * BN + hc * COLS_PER_WARP;
-        for (int s = 0; s < nsb; ++s) {
-            const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
-            if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph)) {
-                ok = false;
-                break;
-            }
-            const uint2* tsc = reinterpret_cast<const uint2*>(sbe + SB_AS_OFF);
-            float2 inner[COLS_PER_WARP / 2];
-#pragma unroll
-            for (int i = 0; i < COLS_PER_WARP / 2; ++i)
-                inner[i] = make_float2(0.0f, 0.0f);
-            uint32_t bufA[COLS_PER_WARP], bufB[COLS_PER_WARP];
-            if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            tmem_ld64_issue(col_base + slot.i * SLOT_COLS, bufA);
-            tmem_wait_ld_tied(bufA, inner);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                uint32_t(&cur)[COLS_PER_WARP] = (k & 1) ? bufB : bufA;
-                uint32_t(&nxt)[COLS_PER_WARP] = (k & 1) ? bufA : bufB;
-                release();                               // chunk k is in registers
-                if (k < 7) {
-                    if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    tmem_ld64_issue(col_base + slot.i * SLOT_COLS, nxt);
-                }
-                const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
-                const float2 da2 = make_float2(da, da);
-#pragma unroll
-                for (int i = 0; i < COLS_PER_WARP / 2; ++i)
-                    inner[i] = ffma2(da2, make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])),
-                                     inner[i]);
-                if (k < 7)
-                    tmem_wait_ld_tied(nxt, inner);
-            }
-            if (!ok)
-                break;
-            // bufB held chunk 7; bufA takes the q4_K min-term slot, bufB the accumulators.
-            if (Q4) {
-                if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_ld64_issue(col_base + slot.i * SLOT_COLS, bufA);
-                tmem_wait_ld_tied(bufA, inner);
-                release();
-            }
-            if (s > 0) {
-                tmem_ld64_issue(acc_t, bufB);
-                tmem_wait_ld_tied(bufB, inner);
-            }
-            const float4* d4 = reinterpret_cast<const float4*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 4);
-#pragma unroll
-            for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
-                const float4 dv = d4[i];
-                float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
-                if (s > 0) {
-                    a0 = make_float2(__uint_as_float(bufB[4 * i]), __uint_as_float(bufB[4 * i + 1]));
-                    a1 = make_float2(__uint_as_float(bufB[4 * i + 2]), __uint_as_float(bufB[4 * i + 3]));
-                }
-                if (Q4) {
-                    a0 = ffma2(make_float2(-1.0f, -1.0f),
-                               make_float2(__uint_as_float(bufA[4 * i]), __uint_as_float(bufA[4 * i + 1])), a0);
-                    a1 = ffma2(make_float2(-1.0f, -1.0f),
-                               make_float2(__uint_as_float(bufA[4 * i + 2]), __uint_as_float(bufA[4 * i + 3])), a1);
-                }
-                a0 = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
-                a1 = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
-                bufB[4 * i] = __float_as_uint(a0.x);
-                bufB[4 * i + 1] = __float_as_uint(a0.y);
-                bufB[4 * i + 2] = __float_as_uint(a1.x);
-                bufB[4 * i + 3] = __float_as_uint(a1.y);
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(BAR_SBEMPTY + sb.i));
-            sb.next();
-            if (s + 1 < nsb) {
-                tmem_st64(acc_t, bufB);
-                tmem_wait_st();
-            } else if (row < g.M) {
-                float* yrow = g.out + static_cast<size_t>(row) * g.ldy;
-#pragma unroll
-                for (int i = 0; i < COLS_PER_WARP; i += 4) {
-                    const int j = jb + i;
-                    const float v[4] = {__uint_as_float(bufB[i]), __uint_as_float(bufB[i + 1]),
-                                        __uint_as_float(bufB[i + 2]), __uint_as_float(bufB[i + 3])};
-                    if (g.vec_store && j + 3 < g.od) {
-                        *reinterpret_cast<float4*>(yrow + j) = make_float4(v[0], v[1], v[2], v[3]);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            if (j + k < g.od)
-                                yrow[j + k] = v[k];
-                    }
-                }
-            }
-        }
-    }
-}
-
 // The three roles of one CTA.  TYPE 12 = q4_K, 14 = q6_K; MODE GEMM_Y or GEMM_DOTS;
 // FOLDED = the codes carry the integer sub-block scale (one accumulator per chunk).
 template <int TYPE, int MODE, bool FOLDED>
@@ -365,8 +216,11 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                                            int warp, int lane)
 {
     constexpr bool Q4 = (TYPE == 12);
-    constexpr uint32_t NSLOT = FOLDED ? FOLDED_SLOTS : 2u;   // TMEM chunk slots
-    constexpr uint32_t SLOT_COLS = FOLDED ? BN : 2 * BN;     // plain q6_K codes: two sub-block accumulators
+    // TMEM holds two 256-column items, synchronised as units: folded codes, one 64-value
+    // k-block (its two chunks' accumulators side by side); plain q6_K codes, one chunk
+    // (its two 16-value sub-block accumulators side by side); q4_K's min term takes an
+    // item of its own per super-block.
+    constexpr uint32_t ITEM_COLS = 2 * BN;
     const int nkb = g.id / BK;
     const int nchunk = g.id / CHUNK;
     const int nsb = g.id / QK_K;
@@ -442,7 +296,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_t = idesc_tf32_f32(BM, BN);
             RingPos<STAGES> op;
-            RingPos<NSLOT> slot;
+            RingPos<2> item;
             RingPos<SBR> sb;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
@@ -451,38 +305,49 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
                     const uint64_t a0 = sdesc_k_sw128(sbase + SMEM_A + op.i * TILE_BYTES);
                     const uint64_t b0 = sdesc_k_sw128(sbase + SMEM_B + op.i * TILE_BYTES);
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        if (!ctl_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u)) {
+                    // K advance inside the 128-byte swizzled rows: 32 bytes per 16 values
+                    // (the descriptor's address field counts 16-byte units).
+                    if (FOLDED) {
+                        // one item per k-block: one wait, one fence, one commit for two chunks
+                        if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d = tmem_base + slot.i * SLOT_COLS;
-                        // K advance inside the 128-byte swizzled rows: 32 bytes per 16 values
-                        // (the descriptor's address field counts 16-byte units).
-                        const uint64_t ak = a0 + static_cast<uint64_t>(4 * cc);
-                        const uint64_t bk = b0 + static_cast<uint64_t>(4 * cc);
-                        umma_f16(d, ak, bk, idesc, 0u);
-                        if (FOLDED)
-                            umma_f16(d, ak + 2, bk + 2, idesc, 1u);
-                        else
-                            umma_f16(d + BN, ak + 2, bk + 2, idesc, 0u);
-                        umma_commit(bar(BAR_TFULL + slot.i));
-                        slot.next();
+                        const uint32_t d = tmem_base + item.i * ITEM_COLS;
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            umma_f16(d + cc * BN, a0 + 4u * cc, b0 + 4u * cc, idesc, 0u);
+                            umma_f16(d + cc * BN, a0 + 4u * cc + 2, b0 + 4u * cc + 2, idesc, 1u);
+                        }
+                        umma_commit(bar(BAR_TFULL + item.i));
+                        item.next();
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t d = tmem_base + item.i * ITEM_COLS;
+                            umma_f16(d, a0 + 4u * cc, b0 + 4u * cc, idesc, 0u);
+                            umma_f16(d + BN, a0 + 4u * cc + 2, b0 + 4u * cc + 2, idesc, 0u);
+                            umma_commit(bar(BAR_TFULL + item.i));
+                            item.next();
+                        }
+                        if (!ok)
+                            break;
                     }
-                    if (!ok)
-                        break;
                     umma_commit(bar(BAR_EMPTY + op.i));  // operand stage free once these MMAs finish
                     op.next();
                     if (Q4 && (kb & 3) == 3) {
                         // Min-term contraction of this super-block (8 chunks, hi/lo split) into
-                        // the next chunk slot, consumed by the promotion like a chunk.
+                        // the next item, consumed by the promotion like a chunk.
                         if (!ctl_wait(bar(BAR_SBFULL + sb.i), sb.ph) ||
-                            !ctl_wait(bar(BAR_TEMPTY + slot.i), slot.ph ^ 1u)) {
+                            !ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -491,13 +356,13 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         const uint32_t bm = am + SB_AM_BYTES;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
-                        const uint32_t d = tmem_base + slot.i * SLOT_COLS;
+                        const uint32_t d = tmem_base + item.i * ITEM_COLS;
                         umma_tf32(d, ahi, bhi, idesc_t, 0u);
                         umma_tf32(d, ahi, blo, idesc_t, 1u);
                         umma_tf32(d, alo, bhi, idesc_t, 1u);
-                        umma_commit(bar(BAR_TFULL + slot.i));
+                        umma_commit(bar(BAR_TFULL + item.i));
                         umma_commit(bar(BAR_SBEMPTY + sb.i));
-                        slot.next();
+                        item.next();
                         sb.next();
                     }
                 }
@@ -511,17 +376,20 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
 
     // ---------------------------------------------------------------- promotion
     regs_grow<PROMO_REGS>();
-    if constexpr (FOLDED && MODE == GEMM_Y) {
-        promote_folded<TYPE>(g, smem, sbase, tmem_base, warp, lane);
-        return;
-    }
     const int pw = warp - PROMO_WARP0;              // 0..7
     const int q = warp & 3;                          // TMEM lane quarter this warp may read
     const int hc = pw >> 2;                          // which 64 of the 128 columns
     const int row_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    RingPos<NSLOT> slot;
+    RingPos<2> item;
     RingPos<SBR> sb;
+    auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar(BAR_TEMPTY + item.i));
+        item.next();
+    };
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const int m = tile % g.num_m, n = tile / g.num_m;
@@ -542,25 +410,25 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
 #pragma unroll
             for (int i = 0; i < COLS_PER_WARP / 2; ++i)
                 inner[i] = make_float2(0.0f, 0.0f);
-            {
-                for (int k = 0; k < 8; ++k) {
-                    const int c = 8 * s + k;                    // chunk index along id
-                    const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
-                    const float2 da2 = make_float2(da, da);
-                    if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
+            for (int k2 = 0; k2 < 4 && ok; ++k2) {             // the super-block's four k-blocks
+                if (FOLDED) {
+                    if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t col0 = lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP;
-                    if (FOLDED) {
+                    const uint32_t col0 = lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP;
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int k = 2 * k2 + cc;
+                        const int c = 8 * s + k;                // chunk index along id
                         float I[COLS_PER_WARP];
-                        tmem_ld64_wait(col0, I);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar(BAR_TEMPTY + slot.i));
+                        tmem_ld64_wait(col0 + cc * BN, I);
+                        if (cc == 1)
+                            release();                          // both chunks are in registers
                         if (MODE == GEMM_Y) {
+                            const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
+                            const float2 da2 = make_float2(da, da);
 #pragma unroll
                             for (int i = 0; i < COLS_PER_WARP / 2; ++i)
                                 inner[i] = ffma2(da2, make_float2(I[2 * i], I[2 * i + 1]), inner[i]);
@@ -572,21 +440,29 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                                     g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] = I[i];
                             }
                         }
-                    } else {
-                        // q6_K with plain codes: one accumulator per 16-value sub-block,
-                        // I' = sc0 * I_0 + sc1 * I_1 (exact: |I'| < 2^24).
-                        const float* scp = reinterpret_cast<const float*>(sbe + SB_X_OFF);
+                    }
+                } else {
+                    // q6_K with plain codes: one item per chunk, one accumulator per 16-value
+                    // sub-block, I' = sc0 * I_0 + sc1 * I_1 (exact: |I'| < 2^24).
+                    const float* scp = reinterpret_cast<const float*>(sbe + SB_X_OFF);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int k = 2 * k2 + cc;
+                        const int c = 8 * s + k;
+                        const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
+                        const float2 da2 = make_float2(da, da);
                         const int s0 = 2 * k;
+                        if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t col0 = lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP;
 #pragma unroll
                         for (int p = 0; p < COLS_PER_WARP / 8; ++p) {
                             float h0[8], h1[8];
                             tmem_ld8x2_wait(col0 + p * 8, col0 + BN + p * 8, h0, h1);
-                            if (p == COLS_PER_WARP / 8 - 1) {
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0)
-                                    mbar_arrive(bar(BAR_TEMPTY + slot.i));
-                            }
+                            if (p == COLS_PER_WARP / 8 - 1)
+                                release();
                             if (MODE == GEMM_DOTS) {
                                 if (row < g.M) {
 #pragma unroll
@@ -611,27 +487,22 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                             }
                         }
                     }
-                    slot.next();
                 }
-                if (!ok)
-                    break;
             }
+            if (!ok)
+                break;
             // acc += d * inner  (d per weight row of this super-block); q4_K also
-            // subtracts the super-block's min term, delivered through the next slot.
+            // subtracts the super-block's min term, delivered through the next item.
             const float4* d4 = reinterpret_cast<const float4*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 4);
             if (Q4) {
-                if (!warp_wait(bar(BAR_TFULL + slot.i), slot.ph)) {
+                if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float mn[COLS_PER_WARP];
-                tmem_ld64_wait(lane_addr + slot.i * SLOT_COLS + hc * COLS_PER_WARP, mn);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(BAR_TEMPTY + slot.i));
-                slot.next();
+                tmem_ld64_wait(lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP, mn);
+                release();
                 if (MODE == GEMM_Y) {
 #pragma unroll
                     for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
