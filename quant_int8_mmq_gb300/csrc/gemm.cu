@@ -19,22 +19,25 @@
 // and one 64-column chunk load in registers:
 //   warp 0      producer: cp.async.bulk copies (no multicast) of the pre-swizzled
 //               f16 operand tiles into a STAGES-deep ring, and once per super-block
-//               the token scales of its 8 chunks, the weight d, and the min-term
-//               operands (q4_K) or sub-block scales (plain-code q6_K) into an SBR
-//               ring; completion on mbarriers.
+//               the token scales of its 8 chunks, the weight d and (plain-code q6_K)
+//               the sub-block scales into an SBR ring; for q4_K, after a tile's last
+//               k-block, the min-term operands of every super-block through the
+//               operand ring; completion on mbarriers.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 (f16-held
 //               integer codes, f32 accumulate) into two 256-column TMEM items that are
 //               synchronised as units: with folded codes an item is one 64-value
 //               k-block (its two chunks' accumulators side by side), so the issuing
 //               thread waits, fences and commits once per two chunks; with plain
 //               q6_K codes an item is one chunk (two 16-value sub-block
-//               accumulators).  q4_K: after each super-block, three kind::tf32 MMAs of
-//               the min term into the next item.
+//               accumulators).  q4_K: the min term sum_c (d_a*ssum)(dmin*m) carries
+//               no per-super-block factor, so it is one kind::tf32 contraction per
+//               tile (three MMAs per super-block, hi/lo split) into one item after the
+//               tile's last k-block.
 //   warps 2-3   idle (they only lend their registers).
 //   warps 4-11  promotion: each owns one TMEM lane quarter (warp % 4) and 64 of the
 //               128 columns; per item: wait, tcgen05.ld of its chunks, one release,
-//               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner
-//               (- the q4_K min-term item); store Y per tile.
+//               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner;
+//               per tile acc -= the q4_K min-term item; store Y.
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
 // set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing
 // thread's wait + fence + commit cost about 80 cycles on top of a chunk's 128 cycles
@@ -88,11 +91,13 @@ constexpr int SB_SBD_BYTES = BN * 4;
 constexpr int SB_AS_OFF = SB_SBD_OFF + SB_SBD_BYTES;
 constexpr int SB_AS_BYTES = 8 * BM * 8;            // {d, ssum} x 8 chunks x 128 tokens
 constexpr int SB_X_OFF = SB_AS_OFF + SB_AS_BYTES;
-constexpr int SB_AM_BYTES = 2 * TF32_TILE_BYTES;   // q4_K: token min-term operand hi, lo
-constexpr int SB_BM_BYTES = 2 * TF32_TILE_BYTES;   // q4_K: weight min-term operand hi, lo
-constexpr int SB_SC_BYTES = 16 * BN * 4;           // q6_K: sub-block scales
-constexpr int SB_BYTES = SB_X_OFF + SB_AM_BYTES + SB_BM_BYTES;
-static_assert(SB_BYTES >= SB_X_OFF + SB_SC_BYTES, "super-block entry");
+constexpr int SB_SC_BYTES = 16 * BN * 4;           // plain-code q6_K: sub-block scales
+constexpr int SB_BYTES = SB_X_OFF + SB_SC_BYTES;
+// q4_K min-term operands per super-block (token hi, lo tiles; weight hi, lo tiles),
+// streamed through the operand ring after a tile's last k-block.
+constexpr int MIN_AM_BYTES = 2 * TF32_TILE_BYTES;
+constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;
+static_assert(MIN_AM_BYTES <= TILE_BYTES && MIN_BM_BYTES <= TILE_BYTES, "min-term operands fit a stage");
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * TILE_BYTES;
@@ -236,8 +241,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             RingPos<STAGES> op;
             RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sb = 0;  // fills issued on each ring
-            constexpr uint32_t sb_tx =
-                SB_SBD_BYTES + SB_AS_BYTES + (Q4 ? (SB_AM_BYTES + SB_BM_BYTES) : (FOLDED ? 0 : SB_SC_BYTES));
+            constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int m = tile % g.num_m, n = tile / g.num_m;
@@ -260,12 +264,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         bulk_g2s(dst + SB_SBD_OFF, g.SBD + (static_cast<size_t>(n) * nsb + s) * SB_SBD_BYTES,
                                  SB_SBD_BYTES, fb);
                         bulk_g2s(dst + SB_AS_OFF, ASb + static_cast<size_t>(s) * SB_AS_BYTES, SB_AS_BYTES, fb);
-                        if (Q4) {
-                            bulk_g2s(dst + SB_X_OFF, g.AM + (static_cast<size_t>(m) * nsb + s) * SB_AM_BYTES,
-                                     SB_AM_BYTES, fb);
-                            bulk_g2s(dst + SB_X_OFF + SB_AM_BYTES,
-                                     g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_BM_BYTES, SB_BM_BYTES, fb);
-                        } else if (!FOLDED) {
+                        if (!FOLDED) {
                             bulk_g2s(dst + SB_X_OFF, g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_SC_BYTES,
                                      SB_SC_BYTES, fb);
                         }
@@ -285,6 +284,24 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     op.next();
                     ++n_ops;
                 }
+                if (Q4 && ok) {
+                    // The tile's min-term operands, one super-block per stage: token hi/lo
+                    // tiles in the A slot, weight hi/lo tiles in the B slot.
+                    for (int s = 0; s < nsb; ++s) {
+                        if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fo = bar(BAR_FULL + op.i);
+                        mbar_arrive_expect_tx(fo, MIN_AM_BYTES + MIN_BM_BYTES);
+                        bulk_g2s(sbase + SMEM_A + op.i * TILE_BYTES,
+                                 g.AM + (static_cast<size_t>(m) * nsb + s) * MIN_AM_BYTES, MIN_AM_BYTES, fo);
+                        bulk_g2s(sbase + SMEM_B + op.i * TILE_BYTES,
+                                 g.AUX + (static_cast<size_t>(n) * nsb + s) * MIN_BM_BYTES, MIN_BM_BYTES, fo);
+                        op.next();
+                        ++n_ops;
+                    }
+                }
             }
             // Our copies must have landed before the CTA may exit.
             for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i)
@@ -297,7 +314,6 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             constexpr uint32_t idesc_t = idesc_tf32_f32(BM, BN);
             RingPos<STAGES> op;
             RingPos<2> item;
-            RingPos<SBR> sb;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -343,28 +359,36 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     }
                     umma_commit(bar(BAR_EMPTY + op.i));  // operand stage free once these MMAs finish
                     op.next();
-                    if (Q4 && (kb & 3) == 3) {
-                        // Min-term contraction of this super-block (8 chunks, hi/lo split) into
-                        // the next item, consumed by the promotion like a chunk.
-                        if (!ctl_wait(bar(BAR_SBFULL + sb.i), sb.ph) ||
-                            !ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                }
+                if (Q4 && ok) {
+                    // Min-term contraction of the whole tile, sum over chunks of
+                    // (d_a*ssum)(dmin*m), one super-block (8 chunks, hi/lo split) per stage
+                    // into one item, consumed by the promotion once per tile.
+                    if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t d = tmem_base + item.i * ITEM_COLS;
+                    for (int s = 0; s < nsb; ++s) {
+                        if (!ctl_wait(bar(BAR_FULL + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t am = sbase + SMEM_SB + sb.i * SB_BYTES + SB_X_OFF;
-                        const uint32_t bm = am + SB_AM_BYTES;
+                        const uint32_t am = sbase + SMEM_A + op.i * TILE_BYTES;
+                        const uint32_t bm = sbase + SMEM_B + op.i * TILE_BYTES;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
-                        const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                        umma_tf32(d, ahi, bhi, idesc_t, 0u);
+                        umma_tf32(d, ahi, bhi, idesc_t, s > 0 ? 1u : 0u);
                         umma_tf32(d, ahi, blo, idesc_t, 1u);
                         umma_tf32(d, alo, bhi, idesc_t, 1u);
-                        umma_commit(bar(BAR_TFULL + item.i));
-                        umma_commit(bar(BAR_SBEMPTY + sb.i));
-                        item.next();
-                        sb.next();
+                        umma_commit(bar(BAR_EMPTY + op.i));
+                        op.next();
                     }
+                    if (!ok)
+                        break;
+                    umma_commit(bar(BAR_TFULL + item.i));
+                    item.next();
                 }
             }
             umma_commit(bar(BAR_DRAIN));  // every MMA issued so far has completed
@@ -491,31 +515,9 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             }
             if (!ok)
                 break;
-            // acc += d * inner  (d per weight row of this super-block); q4_K also
-            // subtracts the super-block's min term, delivered through the next item.
-            const float4* d4 = reinterpret_cast<const float4*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 4);
-            if (Q4) {
-                if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float mn[COLS_PER_WARP];
-                tmem_ld64_wait(lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP, mn);
-                release();
-                if (MODE == GEMM_Y) {
-#pragma unroll
-                    for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
-                        const float4 dv = d4[i];
-                        const float2 a0 =
-                            ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i], mn[4 * i + 1]), acc[2 * i]);
-                        const float2 a1 =
-                            ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[4 * i + 2], mn[4 * i + 3]), acc[2 * i + 1]);
-                        acc[2 * i] = ffma2(make_float2(dv.x, dv.y), inner[2 * i], a0);
-                        acc[2 * i + 1] = ffma2(make_float2(dv.z, dv.w), inner[2 * i + 1], a1);
-                    }
-                }
-            } else if (MODE == GEMM_Y) {
+            // acc += d * inner  (d per weight row of this super-block)
+            if (MODE == GEMM_Y) {
+                const float4* d4 = reinterpret_cast<const float4*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 4);
 #pragma unroll
                 for (int i = 0; i < COLS_PER_WARP / 4; ++i) {
                     const float4 dv = d4[i];
@@ -530,6 +532,22 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
         }
         if (!ok)
             break;
+        if (Q4) {
+            // acc -= the tile's min term, one item per tile
+            if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float mn[COLS_PER_WARP];
+            tmem_ld64_wait(lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP, mn);
+            release();
+            if (MODE == GEMM_Y) {
+#pragma unroll
+                for (int i = 0; i < COLS_PER_WARP / 2; ++i)
+                    acc[i] = ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[2 * i], mn[2 * i + 1]), acc[i]);
+            }
+        }
         if (MODE == GEMM_Y && row < g.M) {
             float* yrow = g.out + static_cast<size_t>(row) * g.ldy;
 #pragma unroll
@@ -569,7 +587,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
         }
         for (int s = 0; s < SBR; ++s) {
             mbar_init(bar(BAR_SBFULL + s), 1);
-            mbar_init(bar(BAR_SBEMPTY + s), NUM_PROMO_WARPS + (TYPE == 12 ? 1 : 0));
+            mbar_init(bar(BAR_SBEMPTY + s), NUM_PROMO_WARPS);
         }
         for (int k = 0; k < 4; ++k) {
             mbar_init(bar(BAR_TFULL + k), 1);
