@@ -37,7 +37,8 @@
 //   warps 4-11  promotion: each owns one TMEM lane quarter (warp % 4) and 64 of the
 //               128 columns; per item: wait, tcgen05.ld of its chunks, one release,
 //               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner;
-//               per tile acc -= the q4_K min-term item; store Y.
+//               per tile acc -= the q4_K min-term item; store Y (or, for the two
+//               K-halves of a last-round tile, add into a zeroed Y).
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
 // set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing
 // thread's wait + fence + commit cost about 80 cycles on top of a chunk's 128 cycles
@@ -131,6 +132,9 @@ struct GemmArgs {
     int ldy;
     int M, od, id;
     int num_m, num_n;
+    int units;            // work units of the launch (see unit_of)
+    int full_units;       // units below this are whole tiles
+    int nsb_half;         // split units: super-blocks [0, nsb_half) and [nsb_half, nsb)
     int vec_store;        // Y is 16-byte aligned and ldy % 4 == 0
 };
 
@@ -201,6 +205,36 @@ __device__ __forceinline__ void regs_shrink()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
 }
 
+// Work unit u of a launch: tile (m, n) and its super-block range [sb0, sb1).  Units
+// below full_units are whole tiles, taken in order; each later pair of units is the
+// two K-halves of one tile of the last round, whose partial sums are added into a
+// zeroed Y (two addends: the order cannot change the sum).  Splitting the last
+// round's tiles keeps SMs busy that would otherwise idle while it runs.
+struct Unit {
+    int m, n, sb0, sb1;
+    bool half;
+};
+__device__ __forceinline__ Unit unit_of(const GemmArgs& g, int u, int nsb)
+{
+    Unit w;
+    int tile;
+    if (u < g.full_units) {
+        tile = u;
+        w.sb0 = 0;
+        w.sb1 = nsb;
+        w.half = false;
+    } else {
+        const int v = u - g.full_units;
+        tile = g.full_units + (v >> 1);
+        w.half = true;
+        w.sb0 = (v & 1) ? g.nsb_half : 0;
+        w.sb1 = (v & 1) ? nsb : g.nsb_half;
+    }
+    w.m = tile % g.num_m;
+    w.n = tile / g.num_m;
+    return w;
+}
+
 // Position in a ring of N entries: entry index and the phase parity of its barriers.
 template <uint32_t N>
 struct RingPos {
@@ -229,7 +263,6 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
     const int nkb = g.id / BK;
     const int nchunk = g.id / CHUNK;
     const int nsb = g.id / QK_K;
-    const int num_tiles = g.num_m * g.num_n;
     auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
 
     if (warp < PROMO_WARP0) {
@@ -243,12 +276,13 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             uint32_t n_ops = 0, n_sb = 0;  // fills issued on each ring
             constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m = tile % g.num_m, n = tile / g.num_m;
+            for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
+                const Unit w = unit_of(g, u, nsb);
+                const int m = w.m, n = w.n;
                 const uint8_t* Ab = g.A + static_cast<size_t>(m) * nkb * TILE_BYTES;
                 const uint8_t* Bb = g.B + static_cast<size_t>(n) * nkb * TILE_BYTES;
                 const uint8_t* ASb = g.AS + static_cast<size_t>(m) * nchunk * BM * 8;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {  // a new super-block
                         const int s = kb >> 2;
                         if (!ctl_wait(bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
@@ -287,7 +321,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 if (Q4 && ok) {
                     // The tile's min-term operands, one super-block per stage: token hi/lo
                     // tiles in the A slot, weight hi/lo tiles in the B slot.
-                    for (int s = 0; s < nsb; ++s) {
+                    for (int s = w.sb0; s < w.sb1; ++s) {
                         if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                             ok = false;
                             break;
@@ -315,8 +349,9 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             RingPos<STAGES> op;
             RingPos<2> item;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int kb = 0; kb < nkb; ++kb) {
+            for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
+                const Unit w = unit_of(g, u, nsb);
+                for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if (!ctl_wait(bar(BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
@@ -369,7 +404,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                    for (int s = 0; s < nsb; ++s) {
+                    for (int s = w.sb0; s < w.sb1; ++s) {
                         if (!ctl_wait(bar(BAR_FULL + op.i), op.ph)) {
                             ok = false;
                             break;
@@ -379,7 +414,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         const uint32_t bm = sbase + SMEM_B + op.i * TILE_BYTES;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
-                        umma_tf32(d, ahi, bhi, idesc_t, s > 0 ? 1u : 0u);
+                        umma_tf32(d, ahi, bhi, idesc_t, s > w.sb0 ? 1u : 0u);
                         umma_tf32(d, ahi, blo, idesc_t, 1u);
                         umma_tf32(d, alo, bhi, idesc_t, 1u);
                         umma_commit(bar(BAR_EMPTY + op.i));
@@ -415,15 +450,16 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
         item.next();
     };
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m = tile % g.num_m, n = tile / g.num_m;
+    for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
+        const Unit w = unit_of(g, u, nsb);
+        const int m = w.m, n = w.n;
         const int row = m * BM + row_in_tile;
         const int jb = n * BN + hc * COLS_PER_WARP;
         float2 acc[COLS_PER_WARP / 2];
 #pragma unroll
         for (int i = 0; i < COLS_PER_WARP / 2; ++i)
             acc[i] = make_float2(0.0f, 0.0f);
-        for (int s = 0; s < nsb; ++s) {
+        for (int s = w.sb0; s < w.sb1; ++s) {
             const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
             if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph)) {
                 ok = false;
@@ -554,7 +590,19 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             for (int i = 0; i < COLS_PER_WARP; i += 4) {
                 const int j = jb + i;
                 const float2 lo = acc[i / 2], hi = acc[i / 2 + 1];
-                if (g.vec_store && j + 3 < g.od) {
+                if (w.half) {
+                    if (g.vec_store && j + 3 < g.od) {
+                        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(yrow + j), "f"(lo.x),
+                                     "f"(lo.y), "f"(hi.x), "f"(hi.y)
+                                     : "memory");
+                    } else {
+                        const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if (j + k < g.od)
+                                atomicAdd(yrow + j + k, v[k]);
+                    }
+                } else if (g.vec_store && j + 3 < g.od) {
                     *reinterpret_cast<float4*>(yrow + j) = make_float4(lo.x, lo.y, hi.x, hi.y);
                 } else {
                     const float v[4] = {lo.x, lo.y, hi.x, hi.y};
@@ -625,6 +673,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
     }
 }
 
+// Zeroes Y over the tiles [first, first + count) of a launch (rows < M, columns < od).
+__global__ void __launch_bounds__(256) zero_tiles_kernel(float* __restrict__ Y, int ldy, int M, int od, int num_m,
+                                                         int first)
+{
+    const int tile = first + blockIdx.x;
+    const int m = tile % num_m, n = tile / num_m;
+    const int r_end = min(BM, M - m * BM), c_end = min(BN, od - n * BN);
+    for (int e = threadIdx.x; e < BM * BN; e += blockDim.x) {
+        const int r = e / BN, c = e % BN;
+        if (r < r_end && c < c_end)
+            Y[static_cast<size_t>(m * BM + r) * ldy + n * BN + c] = 0.0f;
+    }
+}
+
 template <int TYPE, int MODE>
 cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
 {
@@ -687,6 +749,21 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
         return e;
     const int tiles = a.num_m * a.num_n;
     const int grid = tiles < nsm ? tiles : nsm;
+    a.units = tiles;
+    a.full_units = tiles;
+    a.nsb_half = 0;
+    const int rem = tiles % grid;
+    const int nsb = id / QK_K;
+    if (mode == GEMM_Y && tiles > grid && rem > 0 && 2 * rem <= grid && nsb >= 2) {
+        // the last round has `rem` tiles for `grid` CTAs: run each as two K-halves
+        a.full_units = tiles - rem;
+        a.units = a.full_units + 2 * rem;
+        a.nsb_half = nsb / 2;
+        zero_tiles_kernel<<<rem, 256, 0, s>>>(out, ldy, M, od, a.num_m, a.full_units);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
 
     if (type == 14) {
         if (path_label)

@@ -351,6 +351,28 @@ def test_gemm_deterministic():
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+# --------------------------------------------------------------------------- last-round K split
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
+def test_gemm_last_round_split_parity(typ):
+    """160 tiles on 152 SMs: the 8 tiles of the last round run as two K-halves that add
+    into a zeroed Y (odd super-block count: halves of 1 and 2 super-blocks)."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    M, od, id_ = 1024, 2560, 768
+    raw = _q6_raw(od, id_, 41, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, 41)
+    x = synth.activations(M, id_, 42)
+    Y = _run_gemm(t, raw, x).cpu().numpy()
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+def test_gemm_last_round_split_deterministic():
+    raw = synth.q4k_blocks(2560, 512, 43)
+    x = synth.activations(1024, 512, 44)
+    a = _run_gemm("q4_K", raw, x).cpu().numpy()
+    b = _run_gemm("q4_K", raw, x).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
 # --------------------------------------------------------------------------- weight-streaming path (M <= 8)
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
