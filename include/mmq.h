@@ -201,6 +201,11 @@ const char* mmq_status_string(mmq_status st);
  * cannot show it ran). */
 const char* mmq_last_path(void);
 
+/* Number of kernel launches the library has made in this process (every entry
+ * point that launches adds the kernels it launched: prepass 1, repack 3 or 4,
+ * GEMM 1, or 2 when the last round's tiles are split and first zeroed). */
+unsigned long long mmq_launch_count(void);
+
 /* Library version string. */
 const char* mmq_version(void);
 

@@ -22,7 +22,7 @@ __all__ = [
     "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_quantize_act", "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
     "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_get_device_error",
-    "mmq_status_string", "mmq_last_path", "mmq_version",
+    "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
     "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
 ]
 
@@ -152,6 +152,13 @@ def mmq_get_device_error(stream=0) -> int:
 
 def mmq_status_string(st: int) -> str:
     return load().mmq_status_string(st).decode()
+
+
+def mmq_launch_count():
+    """Kernel launches the library has made in this process."""
+    lib = load()
+    lib.mmq_launch_count.restype = ctypes.c_ulonglong
+    return int(lib.mmq_launch_count())
 
 
 def mmq_last_path() -> str:

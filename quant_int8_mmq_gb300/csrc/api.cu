@@ -10,6 +10,13 @@
 #include "mmq.h"
 #include "mmq_internal.h"
 
+namespace mmq {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace mmq
+
 namespace {
 
 std::atomic<const char*> g_last_path{"none"};
@@ -201,6 +208,8 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
 {
     return gemm_common(t, mmq::GEMM_DOTS, packed, od, id, qa, scales, M, dots, od, s);
 }
+
+unsigned long long mmq_launch_count(void) { return mmq::g_launches.load(std::memory_order_relaxed); }
 
 mmq_status mmq_get_device_error(mmq_stream_t s)
 {

@@ -710,6 +710,7 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
             return e;
         attr_set_mask.fetch_or(bit);
     }
+    count_launch();
     gemm_kernel<TYPE, MODE><<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(a);
     return cudaGetLastError();
 }
@@ -759,6 +760,7 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
         a.full_units = tiles - rem;
         a.units = a.full_units + 2 * rem;
         a.nsb_half = nsb / 2;
+        count_launch();
         zero_tiles_kernel<<<rem, 256, 0, s>>>(out, ldy, M, od, a.num_m, a.full_units);
         e = cudaGetLastError();
         if (e != cudaSuccess)

@@ -211,6 +211,7 @@ cudaError_t launch_typed(const uint8_t* raw, int od, int id, const int8_t* qa8, 
 {
     constexpr int R = (MT <= 2) ? ROWS_FEW : ROWS_MANY;
     const int blocks = ceil_div(od, R);
+    count_launch();
     gemm_small_kernel<TYPE, MT, R><<<blocks, THREADS, 0, s>>>(raw, od, id, qa8, pairs, M, Y, ldy);
     return cudaGetLastError();
 }

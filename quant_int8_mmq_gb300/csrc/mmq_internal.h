@@ -109,6 +109,10 @@ inline WeightPlanes weight_planes(int type, int od, int id)
 }
 
 // ---------------------------------------------------------------- launchers
+// Every kernel launch of the library adds to one process-wide counter
+// (mmq_launch_count); count_launch is called once per launch attempt.
+void count_launch();
+
 // Each returns cudaSuccess or the launch error; arguments are already validated.
 cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales,
                                 cudaStream_t s);

@@ -244,10 +244,13 @@ cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed,
         long long sblocks = (nblocks * 16 + 255) / 256;
         if (sblocks > 4096)
             sblocks = 4096;
+        count_launch();
         q6k_scale_scan<<<static_cast<unsigned>(sblocks), 256, 0, s>>>(rb, nblocks, flag);
+        count_launch();
         pack_kernel<14><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
                                                                         sbd, base + wp.aux_off, flag);
     } else {
+        count_launch();
         pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
                                                                         sbd, base + wp.aux_off, flag);
     }
@@ -260,6 +263,7 @@ cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed,
     if (rblocks > 65535LL * 8)
         rblocks = 65535LL * 8;
     uint32_t* rout = reinterpret_cast<uint32_t*>(base + wp.raw_off);
+    count_launch();
     if (type == 14)
         raw_relayout_kernel<14><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(rb, nblocks, rout);
     else

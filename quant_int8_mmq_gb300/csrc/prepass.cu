@@ -158,6 +158,7 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
     const int vec4 = ((ldx % 4) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0) ? 1 : 0;
     const ActPlanes ap = act_planes(M, K);
     uint8_t* sc = static_cast<uint8_t*>(scales);
+    count_launch();
     quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         x, M, K, ldx, Mp, vec4, static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off),
         sc + ap.am_off, ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr);

@@ -102,6 +102,14 @@ def test_valid_calls_without_a_gpu_report_unsupported(mmq_lib):
     assert lib.mmq_gemm_q4k(p16, 8, 256, p16, p16, 4, p16, 8, None) == 6
 
 
+def test_launch_counter_counts_only_launches(mmq_lib):
+    before = mmq.mmq_launch_count()
+    lib = mmq.load()
+    p16 = 0x10000
+    assert lib.mmq_gemm_q4k(None, 8, 256, p16, p16, 4, p16, 8, None) == 1      # argument error
+    assert mmq.mmq_launch_count() == before
+
+
 def test_status_strings_and_labels(mmq_lib):
     for st in range(7):
         assert mmq.mmq_status_string(st).startswith(mmq.STATUS[st])
