@@ -37,6 +37,22 @@ __device__ __forceinline__ int quant_one(float x, float d)
     return static_cast<int>(r);
 }
 
+// The same quotient with the chunk's divisor shared: rd = 1/d correctly rounded
+// (once per chunk), then Markstein's correction step (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
+// 1990): q0 = RN(x * rd) is within one ulp of x/d, e = x - d * q0 is exact as one
+// FMA, and RN(q0 + e * rd) is the correctly rounded quotient RN(x/d) when rd =
+// RN(1/d) and nothing overflows or underflows, which the caller guarantees by using
+// this only for d in [2^-100, 2^100].  The rounding to an integer is unchanged.
+__device__ __forceinline__ int quant_one_shared(float x, float d, float rd)
+{
+    const float q0 = __fmul_rn(x, rd);
+    const float e = __fmaf_rn(-q0, d, x);
+    float r = roundf(__fmaf_rn(e, rd, q0));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
 __device__ __forceinline__ float tf32_rna(float v)
 {
     uint32_t r;
@@ -97,11 +113,13 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const float d = __fdiv_rn(a, 127.0f);
+            const bool shared = (d >= 0x1p-100f && d <= 0x1p100f);
+            const float rd = shared ? __frcp_rn(d) : 0.0f;
             int q[8];
             int s = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                q[i] = (d != 0.0f) ? quant_one(v[i], d) : 0;
+                q[i] = (d == 0.0f) ? 0 : (shared ? quant_one_shared(v[i], d, rd) : quant_one(v[i], d));
                 s += q[i];
             }
             s += __shfl_xor_sync(0xffffffffu, s, 1);

@@ -411,6 +411,22 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[64], float2 (&k)
 #undef MMQ_T64
 #undef MMQ_K2
 
+#define MMQ_T64A(i) "+r"(a[(i)])
+#define MMQ_T64B(i) "+r"(b[(i)])
+
+// Wait for this thread's outstanding TMEM loads into a and b (two loads issued
+// with tmem_ld64_issue); both arrays are tied to the wait.
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[64], uint32_t (&b)[64])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : MMQ_T64A(0), MMQ_T64A(1), MMQ_T64A(2), MMQ_T64A(3), MMQ_T64A(4), MMQ_T64A(5), MMQ_T64A(6), MMQ_T64A(7), MMQ_T64A(8), MMQ_T64A(9), MMQ_T64A(10), MMQ_T64A(11), MMQ_T64A(12), MMQ_T64A(13), MMQ_T64A(14), MMQ_T64A(15), MMQ_T64A(16), MMQ_T64A(17), MMQ_T64A(18), MMQ_T64A(19), MMQ_T64A(20), MMQ_T64A(21), MMQ_T64A(22), MMQ_T64A(23), MMQ_T64A(24), MMQ_T64A(25), MMQ_T64A(26), MMQ_T64A(27), MMQ_T64A(28), MMQ_T64A(29), MMQ_T64A(30), MMQ_T64A(31), MMQ_T64A(32), MMQ_T64A(33), MMQ_T64A(34), MMQ_T64A(35), MMQ_T64A(36), MMQ_T64A(37), MMQ_T64A(38), MMQ_T64A(39), MMQ_T64A(40), MMQ_T64A(41), MMQ_T64A(42), MMQ_T64A(43), MMQ_T64A(44), MMQ_T64A(45), MMQ_T64A(46), MMQ_T64A(47), MMQ_T64A(48), MMQ_T64A(49), MMQ_T64A(50), MMQ_T64A(51), MMQ_T64A(52), MMQ_T64A(53), MMQ_T64A(54), MMQ_T64A(55), MMQ_T64A(56), MMQ_T64A(57), MMQ_T64A(58), MMQ_T64A(59), MMQ_T64A(60), MMQ_T64A(61), MMQ_T64A(62), MMQ_T64A(63), MMQ_T64B(0), MMQ_T64B(1), MMQ_T64B(2), MMQ_T64B(3), MMQ_T64B(4), MMQ_T64B(5), MMQ_T64B(6), MMQ_T64B(7), MMQ_T64B(8), MMQ_T64B(9), MMQ_T64B(10), MMQ_T64B(11), MMQ_T64B(12), MMQ_T64B(13), MMQ_T64B(14), MMQ_T64B(15), MMQ_T64B(16), MMQ_T64B(17), MMQ_T64B(18), MMQ_T64B(19), MMQ_T64B(20), MMQ_T64B(21), MMQ_T64B(22), MMQ_T64B(23), MMQ_T64B(24), MMQ_T64B(25), MMQ_T64B(26), MMQ_T64B(27), MMQ_T64B(28), MMQ_T64B(29), MMQ_T64B(30), MMQ_T64B(31), MMQ_T64B(32), MMQ_T64B(33), MMQ_T64B(34), MMQ_T64B(35), MMQ_T64B(36), MMQ_T64B(37), MMQ_T64B(38), MMQ_T64B(39), MMQ_T64B(40), MMQ_T64B(41), MMQ_T64B(42), MMQ_T64B(43), MMQ_T64B(44), MMQ_T64B(45), MMQ_T64B(46), MMQ_T64B(47), MMQ_T64B(48), MMQ_T64B(49), MMQ_T64B(50), MMQ_T64B(51), MMQ_T64B(52), MMQ_T64B(53), MMQ_T64B(54), MMQ_T64B(55), MMQ_T64B(56), MMQ_T64B(57), MMQ_T64B(58), MMQ_T64B(59), MMQ_T64B(60), MMQ_T64B(61), MMQ_T64B(62), MMQ_T64B(63)
+                 :
+                 : "memory");
+}
+
+#undef MMQ_T64A
+#undef MMQ_T64B
+
 // 64 consecutive 32-bit columns of this thread's TMEM lane from registers (two
 // 32-column stores); tmem_wait_st() waits for them.
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64])

@@ -135,6 +135,27 @@ def test_prepass_row_stride_and_special_values():
     _check_prepass(x, ldx=520)
 
 
+def test_prepass_quotient_ties():
+    """Every chunk: one value sets amax (hence d), the other 31 sit at (k + 1/2) * d and up
+    to two ulps either side, so x/d lands on or next to a rounding tie; the codes must
+    match the oracle's IEEE division and ties-away-from-zero rounding exactly."""
+    rng = np.random.default_rng(12)
+    M, K = 64, 4096
+    nch = M * K // 32
+    amax = rng.uniform(1e-3, 1e3, nch).astype(np.float32)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    k = rng.integers(-126, 126, (nch, 31)).astype(np.float64)
+    vals = ((k + 0.5) * d[:, None].astype(np.float64)).astype(np.float32)
+    bits = vals.view(np.int32) + rng.integers(-2, 3, (nch, 31)).astype(np.int32)
+    vals = bits.view(np.float32)
+    chunks = np.concatenate([amax[:, None] * np.where(rng.random(nch) < 0.5, 1, -1)[:, None].astype(np.float32),
+                             vals], axis=1)
+    perm = rng.permuted(np.tile(np.arange(32), (nch, 1)), axis=1)
+    chunks = np.take_along_axis(chunks, perm, axis=1)
+    assert np.all(np.abs(chunks).max(axis=1) == amax)
+    _check_prepass(chunks.reshape(M, K).astype(np.float32))
+
+
 # --------------------------------------------------------------------------- pack
 def _q6_raw(od, id_, seed, full_range):
     lo, hi = (-128, 127) if full_range else (-32, 31)
