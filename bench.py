@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--peaks", action="store_true", help="run the throughput probes and print their JSON")
+    p.add_argument("--small-m-only", action="store_true",
+                   help="run only the small-M case (q6_K 4097x11008, M = 1) and print its JSON (for profiling)")
     p.add_argument("--only", default="", help="comma-separated GEMM names of the stack (e.g. l0.gate): "
                    "a small case for profiling, not a bench line")
     return p.parse_args()
@@ -299,6 +301,17 @@ def small_m_case(lib, dev, stream, sptr, peaks, typ="q6_K", od=4097, id_=11008, 
             "timing": f"one CUDA graph of {reps} launches, CUDA events around its replay"}
 
 
+def run_small_m_only():
+    import torch
+    import quant_int8_mmq_gb300 as mmq
+    lib = mmq.load()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    print(json.dumps(small_m_case(lib, dev, stream, stream.cuda_stream, measured_peaks())), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     if rank != 0:
@@ -521,6 +534,8 @@ def main():
     args = parse_args()
     if args.peaks:
         return run_peaks()
+    if args.small_m_only:
+        return run_small_m_only()
     world, rank, local = dist_init()
     try:
         if args.impl == "reference":
