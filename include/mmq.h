@@ -189,6 +189,16 @@ mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, cons
 mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa,
                                const void* scales, int M, float* dots, mmq_stream_t s);
 
+/* Debug/verification: which kernel computes Y for M > MMQ_SMALL_M (process-wide).
+ *   0 (default): the super-block kernel for scale-folded codes (q4_K always,
+ *      q6_K when every |sc| <= 64) when its 128 x 256 tiles number at least the
+ *      SM count, else the chunk kernel; plain q6_K codes: the chunk kernel;
+ *   1: the chunk kernel for every case;
+ *   2: the super-block kernel for every scale-folded case.
+ * Returns MMQ_ERR_ARG for any other value.  Not thread-safe against GEMM calls
+ * in flight on other host threads. */
+mmq_status mmq_debug_select_large_m_kernel(int which);
+
 /* Synchronizes `s`, then reports and clears the sticky device error word:
  * MMQ_ERR_TIMEOUT if a bounded wait expired since the last call, MMQ_ERR_CUDA
  * if the synchronization failed, else MMQ_OK. */

@@ -21,8 +21,8 @@ __all__ = [
     "MMQError", "MMQ_Q4_K", "MMQ_Q6_K", "load", "lib_path",
     "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_quantize_act", "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
-    "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_get_device_error",
-    "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
+    "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
+    "mmq_get_device_error", "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
     "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
 ]
 
@@ -69,6 +69,7 @@ def load():
             "mmq_gemm_q6k": [P, I, I, P, P, I, P, I, P],
             "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
             "mmq_debug_gemm_dots": [I, P, I, I, P, P, I, P, P],
+            "mmq_debug_select_large_m_kernel": [I],
             "mmq_get_device_error": [P],
         }
         for name, args in sig.items():
@@ -143,6 +144,10 @@ def mmq_gemm_q4k(packed, od, id_, qa, scales, M, Y, ldy, stream=0):
 def mmq_debug_gemm_dots(t, packed, od, id_, qa, scales, M, dots, stream=0):
     _check(load().mmq_debug_gemm_dots(t, packed, od, id_, qa, scales, M, dots, stream or None),
            "mmq_debug_gemm_dots")
+
+
+def mmq_debug_select_large_m_kernel(which: int):
+    _check(load().mmq_debug_select_large_m_kernel(which), "mmq_debug_select_large_m_kernel")
 
 
 def mmq_get_device_error(stream=0) -> int:

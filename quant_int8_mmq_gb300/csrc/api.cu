@@ -209,6 +209,14 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
     return gemm_common(t, mmq::GEMM_DOTS, packed, od, id, qa, scales, M, dots, od, s);
 }
 
+mmq_status mmq_debug_select_large_m_kernel(int which)
+{
+    if (which < 0 || which > 2)
+        return MMQ_ERR_ARG;
+    mmq::select_large_m_kernel(which);
+    return MMQ_OK;
+}
+
 unsigned long long mmq_launch_count(void) { return mmq::g_launches.load(std::memory_order_relaxed); }
 
 mmq_status mmq_get_device_error(mmq_stream_t s)

@@ -136,6 +136,8 @@ struct GemmArgs {
     int full_units;       // units below this are whole tiles
     int nsb_half;         // split units: super-blocks [0, nsb_half) and [nsb_half, nsb)
     int vec_store;        // Y is 16-byte aligned and ldy % 4 == 0
+    int skip_folded;      // q6_K: return at once when the codes are folded (the
+                          // super-block kernel, launched first, has written Y)
 };
 
 // Bounded wait that ignores the error word (used only to drain our own copies /
@@ -619,6 +621,8 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
 template <int TYPE, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
 {
+    if (TYPE == 14 && g.skip_folded && __ldg(g.FLAG) != 0u)
+        return;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -717,9 +721,38 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
 
 }  // namespace
 
+std::atomic<int> g_large_m_kernel{0};
+
+void select_large_m_kernel(int which) { g_large_m_kernel.store(which); }
+
 cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int id, const void* qa,
                         const void* scales, int M, float* out, int ldy, cudaStream_t s, const char** path_label)
 {
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    // Y of scale-folded codes goes to the super-block kernel when its 128 x 256 tiles
+    // fill every SM at least once (fewer, larger tiles lose more to idle SMs than the
+    // faster contraction wins back); for q6_K the chunk kernel is launched after it
+    // and runs only when the codes are plain.
+    const int sel = g_large_m_kernel.load();
+    const bool sb_fills = static_cast<long long>(ceil_div(M, BM)) * ceil_div(od, 2 * BN) >= nsm;
+    const bool sb_first = mode == GEMM_Y && (sel == 2 || (sel == 0 && sb_fills));
+    if (sb_first) {
+        e = launch_gemm_sb(type, packed, od, id, qa, scales, M, out, ldy, s);
+        if (e != cudaSuccess)
+            return e;
+        if (type == 12) {
+            if (path_label)
+                *path_label = "q4_K: super-block tcgen05 GEMM, 128x256 tiles, activation operand p*d_a*q_a split "
+                              "f16 hi+lo in shared memory, one TMEM accumulator per super-block, tf32 hi/lo min term";
+            return cudaSuccess;
+        }
+    }
     const WeightPlanes wp = weight_planes(type, od, id);
     const ActPlanes ap = act_planes(M, id);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
@@ -740,14 +773,8 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.num_m = ceil_div(M, BM);
     a.num_n = ceil_div(od, BN);
     a.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (ldy & 3) == 0) ? 1 : 0;
+    a.skip_folded = sb_first ? 1 : 0;
 
-    int dev = 0, nsm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess)
-        return e;
     const int tiles = a.num_m * a.num_n;
     const int grid = tiles < nsm ? tiles : nsm;
     a.units = tiles;
@@ -755,7 +782,7 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.nsb_half = 0;
     const int rem = tiles % grid;
     const int nsb = id / QK_K;
-    if (mode == GEMM_Y && tiles > grid && rem > 0 && 2 * rem <= grid && nsb >= 2) {
+    if (mode == GEMM_Y && !sb_first && tiles > grid && rem > 0 && 2 * rem <= grid && nsb >= 2) {
         // the last round has `rem` tiles for `grid` CTAs: run each as two K-halves
         a.full_units = tiles - rem;
         a.units = a.full_units + 2 * rem;
@@ -769,15 +796,17 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
 
     if (type == 14) {
         if (path_label)
-            *path_label = "q6_K: persistent tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes, 4 TMEM chunk slots "
-                          "(plain codes + per-sub-block slots when |sc| > 64), cp.async.bulk rings, "
-                          "f32 d_a per chunk / d per super-block";
+            *path_label = sb_first
+                              ? "q6_K: super-block tcgen05 GEMM on scale-folded codes (128x256 tiles, activation "
+                                "operand split f16 hi+lo), else the chunk GEMM on plain codes (per-sub-block TMEM "
+                                "accumulators, f32 d_a per chunk)"
+                              : "q6_K: chunk GEMM, tcgen05.mma kind::f16 128x128x16 on exact int codes, two 256-column "
+                                "TMEM items, f32 d_a per chunk / d per super-block";
         return mode == GEMM_Y ? launch_typed<14, GEMM_Y>(a, grid, s) : launch_typed<14, GEMM_DOTS>(a, grid, s);
     }
     if (path_label)
-        *path_label = "q4_K: persistent tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes, "
-                      "4 TMEM chunk slots, tf32 hi/lo min-term contraction per super-block through the slots, "
-                      "cp.async.bulk rings, f32 d_a per chunk / d per super-block";
+        *path_label = "q4_K: chunk GEMM, tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes, two "
+                      "256-column TMEM items, tf32 hi/lo min term per tile, f32 d_a per chunk / d per super-block";
     return mode == GEMM_Y ? launch_typed<12, GEMM_Y>(a, grid, s) : launch_typed<12, GEMM_DOTS>(a, grid, s);
 }
 

@@ -122,6 +122,13 @@ enum GemmMode { GEMM_Y = 0, GEMM_DOTS = 1 };
 // Weight-streaming GEMM for M <= SMALL_M (raw blocks x int8 codes, dp4a).
 cudaError_t launch_gemm_small(int type, const void* packed, int od, int id, const void* qa, const void* scales,
                               int M, float* Y, int ldy, cudaStream_t s, const char** path_label);
+// Super-block-accumulating GEMM (Y only; q6_K: returns at once for plain codes).
+cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const void* qa, const void* scales, int M,
+                           float* Y, int ldy, cudaStream_t s);
+// Which kernel takes Y for M > SMALL_M: 0 = the super-block kernel when its tiles
+// fill the GPU, else the chunk kernel; 1 = the chunk kernel; 2 = the super-block
+// kernel (q6_K plain codes always go to the chunk kernel).
+void select_large_m_kernel(int which);
 cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int id, const void* qa,
                         const void* scales, int M, float* out, int ldy, cudaStream_t s,
                         const char** path_label);

@@ -259,6 +259,20 @@ def test_gemm_dots_bit_exact(typ, M, od, id_):
 
 
 # --------------------------------------------------------------------------- Y
+@pytest.fixture(params=["auto", "super-block"])
+def y_kernel(request):
+    """Y through the default kernel choice, and through the super-block kernel forced
+    (the default takes it only when its 128 x 256 tiles fill the GPU)."""
+    mmq.mmq_debug_select_large_m_kernel(0 if request.param == "auto" else 2)
+    yield request.param
+    mmq.mmq_debug_select_large_m_kernel(0)
+
+
+def _check_label(typ, y_kernel, M):
+    if y_kernel == "super-block" and M > mmq.SMALL_M:
+        assert "super-block" in mmq.mmq_last_path()
+
+
 def _run_gemm(typ, raw, x, Y=None):
     M = x.shape[0]
     od, nsb = raw.shape[:2]
@@ -277,10 +291,11 @@ def _run_gemm(typ, raw, x, Y=None):
     ("q6_K", 129, 129, 512),
     ("q4_K", 257, 385, 1280),
 ])
-def test_gemm_small_full_parity(typ, M, od, id_):
+def test_gemm_small_full_parity(y_kernel, typ, M, od, id_):
     raw = _raw(typ, od, id_, seed=od * 7 + M)
     x = synth.activations(M, id_, seed=M * 3 + 1)
     Y = _run_gemm(typ, raw, x).cpu().numpy()
+    _check_label(typ, y_kernel, M)
     Yo, S = oracle_gemm(typ, raw, x)
     assert_y_close(Y, Yo, S)
 
@@ -327,7 +342,7 @@ def test_gemm_cfg4_ffn_down_sampled():
 
 
 @pytest.mark.parametrize("M", [1, 31])
-def test_gemm_cfg4_odd_od_tails_full(M):
+def test_gemm_cfg4_odd_od_tails_full(y_kernel, M):
     cfg = synth.CONFIGS["cfg4_q6k_4096x11008_m2048"]
     raw = synth.q6k_blocks(4097, cfg["id"], cfg["seed"])
     x = synth.activations(M, cfg["id"], cfg["seed"] + 200 + M)
@@ -348,12 +363,12 @@ def test_gemm_stack_shapes_at_prompt_length_sampled(name, typ, od, id_):
     _sampled_check(typ, raw, x, Y, rows)
 
 
-def test_gemm_row_stride_and_unaligned_output():
+def test_gemm_row_stride_and_unaligned_output(y_kernel):
     typ, M, od, id_ = "q4_K", 100, 203, 512
     raw = _raw(typ, od, id_, seed=5)
     x = synth.activations(M, id_, 6)
     Yo, S = oracle_gemm(typ, raw, x)
-    for ldy, off in ((211, 0), (208, 1), (256, 0)):
+    for ldy, off in ((211, 0), (208, 1), (256, 0), (210, 0)):
         buf = torch.full((M * ldy + 8,), -7.0, dtype=torch.float32, device=DEV)
         Yv = buf[off:off + M * ldy].view(M, ldy)
         _run_gemm(typ, raw, x, Y=Yv)
@@ -363,7 +378,7 @@ def test_gemm_row_stride_and_unaligned_output():
         assert np.all(buf[:off].cpu().numpy() == -7.0)
 
 
-def test_gemm_deterministic():
+def test_gemm_deterministic(y_kernel):
     typ = "q6_K"
     raw = _raw(typ, 300, 1024, seed=1)
     x = synth.activations(333, 1024, 2)
@@ -375,23 +390,84 @@ def test_gemm_deterministic():
 # --------------------------------------------------------------------------- last-round K split
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
 def test_gemm_last_round_split_parity(typ):
-    """160 tiles on 152 SMs: the 8 tiles of the last round run as two K-halves that add
-    into a zeroed Y (odd super-block count: halves of 1 and 2 super-blocks)."""
+    """Super-block kernel: 8 x 20 = 160 tiles of 128 x 256 on 152 SMs, the 8 tiles of the
+    last round run as two K-halves that add into a zeroed Y (odd super-block count:
+    halves of 1 and 2); ragged od (last tile 236 rows).  q6_K_full (plain codes) takes
+    the chunk kernel: 8 x 40 = 320 tiles of 128 x 128, 16 split."""
     t = "q6_K" if typ.startswith("q6_K") else typ
-    M, od, id_ = 1024, 2560, 768
+    M, od, id_ = 1024, 5100, 768
     raw = _q6_raw(od, id_, 41, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, 41)
     x = synth.activations(M, id_, 42)
     Y = _run_gemm(t, raw, x).cpu().numpy()
+    want = "chunk GEMM on plain codes" if typ == "q6_K_full" else "super-block"
+    assert want in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
 
 
 def test_gemm_last_round_split_deterministic():
-    raw = synth.q4k_blocks(2560, 512, 43)
+    raw = synth.q4k_blocks(5100, 512, 43)
     x = synth.activations(1024, 512, 44)
     a = _run_gemm("q4_K", raw, x).cpu().numpy()
     b = _run_gemm("q4_K", raw, x).cpu().numpy()
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# --------------------------------------------------------------------------- super-block kernel specifics
+def test_gemm_superblock_wide_dynamic_range():
+    """The activation operand is p * d_a * q_a with one power of two p per (token,
+    super-block): chunks scaled by 2^-8 .. 2^8 inside every super-block, 5 % all-zero
+    chunks, whole rows at 1e-20 and 1e20."""
+    M, od, id_ = 300, 200, 1024
+    rng = np.random.default_rng(91)
+    f = np.exp2(rng.integers(-8, 9, size=(M, id_ // 32))).astype(np.float32)
+    f[rng.random(f.shape) < 0.05] = 0.0
+    x = (synth.activations(M, id_, 92).reshape(M, -1, 32) * f[..., None]).reshape(M, id_)
+    x[0] *= np.float32(1e-20)
+    x[1] *= np.float32(1e20)
+    mmq.mmq_debug_select_large_m_kernel(2)
+    try:
+        _dynamic_range_cases(x, od, id_)
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+
+
+def _dynamic_range_cases(x, od, id_):
+    for typ in ("q4_K", "q6_K"):
+        raw = _raw(typ, od, id_, seed=93)
+        Y = _run_gemm(typ, raw, x).cpu().numpy()
+        assert "super-block" in mmq.mmq_last_path()
+        Yo, S = oracle_gemm(typ, raw, x)
+        assert_y_close(Y, Yo, S)
+
+
+@pytest.fixture
+def chunk_kernel():
+    mmq.mmq_debug_select_large_m_kernel(1)
+    yield
+    mmq.mmq_debug_select_large_m_kernel(0)
+
+
+@pytest.mark.parametrize("typ,M,od,id_", [
+    ("q4_K", 200, 300, 768),
+    ("q6_K", 129, 129, 512),
+    ("q4_K", 1024, 2560, 768),    # 160 tiles of 128 x 128: the chunk kernel's own last-round split
+    ("q6_K", 1024, 2560, 768),
+])
+def test_gemm_chunk_kernel_y_parity(chunk_kernel, typ, M, od, id_):
+    """Y from the chunk-granular kernel (every case when selected; otherwise it serves
+    plain-code q6_K only)."""
+    raw = _raw(typ, od, id_, seed=od + M)
+    x = synth.activations(M, id_, seed=M + 5)
+    Y = _run_gemm(typ, raw, x).cpu().numpy()
+    assert "chunk GEMM" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(typ, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+def test_select_large_m_kernel_rejects_other_values():
+    with pytest.raises(mmq.MMQError):
+        mmq.mmq_debug_select_large_m_kernel(3)
 
 
 # --------------------------------------------------------------------------- weight-streaming path (M <= 8)
