@@ -91,12 +91,16 @@ constexpr int MIN_AM_BYTES = 2 * TF32_TILE_BYTES;      // token hi, lo
 constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;      // per 128-row weight tile: hi, lo
 
 // One super-block entry: weight d of the 256 rows, then {d, ssum} of the 8 chunks
-// for the 128 tokens ([chunk][token]).
+// for the 128 tokens ([chunk][token]) (both copied in), then 1/p per token (written
+// by the converter).
 constexpr int SB_SBD_OFF = 0;
 constexpr int SB_SBD_BYTES = BN * 4;
 constexpr int SB_AS_OFF = SB_SBD_OFF + SB_SBD_BYTES;
 constexpr int SB_AS_BYTES = 8 * BM * 8;
-constexpr int SB_BYTES = SB_AS_OFF + SB_AS_BYTES;
+constexpr int SB_IP_OFF = SB_AS_OFF + SB_AS_BYTES;
+constexpr int SB_IP_BYTES = BM * 4;
+constexpr int SB_COPY_BYTES = SB_SBD_BYTES + SB_AS_BYTES;
+constexpr int SB_BYTES = SB_IP_OFF + SB_IP_BYTES;
 
 constexpr int SMEM_ST = 0;
 constexpr int SMEM_SB = SMEM_ST + STAGES * STAGE_BYTES;
@@ -106,7 +110,8 @@ constexpr int BAR_CONV = BAR_FULL + STAGES;
 constexpr int BAR_EMPTY = BAR_CONV + STAGES;
 constexpr int BAR_SBFULL = BAR_EMPTY + STAGES;
 constexpr int BAR_SBEMPTY = BAR_SBFULL + SBR;
-constexpr int BAR_TFULL = BAR_SBEMPTY + SBR;
+constexpr int BAR_IPREADY = BAR_SBEMPTY + SBR;
+constexpr int BAR_TFULL = BAR_IPREADY + SBR;
 constexpr int BAR_TEMPTY = BAR_TFULL + 2;
 constexpr int BAR_DRAIN = BAR_TEMPTY + 2;
 constexpr int NUM_BARS = BAR_DRAIN + 1;
@@ -319,7 +324,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         fence_proxy_async_smem();   // after the consumers' ordinary loads
                         const uint32_t dst = sbase + SMEM_SB + sb.i * SB_BYTES;
                         const uint32_t fb = bar(BAR_SBFULL + sb.i);
-                        mbar_arrive_expect_tx(fb, SB_BYTES);
+                        mbar_arrive_expect_tx(fb, SB_COPY_BYTES);
                         bulk_g2s(dst + SB_SBD_OFF, g.SBD + (static_cast<size_t>(n0) * nsb + s) * 512, 512, fb);
                         bulk_g2s(dst + SB_SBD_OFF + 512, g.SBD + (static_cast<size_t>(n1) * nsb + s) * 512, 512, fb);
                         bulk_g2s(dst + SB_AS_OFF, ASb + static_cast<size_t>(s) * SB_AS_BYTES, SB_AS_BYTES, fb);
@@ -464,13 +469,19 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     da[k] = __uint_as_float(pr[k * BM + r].x);
                     dmax = fmaxf(dmax, da[k]);
                 }
-                const float p = __uint_as_float(p_field(dmax) << 23);
+                const uint32_t pf = p_field(dmax);
+                const float p = __uint_as_float(pf << 23);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     da[k] *= p;                   // s = d_a * p, exact
+                // 1/p (exact) for the promotion warps
+                reinterpret_cast<float*>(smem + SMEM_SB + sb.i * SB_BYTES + SB_IP_OFF)[r] =
+                    __uint_as_float((254u - pf) << 23);
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
+                    mbar_arrive(bar(BAR_IPREADY + sb.i));
                     mbar_arrive(bar(BAR_SBEMPTY + sb.i));
+                }
                 sb.next();
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) {
@@ -563,23 +574,17 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             float ip[2][2] = {{-1.0f, -1.0f}, {-1.0f, -1.0f}};
             const float2* d2 = nullptr;
             if (!min_item) {
-                if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph)) {
+                if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph) || !warp_wait(bar(BAR_IPREADY + sb.i), sb.ph)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
-                const uint2* pr = reinterpret_cast<const uint2*>(sbe + SB_AS_OFF);
+                const float* ipr = reinterpret_cast<const float*>(sbe + SB_IP_OFF);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int rho = 0; rho < 2; ++rho) {
-                        const int r = q * 32 + 16 * h + 8 * rho + quad;
-                        float dmax = 0.0f;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            dmax = fmaxf(dmax, __uint_as_float(pr[k * BM + r].x));
-                        ip[h][rho] = __uint_as_float((254u - p_field(dmax)) << 23);     // 1/p, exact
-                    }
+                    for (int rho = 0; rho < 2; ++rho)
+                        ip[h][rho] = ipr[q * 32 + 16 * h + 8 * rho + quad];
                 d2 = reinterpret_cast<const float2*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 2) + qi;
             }
             if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
@@ -687,6 +692,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_sb_kernel(const SbArgs g)
         for (int s = 0; s < SBR; ++s) {
             mbar_init(bar(BAR_SBFULL + s), 1);
             mbar_init(bar(BAR_SBEMPTY + s), NUM_CONV_WARPS + NUM_PROMO_WARPS);
+            mbar_init(bar(BAR_IPREADY + s), NUM_CONV_WARPS);
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(bar(BAR_TFULL + k), 1);
