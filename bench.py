@@ -131,8 +131,9 @@ def kernel_traffic(kernel_key):
         return None
     try:
         d = json.load(open(path))
-        src = open(os.path.join(ROOT, "quant_int8_mmq_gb300", "csrc", "gemm.cu"), "rb").read()
-        if d.get("gemm_cu_sha256") != hashlib.sha256(src).hexdigest():
+        name = d.get("source", "gemm.cu")
+        src = open(os.path.join(ROOT, "quant_int8_mmq_gb300", "csrc", name), "rb").read()
+        if d.get("source_sha256") != hashlib.sha256(src).hexdigest():
             return None
         return d.get("per_launch_dram_bytes", {}).get(kernel_key)
     except Exception:
@@ -463,7 +464,7 @@ def run_ours(args, world, rank, local):
 
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16-held int8/int6/int4 codes -> f32 (exact), f32 scales",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 operands: exact int weight codes x activations p*d_a*q_a as f16 hi+lo -> f32",
             "data": "synthetic (seeded random k-quant blocks, N(0,1) activations)",
             "config": config(args, {"parallelism": f"replicas x{world}"}),
             "tops_int8_equiv": world * total_flops / args.steps / (t_max / args.steps) / 1e12,
