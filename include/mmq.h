@@ -162,12 +162,20 @@ mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
  * The GEMM: Y[t][j] (t < M, j < od, row stride ldy floats) is overwritten with
  * the formula at the top of this file.  packed comes from mmq_pack_weights of
  * the same (type, od, id); qa/scales from mmq_quantize_act with K = id and the
- * same M.  The integer dots run exactly on the tensor cores (codes held as f16
- * integers, every partial sum an integer below 2^24 in the f32 accumulator);
- * the f32 scales are applied per chunk (d_a) and per super-block (d); the q4_K
- * min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo tensor-core
- * contraction (relative error about 2^-21 per product).  Rows t >= M and
- * columns j >= od are never written.  ldy >= od.
+ * same M.  Two tensor-core kernels compute it (mmq_last_path names the one
+ * launched; mmq_debug_select_large_m_kernel can force either):
+ *  - super-block kernel (scale-folded codes, when its 128 x 256 tiles number at
+ *    least the SM count): the activation operand is p*d_a*q_a (p a power of two
+ *    per token and super-block) held as an f16 hi + lo pair (about 2^-21
+ *    relative per value), times the exact f16 weight codes, summed over a whole
+ *    super-block in f32; then d and 1/p are applied per super-block;
+ *  - chunk kernel (otherwise): the integer dots run exactly (codes held as f16
+ *    integers, every partial sum an integer below 2^24 in the f32 accumulator)
+ *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
+ * Both: the q4_K min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo
+ * tensor-core contraction (relative error about 2^-21 per product); Y is
+ * deterministic for given inputs and kernel.  Rows t >= M and columns j >= od
+ * are never written.  ldy >= od.
  * M <= MMQ_SMALL_M (decode and tail shapes) takes the weight-streaming path
  * instead: the RAW plane and the int8 activation plane, exact integer dots on
  * the CUDA cores (dp4a), and the scales applied per chunk in the formula's own
