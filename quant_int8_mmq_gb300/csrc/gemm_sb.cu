@@ -105,8 +105,9 @@ constexpr int SB_BYTES = SB_IP_OFF + SB_IP_BYTES;
 constexpr int SMEM_ST = 0;
 constexpr int SMEM_SB = SMEM_ST + STAGES * STAGE_BYTES;
 constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
-constexpr int BAR_FULL = 0;
-constexpr int BAR_CONV = BAR_FULL + STAGES;
+constexpr int BAR_FULL = 0;                      // the stage's activation (or min-term token) tile
+constexpr int BAR_FULLB = BAR_FULL + STAGES;     // the stage's weight tiles
+constexpr int BAR_CONV = BAR_FULLB + STAGES;
 constexpr int BAR_EMPTY = BAR_CONV + STAGES;
 constexpr int BAR_SBFULL = BAR_EMPTY + STAGES;
 constexpr int BAR_SBEMPTY = BAR_SBFULL + SBR;
@@ -337,12 +338,15 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     }
                     fence_proxy_async_smem();       // after the converter's ordinary stores
                     const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
-                    const uint32_t fo = bar(BAR_FULL + op.i);
+                    // the activation tile completes on its own barrier so that the converter
+                    // starts while the weight tiles are still in flight
+                    const uint32_t fo = bar(BAR_FULL + op.i), fw = bar(BAR_FULLB + op.i);
                     const size_t ko = static_cast<size_t>(kb) * TILE_BYTES;
-                    mbar_arrive_expect_tx(fo, 3 * TILE_BYTES);
+                    mbar_arrive_expect_tx(fo, TILE_BYTES);
                     bulk_g2s(st + ST_A, Ab + ko, TILE_BYTES, fo);
-                    bulk_g2s(st + ST_B, B0 + ko, TILE_BYTES, fo);
-                    bulk_g2s(st + ST_B + TILE_BYTES, B1 + ko, TILE_BYTES, fo);
+                    mbar_arrive_expect_tx(fw, 2 * TILE_BYTES);
+                    bulk_g2s(st + ST_B, B0 + ko, TILE_BYTES, fw);
+                    bulk_g2s(st + ST_B + TILE_BYTES, B1 + ko, TILE_BYTES, fw);
                     if (kb + STAGES < 4 * w.sb1) {
                         // warm L2 with the tiles of the k-block this stage takes next
                         // (measured: about 3.5 % off the launch)
@@ -362,23 +366,26 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         }
                         fence_proxy_async_smem();
                         const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
-                        const uint32_t fo = bar(BAR_FULL + op.i);
+                        const uint32_t fo = bar(BAR_FULL + op.i), fw = bar(BAR_FULLB + op.i);
                         const uint8_t* x0 = g.AUX + (static_cast<size_t>(n0) * nsb + s) * MIN_BM_BYTES;
                         const uint8_t* x1 = g.AUX + (static_cast<size_t>(n1) * nsb + s) * MIN_BM_BYTES;
-                        mbar_arrive_expect_tx(fo, MIN_AM_BYTES + 2 * MIN_BM_BYTES);
+                        mbar_arrive_expect_tx(fo, MIN_AM_BYTES);
                         bulk_g2s(st + ST_A, g.AM + (static_cast<size_t>(m) * nsb + s) * MIN_AM_BYTES, MIN_AM_BYTES,
                                  fo);
-                        bulk_g2s(st + ST_B, x0, TF32_TILE_BYTES, fo);
-                        bulk_g2s(st + ST_B + TF32_TILE_BYTES, x1, TF32_TILE_BYTES, fo);
-                        bulk_g2s(st + ST_B + 2 * TF32_TILE_BYTES, x0 + TF32_TILE_BYTES, TF32_TILE_BYTES, fo);
-                        bulk_g2s(st + ST_B + 3 * TF32_TILE_BYTES, x1 + TF32_TILE_BYTES, TF32_TILE_BYTES, fo);
+                        mbar_arrive_expect_tx(fw, 2 * MIN_BM_BYTES);
+                        bulk_g2s(st + ST_B, x0, TF32_TILE_BYTES, fw);
+                        bulk_g2s(st + ST_B + TF32_TILE_BYTES, x1, TF32_TILE_BYTES, fw);
+                        bulk_g2s(st + ST_B + 2 * TF32_TILE_BYTES, x0 + TF32_TILE_BYTES, TF32_TILE_BYTES, fw);
+                        bulk_g2s(st + ST_B + 3 * TF32_TILE_BYTES, x1 + TF32_TILE_BYTES, TF32_TILE_BYTES, fw);
                         op.next();
                         ++n_ops;
                     }
                 }
             }
-            for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i)
+            for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i) {
                 drain_wait(bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
+                drain_wait(bar(BAR_FULLB + i % STAGES), (i / STAGES) & 1u);
+            }
             for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
                 drain_wait(bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
         } else if (warp == 1 && lane == 0) {
@@ -396,7 +403,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         ok = false;
                         break;
                     }
-                    if (!ctl_wait(bar(BAR_CONV + op.i), op.ph)) {
+                    if (!ctl_wait(bar(BAR_CONV + op.i), op.ph) || !ctl_wait(bar(BAR_FULLB + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -426,7 +433,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
                     for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(bar(BAR_CONV + op.i), op.ph)) {
+                        if (!ctl_wait(bar(BAR_CONV + op.i), op.ph) || !ctl_wait(bar(BAR_FULLB + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
@@ -694,6 +701,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_sb_kernel(const SbArgs g)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(BAR_FULL + s), 1);
+            mbar_init(bar(BAR_FULLB + s), 1);
             mbar_init(bar(BAR_CONV + s), NUM_CONV_WARPS);
             mbar_init(bar(BAR_EMPTY + s), 1);
         }
