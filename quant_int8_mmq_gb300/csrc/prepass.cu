@@ -69,21 +69,36 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
     const int nkb = K / TILE_K;
     const int nchunk = K / CHUNK;
     const int nsb = K / QK_K;
-    const long long total = static_cast<long long>(Mp) * nsb;
-    const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    // Item w = sb * Mp + t (token row t, super-block sb), grid-stride over warps; the
+    // (t, sb) pair is advanced incrementally (no 64-bit division per item).
+    const int stride = gridDim.x * (blockDim.x >> 5);
+    const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int st_t = stride % Mp, st_sb = stride / Mp;
+    int t_cur = w0 % Mp, sb_cur = w0 / Mp;
+    auto advance = [&](int& t, int& sb) {
+        t += st_t;
+        sb += st_sb;
+        if (t >= Mp) {
+            t -= Mp;
+            ++sb;
+        }
+    };
     // Two items per pass: both loads are in flight before either is reduced.
-    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
-         w += 2 * stride) {
+    while (sb_cur < nsb) {
+        int ti[2] = {t_cur, t_cur}, si[2] = {sb_cur, sb_cur};
+        advance(ti[1], si[1]);
+        t_cur = ti[1];
+        sb_cur = si[1];
+        advance(t_cur, sb_cur);
         float vv[2][8];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const long long wi = w + u * stride;
-            const int t = static_cast<int>(wi % Mp);
-            const int k0 = static_cast<int>(wi / Mp) * QK_K + 8 * lane;
+            const int t = ti[u];
+            const int k0 = si[u] * QK_K + 8 * lane;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 vv[u][i] = 0.0f;
-            if (wi < total && t < M) {
+            if (si[u] < nsb && t < M) {
                 const float* p = x + static_cast<size_t>(t) * ldx + k0;
                 if (vec4) {
                     const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
@@ -99,11 +114,10 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const long long wi = w + u * stride;
-            if (wi >= total)
+            if (si[u] >= nsb)
                 break;
-            const int t = static_cast<int>(wi % Mp);
-            const int sb = static_cast<int>(wi / Mp);
+            const int t = ti[u];
+            const int sb = si[u];
             const int k0 = sb * QK_K + 8 * lane;
             const float(&v)[8] = vv[u];
             float a = 0.0f;
