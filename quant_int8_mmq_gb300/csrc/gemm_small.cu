@@ -21,7 +21,7 @@
 // the four activation codes it multiplies, no byte shuffles).  Bytes read per weight
 // value: 0.5625 (q4_K) / 0.875 (q6_K, 14 pad bytes per 224-byte block).
 //
-// Mapping: one 128-thread CTA per group of R weight rows; its threads split the
+// Mapping: one 64-thread CTA per group of R weight rows; its threads split the
 // row's 32-value chunks (thread i takes chunks i, i + 128, ...), every token of the
 // call in registers, and each thread issues the loads of all R rows before it
 // computes, so many short CTAs per SM keep the weight stream in flight.  Partial
@@ -30,6 +30,7 @@
 #include <cuda_fp16.h>
 
 #include "mmq_internal.h"
+#include "ptx.cuh"
 
 namespace mmq {
 namespace {
@@ -86,6 +87,12 @@ __global__ void __launch_bounds__(THREADS) gemm_small_kernel(const uint8_t* __re
     const int nchunk = id / CHUNK;
     const int nsb = id / QK_K;
     const int j0 = blockIdx.x * R;
+    if (tid == 0) {
+        // The CTA's rows are contiguous in the raw plane: put the whole range in flight
+        // to L2 at once, so that the per-chunk loads below wait on L2, not on HBM.
+        const int rows = min(R, od - j0);
+        bulk_prefetch_l2(raw + static_cast<size_t>(j0) * nsb * RB, static_cast<uint32_t>(rows * nsb * RB));
+    }
 
     float acc[R][MT];
 #pragma unroll
