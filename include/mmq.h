@@ -74,7 +74,8 @@ typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
  *
  * Layout (fixed, documented so a caller can read it back):
  *   Mp = 128 * ceil(M/128) padded tokens; nkb = K/64; nchunk = K/32; nsb = K/256.
- *   qa:     Mp*K f16 values, the q8 codes held as exact binary16 integers.
+ *   qa:     Mp*K f16 values, the q8 codes held as exact binary16 integers
+ *           (zero as +0).
  *           Tile (mt, kb) = tokens 128*mt.. and values 64*kb.. is a 16384-byte
  *           block at byte (mt*nkb + kb)*16384.  Inside it token r (0..127) and
  *           value k (0..63) sit at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2

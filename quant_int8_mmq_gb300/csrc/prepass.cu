@@ -30,11 +30,12 @@
 namespace mmq {
 namespace {
 
-__device__ __forceinline__ int quant_one(float x, float d)
+// round(x/d) as an integer-valued float, clamped to [-127, 127] (the clamp matters
+// only for subnormal d, whose rounding can leave |x/d| above 127.5).
+__device__ __forceinline__ float quant_one(float x, float d)
 {
-    float r = roundf(__fdiv_rn(x, d));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int>(r);
+    const float r = roundf(__fdiv_rn(x, d));
+    return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;    // + 0: code 0 is +0, never -0
 }
 
 // The same quotient with the chunk's divisor shared: rd = 1/d correctly rounded
@@ -43,14 +44,14 @@ __device__ __forceinline__ int quant_one(float x, float d)
 // 1990): q0 = RN(x * rd) is within one ulp of x/d, e = x - d * q0 is exact as one
 // FMA, and RN(q0 + e * rd) is the correctly rounded quotient RN(x/d) when rd =
 // RN(1/d) and nothing overflows or underflows, which the caller guarantees by using
-// this only for d in [2^-100, 2^100].  The rounding to an integer is unchanged.
-__device__ __forceinline__ int quant_one_shared(float x, float d, float rd)
+// this only for d in [2^-100, 2^100].  The rounding to an integer is unchanged, and
+// no clamp is needed: for finite x with |x| <= amax and d = RN(amax/127) normal,
+// |x/d| <= 127 (1 + 2^-23), so RN(x/d) rounds to at most 127 in magnitude.
+__device__ __forceinline__ float quant_one_shared(float x, float d, float rd)
 {
     const float q0 = __fmul_rn(x, rd);
     const float e = __fmaf_rn(-q0, d, x);
-    float r = roundf(__fmaf_rn(e, rd, q0));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int>(r);
+    return roundf(__fmaf_rn(e, rd, q0)) + 0.0f;        // + 0: code 0 is +0, never -0
 }
 
 __device__ __forceinline__ float tf32_rna(float v)
@@ -129,31 +130,38 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
             const float d = __fdiv_rn(a, 127.0f);
             const bool shared = (d >= 0x1p-100f && d <= 0x1p100f);
             const float rd = shared ? __frcp_rn(d) : 0.0f;
-            int q[8];
-            int s = 0;
+            // codes as integer-valued floats; their chunk sum (|.| <= 4064) is exact in f32
+            float q[8];
+            float sf = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                q[i] = (d == 0.0f) ? 0 : (shared ? quant_one_shared(v[i], d, rd) : quant_one(v[i], d));
-                s += q[i];
+                q[i] = (d == 0.0f) ? 0.0f : (shared ? quant_one_shared(v[i], d, rd) : quant_one(v[i], d));
+                sf += q[i];
             }
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            sf += __shfl_xor_sync(0xffffffffu, sf, 1);
+            sf += __shfl_xor_sync(0xffffffffu, sf, 2);
+            const int s = static_cast<int>(sf);
 
             const int mt = t / TILE_ROWS, r = t % TILE_ROWS;
             const int kb = k0 / TILE_K;
             uint8_t* tile = reinterpret_cast<uint8_t*>(qa) + (static_cast<size_t>(mt) * nkb + kb) * TILE_BYTES;
             uint32_t h[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                h[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2 * i]))) |
-                       (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2 * i + 1]))) << 16);
+            for (int i = 0; i < 4; ++i) {           // exact: |q| <= 127 is an f16 integer
+                const __half2 p2 = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
+                h[i] = *reinterpret_cast<const uint32_t*>(&p2);
+            }
             *reinterpret_cast<uint4*>(tile + tile_byte(r, k0 % TILE_K)) = make_uint4(h[0], h[1], h[2], h[3]);
             if (qa8 != nullptr && t < M) {
                 // small_pos order inside the 8-value group: values (0,2,4,6) then (1,3,5,7)
-                const uint32_t lo = (q[0] & 0xFF) | ((q[2] & 0xFF) << 8) | ((q[4] & 0xFF) << 16) |
-                                    (static_cast<uint32_t>(q[6] & 0xFF) << 24);
-                const uint32_t hi = (q[1] & 0xFF) | ((q[3] & 0xFF) << 8) | ((q[5] & 0xFF) << 16) |
-                                    (static_cast<uint32_t>(q[7] & 0xFF) << 24);
+                int qi[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    qi[i] = static_cast<int>(q[i]);
+                const uint32_t lo = (qi[0] & 0xFF) | ((qi[2] & 0xFF) << 8) | ((qi[4] & 0xFF) << 16) |
+                                    (static_cast<uint32_t>(qi[6] & 0xFF) << 24);
+                const uint32_t hi = (qi[1] & 0xFF) | ((qi[3] & 0xFF) << 8) | ((qi[5] & 0xFF) << 16) |
+                                    (static_cast<uint32_t>(qi[7] & 0xFF) << 24);
                 *reinterpret_cast<uint2*>(qa8 + static_cast<size_t>(t) * K + k0) = make_uint2(lo, hi);
             }
             if ((lane & 3) == 0) {

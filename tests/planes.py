@@ -24,6 +24,7 @@ def untile_codes(buf: np.ndarray, rows_padded: int, K: int) -> np.ndarray:
     """Code plane (uint8 bytes) -> int64 codes [rows_padded, K]."""
     nt, nkb = rows_padded // TILE_ROWS, K // TILE_K
     u16 = np.ascontiguousarray(buf[: rows_padded * K * 2]).view(np.uint16).reshape(nt, nkb, TILE_ROWS * TILE_K)
+    assert not np.any(u16 == 0x8000), "code 0 must be stored as +0"   # pins the bits, not only the values
     tiles = u16[:, :, _IDX]                         # [nt, nkb, 128, 64]
     vals = tiles.view(np.float16).astype(np.float64)
     out = vals.transpose(0, 2, 1, 3).reshape(rows_padded, K)
