@@ -89,6 +89,9 @@ constexpr int ST_B = 2 * TILE_BYTES;
 constexpr int STAGE_BYTES = 4 * TILE_BYTES;
 constexpr int MIN_AM_BYTES = 2 * TF32_TILE_BYTES;      // token hi, lo
 constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;      // per 128-row weight tile: hi, lo
+// Min-term super-blocks per stage: a stage of one super-block holds only 384 cycles of
+// tensor work, too little to cover the copy latency of the next.
+constexpr int MIN_PER_STAGE = 2;
 
 // One super-block entry: weight d of the 256 rows, then {d, ssum} of the 8 chunks
 // for the 128 tokens ([chunk][token]) (both copied in), then 1/p per token (written
@@ -122,7 +125,8 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;    // slack for 1024-byte alignment
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0 && SMEM_SB % 1024 == 0 && SB_BYTES % 16 == 0 && SMEM_BAR % 8 == 0,
               "alignment");
-static_assert(MIN_AM_BYTES <= TILE_BYTES && 2 * MIN_BM_BYTES <= 2 * TILE_BYTES, "min-term operands fit a stage");
+static_assert(MIN_PER_STAGE * MIN_AM_BYTES <= TILE_BYTES && MIN_PER_STAGE * 2 * MIN_BM_BYTES <= 2 * TILE_BYTES,
+              "min-term operands fit a stage");
 
 struct SbArgs {
     const uint8_t* A;     // activation code tiles      [num_m][nkb][16 KiB]
@@ -315,6 +319,14 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 const uint8_t* B0 = g.B + static_cast<size_t>(n0) * nkb * TILE_BYTES;
                 const uint8_t* B1 = g.B + static_cast<size_t>(n1) * nkb * TILE_BYTES;
                 const uint8_t* ASb = g.AS + static_cast<size_t>(m) * nchunk * BM * 8;
+                if (Q4) {
+                    // the tile's min-term operands, consumed after its last k-block
+                    const uint32_t mb = static_cast<uint32_t>(w.sb1 - w.sb0) * MIN_AM_BYTES;
+                    bulk_prefetch_l2(g.AM + (static_cast<size_t>(m) * nsb + w.sb0) * MIN_AM_BYTES, mb);
+                    bulk_prefetch_l2(g.AUX + (static_cast<size_t>(n0) * nsb + w.sb0) * MIN_BM_BYTES, mb);
+                    if (n1 != n0)
+                        bulk_prefetch_l2(g.AUX + (static_cast<size_t>(n1) * nsb + w.sb0) * MIN_BM_BYTES, mb);
+                }
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {
                         const int s = kb >> 2;
@@ -359,7 +371,11 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     ++n_ops;
                 }
                 if (Q4 && ok) {
-                    for (int s = w.sb0; s < w.sb1; ++s) {
+                    // MIN_PER_STAGE super-blocks per stage: token tiles of super-block
+                    // s + e at ST_A + e * 8 KiB, weight tiles [hi n0 | hi n1 | lo n0 | lo n1]
+                    // at ST_B + e * 16 KiB
+                    for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
+                        const int ne = min(MIN_PER_STAGE, w.sb1 - s);
                         if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                             ok = false;
                             break;
@@ -367,16 +383,19 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         fence_proxy_async_smem();
                         const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
                         const uint32_t fo = bar(BAR_FULL + op.i), fw = bar(BAR_FULLB + op.i);
-                        const uint8_t* x0 = g.AUX + (static_cast<size_t>(n0) * nsb + s) * MIN_BM_BYTES;
-                        const uint8_t* x1 = g.AUX + (static_cast<size_t>(n1) * nsb + s) * MIN_BM_BYTES;
-                        mbar_arrive_expect_tx(fo, MIN_AM_BYTES);
-                        bulk_g2s(st + ST_A, g.AM + (static_cast<size_t>(m) * nsb + s) * MIN_AM_BYTES, MIN_AM_BYTES,
-                                 fo);
-                        mbar_arrive_expect_tx(fw, 2 * MIN_BM_BYTES);
-                        bulk_g2s(st + ST_B, x0, TF32_TILE_BYTES, fw);
-                        bulk_g2s(st + ST_B + TF32_TILE_BYTES, x1, TF32_TILE_BYTES, fw);
-                        bulk_g2s(st + ST_B + 2 * TF32_TILE_BYTES, x0 + TF32_TILE_BYTES, TF32_TILE_BYTES, fw);
-                        bulk_g2s(st + ST_B + 3 * TF32_TILE_BYTES, x1 + TF32_TILE_BYTES, TF32_TILE_BYTES, fw);
+                        mbar_arrive_expect_tx(fo, ne * MIN_AM_BYTES);
+                        bulk_g2s(st + ST_A, g.AM + (static_cast<size_t>(m) * nsb + s) * MIN_AM_BYTES,
+                                 ne * MIN_AM_BYTES, fo);
+                        mbar_arrive_expect_tx(fw, ne * 2 * MIN_BM_BYTES);
+                        for (int e = 0; e < ne; ++e) {
+                            const uint8_t* x0 = g.AUX + (static_cast<size_t>(n0) * nsb + s + e) * MIN_BM_BYTES;
+                            const uint8_t* x1 = g.AUX + (static_cast<size_t>(n1) * nsb + s + e) * MIN_BM_BYTES;
+                            const uint32_t bb = st + ST_B + e * 2 * MIN_BM_BYTES;
+                            bulk_g2s(bb, x0, TF32_TILE_BYTES, fw);
+                            bulk_g2s(bb + TF32_TILE_BYTES, x1, TF32_TILE_BYTES, fw);
+                            bulk_g2s(bb + 2 * TF32_TILE_BYTES, x0 + TF32_TILE_BYTES, TF32_TILE_BYTES, fw);
+                            bulk_g2s(bb + 3 * TF32_TILE_BYTES, x1 + TF32_TILE_BYTES, TF32_TILE_BYTES, fw);
+                        }
                         op.next();
                         ++n_ops;
                     }
@@ -432,18 +451,23 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                    for (int s = w.sb0; s < w.sb1; ++s) {
+                    for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
+                        const int ne = min(MIN_PER_STAGE, w.sb1 - s);
                         if (!ctl_wait(bar(BAR_CONV + op.i), op.ph) || !ctl_wait(bar(BAR_FULLB + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
-                        const uint64_t ahi = sdesc_tf32(st + ST_A), alo = sdesc_tf32(st + ST_A + TF32_TILE_BYTES);
-                        const uint64_t bhi = sdesc_tf32(st + ST_B), blo = sdesc_tf32(st + ST_B + 2 * TF32_TILE_BYTES);
-                        mma_tf32(d, ahi, bhi, idesc_t, s > w.sb0 ? 1u : 0u);
-                        mma_tf32(d, ahi, blo, idesc_t, 1u);
-                        mma_tf32(d, alo, bhi, idesc_t, 1u);
+                        for (int e = 0; e < ne; ++e) {
+                            const uint32_t aa = st + ST_A + e * MIN_AM_BYTES;
+                            const uint32_t bb = st + ST_B + e * 2 * MIN_BM_BYTES;
+                            const uint64_t ahi = sdesc_tf32(aa), alo = sdesc_tf32(aa + TF32_TILE_BYTES);
+                            const uint64_t bhi = sdesc_tf32(bb), blo = sdesc_tf32(bb + 2 * TF32_TILE_BYTES);
+                            mma_tf32(d, ahi, bhi, idesc_t, (s + e > w.sb0) ? 1u : 0u);
+                            mma_tf32(d, ahi, blo, idesc_t, 1u);
+                            mma_tf32(d, alo, bhi, idesc_t, 1u);
+                        }
                         umma_commit(bar(BAR_EMPTY + op.i));
                         op.next();
                     }
@@ -541,7 +565,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             }
             if (Q4 && ok) {
                 // min-term stages pass through unchanged
-                for (int s = w.sb0; s < w.sb1; ++s) {
+                for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
                     if (!warp_wait(bar(BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
