@@ -131,13 +131,26 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
             const bool shared = (d >= 0x1p-100f && d <= 0x1p100f);
             const float rd = shared ? __frcp_rn(d) : 0.0f;
             // codes as integer-valued floats; their chunk sum (|.| <= 4064) is exact in f32
+            // (one branch per lane: the 8 values share d, so the division path is never
+            // evaluated next to the shared-reciprocal one)
             float q[8];
+            if (shared) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    q[i] = quant_one_shared(v[i], d, rd);
+            } else if (d != 0.0f) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    q[i] = quant_one(v[i], d);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    q[i] = 0.0f;
+            }
             float sf = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                q[i] = (d == 0.0f) ? 0.0f : (shared ? quant_one_shared(v[i], d, rd) : quant_one(v[i], d));
+            for (int i = 0; i < 8; ++i)
                 sf += q[i];
-            }
             sf += __shfl_xor_sync(0xffffffffu, sf, 1);
             sf += __shfl_xor_sync(0xffffffffu, sf, 2);
             const int s = static_cast<int>(sf);
