@@ -776,19 +776,29 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.skip_folded = sb_first ? 1 : 0;
 
     const int tiles = a.num_m * a.num_n;
-    const int grid = tiles < nsm ? tiles : nsm;
+    int grid = tiles < nsm ? tiles : nsm;
     a.units = tiles;
     a.full_units = tiles;
     a.nsb_half = 0;
     const int rem = tiles % grid;
     const int nsb = id / QK_K;
-    if (mode == GEMM_Y && !sb_first && tiles > grid && rem > 0 && 2 * rem <= grid && nsb >= 2) {
-        // the last round has `rem` tiles for `grid` CTAs: run each as two K-halves
-        a.full_units = tiles - rem;
-        a.units = a.full_units + 2 * rem;
+    // Tiles run as two K-halves added into a zeroed Y (two addends: the order cannot
+    // change the sum): every tile when the launch has at most half as many tiles as SMs
+    // (decode-tail shapes), else the last round's tiles when they fill at most half.
+    int split = 0;
+    if (mode == GEMM_Y && !sb_first && nsb >= 2) {
+        if (2 * tiles <= nsm)
+            split = tiles;
+        else if (tiles > grid && rem > 0 && 2 * rem <= grid)
+            split = rem;
+    }
+    if (split > 0) {
+        a.full_units = tiles - split;
+        a.units = a.full_units + 2 * split;
         a.nsb_half = nsb / 2;
+        grid = a.units < nsm ? a.units : nsm;
         count_launch();
-        zero_tiles_kernel<<<rem, 256, 0, s>>>(out, ldy, M, od, a.num_m, a.full_units);
+        zero_tiles_kernel<<<split, 256, 0, s>>>(out, ldy, M, od, a.num_m, a.full_units);
         e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;

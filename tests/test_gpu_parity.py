@@ -465,6 +465,20 @@ def test_gemm_chunk_kernel_y_parity(chunk_kernel, typ, M, od, id_):
     assert_y_close(Y, Yo, S)
 
 
+@pytest.mark.parametrize("M,od,id_", [(40, 300, 768), (31, 4097, 1024)])
+def test_gemm_chunk_kernel_plain_q6k_all_tiles_split(chunk_kernel, M, od, id_):
+    """Plain-code q6_K (|sc| up to 127) on the chunk kernel with few tiles: every tile
+    runs as two K-halves added into a zeroed Y."""
+    raw = _q6_raw(od, id_, od + 3, True)
+    x = synth.activations(M, id_, seed=M + 6)
+    Y = _run_gemm("q6_K", raw, x).cpu().numpy()
+    assert "chunk GEMM" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm("q6_K", raw, x)
+    assert_y_close(Y, Yo, S)
+    Y2 = _run_gemm("q6_K", raw, x).cpu().numpy()
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+
+
 def test_select_large_m_kernel_rejects_other_values():
     with pytest.raises(mmq.MMQError):
         mmq.mmq_debug_select_large_m_kernel(3)
