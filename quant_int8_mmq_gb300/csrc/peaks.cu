@@ -183,7 +183,7 @@ static float time_ms(F f, int reps)
 
 int main()
 {
-    int dev = 0, nsm = 0, clk = 0;
+    int dev = 0, nsm = 0;
     CK(cudaGetDevice(&dev));
     CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
     cudaDeviceProp prop;
