@@ -54,6 +54,7 @@ def _load():
         I = ctypes.c_int
         lib.oracle_f16_to_f32_array.argtypes = [P, P, ctypes.c_size_t]
         lib.oracle_quantize_act.argtypes = [P, I, I, I, P, P, P]
+        lib.oracle_ggml_to_reading.argtypes = [I, P, ctypes.c_longlong, P]
         lib.oracle_decode_q6k.argtypes = [P, P, P, P]
         lib.oracle_decode_q4k.argtypes = [P, P, P, P, P, P]
         lib.oracle_scale_planes_q6k.argtypes = [P, I, I, P]
@@ -248,3 +249,15 @@ def fields_q4k(raw: np.ndarray):
 
 def cpu_threads() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def ggml_to_reading(typ: str, blocks: np.ndarray) -> np.ndarray:
+    """Blocks in the public ggml q4_K / q6_K layout (uint8, any leading shape, last
+    axis the block bytes) -> the same blocks in the reading the oracle decodes
+    (see mmq_oracle.c, "GGUF interop").  Parity unpinned against real GGUF files."""
+    nb = Q4K_BYTES if typ == "q4_K" else Q6K_BYTES
+    src = np.ascontiguousarray(blocks, dtype=np.uint8)
+    assert src.shape[-1] == nb
+    out = np.empty_like(src)
+    _load().oracle_ggml_to_reading(12 if typ == "q4_K" else 14, src.ctypes.data, src.size // nb, out.ctypes.data)
+    return out

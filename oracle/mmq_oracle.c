@@ -482,3 +482,91 @@ void oracle_fields_q4k(const uint8_t* raw, int od, int id, float* d, float* dmin
             oracle_decode_q4k(raw + b * Q4K_BYTES, d + b, dmin + b, sc + b * 8, m + b * 8, q);
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* GGUF interop: blocks in the public ggml (llama.cpp) q4_K / q6_K layout,
+ * rewritten into the reading above (same byte positions of d, dmin, scales and
+ * the code arrays; only the order of the codes inside qs / ql / qh and the
+ * q4_K scale packing differ).  This part follows the public ggml block format,
+ * not the three pages; it is pinned against hand-worked blocks and an
+ * independent inverse encoder, not against real GGUF files (parity unpinned
+ * against real files).
+ *
+ * ggml q4_K, value v (0..255), j = v / 64, l = v % 64:
+ *   code  = l < 32 ? qs[32 j + l] & 15 : qs[32 j + l - 32] >> 4
+ *   sub-block s = v / 32 (0..7) with scale sc_s and min m_s:
+ *     s < 4:  sc = S[s] & 63,  m = S[s + 4] & 63
+ *     s >= 4: sc = (S[s + 4] & 15) | ((S[s - 4] >> 6) << 4)
+ *             m  = (S[s + 4] >> 4) | ((S[s] >> 6) << 4)
+ * ggml q6_K, value v, n = v / 128, w = v % 128, p = w / 32, l = w % 32:
+ *   low 4 bits  = nibble (p / 2) of ql[64 n + 32 (p % 2) + l]
+ *   high 2 bits = (qh[32 n + l] >> (2 p)) & 3
+ *   code = (low | high << 4) - 32, scale index 8 n + 2 p + l / 16 = v / 16 (as the
+ *   reading: the scales array is copied unchanged). */
+static int ggml_q4k_code(const uint8_t* qs, int v)
+{
+    const int j = v / 64, l = v % 64;
+    return l < 32 ? (qs[32 * j + l] & 15) : (qs[32 * j + l - 32] >> 4);
+}
+
+static void ggml_q4k_scale_min(const uint8_t* S, int s, int* sc, int* m)
+{
+    if (s < 4) {
+        *sc = S[s] & 63;
+        *m = S[s + 4] & 63;
+    } else {
+        *sc = (S[s + 4] & 15) | ((S[s - 4] >> 6) << 4);
+        *m = (S[s + 4] >> 4) | ((S[s] >> 6) << 4);
+    }
+}
+
+static int ggml_q6k_code_unsigned(const uint8_t* ql, const uint8_t* qh, int v)
+{
+    const int n = v / 128, w = v % 128, p = w / 32, l = w % 32;
+    const int byte = ql[64 * n + 32 * (p % 2) + l];
+    const int low = (p / 2) ? (byte >> 4) : (byte & 15);
+    const int high = (qh[32 * n + l] >> (2 * p)) & 3;
+    return low | (high << 4);
+}
+
+/* src and dst may be the same buffer; nblocks blocks of 144 (q4_K) or 210 (q6_K) B. */
+void oracle_ggml_to_reading(int type, const uint8_t* src, long long nblocks, uint8_t* dst)
+{
+    for (long long bi = 0; bi < nblocks; ++bi) {
+        if (type == 12) {
+            uint8_t in[Q4K_BYTES], out[Q4K_BYTES];
+            memcpy(in, src + bi * Q4K_BYTES, Q4K_BYTES);
+            memset(out, 0, sizeof out);
+            memcpy(out, in, 4);                                  /* d, dmin */
+            /* scales: field f (0..15) as 6 bits at bit 6f, little-endian over 12 bytes */
+            for (int s = 0; s < 8; ++s) {
+                int sc, m;
+                ggml_q4k_scale_min(in + 4, s, &sc, &m);
+                const int fields[2] = {sc, m};
+                for (int t = 0; t < 2; ++t) {
+                    const int f = s + 8 * t;
+                    for (int b = 0; b < 6; ++b)
+                        if ((fields[t] >> b) & 1) {
+                            const int bit = 6 * f + b;
+                            out[4 + bit / 8] |= (uint8_t)(1u << (bit % 8));
+                        }
+                }
+            }
+            /* codes: value e at nibble e % 2 of qs[e / 2] */
+            for (int e = 0; e < QK_K; ++e)
+                out[16 + e / 2] |= (uint8_t)(ggml_q4k_code(in + 16, e) << (4 * (e % 2)));
+            memcpy(dst + bi * Q4K_BYTES, out, Q4K_BYTES);
+        } else {
+            uint8_t in[Q6K_BYTES], out[Q6K_BYTES];
+            memcpy(in, src + bi * Q6K_BYTES, Q6K_BYTES);
+            memset(out, 0, sizeof out);
+            memcpy(out + 192, in + 192, 18);                     /* scales[16], d */
+            for (int e = 0; e < QK_K; ++e) {
+                const int u = ggml_q6k_code_unsigned(in, in + 128, e);
+                out[e / 2] |= (uint8_t)((u & 15) << (4 * (e % 2)));            /* ql */
+                out[128 + e / 4] |= (uint8_t)(((u >> 4) & 3) << (2 * (e % 4))); /* qh */
+            }
+            memcpy(dst + bi * Q6K_BYTES, out, Q6K_BYTES);
+        }
+    }
+}

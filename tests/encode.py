@@ -97,3 +97,51 @@ def q4k_matrix(rng, od, id_):
                 c = e // 32
                 W[j, b * QK_K + e] = d * float(sc[c]) * float(q[e]) - dmin * float(m[c])
     return raw, W
+
+
+# --------------------------------------------------------------------------- ggml layout
+# Encoders for the public ggml (llama.cpp) block layouts, written from the format's
+# description of where each value lives (the inverse of the oracle's conversion, so the
+# two are independent statements of the same mapping):
+#   q4_K: the 256 values in four groups of 64; in group j, value l < 32 is the low
+#         nibble of qs[32j + l] and value 32 + l its high nibble; scale/min of sub-block
+#         s (32 values): s < 4 in the low 6 bits of S[s] / S[s + 4]; s >= 4 split into a
+#         low nibble (S[s + 4], sc in bits 0-3, m in bits 4-7) and the top two bits of
+#         S[s - 4] (sc) / S[s] (m).
+#   q6_K: two halves of 128; in half n, quarter p (32 values), value l: low 4 bits in
+#         nibble p // 2 of ql[64n + 32(p % 2) + l], high 2 bits at bit 2p of qh[32n + l];
+#         scales[16] and d as in the reading.
+def encode_q4k_ggml(d_bits: int, dmin_bits: int, sc, m, q) -> np.ndarray:
+    sc = [int(v) for v in sc]
+    m = [int(v) for v in m]
+    out = np.zeros(144, np.uint8)
+    out[0], out[1] = d_bits & 0xFF, d_bits >> 8
+    out[2], out[3] = dmin_bits & 0xFF, dmin_bits >> 8
+    S = [0] * 12
+    for s in range(4):
+        S[s] = sc[s] | ((sc[s + 4] >> 4) << 6)
+        S[s + 4] = m[s] | ((m[s + 4] >> 4) << 6)
+        S[s + 8] = (sc[s + 4] & 15) | ((m[s + 4] & 15) << 4)
+    out[4:16] = S
+    for group in range(4):
+        for l in range(32):
+            lo = int(q[64 * group + l])
+            hi = int(q[64 * group + 32 + l])
+            out[16 + 32 * group + l] = lo | (hi << 4)
+    return out
+
+
+def encode_q6k_ggml(d_bits: int, sc, q) -> np.ndarray:
+    out = np.zeros(210, np.uint8)
+    for n in range(2):
+        for p in range(4):
+            for l in range(32):
+                u = int(q[128 * n + 32 * p + l]) + 32
+                assert 0 <= u < 64
+                out[64 * n + 32 * (p % 2) + l] |= (u & 15) << (4 * (p // 2))
+                out[128 + 32 * n + l] |= (u >> 4) << (2 * p)
+    for i, s in enumerate(sc):
+        out[192 + i] = int(s) & 0xFF
+    out[208] = d_bits & 0xFF
+    out[209] = d_bits >> 8
+    return out

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.encode import (encode_q4k, encode_q6k, f16_bits, q4k_matrix, q6k_matrix,
+from tests.encode import (encode_q4k, encode_q4k_ggml, encode_q6k, encode_q6k_ggml, f16_bits, q4k_matrix, q6k_matrix,
                           random_q4k_fields, random_q6k_fields)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -414,3 +414,60 @@ def test_block_fields_match_encoder(oracle_lib):
     for i, (d, dmin, sc, m) in enumerate(want4):
         assert d4.reshape(-1)[i] == d and dm4.reshape(-1)[i] == dmin
         assert np.array_equal(sc4.reshape(-1, 8)[i], sc) and np.array_equal(m4.reshape(-1, 8)[i], m)
+
+
+# --------------------------------------------------------------------------- ggml interop
+def test_ggml_q4k_hand_worked_block(oracle_lib):
+    """Bytes placed by hand in the ggml q4_K layout; the decoded values are worked out
+    from the layout's description (value 64j + l < 32: low nibble of qs[32j + l];
+    64j + 32 + l: its high nibble; sub-block 4: sc from S[8] low nibble and S[0] top
+    bits, m from S[8] high nibble and S[4] top bits)."""
+    g = np.zeros(144, np.uint8)
+    g[0:4] = [0x00, 0x3C, 0x00, 0x38]             # d = 1.0, dmin = 0.5
+    g[4 + 0] = 0xC5                               # sc_0 = 5, top bits 3 -> sc_4 += 48
+    g[4 + 4] = 0x87                               # m_0 = 7, top bits 2 -> m_4 += 32
+    g[4 + 8] = 0x9A                               # sc_4 low 10, m_4 low 9
+    g[16 + 0], g[16 + 31], g[16 + 32] = 0x21, 0x43, 0x65
+    r = oracle.ggml_to_reading("q4_K", g)
+    d, dmin, sc, m, q = oracle.decode_q4k(r)
+    assert (d, dmin) == (1.0, 0.5)
+    assert (sc[0], m[0], sc[4], m[4]) == (5, 7, 58, 41)
+    assert sc[1] == sc[2] == sc[3] == sc[5] == 0 and m[1] == m[5] == 0
+    assert (q[0], q[32], q[31], q[63], q[64], q[96]) == (1, 2, 3, 4, 5, 6)
+    assert q[1] == q[33] == q[65] == q[255] == 0
+
+
+def test_ggml_q6k_hand_worked_block(oracle_lib):
+    """Value 128n + 32p + l: low 4 bits = nibble p // 2 of ql[64n + 32(p % 2) + l],
+    high 2 bits = bits 2p of qh[32n + l], code = that 6-bit value - 32."""
+    g = np.zeros(210, np.uint8)
+    g[0], g[32], g[64] = 0x21, 0x43, 0x0F
+    g[128 + 0], g[128 + 32] = 0xE4, 0x01
+    g[192:208] = np.arange(16, dtype=np.int8).view(np.uint8) - 8
+    g[208], g[209] = 0x00, 0x3C
+    r = oracle.ggml_to_reading("q6_K", g)
+    d, sc, q = oracle.decode_q6k(r)
+    assert d == 1.0 and list(sc) == list(range(-8, 8))
+    assert (q[0], q[32], q[64], q[96], q[128]) == (-31, -13, 2, 20, -1)
+    assert q[1] == q[33] == q[129] == q[255] == -32
+
+
+def test_ggml_roundtrip_against_independent_encoder(oracle_lib):
+    """Fields -> ggml bytes (tests/encode.py) -> oracle conversion -> the reading's
+    decoder gives the same fields, and equals the reading's own encoder byte for byte."""
+    rng = np.random.default_rng(11)
+    for _ in range(30):
+        d, dmin, sc, m, q = random_q4k_fields(rng)
+        g = encode_q4k_ggml(f16_bits(d), f16_bits(dmin), sc, m, q)
+        r = oracle.ggml_to_reading("q4_K", g)
+        assert np.array_equal(r, encode_q4k(f16_bits(d), f16_bits(dmin), sc, m, q))
+        d, sc, q = random_q6k_fields(rng, (-128, 127))
+        g = encode_q6k_ggml(f16_bits(d), sc, q)
+        r = oracle.ggml_to_reading("q6_K", g)
+        assert np.array_equal(r, encode_q6k(f16_bits(d), sc, q))
+    # in place (the same buffer as source and destination)
+    blocks = np.stack([encode_q6k_ggml(f16_bits(1.0), np.zeros(16), rng.integers(-32, 32, 256)) for _ in range(3)])
+    want = oracle.ggml_to_reading("q6_K", blocks)
+    lib = oracle._load()
+    lib.oracle_ggml_to_reading(14, blocks.ctypes.data, 3, blocks.ctypes.data)
+    assert np.array_equal(blocks, want)
