@@ -159,6 +159,22 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
 mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
                             void* packed, mmq_stream_t s);
 
+/* GGUF interop (registration time): nblocks q4_K (144 B) or q6_K (210 B) blocks in
+ * the public ggml (llama.cpp) block layout, rewritten into the layout documented
+ * above for raw_blocks, so that mmq_pack_weights can take weights read from a GGUF
+ * file.  The byte offsets of d, dmin, scales and the code arrays are the same in
+ * both; what moves is the position of each code and the q4_K scale packing:
+ *   ggml q4_K: value 64j+l (l < 32) = low nibble of qs[32j+l], value 64j+32+l = its
+ *     high nibble; sub-block s < 4: sc = S[s] & 63, m = S[s+4] & 63; s >= 4:
+ *     sc = (S[s+4] & 15) | (S[s-4] >> 6) << 4, m = (S[s+4] >> 4) | (S[s] >> 6) << 4
+ *     (S = scales[12]);
+ *   ggml q6_K: value 128n+32p+l: low 4 bits = nibble p/2 of ql[64n+32(p%2)+l],
+ *     high 2 bits = bits 2p..2p+1 of qh[32n+l]; scales[16] and d unchanged.
+ * src and dst are device pointers (any alignment); dst == src converts in place;
+ * other overlaps are undefined.  nblocks = 0 is a no-op.  MMQ_ERR_ARG for a bad
+ * type or a null pointer. */
+mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, void* dst, mmq_stream_t s);
+
 /* --------------------------------------------------------------------------
  * The GEMM: Y[t][j] (t < M, j < od, row stride ldy floats) is overwritten with
  * the formula at the top of this file.  packed comes from mmq_pack_weights of

@@ -21,7 +21,7 @@ __all__ = [
     "MMQError", "MMQ_Q4_K", "MMQ_Q6_K", "load", "lib_path",
     "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_quantize_act", "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
-    "mmq_pack_weights", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
+    "mmq_pack_weights", "mmq_convert_ggml_blocks", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
     "mmq_get_device_error", "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
     "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
 ]
@@ -66,6 +66,7 @@ def load():
             "mmq_packed_weight_layout": [I, I, I, S, S],
             "mmq_act_scale_layout": [I, I, S, S, S, S],
             "mmq_pack_weights": [I, P, I, I, P, P],
+            "mmq_convert_ggml_blocks": [I, P, ctypes.c_size_t, P, P],
             "mmq_gemm_q6k": [P, I, I, P, P, I, P, I, P],
             "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
             "mmq_debug_gemm_dots": [I, P, I, I, P, P, I, P, P],
@@ -131,6 +132,10 @@ def mmq_act_scale_layout(M, K):
 
 def mmq_pack_weights(t, raw, od, id_, packed, stream=0):
     _check(load().mmq_pack_weights(t, raw, od, id_, packed, stream or None), "mmq_pack_weights")
+
+
+def mmq_convert_ggml_blocks(t, src, nblocks, dst, stream=0):
+    _check(load().mmq_convert_ggml_blocks(t, src, nblocks, dst, stream or None), "mmq_convert_ggml_blocks")
 
 
 def mmq_gemm_q6k(packed, od, id_, qa, scales, M, Y, ldy, stream=0):

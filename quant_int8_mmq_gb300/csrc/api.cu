@@ -191,6 +191,21 @@ mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id, 
                                       reinterpret_cast<cudaStream_t>(s)));
 }
 
+mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, void* dst, mmq_stream_t s)
+{
+    if (t != MMQ_Q4_K && t != MMQ_Q6_K)
+        return MMQ_ERR_ARG;
+    if (!src || !dst)
+        return MMQ_ERR_ARG;
+    if (nblocks > (static_cast<size_t>(1) << 40))
+        return MMQ_ERR_SHAPE;
+    const mmq_status st = check_device();
+    if (st != MMQ_OK)
+        return st;
+    return from_cuda(mmq::launch_convert_ggml(static_cast<int>(t), src, nblocks, dst,
+                                              reinterpret_cast<cudaStream_t>(s)));
+}
+
 mmq_status mmq_gemm_q6k(const void* packed, int od, int id, const void* qa, const void* scales, int M, float* Y,
                         int ldy, mmq_stream_t s)
 {

@@ -117,6 +117,8 @@ void count_launch();
 cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales,
                                 cudaStream_t s);
 cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed, cudaStream_t s);
+// ggml-layout blocks -> the layout launch_pack reads (src == dst allowed).
+cudaError_t launch_convert_ggml(int type, const void* src, size_t nblocks, void* dst, cudaStream_t s);
 
 enum GemmMode { GEMM_Y = 0, GEMM_DOTS = 1 };
 // Weight-streaming GEMM for M <= SMALL_M (raw blocks x int8 codes, dp4a).

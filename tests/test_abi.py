@@ -90,6 +90,10 @@ def test_argument_errors_are_synchronous_and_cuda_free(mmq_lib):
     # bad type id
     assert lib.mmq_pack_weights(7, p16, 8, 256, p16, None) == 1
     assert lib.mmq_debug_gemm_dots(7, p16, 8, 256, p16, p16, 4, p16, None) == 1
+    # ggml conversion: bad type, null pointers
+    assert lib.mmq_convert_ggml_blocks(7, p16, 4, p16, None) == 1
+    assert lib.mmq_convert_ggml_blocks(12, None, 4, p16, None) == 1
+    assert lib.mmq_convert_ggml_blocks(14, p16, 4, None, None) == 1
     # kernel selector: 0 or 1 only (host state, no CUDA call)
     assert lib.mmq_debug_select_large_m_kernel(3) == 1
     assert lib.mmq_debug_select_large_m_kernel(-1) == 1

@@ -15,6 +15,7 @@ import torch
 import oracle
 import synth
 import quant_int8_mmq_gb300 as mmq
+from tests.encode import encode_q4k_ggml, encode_q6k_ggml
 from tests.planes import is_tf32, padded, untile_codes, untile_pairs, untile_rows, untile_tf32_pair
 
 pytestmark = pytest.mark.gpu
@@ -539,3 +540,59 @@ def test_status_codes_on_device():
                             None) == 0
     assert mmq.mmq_last_path().startswith("q4_K")
     _sync()
+
+
+# --------------------------------------------------------------------------- GGUF interop
+def _ggml_from_reading(typ, raw):
+    """Reading-layout blocks [od, nsb, B] -> the same weights in the ggml layout (through
+    the independent test encoder)."""
+    od, nsb = raw.shape[:2]
+    out = np.empty_like(raw)
+    for j in range(od):
+        for s in range(nsb):
+            blk = raw[j, s]
+            if typ == "q4_K":
+                d, dmin, sc, m, q = oracle.decode_q4k(blk)
+                g = encode_q4k_ggml(int(blk[0]) | (int(blk[1]) << 8), int(blk[2]) | (int(blk[3]) << 8), sc, m, q)
+            else:
+                d, sc, q = oracle.decode_q6k(blk)
+                g = encode_q6k_ggml(int(blk[208]) | (int(blk[209]) << 8), sc, q)
+            out[j, s] = g
+    return out
+
+
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
+def test_ggml_conversion_bit_exact_random_bytes(typ):
+    nb = 144 if typ == "q4_K" else 210
+    blocks = np.random.default_rng(5).integers(0, 256, size=(777, nb), dtype=np.uint8)
+    want = oracle.ggml_to_reading(typ, blocks)
+    src = _to_dev(blocks.reshape(-1))
+    dst = torch.full_like(src, 0xAB)
+    mmq.mmq_convert_ggml_blocks(mmq.TYPES[typ], src.data_ptr(), 777, dst.data_ptr())
+    _sync()
+    assert np.array_equal(dst.cpu().numpy().reshape(777, nb), want)
+    assert np.array_equal(src.cpu().numpy().reshape(777, nb), blocks)          # source untouched
+    mmq.mmq_convert_ggml_blocks(mmq.TYPES[typ], src.data_ptr(), 777, src.data_ptr())   # in place
+    _sync()
+    assert np.array_equal(src.cpu().numpy().reshape(777, nb), want)
+    mmq.mmq_convert_ggml_blocks(mmq.TYPES[typ], src.data_ptr(), 0, src.data_ptr())     # no-op
+    _sync()
+
+
+@pytest.mark.parametrize("typ,M,od,id_", [("q4_K", 40, 130, 768), ("q6_K", 200, 300, 512)])
+def test_ggml_weights_end_to_end(typ, M, od, id_):
+    """Weights given in the ggml layout: convert, pack, GEMM; the converted blocks equal
+    the reading-layout originals and Y matches the oracle on them."""
+    raw = _raw(typ, od, id_, seed=od + 9)
+    g = _ggml_from_reading(typ, raw)
+    gd = _to_dev(g.reshape(-1))
+    mmq.mmq_convert_ggml_blocks(mmq.TYPES[typ], gd.data_ptr(), od * (id_ // 256), gd.data_ptr())
+    _sync()
+    assert np.array_equal(gd.cpu().numpy().reshape(raw.shape), raw)
+    x = synth.activations(M, id_, seed=M + 8)
+    qa, sc = gpu_quantize(x)
+    packed = mmq.pack_weights(typ, gd, od, id_)
+    Y = mmq.gemm(typ, packed, od, id_, qa, sc, M)
+    _sync()
+    Yo, S = oracle_gemm(typ, raw, x)
+    assert_y_close(Y.cpu().numpy(), Yo, S)
