@@ -57,6 +57,9 @@ def parse_args():
                    help="run only the small-M case (q6_K 4097x11008, M = 1) and print its JSON (for profiling)")
     p.add_argument("--only", default="", help="comma-separated GEMM names of the stack (e.g. l0.gate): "
                    "a small case for profiling, not a bench line")
+    p.add_argument("--fuse-shared-inputs", action="store_true",
+                   help="run q+k and gate+up of every layer as one GEMM each over row-concatenated weights "
+                        "(same outputs, one prepass per GEMM): the fused gate/up follow-up, reported as its own line")
     return p.parse_args()
 
 
@@ -72,13 +75,42 @@ def stack_list(layers, only=""):
     return out
 
 
+# Pairs of stack GEMMs that read the same activations and share type and id: with
+# --fuse-shared-inputs each pair runs as one GEMM over the row-concatenated weights.
+FUSED_PAIRS = (("q", "k"), ("gate", "up"))
+
+
+def fuse_shared_inputs(gemms):
+    """[(name, typ, od, id, seed)] -> [(name, typ, od, id, [(od_part, seed), ...])]."""
+    by_name = {g[0]: g for g in gemms}
+    out, done = [], set()
+    for name, typ, od, id_, seed in gemms:
+        if name in done:
+            continue
+        layer, _, short = name.partition(".")
+        pair = next((p for p in FUSED_PAIRS if short == p[0]), None)
+        if pair and f"{layer}.{pair[1]}" in by_name:
+            other = by_name[f"{layer}.{pair[1]}"]
+            out.append((f"{layer}.{pair[0]}+{pair[1]}", typ, od + other[2], id_, [(od, seed), (other[2], other[4])]))
+            done.add(other[0])
+        else:
+            out.append((name, typ, od, id_, [(od, seed)]))
+    return out
+
+
 def config(args, extra=None):
+    gemms = stack_list(args.layers, getattr(args, "only", ""))
+    if getattr(args, "fuse_shared_inputs", False):
+        gemms = fuse_shared_inputs(gemms)
     c = {"workload": WORKLOAD, "tokens": args.tokens, "layers": args.layers,
-         "gemms_per_step": len(stack_list(args.layers, getattr(args, "only", ""))),
+         "gemms_per_step": len(gemms),
          "prepass_per_gemm": True,
          "l2": "inputs larger than L2: every step streams ~14.9 GB of repacked weights (129 MB L2)"}
     if getattr(args, "only", ""):
         c["only"] = args.only
+    if getattr(args, "fuse_shared_inputs", False):
+        c["fused"] = ("q+k and gate+up of every layer as one GEMM each over row-concatenated weights "
+                      "(same outputs and MACs, one prepass per GEMM)")
     if extra:
         c.update(extra)
     return c
@@ -374,10 +406,11 @@ def run_ours(args, world, rank, local):
     host_raws = []
     packed = []
     for g in gemms:
-        name, typ, od, id_, seed = g
-        raw = synth.blocks(typ, od, id_, seed)
         if want_cpu:
-            host_raws.append((g, raw))
+            host_raws.append((g, synth.blocks(*g[1:])))
+    units = fuse_shared_inputs(gemms) if args.fuse_shared_inputs else [g[:4] + ([(g[2], g[4])],) for g in gemms]
+    for name, typ, od, id_, parts in units:
+        raw = np.concatenate([synth.blocks(typ, od_p, id_, seed) for od_p, seed in parts], axis=0)
         rt = torch.from_numpy(raw.reshape(-1)).to(dev)
         pk = mmq.pack_weights(typ, rt, od, id_)
         packed.append((typ, od, id_, pk))
@@ -388,7 +421,7 @@ def run_ours(args, world, rank, local):
     qa_b, sc_b = mmq.mmq_act_plane_bytes(M, 11008)
     qa = torch.empty(qa_b, dtype=torch.uint8, device=dev)
     sc = torch.empty(sc_b, dtype=torch.uint8, device=dev)
-    ys = {od: torch.empty((M, od), dtype=torch.float32, device=dev) for od in sorted({g[2] for g in gemms})}
+    ys = {od: torch.empty((M, od), dtype=torch.float32, device=dev) for od in sorted({p[1] for p in packed})}
     torch.cuda.synchronize()
     assert mmq.mmq_get_device_error() == 0
 
