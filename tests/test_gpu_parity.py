@@ -291,6 +291,8 @@ def _run_gemm(typ, raw, x, Y=None):
     ("q4_K", 1, 1, 256),
     ("q6_K", 129, 129, 512),
     ("q4_K", 257, 385, 1280),
+    ("q4_K", 40, 200, 256),       # one super-block: no K split, one min-term stage
+    ("q6_K", 9, 260, 256),
 ])
 def test_gemm_small_full_parity(y_kernel, typ, M, od, id_):
     raw = _raw(typ, od, id_, seed=od * 7 + M)
@@ -454,6 +456,7 @@ def chunk_kernel():
     ("q6_K", 129, 129, 512),
     ("q4_K", 1024, 2560, 768),    # 160 tiles of 128 x 128: the chunk kernel's own last-round split
     ("q6_K", 1024, 2560, 768),
+    ("q4_K", 40, 200, 256),       # one super-block per row
 ])
 def test_gemm_chunk_kernel_y_parity(chunk_kernel, typ, M, od, id_):
     """Y from the chunk-granular kernel (every case when selected; otherwise it serves
