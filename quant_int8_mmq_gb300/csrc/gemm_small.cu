@@ -21,7 +21,7 @@
 // the four activation codes it multiplies, no byte shuffles).  Bytes read per weight
 // value: 0.5625 (q4_K) / 0.875 (q6_K, 14 pad bytes per 224-byte block).
 //
-// Mapping: one 64-thread CTA per group of R weight rows; its threads split the
+// Mapping: one 64-thread CTA (128 for q6_K at M = 1) per group of R weight rows; its threads split the
 // row's 32-value chunks (thread i takes chunks i, i + 128, ...), every token of the
 // call in registers, and each thread issues the loads of all R rows before it
 // computes, so many short CTAs per SM keep the weight stream in flight.  Partial
@@ -35,8 +35,9 @@
 namespace mmq {
 namespace {
 
-constexpr int WARPS = 2;
-constexpr int THREADS = WARPS * 32;
+// Warps per CTA: 2, except 4 for q6_K at one token (measured on GB300: q6_K 4097x11008
+// M = 1 13.4 -> 11.8 us with 4; every other measured case was faster with 2).
+__host__ __device__ constexpr int small_warps(int type, int mt) { return (type == 14 && mt == 1) ? 4 : 2; }
 constexpr int UNR = 1;             // chunk iterations whose loads are issued together
 constexpr int ROWS_FEW = 4;        // rows per CTA for MT <= 2
 constexpr int ROWS_MANY = 4;       // rows per CTA for MT > 2
@@ -75,7 +76,7 @@ __device__ __forceinline__ void q6k_group(uint32_t ql_word, uint32_t h16, uint32
     odd = __vsub4(qo, 0x20202020u);
 }
 
-template <int TYPE, int MT, int R>
+template <int TYPE, int MT, int R, int WARPS = small_warps(TYPE, MT), int THREADS = WARPS * 32>
 __global__ void __launch_bounds__(THREADS) gemm_small_kernel(const uint8_t* __restrict__ raw, int od, int id,
                                                              const int8_t* __restrict__ qa8,
                                                              const uint2* __restrict__ pairs, int M,
@@ -219,7 +220,7 @@ cudaError_t launch_typed(const uint8_t* raw, int od, int id, const int8_t* qa8, 
     constexpr int R = (MT <= 2) ? ROWS_FEW : ROWS_MANY;
     const int blocks = ceil_div(od, R);
     count_launch();
-    gemm_small_kernel<TYPE, MT, R><<<blocks, THREADS, 0, s>>>(raw, od, id, qa8, pairs, M, Y, ldy);
+    gemm_small_kernel<TYPE, MT, R><<<blocks, small_warps(TYPE, MT) * 32, 0, s>>>(raw, od, id, qa8, pairs, M, Y, ldy);
     return cudaGetLastError();
 }
 
