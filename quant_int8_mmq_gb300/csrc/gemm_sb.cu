@@ -23,24 +23,28 @@
 //
 // One CTA per SM, persistent over 128-token x 256-row tiles (N = 256: two 128-row
 // weight tiles side by side); 16 warps in four warpgroups:
-//   warp 0      producer: cp.async.bulk of the f16 activation code tile and the two
-//               weight code tiles of each 64-value k-block into a 3-deep ring, the
-//               super-block entries (weight d of 256 rows, token {d, ssum} of its 8
-//               chunks) into a 3-deep ring, then the q4_K min-term operands.
+//   warp 0      producer: cp.async.bulk of the f16 activation code tile (on its own
+//               barrier) and the two weight code tiles of each 64-value k-block into
+//               a 3-deep ring, with an L2 prefetch of the tiles the stage takes next;
+//               the super-block entries (weight d of 256 rows, token {d, ssum} of its
+//               8 chunks) into a 3-deep ring; then the q4_K min-term operands, two
+//               super-blocks per stage, prefetched into L2 when the tile starts.
 //   warp 1      allocates TMEM (two 256-column items); one thread issues per k-block
 //               eight tcgen05.mma kind::f16 128x256x16 (hi and lo for each 16 values)
 //               into the item of the current super-block, commits the stage, and
 //               commits the item after the super-block's fourth k-block.
 //   warps 2-3   idle (they lend their registers).
-//   warps 4-7   converter: thread r owns token row r of the tile; per k-block it
-//               reads its row's 64 codes from the stage, writes hi in place and lo
-//               into the stage's second slot (same swizzled positions), fences the
-//               async proxy and arrives on the stage's CONV barrier.
+//   warps 4-7   converter: thread r owns token row r of the tile; per super-block it
+//               derives p from the row's 8 chunk scales and publishes 1/p; per
+//               k-block it reads its row's 64 codes from the stage (all eight 16-byte
+//               groups first), writes hi in place and lo into the stage's second slot
+//               (same swizzled positions), fences the async proxy and arrives on the
+//               stage's CONV barrier.
 //   warps 8-15  promotion: each owns one TMEM lane quarter (warp % 4) and 128 of the
 //               256 columns; per super-block: wait, four tcgen05.ld (16x256b shape,
 //               64 columns), release, acc += d_sb * (D / p); per tile acc -= the q4_K
-//               min term; store Y (or, for the K-halves of a last-round tile, add into
-//               a zeroed Y) in whole 32-byte sectors.
+//               min term; store Y (or, for K-halves, add into a zeroed Y) as float2,
+//               whole 32-byte sectors per quad.
 // The synchronisation count per tensor-core FLOP is 8x lower than in gemm.cu and
 // the promotion does one FMA pair per accumulator element per super-block rather
 // than one FMA per chunk; the tensor pipe does twice the MMAs (hi and lo).
