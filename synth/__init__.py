@@ -73,10 +73,10 @@ def activations(M: int, K: int, seed: int, scale: float = 1.0) -> np.ndarray:
 # The workload configurations (sizes and seeds).
 # ---------------------------------------------------------------------------
 CONFIGS = {
-    "cfg1_q6k_64x512_m16": dict(type="q6_K", od=64, id=512, M=16, seed=0),
-    "cfg2_q4k_4096x4096_m512": dict(type="q4_K", od=4096, id=4096, M=512, seed=1),
-    "cfg3_q4k_11008x4096_m2048": dict(type="q4_K", od=11008, id=4096, M=2048, seed=2, tail_M=2047),
-    "cfg4_q6k_4096x11008_m2048": dict(type="q6_K", od=4096, id=11008, M=2048, seed=3,
+    "q6k_64x512_m16": dict(type="q6_K", od=64, id=512, M=16, seed=0),
+    "q4k_attn_4096x4096_m512": dict(type="q4_K", od=4096, id=4096, M=512, seed=1),
+    "q4k_ffn_gate_11008x4096_m2048": dict(type="q4_K", od=11008, id=4096, M=2048, seed=2, tail_M=2047),
+    "q6k_ffn_down_4096x11008_m2048": dict(type="q6_K", od=4096, id=11008, M=2048, seed=3,
                                       tail=dict(od=4097, M=(1, 31))),
 }
 

@@ -311,8 +311,8 @@ def test_gemm_q6k_full_int8_scale_range():
     assert_y_close(Y, Yo, S)
 
 
-def test_gemm_cfg2_attention_projection_full():
-    cfg = synth.CONFIGS["cfg2_q4k_4096x4096_m512"]
+def test_gemm_attention_projection_4096x4096_m512_full():
+    cfg = synth.CONFIGS["q4k_attn_4096x4096_m512"]
     raw = synth.q4k_blocks(cfg["od"], cfg["id"], cfg["seed"])
     x = synth.activations(cfg["M"], cfg["id"], cfg["seed"] + 100)
     Y = _run_gemm("q4_K", raw, x).cpu().numpy()
@@ -326,8 +326,8 @@ def _sampled_check(typ, raw, x, Y, rows):
 
 
 @pytest.mark.parametrize("M", [2048, 2047])
-def test_gemm_cfg3_ffn_gate_up_sampled(M):
-    cfg = synth.CONFIGS["cfg3_q4k_11008x4096_m2048"]
+def test_gemm_ffn_gate_up_11008x4096_sampled(M):
+    cfg = synth.CONFIGS["q4k_ffn_gate_11008x4096_m2048"]
     raw = synth.q4k_blocks(cfg["od"], cfg["id"], cfg["seed"])
     x = synth.activations(M, cfg["id"], cfg["seed"] + 100)
     Y = _run_gemm("q4_K", raw, x).cpu().numpy()
@@ -335,8 +335,8 @@ def test_gemm_cfg3_ffn_gate_up_sampled(M):
     _sampled_check("q4_K", raw, x, Y, rows)
 
 
-def test_gemm_cfg4_ffn_down_sampled():
-    cfg = synth.CONFIGS["cfg4_q6k_4096x11008_m2048"]
+def test_gemm_ffn_down_4096x11008_sampled():
+    cfg = synth.CONFIGS["q6k_ffn_down_4096x11008_m2048"]
     raw = synth.q6k_blocks(cfg["od"], cfg["id"], cfg["seed"])
     x = synth.activations(cfg["M"], cfg["id"], cfg["seed"] + 100)
     Y = _run_gemm("q6_K", raw, x).cpu().numpy()
@@ -345,8 +345,8 @@ def test_gemm_cfg4_ffn_down_sampled():
 
 
 @pytest.mark.parametrize("M", [1, 31])
-def test_gemm_cfg4_odd_od_tails_full(y_kernel, M):
-    cfg = synth.CONFIGS["cfg4_q6k_4096x11008_m2048"]
+def test_gemm_ffn_down_odd_od_tails_full(y_kernel, M):
+    cfg = synth.CONFIGS["q6k_ffn_down_4096x11008_m2048"]
     raw = synth.q6k_blocks(4097, cfg["id"], cfg["seed"])
     x = synth.activations(M, cfg["id"], cfg["seed"] + 200 + M)
     Y = _run_gemm("q6_K", raw, x).cpu().numpy()
