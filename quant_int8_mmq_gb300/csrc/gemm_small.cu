@@ -21,12 +21,16 @@
 // the four activation codes it multiplies, no byte shuffles).  Bytes read per weight
 // value: 0.5625 (q4_K) / 0.875 (q6_K, 14 pad bytes per 224-byte block).
 //
-// Mapping: one 64-thread CTA (128 for q6_K at M = 1) per group of R weight rows; its threads split the
-// row's 32-value chunks (thread i takes chunks i, i + 128, ...), every token of the
-// call in registers, and each thread issues the loads of all R rows before it
-// computes, so many short CTAs per SM keep the weight stream in flight.  Partial
-// sums are reduced with a fixed butterfly per warp and then in warp order through
-// shared memory, so the result does not depend on scheduling.
+// Mapping: one 64-thread CTA (128 for q6_K at M <= 2) per group of R weight rows; its
+// threads split the row's 32-value chunks (thread i takes chunks i, i + THREADS, ...),
+// every token of the call in registers, and each thread issues the loads of all R rows
+// before it computes, so many short CTAs per SM keep the weight stream in flight.  A
+// CTA whose rows span at most 16 KB first prefetches them to L2 in one bulk operation.
+// The kernel is a dependent launch: its CTAs may start while the kernel ahead (the
+// prepass, or another GEMM) finishes, issue that prefetch, and wait for it before they
+// read anything an earlier kernel writes.  Partial sums are reduced with a fixed
+// butterfly per warp and then in warp order through shared memory, so the result does
+// not depend on scheduling.
 #include <cuda_fp16.h>
 
 #include "mmq_internal.h"
@@ -35,12 +39,19 @@
 namespace mmq {
 namespace {
 
-// Warps per CTA: 2, except 4 for q6_K at one token (measured on GB300: q6_K 4097x11008
-// M = 1 13.4 -> 11.8 us with 4; every other measured case was faster with 2).
-__host__ __device__ constexpr int small_warps(int type, int mt) { return (type == 14 && mt == 1) ? 4 : 2; }
+// Warps per CTA: 2, except 4 for q6_K at one or two tokens (measured on GB300 with the
+// weights streamed from HBM: q6_K 4097x11008 M = 2 15.3 -> 13.2 us with 4; M = 1 equal;
+// q4_K and M = 4, 8 as fast or faster with 2, slower with 8).
+__host__ __device__ constexpr int small_warps(int type, int mt) { return (type == 14 && mt <= 2) ? 4 : 2; }
 constexpr int UNR = 1;             // chunk iterations whose loads are issued together
 constexpr int ROWS_FEW = 4;        // rows per CTA for MT <= 2
 constexpr int ROWS_MANY = 4;       // rows per CTA for MT > 2
+// Largest row-group range a CTA prefetches to L2 in one bulk operation.  Measured on
+// GB300 with the weights streamed from HBM (8 rotated copies): the prefetch helps at
+// id = 4096 (9-14 KB per CTA; q6_K 32000x4096 M = 1: 25.8 -> 22.9 us, q4_K 11008x4096:
+// 6.8 -> 6.3 us) and hurts at q6_K id = 11008 (38.5 KB: 10.0 -> 12.4 us), where the
+// demand loads queue behind it.
+constexpr uint32_t PREFETCH_MAX_BYTES = 16384;
 
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits)
 {
@@ -89,11 +100,17 @@ __global__ void __launch_bounds__(THREADS) gemm_small_kernel(const uint8_t* __re
     const int nsb = id / QK_K;
     const int j0 = blockIdx.x * R;
     if (tid == 0) {
-        // The CTA's rows are contiguous in the raw plane: put the whole range in flight
-        // to L2 at once, so that the per-chunk loads below wait on L2, not on HBM.
+        // The CTA's rows are contiguous in the raw plane: a short range is put in flight
+        // to L2 at once, so that the per-chunk loads below wait on L2, not on HBM.  A
+        // prefetch changes no value, so it is issued before the wait on the kernel
+        // ahead: the weight stream starts while that kernel finishes.
         const int rows = min(R, od - j0);
-        bulk_prefetch_l2(raw + static_cast<size_t>(j0) * nsb * RB, static_cast<uint32_t>(rows * nsb * RB));
+        const uint32_t bytes = static_cast<uint32_t>(rows * nsb * RB);
+        if (bytes <= PREFETCH_MAX_BYTES)
+            bulk_prefetch_l2(raw + static_cast<size_t>(j0) * nsb * RB, bytes);
     }
+    grid_dep_launch();
+    grid_dep_wait();
 
     float acc[R][MT];
 #pragma unroll
@@ -218,10 +235,9 @@ cudaError_t launch_typed(const uint8_t* raw, int od, int id, const int8_t* qa8, 
                          int ldy, cudaStream_t s)
 {
     constexpr int R = (MT <= 2) ? ROWS_FEW : ROWS_MANY;
-    const int blocks = ceil_div(od, R);
     count_launch();
-    gemm_small_kernel<TYPE, MT, R><<<blocks, small_warps(TYPE, MT) * 32, 0, s>>>(raw, od, id, qa8, pairs, M, Y, ldy);
-    return cudaGetLastError();
+    return launch_dependent(gemm_small_kernel<TYPE, MT, R>, dim3(ceil_div(od, R)), dim3(small_warps(TYPE, MT) * 32), s,
+                            raw, od, id, qa8, pairs, M, Y, ldy);
 }
 
 template <int TYPE>

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -112,6 +113,26 @@ inline WeightPlanes weight_planes(int type, int od, int id)
 // Every kernel launch of the library adds to one process-wide counter
 // (mmq_launch_count); count_launch is called once per launch attempt.
 void count_launch();
+
+// Launches `kernel` with programmatic stream serialization: its CTAs may start while
+// the kernel ahead of it on `s` finishes, so the kernel calls grid_dep_wait() before
+// it touches memory that an earlier kernel may write (only an L2 prefetch may precede
+// the wait).  Returns the launch error.
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, cudaStream_t s, A&&... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Each returns cudaSuccess or the launch error; arguments are already validated.
 cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales,

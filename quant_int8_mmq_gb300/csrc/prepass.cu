@@ -26,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include "mmq_internal.h"
+#include "ptx.cuh"
 
 namespace mmq {
 namespace {
@@ -66,6 +67,9 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                                                            uint2* __restrict__ scales, uint8_t* __restrict__ am,
                                                            int8_t* __restrict__ qa8)
 {
+    // x may come from the kernel ahead, and qa / scales may still be read by it.
+    grid_dep_wait();
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int nkb = K / TILE_K;
     const int nchunk = K / CHUNK;
@@ -212,10 +216,10 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
     const ActPlanes ap = act_planes(M, K);
     uint8_t* sc = static_cast<uint8_t*>(scales);
     count_launch();
-    quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, M, K, ldx, Mp, vec4, static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off),
-        sc + ap.am_off, ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr);
-    return cudaGetLastError();
+    return launch_dependent(
+        quantize_act_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), s, x, M, K, ldx, Mp, vec4,
+        static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off), sc + ap.am_off,
+        ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr);
 }
 
 }  // namespace mmq

@@ -513,6 +513,42 @@ def test_gemm_streaming_boundary(M):
     assert_y_close(Y, Yo, S)
 
 
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
+def test_streaming_back_to_back_calls_share_buffers(typ):
+    """Prepass and weight-streaming GEMM calls queued on one stream with no synchronisation
+    in between, all through the same activation planes, and the last two GEMMs writing the
+    same Y.  The prepass and the streaming GEMM start while the kernel ahead of them still
+    runs; each result must still be the oracle's for its own inputs: a prepass does not
+    overwrite codes the GEMM ahead still reads, a GEMM reads the codes of its own prepass,
+    and a later GEMM's Y is the one left."""
+    od, id_ = 300, 1024
+    raws = [_raw(typ, od, id_, seed=900 + i) for i in range(2)]
+    packs = [gpu_pack(typ, r) for r in raws]
+    xs = [synth.activations(M, id_, seed=910 + i) for i, M in enumerate([1, 8, 3, 5, 2])]
+    xd = [_to_dev(x) for x in xs]
+    qb, sb = mmq.mmq_act_plane_bytes(8, id_)
+    qa = torch.empty(qb, dtype=torch.uint8, device=DEV)
+    sc = torch.empty(sb, dtype=torch.uint8, device=DEV)
+    shared = torch.full((8, od), float("nan"), dtype=torch.float32, device=DEV)
+    _sync()
+    outs = []
+    for i, x in enumerate(xd):
+        M = x.shape[0]
+        mmq.quantize_act(x, qa, sc)
+        Y = shared[:M] if i >= len(xd) - 2 else None
+        outs.append(mmq.gemm(typ, packs[i % 2], od, id_, qa, sc, M, Y=Y))
+    _sync()
+    assert "weight-streaming" in mmq.mmq_last_path()
+    for i, (x, Y) in enumerate(zip(xs, outs)):
+        if i == len(xs) - 2:
+            continue   # overwritten by the last call
+        Yo, S = oracle_gemm(typ, raws[i % 2], x)
+        assert_y_close(Y.cpu().numpy(), Yo, S)
+    # rows the last call (M = 2) did not write still hold the one before it (M = 5)
+    Yo, S = oracle_gemm(typ, raws[(len(xs) - 2) % 2], xs[-2])
+    assert_y_close(shared[2:5].cpu().numpy(), Yo[2:], S[2:])
+
+
 def test_gemm_streaming_row_stride_unaligned_and_deterministic():
     typ, M, od, id_ = "q6_K", 5, 203, 512
     raw = _raw(typ, od, id_, seed=15)
