@@ -189,6 +189,9 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *  - chunk kernel (otherwise): the integer dots run exactly (codes held as f16
  *    integers, every partial sum an integer below 2^24 in the f32 accumulator)
  *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
+ *    For M <= 64 it runs in a few-token layout: the weight tile is the MMA's A
+ *    operand and the tokens its N (M rounded up to 16), the same arithmetic per
+ *    element with only the tokens present copied and contracted.
  * Both: the q4_K min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo
  * tensor-core contraction (relative error about 2^-21 per product); Y is
  * deterministic for given inputs and kernel.  Rows t >= M and columns j >= od
@@ -217,8 +220,9 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
 /* Debug/verification: which kernel computes Y for M > MMQ_SMALL_M (process-wide).
  *   0 (default): the super-block kernel for scale-folded codes (q4_K always,
  *      q6_K when every |sc| <= 64) when its 128 x 256 tiles number at least the
- *      SM count, else the chunk kernel; plain q6_K codes: the chunk kernel;
- *   1: the chunk kernel for every case;
+ *      SM count, else the chunk kernel; plain q6_K codes: the chunk kernel; the
+ *      chunk kernel takes its few-token layout when M <= 64;
+ *   1: the chunk kernel for every case, always in its 128-token tile layout;
  *   2: the super-block kernel for every scale-folded case.
  * Returns MMQ_ERR_ARG for any other value.  Not thread-safe against GEMM calls
  * in flight on other host threads. */

@@ -270,17 +270,27 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, float (&v)[64])
         v[i] = __uint_as_float(r[i]);
 }
 
-#define MMQ_T64(i) "+r"(r[(i)])
-#define MMQ_K2(i) "+f"(k[(i)].x), "+f"(k[(i)].y)
-
-#undef MMQ_T64
-#undef MMQ_K2
-
-#define MMQ_T64A(i) "+r"(a[(i)])
-#define MMQ_T64B(i) "+r"(b[(i)])
-
-#undef MMQ_T64A
-#undef MMQ_T64B
+// Two 16-column loads (columns taddr .. taddr + 31) with a single wait.
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : MMQ_R32(0), MMQ_R32(1), MMQ_R32(2), MMQ_R32(3), MMQ_R32(4), MMQ_R32(5), MMQ_R32(6), MMQ_R32(7),
+          MMQ_R32(8), MMQ_R32(9), MMQ_R32(10), MMQ_R32(11), MMQ_R32(12), MMQ_R32(13), MMQ_R32(14),
+          MMQ_R32(15), MMQ_R32(16), MMQ_R32(17), MMQ_R32(18), MMQ_R32(19), MMQ_R32(20), MMQ_R32(21),
+          MMQ_R32(22), MMQ_R32(23), MMQ_R32(24), MMQ_R32(25), MMQ_R32(26), MMQ_R32(27), MMQ_R32(28),
+          MMQ_R32(29), MMQ_R32(30), MMQ_R32(31)
+        : "r"(taddr), "r"(taddr + 16)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
 
 #undef MMQ_R32
 

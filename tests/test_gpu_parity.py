@@ -483,6 +483,65 @@ def test_gemm_chunk_kernel_plain_q6k_all_tiles_split(chunk_kernel, M, od, id_):
     assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
 
 
+# --------------------------------------------------------------------------- few-token layout (8 < M <= 64)
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
+@pytest.mark.parametrize("M", [9, 16, 17, 31, 32, 33, 48, 63, 64])
+def test_gemm_few_token_layout_parity(typ, M):
+    """The chunk kernel with the tokens as the MMA's N (16 * ceil(M / 16) columns):
+    ragged token counts around every multiple of 16, an odd od (ragged last weight
+    tile), 3 tiles so that every tile runs as two K-halves (odd super-block count)."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    od, id_ = 259, 768
+    raw = _q6_raw(od, id_, od + M, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, od + M)
+    x = synth.activations(M, id_, 20 * M + 1)
+    Y = _run_gemm(t, raw, x).cpu().numpy()
+    assert "few-token layout" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
+@pytest.mark.parametrize("M,od,id_", [(31, 4097, 11008), (64, 11008, 4096), (20, 32000, 4096)])
+def test_gemm_few_token_layout_stack_shapes(typ, M, od, id_):
+    """FFN-down (odd od), FFN-gate and lm_head shapes at decode-tail token counts: many
+    tiles (the persistent rounds and the last-round split) against the oracle, and the
+    result equals the 128-token tile layout's to the tolerance, run to run bit-identical."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    if t == "q4_K" and od == 32000:
+        pytest.skip("lm_head is q6_K")
+    raw = _q6_raw(od, id_, M + 7, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, M + 7)
+    x = synth.activations(M, id_, M + 8)
+    Y = _run_gemm(t, raw, x).cpu().numpy()
+    assert "few-token layout" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+    Y2 = _run_gemm(t, raw, x).cpu().numpy()
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+    mmq.mmq_debug_select_large_m_kernel(1)
+    try:
+        Yr = _run_gemm(t, raw, x).cpu().numpy()
+        assert "few-token" not in mmq.mmq_last_path()
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+    assert_y_close(Y, Yr.astype(np.float64), S)
+
+
+def test_gemm_few_token_layout_row_stride_unaligned():
+    typ, M, od, id_ = "q4_K", 27, 203, 512
+    raw = _raw(typ, od, id_, seed=25)
+    x = synth.activations(M, id_, 26)
+    Yo, S = oracle_gemm(typ, raw, x)
+    for ldy, off in ((211, 0), (208, 1), (256, 0)):
+        buf = torch.full((M * ldy + 8,), -7.0, dtype=torch.float32, device=DEV)
+        Yv = buf[off:off + M * ldy].view(M, ldy)
+        _run_gemm(typ, raw, x, Y=Yv)
+        assert "few-token layout" in mmq.mmq_last_path()
+        host = Yv.cpu().numpy()
+        assert_y_close(host[:, :od], Yo, S)
+        assert np.all(host[:, od:] == -7.0)
+        assert np.all(buf[:off].cpu().numpy() == -7.0)
+
+
 def test_select_large_m_kernel_rejects_other_values():
     with pytest.raises(mmq.MMQError):
         mmq.mmq_debug_select_large_m_kernel(3)
