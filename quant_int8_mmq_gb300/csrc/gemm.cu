@@ -39,6 +39,10 @@
 //               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner;
 //               per tile acc -= the q4_K min-term item; store Y (or, for the two
 //               K-halves of a last-round tile, add into a zeroed Y).
+// Few tokens (M <= 64, Y only): the same roles in a transposed layout, with the
+// weight tile as the MMA's A operand on the TMEM lanes and the tokens as N (M rounded
+// up to 16), only those token rows copied, a deeper operand ring (7 stages with 8 KiB
+// token slots) and four 128-column TMEM items; see gemm_roles_tc.
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
 // set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing
 // thread's wait + fence + commit cost about 80 cycles on top of a chunk's 128 cycles
