@@ -513,6 +513,7 @@ def run_ours(args, world, rank, local):
             "tops_int8_equiv": world * total_flops / args.steps / (t_max / args.steps) / 1e12,
             "gemm_only_tops": total_flops / gemm_time / 1e12,
             "gemm_share_of_step": gemm_time / t,
+            "gemm_only_tok_s": world * M * args.steps / gemm_time,
             "roofline": roof,
             "gpu_launches": launches,
             "path": mmq.mmq_last_path()}
