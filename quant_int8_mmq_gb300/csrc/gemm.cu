@@ -154,6 +154,7 @@ static_assert(TC_SMEM_A % 1024 == 0 && TC_A_BYTES % 1024 == 0 && TC_SMEM_SB % 16
               "alignment (few-token layout)");
 static_assert(MIN_AM_BYTES <= TC_A_BYTES && MIN_BM_BYTES <= TILE_BYTES, "min-term operands fit a few-token stage");
 static_assert(2 * TC_COLS <= static_cast<int>(TC_ITEM_COLS), "an item holds two chunks (or sub-blocks) of columns");
+static_assert(TC_MAX_M * BM * 4 <= TC_STAGES * TILE_BYTES, "K-slice partial sums fit the idle weight stages");
 
 struct GemmArgs {
     const uint8_t* A;     // activation code tiles      [num_m][nkb][16 KiB]
@@ -174,6 +175,7 @@ struct GemmArgs {
     int skip_folded;      // q6_K: return at once when the codes are folded (the
                           // super-block kernel, launched first, has written Y)
     int n_tok;            // few-token layout: MMA N (M rounded up to 16, <= TC_MAX_M)
+    int kslices;          // few-token layout: CTAs per weight tile (a cluster along K), 1 = none
 };
 
 // Bounded wait that ignores the error word (used only to drain our own copies /
@@ -661,6 +663,23 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
 // weight row and half of the token columns.  The arithmetic is the token-row
 // layout's, element by element: inner += d_a * I' per chunk, acc += d * inner per
 // super-block, acc -= the q4_K min term, in the same order.
+// Work unit u of a few-token launch.  With kslices > 1 the launch is one cluster of
+// kslices CTAs per weight tile; CTA rank r takes super-blocks
+// [r*nsb/kslices, (r+1)*nsb/kslices) and the partial sums meet in rank 0.
+__device__ __forceinline__ Unit tc_unit(const GemmArgs& g, int u, int nsb)
+{
+    if (g.kslices <= 1)
+        return unit_of(g, u, nsb);
+    Unit w;
+    const int r = u % g.kslices;
+    w.m = 0;
+    w.n = u / g.kslices;
+    w.sb0 = r * nsb / g.kslices;
+    w.sb1 = (r + 1) * nsb / g.kslices;
+    w.half = false;
+    return w;
+}
+
 template <int TYPE, bool FOLDED>
 __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
                                               int warp, int lane)
@@ -668,7 +687,6 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
     constexpr bool Q4 = (TYPE == 12);
     constexpr uint32_t ITEM_COLS = TC_ITEM_COLS;
     const int nkb = g.id / BK;
-    const int nchunk = g.id / CHUNK;
     const int nsb = g.id / QK_K;
     const uint32_t a_bytes = static_cast<uint32_t>(g.n_tok) * 128u;  // first n_tok rows of a 128-row tile
     auto bar = [&](int i) -> uint32_t { return sbase + TC_SMEM_BAR + 8u * static_cast<uint32_t>(i); };
@@ -682,7 +700,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
-                const Unit w = unit_of(g, u, nsb);
+                const Unit w = tc_unit(g, u, nsb);
                 const int n = w.n;
                 const uint8_t* Ab = g.A;   // one token tile (num_m == 1)
                 const uint8_t* Bb = g.B + static_cast<size_t>(n) * nkb * TILE_BYTES;
@@ -749,7 +767,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             RingPos<TC_ITEMS> item;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
-                const Unit w = unit_of(g, u, nsb);
+                const Unit w = tc_unit(g, u, nsb);
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if (!ctl_wait(bar(TC_BAR_FULL + op.i), op.ph)) {
                         ok = false;
@@ -823,6 +841,10 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             drain_wait(bar(TC_BAR_DRAIN), 0u);
         }
         __syncwarp();
+        if (g.kslices > 1) {   // the promotion warps' two cluster barriers
+            cluster_sync();
+            cluster_sync();
+        }
         return;
     }
 
@@ -842,10 +864,17 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
         item.next();
     };
     bool ok = true;
+    const bool clustered = g.kslices > 1;   // then the launch gives this CTA exactly one unit
+    bool had_unit = false;
+    int j = 0;
+    float acc[TC_HALF];
+#pragma unroll
+    for (int t = 0; t < TC_HALF; ++t)
+        acc[t] = 0.0f;
     for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
-        const Unit w = unit_of(g, u, nsb);
-        const int j = w.n * BN + row_in_tile;
-        float acc[TC_HALF];
+        const Unit w = tc_unit(g, u, nsb);
+        j = w.n * BN + row_in_tile;
+        had_unit = true;
 #pragma unroll
         for (int t = 0; t < TC_HALF; ++t)
             acc[t] = 0.0f;
@@ -938,7 +967,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             for (int t = 0; t < TC_HALF; ++t)
                 acc[t] = fmaf(-1.0f, mn[t], acc[t]);
         }
-        if (j < g.od) {
+        if (!clustered && j < g.od) {
 #pragma unroll
             for (int t = 0; t < TC_HALF; ++t) {
                 const int tok = t0 + t;
@@ -951,6 +980,37 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                 }
             }
         }
+    }
+    if (clustered) {
+        // The K slices' partial sums meet in rank 0 and are added in rank order (the
+        // result does not depend on scheduling).  The operand ring is idle by now: every
+        // copy into it has been consumed by an MMA that completed before the last item.
+        // Every thread passes both cluster barriers, also after an expired wait.
+        const uint32_t rank = cluster_ctarank();
+        float* scratch = reinterpret_cast<float*>(smem + TC_SMEM_B);
+        if (rank != 0) {
+#pragma unroll
+            for (int t = 0; t < TC_HALF; ++t)
+                scratch[(t0 + t) * BM + row_in_tile] = acc[t];
+        }
+        cluster_sync();
+        if (rank == 0 && ok && had_unit) {
+            for (int r = 1; r < g.kslices; ++r) {
+                const uint32_t rbase = cluster_map(sbase + TC_SMEM_B, static_cast<uint32_t>(r));
+#pragma unroll
+                for (int t = 0; t < TC_HALF; ++t)
+                    acc[t] += ld_cluster_f32(rbase + 4u * static_cast<uint32_t>((t0 + t) * BM + row_in_tile));
+            }
+            if (j < g.od) {
+#pragma unroll
+                for (int t = 0; t < TC_HALF; ++t) {
+                    const int tok = t0 + t;
+                    if (tok < g.M)
+                        g.out[static_cast<size_t>(tok) * g.ldy + j] = acc[t];
+                }
+            }
+        }
+        cluster_sync();
     }
 }
 
@@ -1071,8 +1131,57 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
         attr_set_mask.fetch_or(bit);
     }
     count_launch();
+    if (TC && a.kslices > 1) {   // one cluster of kslices CTAs per weight tile
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = static_cast<unsigned>(a.kslices);
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = TC_SMEM_ALLOC;
+        cfg.stream = s;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<TYPE, MODE, TC>, a);
+    }
     gemm_kernel<TYPE, MODE, TC><<<grid, NUM_THREADS, TC ? TC_SMEM_ALLOC : SMEM_ALLOC, s>>>(a);
     return cudaGetLastError();
+}
+
+// Clusters of `size` few-token CTAs that can be resident at once on this device (0 if
+// the query fails); cached per type, size and device ordinal.
+template <int TYPE>
+int tc_max_clusters(int size)
+{
+    static std::atomic<int> cache[5][64];   // size 0..4 (2..4 used) x device ordinal
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || size < 2 || size > 4)
+        return 0;
+    const int c = cache[size][dev].load();
+    if (c != 0)
+        return c > 0 ? c : 0;
+    int n = 0;
+    if (cudaFuncSetAttribute(gemm_kernel<TYPE, GEMM_Y, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TC_SMEM_ALLOC) == cudaSuccess) {
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = static_cast<unsigned>(size);
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(size));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = TC_SMEM_ALLOC;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<TYPE, GEMM_Y, true>, &cfg) != cudaSuccess)
+            n = 0;
+    }
+    cudaGetLastError();   // a failed query leaves no sticky error
+    cache[size][dev].store(n > 0 ? n : -1);
+    return n;
 }
 
 }  // namespace
@@ -1134,6 +1243,7 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     // token-row layout or the super-block kernel was selected.
     const bool tc = mode == GEMM_Y && !sb_first && sel != 1 && M <= TC_MAX_M;
     a.n_tok = tc ? ceil_div(M, 16) * 16 : 0;
+    a.kslices = 1;
 
     const int tiles = a.num_m * a.num_n;
     int grid = tiles < nsm ? tiles : nsm;
@@ -1145,8 +1255,28 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     // Tiles run as two K-halves added into a zeroed Y (two addends: the order cannot
     // change the sum): every tile when the launch has at most half as many tiles as SMs
     // (decode-tail shapes), else the last round's tiles when they fill at most half.
+    // Few tokens and few weight tiles: one cluster of kslices CTAs per tile, each on a
+    // slice of K (partial sums added in rank order in shared memory), as many CTAs as
+    // the clusters that fit at once allow.
+    if (tc) {
+        const int ts = ceil_div(od, BN);
+        for (int ks = 4; ks >= 2; --ks) {
+            if (nsb < ks || ts * ks > nsm)
+                continue;
+            const int fit = type == 14 ? tc_max_clusters<14>(ks) : tc_max_clusters<12>(ks);
+            if (fit >= ts) {
+                a.kslices = ks;
+                break;
+            }
+        }
+    }
+    if (a.kslices > 1) {
+        a.units = tiles * a.kslices;
+        a.full_units = a.units;
+        grid = a.units;
+    }
     int split = 0;
-    if (mode == GEMM_Y && !sb_first && nsb >= 2) {
+    if (mode == GEMM_Y && !sb_first && nsb >= 2 && a.kslices == 1) {
         if (2 * tiles <= nsm)
             split = tiles;
         else if (tiles > grid && rem > 0 && 2 * rem <= grid)
