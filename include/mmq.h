@@ -191,7 +191,9 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
  *    For M <= 64 it runs in a few-token layout: the weight tile is the MMA's A
  *    operand and the tokens its N (M rounded up to 16), the same arithmetic per
- *    element with only the tokens present copied and contracted.
+ *    element with only the tokens present copied and contracted; when the weight
+ *    tiles are few, each is split along K over a cluster of up to 4 CTAs whose
+ *    partial sums are added in a fixed order (deterministic).
  * Both: the q4_K min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo
  * tensor-core contraction (relative error about 2^-21 per product); Y is
  * deterministic for given inputs and kernel.  Rows t >= M and columns j >= od

@@ -42,7 +42,9 @@
 // Few tokens (M <= 64, Y only): the same roles in a transposed layout, with the
 // weight tile as the MMA's A operand on the TMEM lanes and the tokens as N (M rounded
 // up to 16), only those token rows copied, a deeper operand ring (7 stages with 8 KiB
-// token slots) and four 128-column TMEM items; see gemm_roles_tc.
+// token slots) and four 128-column TMEM items; when the weight tiles are few, each runs
+// on a cluster of up to 4 CTAs along K whose partial sums meet in rank 0 through
+// distributed shared memory; see gemm_roles_tc.
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
 // set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing
 // thread's wait + fence + commit cost about 80 cycles on top of a chunk's 128 cycles
@@ -1299,10 +1301,11 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
             *path_label = type == 14
                               ? "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A on the TMEM "
                                 "lanes, tokens as N = 16*ceil(M/16), tcgen05.mma kind::f16 on exact int codes, f32 d_a "
-                                "per chunk / d per super-block"
+                                "per chunk / d per super-block, few tiles split along K over a CTA cluster"
                               : "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A on the TMEM "
                                 "lanes, tokens as N = 16*ceil(M/16), tcgen05.mma kind::f16 on scale-folded exact int "
-                                "codes, tf32 hi/lo min term, f32 d_a per chunk / d per super-block";
+                                "codes, tf32 hi/lo min term, f32 d_a per chunk / d per super-block, few tiles split "
+                                "along K over a CTA cluster";
         return type == 14 ? launch_typed<14, GEMM_Y, true>(a, grid, s) : launch_typed<12, GEMM_Y, true>(a, grid, s);
     }
     if (type == 14) {
