@@ -197,6 +197,30 @@ def _type_id(t) -> int:
     return TYPES[t] if isinstance(t, str) else int(t)
 
 
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _require(cond, msg):
+    # ValueError rather than assert: a buffer too small for the kernel must never reach it
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_gemm_buffers(tid, packed, od, id_, qa, scales, M):
+    """Sizes first (testable without a GPU), then placement: every buffer a GEMM kernel reads
+    must hold what the size queries of the C ABI say it reads."""
+    _require(packed.is_contiguous() and _nbytes(packed) >= mmq_packed_weight_bytes(tid, od, id_),
+             f"packed holds {_nbytes(packed)} bytes, the ({od} x {id_}) weights need "
+             f"{mmq_packed_weight_bytes(tid, od, id_)}")
+    qb, sb = mmq_act_plane_bytes(M, id_)
+    _require(qa.is_contiguous() and _nbytes(qa) >= qb, f"qa holds {_nbytes(qa)} bytes, M={M} K={id_} needs {qb}")
+    _require(scales.is_contiguous() and _nbytes(scales) >= sb,
+             f"scales holds {_nbytes(scales)} bytes, M={M} K={id_} needs {sb}")
+    _require(packed.is_cuda and qa.is_cuda and scales.is_cuda, "packed, qa and scales must be CUDA tensors")
+    _require(packed.device == qa.device == scales.device, "packed, qa and scales must be on one device")
+
+
 def quantize_act(x, qa=None, scales=None, stream=None):
     """x: float32 CUDA tensor [M, K] (row stride >= K).  Returns (qa, scales) uint8 buffers."""
     torch = _torch()
@@ -221,6 +245,8 @@ def pack_weights(t, raw, od, id_, packed=None, stream=None):
     nb = mmq_packed_weight_bytes(tid, od, id_)
     if packed is None:
         packed = torch.empty(nb, dtype=torch.uint8, device=raw.device)
+    _require(packed.is_cuda and packed.is_contiguous() and _nbytes(packed) >= nb,
+             f"packed must be a contiguous CUDA buffer of at least {nb} bytes")
     mmq_pack_weights(tid, raw.data_ptr(), od, id_, packed.data_ptr(), _stream(stream))
     return packed
 
@@ -229,9 +255,12 @@ def gemm(t, packed, od, id_, qa, scales, M, Y=None, stream=None):
     """Y [M, od] float32 (allocated if not given; a given Y may have row stride >= od)."""
     torch = _torch()
     tid = _type_id(t)
+    _check_gemm_buffers(tid, packed, od, id_, qa, scales, M)
     if Y is None:
         Y = torch.empty((M, od), dtype=torch.float32, device=packed.device)
-    assert Y.dtype == torch.float32 and Y.stride(1) == 1 and Y.shape[0] >= M
+    _require(Y.dtype == torch.float32 and Y.dim() == 2 and Y.stride(1) == 1 and Y.shape[0] >= M
+             and Y.shape[1] >= od and Y.is_cuda and Y.device == packed.device,
+             f"Y must be a float32 CUDA tensor [>= {M}, >= {od}] with unit column stride on the weights' device")
     fn = mmq_gemm_q6k if tid == MMQ_Q6_K else mmq_gemm_q4k
     fn(packed.data_ptr(), od, id_, qa.data_ptr(), scales.data_ptr(), M, Y.data_ptr(), Y.stride(0), _stream(stream))
     return Y
@@ -242,6 +271,7 @@ def gemm_dots(t, packed, od, id_, qa, scales, M, stream=None):
     (nsub = id/32, or id/16 for q6_K tensors with plain codes; see include/mmq.h)."""
     torch = _torch()
     tid = _type_id(t)
+    _check_gemm_buffers(tid, packed, od, id_, qa, scales, M)
     nsub = id_ // 16 if tid == MMQ_Q6_K else id_ // 32
     dots = torch.full((M * od * nsub,), float("nan"), dtype=torch.float32, device=packed.device)
     mmq_debug_gemm_dots(tid, packed.data_ptr(), od, id_, qa.data_ptr(), scales.data_ptr(), M, dots.data_ptr(),

@@ -123,3 +123,26 @@ def test_status_strings_and_labels(mmq_lib):
         assert mmq.mmq_status_string(st).startswith(mmq.STATUS[st])
     assert "sm_103a" in mmq.mmq_version()
     assert isinstance(mmq.mmq_last_path(), str)
+
+
+def test_python_helpers_refuse_short_or_host_buffers(mmq_lib):
+    """The tensor helpers check every buffer a GEMM kernel reads against the size queries
+    before calling the library, so a wrong buffer raises instead of reaching the GPU."""
+    torch = pytest.importorskip("torch")
+    od, id_, M = 300, 768, 20
+    nb = mmq.mmq_packed_weight_bytes(mmq.MMQ_Q4_K, od, id_)
+    qb, sb = mmq.mmq_act_plane_bytes(M, id_)
+    p = torch.empty(nb, dtype=torch.uint8)
+    q = torch.empty(qb, dtype=torch.uint8)
+    s = torch.empty(sb, dtype=torch.uint8)
+    for args, what in (((p[:-1], q, s), "packed"), ((p, q[:-16], s), "qa"), ((p, q, s[:-8]), "scales")):
+        with pytest.raises(ValueError, match=what):
+            mmq.gemm("q4_K", args[0], od, id_, args[1], args[2], M)
+        with pytest.raises(ValueError, match=what):
+            mmq.gemm_dots("q4_K", args[0], od, id_, args[1], args[2], M)
+    with pytest.raises(ValueError, match="qa"):          # planes sized for fewer tokens
+        mmq.gemm("q4_K", p, od, id_, q, s, 200)
+    with pytest.raises(ValueError, match="packed"):      # weights of another shape
+        mmq.gemm("q6_K", p, od + 128, id_, q, s, M)
+    with pytest.raises(ValueError, match="CUDA"):        # right sizes, host memory
+        mmq.gemm("q4_K", p, od, id_, q, s, M)
