@@ -224,14 +224,20 @@ def _check_gemm_buffers(tid, packed, od, id_, qa, scales, M):
 def quantize_act(x, qa=None, scales=None, stream=None):
     """x: float32 CUDA tensor [M, K] (row stride >= K).  Returns (qa, scales) uint8 buffers."""
     torch = _torch()
-    assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    _require(x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1,
+             "x must be a float32 [M, K] tensor with unit column stride")
     M, K = x.shape
     qb, sb = mmq_act_plane_bytes(M, K)
+    _require(x.is_cuda, "x must be a CUDA tensor")
     if qa is None:
         qa = torch.empty(qb, dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty(sb, dtype=torch.uint8, device=x.device)
-    assert qa.numel() * qa.element_size() >= qb and scales.numel() * scales.element_size() >= sb
+    _require(qa.is_contiguous() and _nbytes(qa) >= qb, f"qa holds {_nbytes(qa)} bytes, M={M} K={K} needs {qb}")
+    _require(scales.is_contiguous() and _nbytes(scales) >= sb,
+             f"scales holds {_nbytes(scales)} bytes, M={M} K={K} needs {sb}")
+    _require(qa.is_cuda and scales.is_cuda and qa.device == x.device == scales.device,
+             "qa and scales must be CUDA tensors on x's device")
     mmq_quantize_act(x.data_ptr(), M, K, x.stride(0), qa.data_ptr(), scales.data_ptr(), _stream(stream))
     return qa, scales
 
@@ -240,8 +246,10 @@ def pack_weights(t, raw, od, id_, packed=None, stream=None):
     """raw: uint8 CUDA tensor holding od * id/256 super-blocks.  Returns the packed buffer."""
     torch = _torch()
     tid = _type_id(t)
-    assert raw.is_cuda and raw.dtype == torch.uint8 and raw.is_contiguous()
-    assert raw.numel() == od * (id_ // 256) * BLOCK_BYTES[tid]
+    _require(raw.dtype == torch.uint8 and raw.is_contiguous(), "raw must be a contiguous uint8 tensor")
+    _require(raw.numel() == od * (id_ // 256) * BLOCK_BYTES[tid],
+             f"raw holds {raw.numel()} bytes, {od} x {id_} {t} weights are {od * (id_ // 256) * BLOCK_BYTES[tid]}")
+    _require(raw.is_cuda, "raw must be a CUDA tensor")
     nb = mmq_packed_weight_bytes(tid, od, id_)
     if packed is None:
         packed = torch.empty(nb, dtype=torch.uint8, device=raw.device)

@@ -146,3 +146,17 @@ def test_python_helpers_refuse_short_or_host_buffers(mmq_lib):
         mmq.gemm("q6_K", p, od + 128, id_, q, s, M)
     with pytest.raises(ValueError, match="CUDA"):        # right sizes, host memory
         mmq.gemm("q4_K", p, od, id_, q, s, M)
+
+
+def test_quantize_and_pack_helpers_refuse_bad_inputs(mmq_lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4, 512)
+    with pytest.raises(ValueError, match="float32"):
+        mmq.quantize_act(x.double())
+    with pytest.raises(ValueError, match="CUDA"):
+        mmq.quantize_act(x)
+    raw = torch.zeros(3 * 2 * 144, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="raw holds"):
+        mmq.pack_weights("q4_K", raw[:-1], 3, 512)
+    with pytest.raises(ValueError, match="CUDA"):
+        mmq.pack_weights("q4_K", raw, 3, 512)
