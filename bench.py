@@ -293,7 +293,7 @@ def small_m_case(lib, dev, stream, sptr, peaks, typ="q6_K", od=4097, id_=11008, 
     """FFN-down q6_K 4097x11008 at M = 1 token: the weight-streaming path against HBM.
 
     Algorithmic bytes = the raw k-quant blocks (210 B per 256 values); `copies` packed
-    weight buffers are rotated so the raw plane (~37 MB each) cannot stay in L2."""
+    weight buffers are rotated so the raw plane (39.5 MB each) cannot stay in L2."""
     import torch
     import quant_int8_mmq_gb300 as mmq
     raw = torch.from_numpy(synth.blocks(typ, od, id_, 77).reshape(-1)).to(dev)
@@ -327,10 +327,11 @@ def small_m_case(lib, dev, stream, sptr, peaks, typ="q6_K", od=4097, id_=11008, 
         raise RuntimeError("device error in the small-M case")
     t = a.elapsed_time(b) * 1e-3 / reps
     alg = od * (id_ // 256) * (210 if typ == "q6_K" else 144)
+    raw_plane_mb = mmq.mmq_packed_weight_layout(mmq.TYPES[typ], od, id_)["raw"][1] / 1e6
     return {"workload": f"{typ} {od}x{id_} (FFN down, odd od), M={M}", "us": t * 1e6,
             "achieved_gbs": alg / t / 1e9, "peak_gbs": peaks["hbm_gbs"],
             "frac_hbm": alg / t / 1e9 / peaks["hbm_gbs"], "bytes_def": "raw block bytes od*id/256*210 per launch",
-            "path": mmq.mmq_last_path(), "l2": f"{copies} rotated weight copies (raw plane 37 MB each)",
+            "path": mmq.mmq_last_path(), "l2": f"{copies} rotated weight copies (raw plane {raw_plane_mb:.1f} MB each, {copies * raw_plane_mb:.0f} MB in all)",
             "timing": f"one CUDA graph of {reps} launches, CUDA events around its replay"}
 
 
