@@ -30,9 +30,12 @@
  *  - K = id must be a multiple of 256 (one super-block); od >= 1 may be odd; M >= 1.
  *  - Buffers read by bulk copies (qa, scales, packed) must be 16-byte aligned,
  *    else MMQ_ERR_ALIGN.  x and Y need 4-byte alignment.
- *  - Every bounded wait inside a kernel gives up after about two seconds, sets a
- *    sticky device error word and lets the kernel exit; mmq_get_device_error()
- *    reports (and clears) it.  Results of a launch that timed out are undefined.
+ *  - Every bounded wait inside a kernel gives up after about two seconds, sets the
+ *    library's one sticky device error word (one per device) and lets the kernel
+ *    exit; mmq_get_device_error() reports and clears it, whichever kernel set it.
+ *    Results of a launch that timed out are undefined, and so are those of launches
+ *    queued after it until the word is cleared (their waits give up early once they
+ *    see it set).
  *  - Calls may come from several host threads; the one piece of shared host
  *    state is the label mmq_last_path() returns (the most recent GEMM launch
  *    of the process).
@@ -225,10 +228,24 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
  *      SM count, else the chunk kernel; plain q6_K codes: the chunk kernel; the
  *      chunk kernel takes its few-token layout when M <= 64;
  *   1: the chunk kernel for every case, always in its 128-token tile layout;
- *   2: the super-block kernel for every scale-folded case.
+ *   2: the super-block kernel for every scale-folded case;
+ *   3: as 0, but the few-token layout never splits a tile over a CTA cluster
+ *      (tiles are split into two K-halves instead when they are few).
  * Returns MMQ_ERR_ARG for any other value.  Not thread-safe against GEMM calls
  * in flight on other host threads. */
 mmq_status mmq_debug_select_large_m_kernel(int which);
+
+/* Debug/verification of the timeout path (a loud error, never a silent wrong
+ * result: [r56] §3.1).  Arms a one-shot injection for the next GEMM launch that
+ * runs a tile kernel (M > MMQ_SMALL_M): its waits give up after limit_ns
+ * (1 us .. 2 s) instead of about two seconds, and the producer of its first CTA
+ * leaves operand fill number `fill` (0-based, counted over that CTA's k-blocks)
+ * out, so the wait for it runs out, the launch exits early and
+ * mmq_get_device_error() then returns MMQ_ERR_TIMEOUT (and clears the word).
+ * That launch takes no CTA-cluster split.  Its Y is undefined.  fill < 0
+ * disarms a pending injection.  MMQ_ERR_ARG for a limit outside the range.
+ * Process-wide host state; no CUDA call. */
+mmq_status mmq_debug_inject_wait_timeout(int fill, unsigned long long limit_ns);
 
 /* Synchronizes `s`, then reports and clears the sticky device error word:
  * MMQ_ERR_TIMEOUT if a bounded wait expired since the last call, MMQ_ERR_CUDA

@@ -22,6 +22,7 @@ __all__ = [
     "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_quantize_act", "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
     "mmq_pack_weights", "mmq_convert_ggml_blocks", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
+    "mmq_debug_inject_wait_timeout",
     "mmq_get_device_error", "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
     "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
 ]
@@ -71,6 +72,7 @@ def load():
             "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
             "mmq_debug_gemm_dots": [I, P, I, I, P, P, I, P, P],
             "mmq_debug_select_large_m_kernel": [I],
+            "mmq_debug_inject_wait_timeout": [I, ctypes.c_ulonglong],
             "mmq_get_device_error": [P],
         }
         for name, args in sig.items():
@@ -153,6 +155,12 @@ def mmq_debug_gemm_dots(t, packed, od, id_, qa, scales, M, dots, stream=0):
 
 def mmq_debug_select_large_m_kernel(which: int):
     _check(load().mmq_debug_select_large_m_kernel(which), "mmq_debug_select_large_m_kernel")
+
+
+def mmq_debug_inject_wait_timeout(fill: int, limit_ns: int = 0):
+    """Arm (fill >= 0) or disarm (fill < 0) the one-shot wait-timeout injection of the
+    next tile-GEMM launch (see include/mmq.h)."""
+    _check(load().mmq_debug_inject_wait_timeout(fill, limit_ns), "mmq_debug_inject_wait_timeout")
 
 
 def mmq_get_device_error(stream=0) -> int:

@@ -13,8 +13,73 @@
 namespace mmq {
 namespace {
 std::atomic<unsigned long long> g_launches{0};
+
+// The sticky device error word of the whole library (one per device the library
+// is loaded on).  Kernels receive its address in their arguments; nothing else
+// names it in device code.
+__device__ unsigned int g_device_error_word;
+std::atomic<unsigned int*> g_error_word_addr[64];   // per device ordinal, looked up once
+
+// One-shot wait-timeout injection (verification only): fill index, wait limit.
+std::atomic<int> g_inject_fill{-1};
+std::atomic<unsigned long long> g_inject_limit_ns{0};
 }  // namespace
+
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t device_error_word(unsigned int** word)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64) {
+        unsigned int* c = g_error_word_addr[dev].load(std::memory_order_acquire);
+        if (c != nullptr) {
+            *word = c;
+            return cudaSuccess;
+        }
+    }
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_device_error_word);
+    if (e != cudaSuccess)
+        return e;
+    *word = static_cast<unsigned int*>(a);
+    if (dev >= 0 && dev < 64)
+        g_error_word_addr[dev].store(*word, std::memory_order_release);
+    return cudaSuccess;
+}
+
+cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned int* value)
+{
+    *value = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaMemcpyFromSymbol(value, g_device_error_word, sizeof(unsigned int));
+    if (e != cudaSuccess)
+        return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(unsigned int));
+}
+
+void arm_wait_injection(int fill, unsigned long long limit_ns)
+{
+    g_inject_limit_ns.store(limit_ns);
+    g_inject_fill.store(fill < 0 ? -1 : fill);
+}
+
+cudaError_t take_wait_ctl(WaitCtl* wc, bool* injected)
+{
+    const cudaError_t e = device_error_word(&wc->err);
+    if (e != cudaSuccess)
+        return e;
+    const int fill = g_inject_fill.exchange(-1);
+    *injected = fill >= 0;
+    wc->withhold_fill = fill;
+    wc->limit_ns = *injected ? g_inject_limit_ns.load() : WAIT_LIMIT_NS;
+    return cudaSuccess;
+}
 }  // namespace mmq
 
 namespace {
@@ -226,7 +291,7 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
 
 mmq_status mmq_debug_select_large_m_kernel(int which)
 {
-    if (which < 0 || which > 2)
+    if (which < 0 || which > 3)
         return MMQ_ERR_ARG;
     mmq::select_large_m_kernel(which);
     return MMQ_OK;
@@ -234,13 +299,25 @@ mmq_status mmq_debug_select_large_m_kernel(int which)
 
 unsigned long long mmq_launch_count(void) { return mmq::g_launches.load(std::memory_order_relaxed); }
 
+mmq_status mmq_debug_inject_wait_timeout(int fill, unsigned long long limit_ns)
+{
+    if (fill < 0) {
+        mmq::arm_wait_injection(-1, 0);
+        return MMQ_OK;
+    }
+    if (limit_ns < 1000ull || limit_ns > mmq::WAIT_LIMIT_NS)
+        return MMQ_ERR_ARG;
+    mmq::arm_wait_injection(fill, limit_ns);
+    return MMQ_OK;
+}
+
 mmq_status mmq_get_device_error(mmq_stream_t s)
 {
     const mmq_status st = check_device();
     if (st != MMQ_OK)
         return st;
     unsigned int word = 0;
-    const cudaError_t e = mmq::gemm_read_and_clear_error(reinterpret_cast<cudaStream_t>(s), &word);
+    const cudaError_t e = mmq::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(s), &word);
     if (e != cudaSuccess)
         return MMQ_ERR_CUDA;
     return word ? MMQ_ERR_TIMEOUT : MMQ_OK;

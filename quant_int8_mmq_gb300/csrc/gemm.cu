@@ -87,7 +87,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int TC_MAX_M = 64;
 constexpr int TC_COLS = 64;
 constexpr int TC_HALF = TC_COLS / 2;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // Register split: the launch gives every thread LAUNCH_REGS; the control warpgroup
 // drops to CTRL_REGS and the two promotion warpgroups grow to PROMO_REGS out of the
 // same pool (the host checks the compiled count before launching).
@@ -156,7 +155,11 @@ static_assert(TC_SMEM_A % 1024 == 0 && TC_A_BYTES % 1024 == 0 && TC_SMEM_SB % 16
               "alignment (few-token layout)");
 static_assert(MIN_AM_BYTES <= TC_A_BYTES && MIN_BM_BYTES <= TILE_BYTES, "min-term operands fit a few-token stage");
 static_assert(2 * TC_COLS <= static_cast<int>(TC_ITEM_COLS), "an item holds two chunks (or sub-blocks) of columns");
-static_assert(TC_MAX_M * BM * 4 <= TC_STAGES * TILE_BYTES, "K-slice partial sums fit the idle weight stages");
+// K-slice partial sums of a cluster rank (one float per weight row and token) and, after
+// them, one ok flag per promotion warp, in the rank's idle weight stages.
+constexpr int TC_OKF_OFF = TC_MAX_M * BM * 4;
+static_assert(TC_OKF_OFF + NUM_PROMO_WARPS * 4 <= TC_STAGES * TILE_BYTES,
+              "K-slice partial sums and ok flags fit the idle weight stages");
 
 struct GemmArgs {
     const uint8_t* A;     // activation code tiles      [num_m][nkb][16 KiB]
@@ -178,32 +181,36 @@ struct GemmArgs {
                           // super-block kernel, launched first, has written Y)
     int n_tok;            // few-token layout: MMA N (M rounded up to 16, <= TC_MAX_M)
     int kslices;          // few-token layout: CTAs per weight tile (a cluster along K), 1 = none
+    unsigned int* err;    // the library's sticky error word
+    unsigned long long wait_ns;   // limit of each bounded wait
+    int withhold;         // verification: operand fill CTA 0's producer leaves out (-1: none)
 };
 
 // Bounded wait that ignores the error word (used only to drain our own copies /
 // MMAs in flight before the CTA exits; those always complete).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ void drain_wait(const GemmArgs& g, uint32_t bar, uint32_t parity)
 {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-            atomicOr(&g_error_word, 1u);
-            return;
-        }
-    }
+    mbar_drain_wait(bar, parity, WAIT_LIMIT_NS, g.err);
 }
 
 // Bounded wait of the single producer / MMA thread.
-__device__ __forceinline__ bool ctl_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool ctl_wait(const GemmArgs& g, uint32_t bar, uint32_t parity)
 {
-    return mbar_wait(bar, parity, WAIT_LIMIT_NS);
+    return mbar_wait(bar, parity, g.wait_ns, g.err);
 }
 
 // Bounded wait by a whole warp; the verdict is made warp-uniform so that every lane
 // takes the same branch after it.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait(const GemmArgs& g, uint32_t bar, uint32_t parity)
 {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, WAIT_LIMIT_NS));
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, g.wait_ns, g.err));
+}
+
+// Verification: the operand fill of this CTA's producer that is left out (never
+// armed, never copied) so that the consumers' wait for it runs out; ~0 for none.
+__device__ __forceinline__ uint32_t withheld_fill(const GemmArgs& g)
+{
+    return (blockIdx.x == 0 && g.withhold >= 0) ? static_cast<uint32_t>(g.withhold) : ~0u;
 }
 
 // Shared-memory descriptor of a 128 x 8 tf32 tile in the no-swizzle K-major
@@ -317,6 +324,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sb = 0;  // fills issued on each ring
             constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
+            const uint32_t skip = withheld_fill(g);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
@@ -327,7 +335,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {  // a new super-block
                         const int s = kb >> 2;
-                        if (!ctl_wait(bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -347,9 +355,14 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         sb.next();
                         ++n_sb;
                     }
-                    if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                         ok = false;
                         break;
+                    }
+                    if (n_ops == skip) {
+                        op.next();
+                        ++n_ops;
+                        continue;
                     }
                     const uint32_t fo = bar(BAR_FULL + op.i);
                     mbar_arrive_expect_tx(fo, 2 * TILE_BYTES);
@@ -364,7 +377,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     // The tile's min-term operands, one super-block per stage: token hi/lo
                     // tiles in the A slot, weight hi/lo tiles in the B slot.
                     for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -381,9 +394,10 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             }
             // Our copies must have landed before the CTA may exit.
             for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i)
-                drain_wait(bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
+                if (i != skip)
+                    drain_wait(g, bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
             for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
-                drain_wait(bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
+                drain_wait(g, bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
@@ -394,7 +408,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
-                    if (!ctl_wait(bar(BAR_FULL + op.i), op.ph)) {
+                    if (!ctl_wait(g, bar(BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -404,7 +418,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     // (the descriptor's address field counts 16-byte units).
                     if (FOLDED) {
                         // one item per k-block: one wait, one fence, one commit for two chunks
-                        if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -420,7 +434,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     } else {
 #pragma unroll
                         for (int cc = 0; cc < 2; ++cc) {
-                            if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                            if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                                 ok = false;
                                 break;
                             }
@@ -441,13 +455,13 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     // Min-term contraction of the whole tile, sum over chunks of
                     // (d_a*ssum)(dmin*m), one super-block (8 chunks, hi/lo split) per stage
                     // into one item, consumed by the promotion once per tile.
-                    if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
                     for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(bar(BAR_FULL + op.i), op.ph)) {
+                        if (!ctl_wait(g, bar(BAR_FULL + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
@@ -469,7 +483,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 }
             }
             umma_commit(bar(BAR_DRAIN));  // every MMA issued so far has completed
-            drain_wait(bar(BAR_DRAIN), 0u);
+            drain_wait(g, bar(BAR_DRAIN), 0u);
         }
         __syncwarp();
         return;
@@ -503,7 +517,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             acc[i] = make_float2(0.0f, 0.0f);
         for (int s = w.sb0; s < w.sb1; ++s) {
             const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
-            if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph)) {
+            if (!warp_wait(g, bar(BAR_SBFULL + sb.i), sb.ph)) {
                 ok = false;
                 break;
             }
@@ -514,7 +528,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 inner[i] = make_float2(0.0f, 0.0f);
             for (int k2 = 0; k2 < 4 && ok; ++k2) {             // the super-block's four k-blocks
                 if (FOLDED) {
-                    if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
+                    if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
                         ok = false;
                         break;
                     }
@@ -553,7 +567,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
                         const float2 da2 = make_float2(da, da);
                         const int s0 = 2 * k;
-                        if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
+                        if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
                             ok = false;
                             break;
                         }
@@ -612,7 +626,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             break;
         if (Q4) {
             // acc -= the tile's min term, one item per tile
-            if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
+            if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
                 ok = false;
                 break;
             }
@@ -700,6 +714,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sb = 0;
             constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
+            const uint32_t skip = withheld_fill(g);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = tc_unit(g, u, nsb);
@@ -709,7 +724,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {
                         const int s = kb >> 2;
-                        if (!ctl_wait(bar(TC_BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(TC_BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -727,9 +742,14 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                         sb.next();
                         ++n_sb;
                     }
-                    if (!ctl_wait(bar(TC_BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(TC_BAR_EMPTY + op.i), op.ph ^ 1u)) {
                         ok = false;
                         break;
+                    }
+                    if (n_ops == skip) {
+                        op.next();
+                        ++n_ops;
+                        continue;
                     }
                     const uint32_t fo = bar(TC_BAR_FULL + op.i);
                     mbar_arrive_expect_tx(fo, TILE_BYTES + a_bytes);
@@ -742,7 +762,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                 }
                 if (Q4 && ok) {
                     for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(bar(TC_BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(TC_BAR_EMPTY + op.i), op.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -758,9 +778,10 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                 }
             }
             for (uint32_t i = (n_ops > TC_STAGES ? n_ops - TC_STAGES : 0); i < n_ops; ++i)
-                drain_wait(bar(TC_BAR_FULL + i % TC_STAGES), (i / TC_STAGES) & 1u);
+                if (i != skip)
+                    drain_wait(g, bar(TC_BAR_FULL + i % TC_STAGES), (i / TC_STAGES) & 1u);
             for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
-                drain_wait(bar(TC_BAR_SBFULL + i % SBR), (i / SBR) & 1u);
+                drain_wait(g, bar(TC_BAR_SBFULL + i % SBR), (i / SBR) & 1u);
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
             const uint32_t idesc = idesc_f16_f32(BM, g.n_tok);
@@ -771,14 +792,14 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = tc_unit(g, u, nsb);
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
-                    if (!ctl_wait(bar(TC_BAR_FULL + op.i), op.ph)) {
+                    if (!ctl_wait(g, bar(TC_BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
                     const uint64_t w0 = sdesc_k_sw128(sbase + TC_SMEM_B + op.i * TILE_BYTES);  // weights: A
                     const uint64_t x0 = sdesc_k_sw128(sbase + TC_SMEM_A + op.i * TC_A_BYTES);  // tokens: B
                     if (FOLDED) {
-                        if (!ctl_wait(bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -794,7 +815,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                     } else {
 #pragma unroll
                         for (int cc = 0; cc < 2; ++cc) {
-                            if (!ctl_wait(bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                            if (!ctl_wait(g, bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                                 ok = false;
                                 break;
                             }
@@ -812,13 +833,13 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                     op.next();
                 }
                 if (Q4 && ok) {
-                    if (!ctl_wait(bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
                     for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(bar(TC_BAR_FULL + op.i), op.ph)) {
+                        if (!ctl_wait(g, bar(TC_BAR_FULL + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
@@ -840,10 +861,11 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                 }
             }
             umma_commit(bar(TC_BAR_DRAIN));
-            drain_wait(bar(TC_BAR_DRAIN), 0u);
+            drain_wait(g, bar(TC_BAR_DRAIN), 0u);
         }
         __syncwarp();
-        if (g.kslices > 1) {   // the promotion warps' two cluster barriers
+        if (g.kslices > 1) {   // the CTA barrier and the two cluster barriers of the promotion warps
+            named_bar_sync(1, NUM_THREADS);
             cluster_sync();
             cluster_sync();
         }
@@ -882,7 +904,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
             acc[t] = 0.0f;
         for (int s = w.sb0; s < w.sb1; ++s) {
             const uint8_t* sbe = smem + TC_SMEM_SB + sb.i * SB_BYTES;
-            if (!warp_wait(bar(TC_BAR_SBFULL + sb.i), sb.ph)) {
+            if (!warp_wait(g, bar(TC_BAR_SBFULL + sb.i), sb.ph)) {
                 ok = false;
                 break;
             }
@@ -895,7 +917,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                 inner[t] = 0.0f;
             for (int k2 = 0; k2 < 4 && ok; ++k2) {
                 if (FOLDED) {
-                    if (!warp_wait(bar(TC_BAR_TFULL + item.i), item.ph)) {
+                    if (!warp_wait(g, bar(TC_BAR_TFULL + item.i), item.ph)) {
                         ok = false;
                         break;
                     }
@@ -920,7 +942,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
                     const float* scp = reinterpret_cast<const float*>(sbe + SB_X_OFF);
                     for (int cc = 0; cc < 2; ++cc) {
                         const int k = 2 * k2 + cc;
-                        if (!warp_wait(bar(TC_BAR_TFULL + item.i), item.ph)) {
+                        if (!warp_wait(g, bar(TC_BAR_TFULL + item.i), item.ph)) {
                             ok = false;
                             break;
                         }
@@ -957,7 +979,7 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
         if (!ok)
             break;
         if (Q4) {
-            if (!warp_wait(bar(TC_BAR_TFULL + item.i), item.ph)) {
+            if (!warp_wait(g, bar(TC_BAR_TFULL + item.i), item.ph)) {
                 ok = false;
                 break;
             }
@@ -985,18 +1007,32 @@ __device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, 
     }
     if (clustered) {
         // The K slices' partial sums meet in rank 0 and are added in rank order (the
-        // result does not depend on scheduling).  The operand ring is idle by now: every
-        // copy into it has been consumed by an MMA that completed before the last item.
-        // Every thread passes both cluster barriers, also after an expired wait.
+        // result does not depend on scheduling).  The CTA barrier first lets the
+        // producer and the MMA thread finish draining their copies and MMAs, so that the
+        // operand ring is idle before the partial sums overwrite it.  Every rank also
+        // leaves the ok flag of each promotion warp, and rank 0 stores Y only if every
+        // flag of every rank is set.  Every thread passes the CTA barrier and both
+        // cluster barriers, also after an expired wait.
         const uint32_t rank = cluster_ctarank();
         float* scratch = reinterpret_cast<float*>(smem + TC_SMEM_B);
+        named_bar_sync(1, NUM_THREADS);
         if (rank != 0) {
 #pragma unroll
             for (int t = 0; t < TC_HALF; ++t)
                 scratch[(t0 + t) * BM + row_in_tile] = acc[t];
         }
+        if (lane == 0)
+            reinterpret_cast<int*>(smem + TC_SMEM_B + TC_OKF_OFF)[pw] = ok ? 1 : 0;
         cluster_sync();
-        if (rank == 0 && ok && had_unit) {
+        bool all_ok = ok;
+        if (rank == 0) {
+            for (int r = 0; r < g.kslices; ++r) {
+                const uint32_t fbase = cluster_map(sbase + TC_SMEM_B + TC_OKF_OFF, static_cast<uint32_t>(r));
+                for (int w = 0; w < NUM_PROMO_WARPS; ++w)
+                    all_ok = all_ok && ld_cluster_u32(fbase + 4u * static_cast<uint32_t>(w)) != 0u;
+            }
+        }
+        if (rank == 0 && all_ok && had_unit) {
             for (int r = 1; r < g.kslices; ++r) {
                 const uint32_t rbase = cluster_map(sbase + TC_SMEM_B, static_cast<uint32_t>(r));
 #pragma unroll
@@ -1178,10 +1214,13 @@ int tc_max_clusters(int size)
         cfg.dynamicSmemBytes = TC_SMEM_ALLOC;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<TYPE, GEMM_Y, true>, &cfg) != cudaSuccess)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<TYPE, GEMM_Y, true>, &cfg) != cudaSuccess) {
             n = 0;
+            cudaGetLastError();   // clear the failed query's error, and only that one
+        }
+    } else {
+        cudaGetLastError();
     }
-    cudaGetLastError();   // a failed query leaves no sticky error
     cache[size][dev].store(n > 0 ? n : -1);
     return n;
 }
@@ -1209,8 +1248,16 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     const int sel = g_large_m_kernel.load();
     const bool sb_fills = static_cast<long long>(ceil_div(M, BM)) * ceil_div(od, 2 * BN) >= nsm;
     const bool sb_first = mode == GEMM_Y && (sel == 2 || (sel == 0 && sb_fills));
+    WaitCtl wc;
+    bool injected = false;
+    e = take_wait_ctl(&wc, &injected);
+    if (e != cudaSuccess)
+        return e;
     if (sb_first) {
-        e = launch_gemm_sb(type, packed, od, id, qa, scales, M, out, ldy, s);
+        e = launch_gemm_sb(type, packed, od, id, qa, scales, M, out, ldy, s, wc);
+        // the chunk kernel launched after it (q6_K) only reads the flag or runs plain codes
+        wc.withhold_fill = -1;
+        wc.limit_ns = WAIT_LIMIT_NS;
         if (e != cudaSuccess)
             return e;
         if (type == 12) {
@@ -1241,6 +1288,9 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.num_n = ceil_div(od, BN);
     a.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (ldy & 3) == 0) ? 1 : 0;
     a.skip_folded = sb_first ? 1 : 0;
+    a.err = wc.err;
+    a.wait_ns = wc.limit_ns;
+    a.withhold = wc.withhold_fill;
     // Few tokens: the tokens become the MMA's N (one accumulator column each) unless the
     // token-row layout or the super-block kernel was selected.
     const bool tc = mode == GEMM_Y && !sb_first && sel != 1 && M <= TC_MAX_M;
@@ -1260,7 +1310,9 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     // Few tokens and few weight tiles: one cluster of kslices CTAs per tile, each on a
     // slice of K (partial sums added in rank order in shared memory), as many CTAs as
     // the clusters that fit at once allow.
-    if (tc) {
+    // (No cluster split under a wait-timeout injection or when selector 3 asks for the
+    // few-token layout without it: a cluster barrier has no time limit.)
+    if (tc && !injected && sel != 3) {
         const int ts = ceil_div(od, BN);
         for (int ks = 4; ks >= 2; --ks) {
             if (nsb < ks || ts * ks > nsm)
@@ -1297,15 +1349,37 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     }
 
     if (tc) {
-        if (path_label)
-            *path_label = type == 14
-                              ? "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A on the TMEM "
-                                "lanes, tokens as N = 16*ceil(M/16), tcgen05.mma kind::f16 on exact int codes, f32 d_a "
-                                "per chunk / d per super-block, few tiles split along K over a CTA cluster"
-                              : "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A on the TMEM "
-                                "lanes, tokens as N = 16*ceil(M/16), tcgen05.mma kind::f16 on scale-folded exact int "
-                                "codes, tf32 hi/lo min term, f32 d_a per chunk / d per super-block, few tiles split "
-                                "along K over a CTA cluster";
+        if (path_label) {
+            // the K split actually taken: a cluster of S CTAs per tile, two K-halves, or none
+            static const char* const lab[2][5] = {
+                {"q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
+                 "super-block; K split: none",
+                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
+                 "super-block; K split: two K-halves added into a zeroed Y",
+                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
+                 "super-block; K split: cluster of S=2 CTAs",
+                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
+                 "super-block; K split: cluster of S=3 CTAs",
+                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
+                 "super-block; K split: cluster of S=4 CTAs"},
+                {"q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: none",
+                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: two K-halves added "
+                 "into a zeroed Y",
+                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: cluster of S=2 CTAs",
+                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: cluster of S=3 CTAs",
+                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
+                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: cluster of S=4 CTAs"}};
+            *path_label = lab[type == 14 ? 1 : 0][a.kslices > 1 ? a.kslices : (split > 0 ? 1 : 0)];
+        }
         return type == 14 ? launch_typed<14, GEMM_Y, true>(a, grid, s) : launch_typed<12, GEMM_Y, true>(a, grid, s);
     }
     if (type == 14) {
@@ -1322,19 +1396,6 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
         *path_label = "q4_K: chunk GEMM, tcgen05.mma kind::f16 128x128x16 on scale-folded exact int codes, two "
                       "256-column TMEM items, tf32 hi/lo min term per tile, f32 d_a per chunk / d per super-block";
     return mode == GEMM_Y ? launch_typed<12, GEMM_Y>(a, grid, s) : launch_typed<12, GEMM_DOTS>(a, grid, s);
-}
-
-cudaError_t gemm_read_and_clear_error(cudaStream_t s, unsigned int* word)
-{
-    *word = 0;
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess)
-        return e;
-    e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned int));
-    if (e != cudaSuccess)
-        return e;
-    const unsigned int zero = 0;
-    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned int));
 }
 
 }  // namespace mmq

@@ -75,7 +75,6 @@ constexpr int NUM_PROMO_WARPS = 8;
 constexpr int COLS_PER_WARP = BN / 2;  // 128
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ITEM_COLS = BN;     // one super-block accumulator
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // Register split out of the launch's 128 x 512: control 56, converter 56,
 // promotion 200 (128 tile accumulators + one 32-column load per thread).
 constexpr int LAUNCH_REGS = 128;
@@ -147,27 +146,24 @@ struct SbArgs {
     int num_n128;         // 128-row weight tiles in the packed planes
     int units, full_units, nsb_half;
     int vec_store;        // Y is 8-byte aligned and ldy is even (float2 stores)
+    unsigned int* err;    // the library's sticky error word
+    unsigned long long wait_ns;   // limit of each bounded wait
+    int withhold;         // verification: operand fill CTA 0's producer leaves out (-1: none)
 };
 
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ void drain_wait(const SbArgs& g, uint32_t bar, uint32_t parity)
 {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-            atomicOr(&g_error_word, 1u);
-            return;
-        }
-    }
+    mbar_drain_wait(bar, parity, WAIT_LIMIT_NS, g.err);
 }
 
-__device__ __forceinline__ bool ctl_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool ctl_wait(const SbArgs& g, uint32_t bar, uint32_t parity)
 {
-    return mbar_wait(bar, parity, WAIT_LIMIT_NS);
+    return mbar_wait(bar, parity, g.wait_ns, g.err);
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait(const SbArgs& g, uint32_t bar, uint32_t parity)
 {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, WAIT_LIMIT_NS));
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, g.wait_ns, g.err));
 }
 
 // 128 x 8 tf32 tile, no swizzle, K-major core matrices (see tf32_tile_byte): K-direction
@@ -313,6 +309,9 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             RingPos<STAGES> op;
             RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sb = 0;
+            // verification only: the fill of this CTA that is left out (never armed,
+            // never copied), so that the consumers' wait for it runs out
+            const uint32_t skip = (blockIdx.x == 0 && g.withhold >= 0) ? static_cast<uint32_t>(g.withhold) : ~0u;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
@@ -334,7 +333,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {
                         const int s = kb >> 2;
-                        if (!ctl_wait(bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -348,9 +347,14 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         sb.next();
                         ++n_sb;
                     }
-                    if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                         ok = false;
                         break;
+                    }
+                    if (n_ops == skip) {
+                        op.next();
+                        ++n_ops;
+                        continue;
                     }
                     fence_proxy_async_smem();       // after the converter's ordinary stores
                     const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
@@ -380,7 +384,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     // at ST_B + e * 16 KiB
                     for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
                         const int ne = min(MIN_PER_STAGE, w.sb1 - s);
-                        if (!ctl_wait(bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -406,11 +410,13 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 }
             }
             for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i) {
-                drain_wait(bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
-                drain_wait(bar(BAR_FULLB + i % STAGES), (i / STAGES) & 1u);
+                if (i == skip)
+                    continue;
+                drain_wait(g, bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
+                drain_wait(g, bar(BAR_FULLB + i % STAGES), (i / STAGES) & 1u);
             }
             for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
-                drain_wait(bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
+                drain_wait(g, bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
@@ -422,11 +428,11 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 const Unit w = unit_of(g, u, nsb);
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     const int k2 = kb & 3;
-                    if (k2 == 0 && !ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                    if (k2 == 0 && !ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    if (!ctl_wait(bar(BAR_CONV + op.i), op.ph) || !ctl_wait(bar(BAR_FULLB + op.i), op.ph)) {
+                    if (!ctl_wait(g, bar(BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(BAR_FULLB + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -450,14 +456,14 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     }
                 }
                 if (Q4 && ok) {
-                    if (!ctl_wait(bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
                     for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
                         const int ne = min(MIN_PER_STAGE, w.sb1 - s);
-                        if (!ctl_wait(bar(BAR_CONV + op.i), op.ph) || !ctl_wait(bar(BAR_FULLB + op.i), op.ph)) {
+                        if (!ctl_wait(g, bar(BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(BAR_FULLB + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
@@ -482,7 +488,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 }
             }
             umma_commit(bar(BAR_DRAIN));
-            drain_wait(bar(BAR_DRAIN), 0u);
+            drain_wait(g, bar(BAR_DRAIN), 0u);
         }
         __syncwarp();
         return;
@@ -500,7 +506,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
         for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
             const Unit w = unit_of(g, u, nsb);
             for (int s = w.sb0; ok && s < w.sb1; ++s) {
-                if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph)) {
+                if (!warp_wait(g, bar(BAR_SBFULL + sb.i), sb.ph)) {
                     ok = false;
                     break;
                 }
@@ -528,7 +534,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 sb.next();
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) {
-                    if (!warp_wait(bar(BAR_FULL + op.i), op.ph)) {
+                    if (!warp_wait(g, bar(BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -570,7 +576,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             if (Q4 && ok) {
                 // min-term stages pass through unchanged
                 for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
-                    if (!warp_wait(bar(BAR_FULL + op.i), op.ph)) {
+                    if (!warp_wait(g, bar(BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -617,7 +623,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             float ip[2][2] = {{-1.0f, -1.0f}, {-1.0f, -1.0f}};
             const float2* d2 = nullptr;
             if (!min_item) {
-                if (!warp_wait(bar(BAR_SBFULL + sb.i), sb.ph) || !warp_wait(bar(BAR_IPREADY + sb.i), sb.ph)) {
+                if (!warp_wait(g, bar(BAR_SBFULL + sb.i), sb.ph) || !warp_wait(g, bar(BAR_IPREADY + sb.i), sb.ph)) {
                     ok = false;
                     break;
                 }
@@ -630,7 +636,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         ip[h][rho] = ipr[q * 32 + 16 * h + 8 * rho + quad];
                 d2 = reinterpret_cast<const float2*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 2) + qi;
             }
-            if (!warp_wait(bar(BAR_TFULL + item.i), item.ph)) {
+            if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
                 ok = false;
                 break;
             }
@@ -810,7 +816,7 @@ cudaError_t launch_sb_typed(const SbArgs& a, int grid, cudaStream_t s)
 }  // namespace
 
 cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const void* qa, const void* scales, int M,
-                           float* Y, int ldy, cudaStream_t s)
+                           float* Y, int ldy, cudaStream_t s, const WaitCtl& wc)
 {
     const WeightPlanes wp = weight_planes(type, od, id);
     const ActPlanes ap = act_planes(M, id);
@@ -833,6 +839,9 @@ cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const v
     a.num_n = ceil_div(od, BN);
     a.num_n128 = ceil_div(od, TILE_ROWS);
     a.vec_store = ((reinterpret_cast<uintptr_t>(Y) & 7u) == 0 && (ldy & 1) == 0) ? 1 : 0;
+    a.err = wc.err;
+    a.wait_ns = wc.limit_ns;
+    a.withhold = wc.withhold_fill;
 
     int dev = 0, nsm = 0;
     cudaError_t e = cudaGetDevice(&dev);

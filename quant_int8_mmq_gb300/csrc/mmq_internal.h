@@ -114,6 +114,28 @@ inline WeightPlanes weight_planes(int type, int od, int id)
 // (mmq_launch_count); count_launch is called once per launch attempt.
 void count_launch();
 
+// The library's sticky device error word (api.cu): its device address on the
+// current device (looked up once per device), and the host-side read-and-clear
+// behind mmq_get_device_error (synchronizes the stream first).
+cudaError_t device_error_word(unsigned int** word);
+cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned int* value);
+
+// What a tile-GEMM launch's bounded waits use: the error word, the time limit of
+// each wait, and (verification only) one operand-ring fill that CTA 0's producer
+// leaves out, so that the wait for it runs out (-1: none).
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+struct WaitCtl {
+    unsigned int* err;
+    unsigned long long limit_ns;
+    int withhold_fill;
+};
+// The WaitCtl of the next tile-GEMM launch: the default limit and no withheld fill,
+// unless mmq_debug_inject_wait_timeout armed a one-shot injection, which this call
+// consumes.  *injected tells which.
+cudaError_t take_wait_ctl(WaitCtl* wc, bool* injected);
+// Arms (fill >= 0) or disarms (fill < 0) the one-shot injection.
+void arm_wait_injection(int fill, unsigned long long limit_ns);
+
 // Launches `kernel` with programmatic stream serialization: its CTAs may start while
 // the kernel ahead of it on `s` finishes, so the kernel calls grid_dep_wait() before
 // it touches memory that an earlier kernel may write (only an L2 prefetch may precede
@@ -147,7 +169,7 @@ cudaError_t launch_gemm_small(int type, const void* packed, int od, int id, cons
                               int M, float* Y, int ldy, cudaStream_t s, const char** path_label);
 // Super-block-accumulating GEMM (Y only; q6_K: returns at once for plain codes).
 cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const void* qa, const void* scales, int M,
-                           float* Y, int ldy, cudaStream_t s);
+                           float* Y, int ldy, cudaStream_t s, const WaitCtl& wc);
 // Which kernel takes Y for M > SMALL_M: 0 = the super-block kernel when its tiles
 // fill the GPU, else the chunk kernel; 1 = the chunk kernel; 2 = the super-block
 // kernel (q6_K plain codes always go to the chunk kernel).
@@ -156,8 +178,5 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
                         const void* scales, int M, float* out, int ldy, cudaStream_t s,
                         const char** path_label);
 
-// Reads and clears the GEMM translation unit's sticky error word (stream-ordered,
-// then synchronizes the stream).  *word receives the old value.
-cudaError_t gemm_read_and_clear_error(cudaStream_t s, unsigned int* word);
 
 }  // namespace mmq

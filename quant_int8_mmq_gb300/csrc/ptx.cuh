@@ -7,10 +7,11 @@
 
 namespace mmq {
 
-// Sticky device error word of this translation unit (bit 0: a bounded wait
-// expired).  Each .cu file that includes this header gets its own copy and
-// exposes a host-side reader (see mmq_internal.h).
-static __device__ unsigned int g_error_word;
+// Bits of the library's sticky device error word.  The word itself is one
+// __device__ variable of the library (api.cu); a kernel that waits receives its
+// device address among its arguments, so every kernel sets the same word and
+// mmq_get_device_error reads and clears exactly that one.
+constexpr unsigned int ERR_WAIT_EXPIRED = 1u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -82,11 +83,11 @@ __device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint32_t bar, uint32_t p
 }
 
 // Wait until the phase with the given parity has completed.  Gives up (returns
-// false) once the sticky error word is set by anyone, or after limit_ns of
-// global time, in which case it sets the error word itself.  The error word and
-// the global timer are first read after 64 unsuccessful polls, so short waits
-// cost one or a few try_wait round trips.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+// false) once the sticky error word *err is set by anyone, or after limit_ns of
+// global time, in which case it sets ERR_WAIT_EXPIRED in *err itself.  The error
+// word and the global timer are first read after 64 unsuccessful polls, so short
+// waits cost one or a few try_wait round trips.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, unsigned int* err)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -95,15 +96,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
         if (mbar_try_wait(bar, parity))
             return true;
         if ((i & 63u) == 0) {
-            if (*reinterpret_cast<volatile unsigned int*>(&g_error_word) != 0u)
+            if (*reinterpret_cast<volatile unsigned int*>(err) != 0u)
                 return false;
             const uint64_t now = globaltimer_ns();
             if (i == 64u)
                 t0 = now;
             else if (now - t0 > limit_ns) {
-                atomicOr(&g_error_word, 1u);
+                atomicOr(err, ERR_WAIT_EXPIRED);
                 return false;
             }
+        }
+    }
+}
+
+// Bounded wait that ignores the error word, used only to drain a CTA's own copies
+// and MMAs in flight before it exits (those always complete): sleeps between polls
+// and gives up after limit_ns, setting ERR_WAIT_EXPIRED.
+__device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, unsigned int* err)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(err, ERR_WAIT_EXPIRED);
+            return;
         }
     }
 }
@@ -171,6 +186,18 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Named CTA barrier `id` over `nthreads` threads (a multiple of 32; every thread of each
+// participating warp arrives).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

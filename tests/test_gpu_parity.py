@@ -489,30 +489,59 @@ def test_gemm_chunk_kernel_plain_q6k_all_tiles_split(chunk_kernel, M, od, id_):
 def test_gemm_few_token_layout_parity(typ, M):
     """The chunk kernel with the tokens as the MMA's N (16 * ceil(M / 16) columns):
     ragged token counts around every multiple of 16, an odd od (ragged last weight
-    tile), 3 tiles so that every tile runs as two K-halves (odd super-block count)."""
+    tile); 3 weight tiles of 3 super-blocks, so each tile runs on a cluster of 3 CTAs,
+    one super-block each, whose partial sums meet in rank 0."""
     t = "q6_K" if typ.startswith("q6_K") else typ
     od, id_ = 259, 768
     raw = _q6_raw(od, id_, od + M, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, od + M)
     x = synth.activations(M, id_, 20 * M + 1)
     Y = _run_gemm(t, raw, x).cpu().numpy()
     assert "few-token layout" in mmq.mmq_last_path()
+    assert "K split: cluster of S=3 CTAs" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
 
 
-@pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
-@pytest.mark.parametrize("M,od,id_", [(31, 4097, 11008), (64, 11008, 4096), (20, 32000, 4096)])
-def test_gemm_few_token_layout_stack_shapes(typ, M, od, id_):
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
+@pytest.mark.parametrize("M", [9, 31, 64])
+def test_gemm_few_token_layout_k_halves(typ, M):
+    """Selector 3: the few-token layout without the cluster split.  With 3 weight tiles
+    every tile runs as two K-halves (odd super-block count: 1 and 2) that add into a
+    zeroed Y; bit-identical run to run."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    od, id_ = 259, 768
+    raw = _q6_raw(od, id_, od + M + 1, True) if t == "q6_K" else synth.q4k_blocks(od, id_, od + M + 1)
+    x = synth.activations(M, id_, 20 * M + 2)
+    mmq.mmq_debug_select_large_m_kernel(3)
+    try:
+        Y = _run_gemm(t, raw, x).cpu().numpy()
+        assert "K split: two K-halves" in mmq.mmq_last_path()
+        Y2 = _run_gemm(t, raw, x).cpu().numpy()
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+
+
+_FEW_TOKEN_STACK = [(typ, M, od, id_, split)
+                    for typ in ("q4_K", "q6_K", "q6_K_full")
+                    for M, od, id_, split in ((31, 4097, 11008, "cluster of S=4"), (64, 11008, 4096, "none"),
+                                              (20, 32000, 4096, "none"))
+                    if not (typ == "q4_K" and od == 32000)]     # lm_head is q6_K
+
+
+@pytest.mark.parametrize("typ,M,od,id_,split", _FEW_TOKEN_STACK)
+def test_gemm_few_token_layout_stack_shapes(typ, M, od, id_, split):
     """FFN-down (odd od), FFN-gate and lm_head shapes at decode-tail token counts: many
     tiles (the persistent rounds and the last-round split) against the oracle, and the
     result equals the 128-token tile layout's to the tolerance, run to run bit-identical."""
     t = "q6_K" if typ.startswith("q6_K") else typ
-    if t == "q4_K" and od == 32000:
-        pytest.skip("lm_head is q6_K")
     raw = _q6_raw(od, id_, M + 7, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, M + 7)
     x = synth.activations(M, id_, M + 8)
     Y = _run_gemm(t, raw, x).cpu().numpy()
     assert "few-token layout" in mmq.mmq_last_path()
+    assert f"K split: {split}" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
     Y2 = _run_gemm(t, raw, x).cpu().numpy()
@@ -544,7 +573,7 @@ def test_gemm_few_token_layout_row_stride_unaligned():
 
 def test_select_large_m_kernel_rejects_other_values():
     with pytest.raises(mmq.MMQError):
-        mmq.mmq_debug_select_large_m_kernel(3)
+        mmq.mmq_debug_select_large_m_kernel(4)
 
 
 # --------------------------------------------------------------------------- weight-streaming path (M <= 8)
