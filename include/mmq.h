@@ -98,11 +98,25 @@ typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
  *     (0,2,4,6,1,3,5,7): value k of token t at byte t*K + (k & ~7) +
  *     ((k & 7) >> 1) + 4*(k & 1).  The weight-streaming GEMM reads this plane.
  *     mmq_act_plane_bytes includes it in qa_bytes.
+ *   M <= MMQ_FT_MAX_M only (offsets from mmq_act_ft_layout), the few-token GEMM's
+ *     activation operand, with N = 16*ceil(M/16):
+ *     tq (in qa, after the int8 plane if any) per k-block kb a 2*N*128-byte block
+ *        at kb*2*N*128: N rows of hi then N rows of lo, row t / value k at byte
+ *        t*128 + (((k/8) ^ (t%8))*16) + (k%8)*2 (f16), where for the token's
+ *        super-block p = 2^(P-127), P = min(260 - E, 253) and E the f32 exponent
+ *        field of the largest of its 8 chunk scales d, s = p*d (exact),
+ *        s_hi = rn_f16(s), s_lo = rn_f16(s - s_hi), and for each code q:
+ *        hi = rn_f16(s_hi*q), lo = rn_f16(fma(s_hi, q, -hi) + s_lo*q) (f16 fma);
+ *     ip (in scales, after am) f32 1/p at index sb*MMQ_FT_MAX_M + t (t < N).
  * -------------------------------------------------------------------------- */
 #define MMQ_SMALL_M 8
+#define MMQ_FT_MAX_M 64
 mmq_status mmq_act_plane_bytes(int M, int K, size_t* qa_bytes, size_t* scale_bytes);
 mmq_status mmq_act_scale_layout(int M, int K, size_t* pair_offset, size_t* pair_bytes,
                                 size_t* am_offset, size_t* am_bytes);
+/* Offsets and sizes of the few-token planes (all four 0 when M > MMQ_FT_MAX_M). */
+mmq_status mmq_act_ft_layout(int M, int K, size_t* tq_offset, size_t* tq_bytes,
+                             size_t* ip_offset, size_t* ip_bytes);
 
 /* Quantize x [M][ldx] f32 (row-major, first K values of each row used) per
  * 32-value chunk: d = amax/127 (IEEE f32 division), q = round(x/d) (IEEE f32
@@ -145,6 +159,16 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *   RAW    the raw blocks re-laid for the weight-streaming GEMM, od rows x nsb
  *          blocks, row-major: q4_K 144 B [qs[128] | d | dmin | scales[12]],
  *          q6_K 224 B [ql[128] | qh[64] | scales[16] | d | 14 zero bytes].
+ *   CW     compact codes for the few-token GEMM, which widens them to f16 in
+ *          shared memory: per (nt, kb) W = 2 (q4_K) or 3 (q6_K) words of 16 bytes
+ *          per row, word-major: word w of row r at ((nt*nkb + kb)*W + w)*2048 + r*16.
+ *          Words 0, 1 hold chunk 2*kb + w: the 4-bit code (q4_K) or the low 4 bits
+ *          of q + 32 (q6_K) of value 8u + 2p + h of the chunk (u, p = 0..3, h = 0,1)
+ *          at bit 4p + 16h of its 32-bit word u.  q6_K word 2 holds the high 2 bits
+ *          of q + 32: chunk hc (0, 1) in its 32-bit words 2hc and 2hc + 1, value
+ *          8u + 2p + h of the chunk in word 2hc + u/2 at bit 8(u%2) + 2p + 16h.
+ *   SC     sub-block scales per (nt, sb): 16 bytes per row at ((nt*nsb + sb)*128 + r)*16:
+ *          q4_K the six-bit sc_0..sc_7 then m_0..m_7, one per byte; q6_K scales[16].
  * -------------------------------------------------------------------------- */
 typedef enum {
     MMQ_PLANE_CODES = 0,
@@ -153,7 +177,9 @@ typedef enum {
     MMQ_PLANE_AUX = 3,
     MMQ_PLANE_FLAG = 4,
     MMQ_PLANE_RAW = 5,
-    MMQ_NUM_WEIGHT_PLANES = 6
+    MMQ_PLANE_CW = 6,
+    MMQ_PLANE_SC = 7,
+    MMQ_NUM_WEIGHT_PLANES = 8
 } mmq_weight_plane;
 
 mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes);

@@ -19,7 +19,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "MMQError", "MMQ_Q4_K", "MMQ_Q6_K", "load", "lib_path",
-    "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_quantize_act", "mmq_packed_weight_bytes",
+    "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_act_ft_layout", "mmq_quantize_act",
+    "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
     "mmq_pack_weights", "mmq_convert_ggml_blocks", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
     "mmq_debug_inject_wait_timeout",
@@ -66,6 +67,7 @@ def load():
             "mmq_packed_weight_bytes": [I, I, I, S],
             "mmq_packed_weight_layout": [I, I, I, S, S],
             "mmq_act_scale_layout": [I, I, S, S, S, S],
+            "mmq_act_ft_layout": [I, I, S, S, S, S],
             "mmq_pack_weights": [I, P, I, I, P, P],
             "mmq_convert_ggml_blocks": [I, P, ctypes.c_size_t, P, P],
             "mmq_gemm_q6k": [P, I, I, P, P, I, P, I, P],
@@ -113,8 +115,9 @@ def mmq_packed_weight_bytes(t, od, id_):
     return b.value
 
 
-PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw")
+PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw", "cw", "sc")
 SMALL_M = 8          # token counts up to this take the weight-streaming path
+FT_MAX_M = 64        # token counts up to this take the few-token GEMM (and get its planes)
 
 
 def mmq_packed_weight_layout(t, od, id_):
@@ -130,6 +133,13 @@ def mmq_act_scale_layout(M, K):
     v = [ctypes.c_size_t() for _ in range(4)]
     _check(load().mmq_act_scale_layout(M, K, *[ctypes.byref(x) for x in v]), "mmq_act_scale_layout")
     return {"pairs": (v[0].value, v[1].value), "am": (v[2].value, v[3].value)}
+
+
+def mmq_act_ft_layout(M, K):
+    """{"tq": (offset, size), "ip": (offset, size)} of the few-token planes (sizes 0 when M > 64)."""
+    v = [ctypes.c_size_t() for _ in range(4)]
+    _check(load().mmq_act_ft_layout(M, K, *[ctypes.byref(x) for x in v]), "mmq_act_ft_layout")
+    return {"tq": (v[0].value, v[1].value), "ip": (v[2].value, v[3].value)}
 
 
 def mmq_pack_weights(t, raw, od, id_, packed, stream=0):

@@ -148,7 +148,7 @@ mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int o
         return st;
     const char* label = nullptr;
     const cudaError_t e =
-        (mode == mmq::GEMM_Y && M <= mmq::SMALL_M)
+        (mode == mmq::GEMM_Y && M <= mmq::SMALL_M && mmq::large_m_kernel() != 5)
             ? mmq::launch_gemm_small(static_cast<int>(t), packed, od, id, qa, scales, M, out, ldy,
                                      reinterpret_cast<cudaStream_t>(s), &label)
             : mmq::launch_gemm(static_cast<int>(t), mode, packed, od, id, qa, scales, M, out, ldy,
@@ -222,6 +222,25 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
     sizes[MMQ_PLANE_FLAG] = w.flag_bytes;
     offsets[MMQ_PLANE_RAW] = w.raw_off;
     sizes[MMQ_PLANE_RAW] = w.raw_bytes;
+    offsets[MMQ_PLANE_CW] = w.cw_off;
+    sizes[MMQ_PLANE_CW] = w.cw_bytes;
+    offsets[MMQ_PLANE_SC] = w.sc_off;
+    sizes[MMQ_PLANE_SC] = w.sc_bytes;
+    return MMQ_OK;
+}
+
+mmq_status mmq_act_ft_layout(int M, int K, size_t* tq_offset, size_t* tq_bytes, size_t* ip_offset,
+                             size_t* ip_bytes)
+{
+    if (!tq_offset || !tq_bytes || !ip_offset || !ip_bytes)
+        return MMQ_ERR_ARG;
+    if (M < 1 || M > MMQ_MAX_M || !valid_k(K))
+        return MMQ_ERR_SHAPE;
+    const mmq::ActPlanes p = mmq::act_planes(M, K);
+    *tq_offset = p.tq_bytes ? p.tq_off : 0;
+    *tq_bytes = p.tq_bytes;
+    *ip_offset = p.ip_bytes ? p.ip_off : 0;
+    *ip_bytes = p.ip_bytes;
     return MMQ_OK;
 }
 
@@ -291,7 +310,7 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
 
 mmq_status mmq_debug_select_large_m_kernel(int which)
 {
-    if (which < 0 || which > 3)
+    if (which < 0 || which > 5)
         return MMQ_ERR_ARG;
     mmq::select_large_m_kernel(which);
     return MMQ_OK;

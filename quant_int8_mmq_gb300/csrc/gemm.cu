@@ -1230,6 +1230,7 @@ int tc_max_clusters(int size)
 std::atomic<int> g_large_m_kernel{0};
 
 void select_large_m_kernel(int which) { g_large_m_kernel.store(which); }
+int large_m_kernel() { return g_large_m_kernel.load(); }
 
 cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int id, const void* qa,
                         const void* scales, int M, float* out, int ldy, cudaStream_t s, const char** path_label)
@@ -1253,6 +1254,11 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     e = take_wait_ctl(&wc, &injected);
     if (e != cudaSuccess)
         return e;
+    // Few tokens: the few-token GEMM (compact codes widened in shared memory, one TMEM
+    // accumulator per super-block), unless a tile layout was selected.
+    if (mode == GEMM_Y && M <= FT_MAX_M && (sel == 0 || sel == 3 || sel == 5))
+        return launch_gemm_ft(type, packed, od, id, qa, scales, M, out, ldy, s, wc, !injected && sel != 3,
+                              path_label);
     if (sb_first) {
         e = launch_gemm_sb(type, packed, od, id, qa, scales, M, out, ldy, s, wc);
         // the chunk kernel launched after it (q6_K) only reads the flag or runs plain codes
@@ -1293,7 +1299,7 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.withhold = wc.withhold_fill;
     // Few tokens: the tokens become the MMA's N (one accumulator column each) unless the
     // token-row layout or the super-block kernel was selected.
-    const bool tc = mode == GEMM_Y && !sb_first && sel != 1 && M <= TC_MAX_M;
+    const bool tc = mode == GEMM_Y && !sb_first && sel == 4 && M <= TC_MAX_M;
     a.n_tok = tc ? ceil_div(M, 16) * 16 : 0;
     a.kslices = 1;
 
@@ -1310,9 +1316,8 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     // Few tokens and few weight tiles: one cluster of kslices CTAs per tile, each on a
     // slice of K (partial sums added in rank order in shared memory), as many CTAs as
     // the clusters that fit at once allow.
-    // (No cluster split under a wait-timeout injection or when selector 3 asks for the
-    // few-token layout without it: a cluster barrier has no time limit.)
-    if (tc && !injected && sel != 3) {
+    // (No cluster split under a wait-timeout injection: a cluster barrier has no time limit.)
+    if (tc && !injected) {
         const int ts = ceil_div(od, BN);
         for (int ks = 4; ks >= 2; --ks) {
             if (nsb < ks || ts * ks > nsm)

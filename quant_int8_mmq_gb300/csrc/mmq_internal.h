@@ -48,13 +48,24 @@ __host__ __device__ constexpr int small_pos(int k)   // byte position of value k
     return (k & ~7) + ((k & 7) >> 1) + 4 * (k & 1);
 }
 
+// Token counts up to FT_MAX_M take the few-token GEMM, whose activation operand the
+// prepass writes as well: per 64-value k-block, the FT_N = 16*ceil(M/16) token rows of
+// hi = rn_f16(s_hi*q) then of lo = rn_f16(s_hi*q - hi + s_lo*q) (s = p*d, split into
+// two f16 values s_hi + s_lo; p a power of two per token and super-block), in the
+// 128-byte-swizzled operand layout (row t at t*128); and 1/p per (super-block, token),
+// FT_MAX_M entries per super-block.
+constexpr int FT_MAX_M = 64;   // MMQ_FT_MAX_M
+__host__ __device__ constexpr int ft_n(int M) { return ((M + 15) / 16) * 16; }
+
 struct ActPlanes {       // layout of mmq_quantize_act's outputs
     size_t tile_bytes;   // f16 code tiles (start of the qa buffer)
     size_t i8_off, i8_bytes;       // M <= SMALL_M: int8 codes [M][K] (small_pos order), else 0
-    size_t qa_bytes;     // tiles + int8 plane
+    size_t tq_off, tq_bytes;       // M <= FT_MAX_M: hi/lo operand tiles [K/64][2][FT_N rows], else 0
+    size_t qa_bytes;     // tiles + int8 plane + hi/lo tiles
     size_t pair_off, pair_bytes;   // {f32 d, i32 ssum} per (token, chunk)
     size_t am_off, am_bytes;       // tf32 hi/lo tiles of d*ssum per (token tile, super-block)
-    size_t scale_bytes;            // pairs + am
+    size_t ip_off, ip_bytes;       // M <= FT_MAX_M: f32 1/p [K/256][FT_MAX_M], else 0
+    size_t scale_bytes;            // pairs + am + 1/p
 };
 inline ActPlanes act_planes(int M, int K)
 {
@@ -63,12 +74,16 @@ inline ActPlanes act_planes(int M, int K)
     a.tile_bytes = Mp * static_cast<size_t>(K) * 2;
     a.i8_off = a.tile_bytes;
     a.i8_bytes = (M <= SMALL_M) ? static_cast<size_t>(M) * static_cast<size_t>(K) : 0;
-    a.qa_bytes = a.i8_off + a.i8_bytes;
+    a.tq_off = a.i8_off + a.i8_bytes;
+    a.tq_bytes = (M <= FT_MAX_M) ? static_cast<size_t>(K / TILE_K) * 2 * ft_n(M) * 128 : 0;
+    a.qa_bytes = a.tq_off + a.tq_bytes;
     a.pair_off = 0;
     a.pair_bytes = Mp * static_cast<size_t>(K / CHUNK) * 8;
     a.am_off = a.pair_bytes;
     a.am_bytes = Mp / TILE_ROWS * static_cast<size_t>(K / QK_K) * 2 * TF32_TILE_BYTES;
-    a.scale_bytes = a.am_off + a.am_bytes;
+    a.ip_off = a.am_off + a.am_bytes;
+    a.ip_bytes = (M <= FT_MAX_M) ? static_cast<size_t>(K / QK_K) * FT_MAX_M * 4 : 0;
+    a.scale_bytes = a.ip_off + a.ip_bytes;
     return a;
 }
 
@@ -79,6 +94,19 @@ constexpr int RAW4_BYTES = 144;
 constexpr int RAW6_BYTES = 224;
 __host__ __device__ constexpr int raw_block_bytes(int type) { return type == 12 ? RAW4_BYTES : RAW6_BYTES; }
 
+// Compact code plane (the few-token GEMM's weight operand, widened to f16 in shared
+// memory): per (128-row tile, 64-value k-block) CW_WORDS 16-byte words per row, stored
+// word-major ([word][row][16 B]) so that the 128 rows of one word are 2048 contiguous
+// bytes.  q4_K: words 0, 1 = the 4-bit codes of the k-block's two chunks; q6_K: words
+// 0, 1 = the low 4 bits of q + 32 of the two chunks, word 2 = the high 2 bits of all 64
+// values.  Bit positions: see pack.cu.
+__host__ __device__ constexpr int cw_words(int type) { return type == 12 ? 2 : 3; }
+__host__ __device__ constexpr int cw_kblock_bytes(int type) { return cw_words(type) * TILE_ROWS * 16; }
+// Sub-block scale plane: per (128-row tile, super-block) 16 bytes per row, [row][16 B]:
+// q4_K the 8 six-bit scales sc_c then the 8 mins m_c (one byte each); q6_K the 16 int8
+// scales.
+constexpr int SC_ROW_BYTES = 16;
+
 struct WeightPlanes {    // layout of mmq_pack_weights' output
     size_t code_off, code_bytes;   // f16 code tiles (scale-folded where exact)
     size_t pair_off, pair_bytes;   // f32 scale pairs per (row, chunk)
@@ -86,6 +114,8 @@ struct WeightPlanes {    // layout of mmq_pack_weights' output
     size_t aux_off, aux_bytes;     // q4_K: tf32 hi/lo tiles of dmin*m; q6_K: f32 scales per sub-block
     size_t flag_off, flag_bytes;   // q6_K: word 0 = 1 if codes hold sc*q, word 1 = max |sc|
     size_t raw_off, raw_bytes;     // re-laid raw blocks [od][id/256]
+    size_t cw_off, cw_bytes;       // compact codes [row tile][k-block][word][128][16 B]
+    size_t sc_off, sc_bytes;       // sub-block scales [row tile][super-block][128][16 B]
     size_t total;
 };
 inline WeightPlanes weight_planes(int type, int od, int id)
@@ -105,7 +135,11 @@ inline WeightPlanes weight_planes(int type, int od, int id)
     w.flag_bytes = 256;
     w.raw_off = w.flag_off + w.flag_bytes;
     w.raw_bytes = static_cast<size_t>(od) * nsb * static_cast<size_t>(raw_block_bytes(type));
-    w.total = w.raw_off + ((w.raw_bytes + 255) / 256) * 256;
+    w.cw_off = w.raw_off + ((w.raw_bytes + 255) / 256) * 256;
+    w.cw_bytes = (Np / TILE_ROWS) * static_cast<size_t>(id / TILE_K) * cw_kblock_bytes(type);
+    w.sc_off = w.cw_off + w.cw_bytes;
+    w.sc_bytes = Np * nsb * SC_ROW_BYTES;
+    w.total = w.sc_off + w.sc_bytes;
     return w;
 }
 
@@ -174,9 +208,15 @@ cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const v
 // fill the GPU, else the chunk kernel; 1 = the chunk kernel; 2 = the super-block
 // kernel (q6_K plain codes always go to the chunk kernel).
 void select_large_m_kernel(int which);
+int large_m_kernel();
 cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int id, const void* qa,
                         const void* scales, int M, float* out, int ldy, cudaStream_t s,
                         const char** path_label);
+// Few-token GEMM (M <= FT_MAX_M, Y only): compact codes widened in shared memory, the
+// prepass's hi/lo token operand, one TMEM accumulator per super-block.
+cudaError_t launch_gemm_ft(int type, const void* packed, int od, int id, const void* qa, const void* scales,
+                           int M, float* Y, int ldy, cudaStream_t s, const WaitCtl& wc, bool allow_cluster,
+                           const char** path_label);
 
 
 }  // namespace mmq

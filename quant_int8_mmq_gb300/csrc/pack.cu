@@ -221,6 +221,88 @@ __global__ void __launch_bounds__(256) raw_relayout_kernel(const uint8_t* __rest
     }
 }
 
+// Compact codes and sub-block scales for the few-token GEMM, one thread per (padded row
+// j, k-block kb), the rows of a tile on consecutive threads.  Bit positions are chosen
+// so that the GEMM's converter turns each 32-bit word into f16 pairs with a mask and
+// an OR of the exponent 0x6400 (1024 + the field), no per-value shifts:
+//   nibble word (q4_K code q; q6_K the low 4 bits of q + 32) of a 32-value chunk:
+//     value 8u + 2p + h (u, p = 0..3, h = 0, 1) at bit 4p + 16h of byte group u
+//     (bytes 4u..4u+3);
+//   q6_K high word (the high 2 bits of q + 32 for the k-block's 64 values): chunk hc
+//     in bytes 8hc..8hc+7, byte group s = 0, 1 of it holding units u = 2s and 2s + 1
+//     of the chunk, value 8u + 2p + h at bit 8(u - 2s) + 2p + 16h.
+template <int TYPE>
+__global__ void __launch_bounds__(256) compact_kernel(const uint8_t* __restrict__ raw, int od, int id, int Np,
+                                                      uint4* __restrict__ cw, uint4* __restrict__ scp)
+{
+    constexpr int W = cw_words(TYPE);
+    const int nkb = id / TILE_K;
+    const int nsb = id / QK_K;
+    const long long total = static_cast<long long>(Np) * nkb;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i % TILE_ROWS);
+        const long long tk = i / TILE_ROWS;
+        const int kb = static_cast<int>(tk % nkb);
+        const int nt = static_cast<int>(tk / nkb);
+        const int j = nt * TILE_ROWS + r;
+        const int sb = kb >> 2;
+        uint32_t word[W][4];
+#pragma unroll
+        for (int w = 0; w < W; ++w)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                word[w][u] = 0u;
+        uint32_t sc4[4] = {0u, 0u, 0u, 0u};
+        if (j < od) {
+            const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + sb) * (TYPE == 12 ? Q4K_BYTES : Q6K_BYTES);
+            for (int hc = 0; hc < 2; ++hc) {
+                const int e0 = 64 * (kb & 3) + 32 * hc;      // first value of the chunk in its block
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const int e = e0 + i2;
+                    const int u = i2 >> 3, pp = (i2 & 7) >> 1, h = i2 & 1;
+                    uint32_t lo4, hi2 = 0u;
+                    if (TYPE == 12) {
+                        lo4 = (b[16 + e / 2] >> (4 * (e & 1))) & 15u;
+                    } else {
+                        lo4 = (b[e / 2] >> (4 * (e & 1))) & 15u;
+                        hi2 = (b[128 + e / 4] >> (2 * (e & 3))) & 3u;
+                    }
+                    word[hc][u] |= lo4 << (4 * pp + 16 * h);
+                    if constexpr (TYPE == 14) {
+                        const int sgrp = u >> 1;                  // byte group of the high word
+                        word[2][2 * hc + sgrp] |= hi2 << (8 * (u - 2 * sgrp) + 2 * pp + 16 * h);
+                    }
+                }
+            }
+            if ((kb & 3) == 0) {
+                uint8_t v[16];
+                if (TYPE == 12) {
+                    for (int f = 0; f < 16; ++f) {   // the 16 six-bit fields, little-endian
+                        const int bit = 6 * f, byte = bit >> 3, sh = bit & 7;
+                        unsigned x = static_cast<unsigned>(b[4 + byte]) >> sh;
+                        if (sh > 2)
+                            x |= static_cast<unsigned>(b[4 + byte + 1]) << (8 - sh);
+                        v[f] = static_cast<uint8_t>(x & 63u);
+                    }
+                } else {
+                    for (int f = 0; f < 16; ++f)
+                        v[f] = b[192 + f];
+                }
+                for (int q = 0; q < 4; ++q)
+                    sc4[q] = static_cast<uint32_t>(v[4 * q]) | (static_cast<uint32_t>(v[4 * q + 1]) << 8) |
+                             (static_cast<uint32_t>(v[4 * q + 2]) << 16) | (static_cast<uint32_t>(v[4 * q + 3]) << 24);
+            }
+        }
+        uint4* dst = cw + (static_cast<size_t>(nt) * nkb + kb) * (W * TILE_ROWS);
+#pragma unroll
+        for (int w = 0; w < W; ++w)
+            dst[w * TILE_ROWS + r] = make_uint4(word[w][0], word[w][1], word[w][2], word[w][3]);
+        if ((kb & 3) == 0)
+            scp[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = make_uint4(sc4[0], sc4[1], sc4[2], sc4[3]);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed, cudaStream_t s)
@@ -268,6 +350,20 @@ cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed,
         raw_relayout_kernel<14><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(rb, nblocks, rout);
     else
         raw_relayout_kernel<12><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(rb, nblocks, rout);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const long long citems = static_cast<long long>(Np) * (id / TILE_K);
+    long long cblocks = (citems + 255) / 256;
+    if (cblocks > 65535LL * 8)
+        cblocks = 65535LL * 8;
+    uint4* cw = reinterpret_cast<uint4*>(base + wp.cw_off);
+    uint4* scp = reinterpret_cast<uint4*>(base + wp.sc_off);
+    count_launch();
+    if (type == 14)
+        compact_kernel<14><<<static_cast<unsigned>(cblocks), 256, 0, s>>>(rb, od, id, Np, cw, scp);
+    else
+        compact_kernel<12><<<static_cast<unsigned>(cblocks), 256, 0, s>>>(rb, od, id, Np, cw, scp);
     return cudaGetLastError();
 }
 

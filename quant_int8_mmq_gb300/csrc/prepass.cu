@@ -62,10 +62,33 @@ __device__ __forceinline__ float tf32_rna(float v)
     return __uint_as_float(r);
 }
 
+// The few-token GEMM's activation operand for one token and super-block.  p = 2^e is
+// chosen from the largest chunk scale dmax of the super-block so that 127 * dmax * p
+// < 2^14 (f32 exponent field of p: min(260 - E, 253), E that of dmax; 1/p is exact and
+// normal); s = p * d is exact and is split into f16 s_hi = rn(s), s_lo = rn(s - s_hi);
+// each code c (an exact f16 integer, |c| <= 127) gives hi = rn(s_hi * c) and
+// lo = rn(s_hi * c - hi + s_lo * c), the residual s_hi * c - hi being exact in one fma,
+// so that hi + lo carries about 21 significant bits of s * c.
+__device__ __forceinline__ uint32_t ft_p_field(float dmax)
+{
+    const int E = static_cast<int>((__float_as_uint(dmax) >> 23) & 0xFFu);
+    return static_cast<uint32_t>(min(260 - E, 253));
+}
+__device__ __forceinline__ void ft_split_pair(uint32_t cbits, __half2 s_hi, __half2 s_lo, uint32_t& hi, uint32_t& lo)
+{
+    const __half2 c = *reinterpret_cast<const __half2*>(&cbits);
+    const __half2 h = __hmul2_rn(s_hi, c);
+    const __half2 r = __hfma2(s_hi, c, __hneg2(h));
+    const __half2 l = __hfma2(s_lo, c, r);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int M, int K, int ldx,
                                                            int Mp, int vec4, uint16_t* __restrict__ qa,
                                                            uint2* __restrict__ scales, uint8_t* __restrict__ am,
-                                                           int8_t* __restrict__ qa8)
+                                                           int8_t* __restrict__ qa8, uint8_t* __restrict__ tq,
+                                                           float* __restrict__ ip, int ftn)
 {
     // x may come from the kernel ahead, and qa / scales may still be read by it.
     grid_dep_wait();
@@ -169,6 +192,28 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                 h[i] = *reinterpret_cast<const uint32_t*>(&p2);
             }
             *reinterpret_cast<uint4*>(tile + tile_byte(r, k0 % TILE_K)) = make_uint4(h[0], h[1], h[2], h[3]);
+            if (tq != nullptr && t < ftn) {
+                // few-token operand: hi and lo tiles of p * d * q for this token row
+                float dm = d;
+                dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 4));
+                dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 8));
+                dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 16));
+                const uint32_t pf = ft_p_field(dm);
+                const float sv = __fmul_rn(d, __uint_as_float(pf << 23));  // exact: a power of two
+                const __half shh = __float2half_rn(sv);
+                const __half2 s_hi = __half2half2(shh);
+                const __half2 s_lo = __half2half2(__float2half_rn(sv - __half2float(shh)));
+                uint32_t hv[4], lv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    ft_split_pair(h[i], s_hi, s_lo, hv[i], lv[i]);
+                uint8_t* kt = tq + static_cast<size_t>(kb) * (2 * ftn * 128);
+                const int off = tile_byte(t, k0 % TILE_K);
+                *reinterpret_cast<uint4*>(kt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4*>(kt + ftn * 128 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+                if (lane == 0)
+                    ip[static_cast<size_t>(sb) * FT_MAX_M + t] = __uint_as_float((254u - pf) << 23);
+            }
             if (qa8 != nullptr && t < M) {
                 // small_pos order inside the 8-value group: values (0,2,4,6) then (1,3,5,7)
                 int qi[8];
@@ -219,7 +264,9 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
     return launch_dependent(
         quantize_act_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), s, x, M, K, ldx, Mp, vec4,
         static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off), sc + ap.am_off,
-        ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr);
+        ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr,
+        ap.tq_bytes ? static_cast<uint8_t*>(qa) + ap.tq_off : nullptr,
+        ap.ip_bytes ? reinterpret_cast<float*>(sc + ap.ip_off) : nullptr, ap.tq_bytes ? ft_n(M) : 0);
 }
 
 }  // namespace mmq

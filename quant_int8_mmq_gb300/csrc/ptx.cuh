@@ -199,6 +199,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// The same barrier, also returning the AND of `v` over the participating threads.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}\n"
+        : "=r"(out)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+        : "memory");
+    return out != 0u;
+}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
@@ -264,6 +278,38 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// Shared-memory descriptor of a 128 x 8 tf32 tile in the no-swizzle K-major core-matrix
+// layout (tf32_tile_byte in mmq_internal.h): K-direction core-matrix stride 128 B
+// (leading byte offset), 8-row group stride 256 B (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_tf32_core(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 16;
+    d |= static_cast<uint64_t>(256u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;   // layout type 0: no swizzle
+}
+
+// Instruction descriptor, kind::tf32: tf32 A and B, f32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_acc32(int m, int n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 8 tf32 step, issued by one thread.
+__device__ __forceinline__ void umma_tf32_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
@@ -320,6 +366,24 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, float (&v)[64])
         : "memory");
 #pragma unroll
     for (int i = 0; i < 64; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// One 16-column load (columns taddr .. taddr + 15) and its wait.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : MMQ_R32(0), MMQ_R32(1), MMQ_R32(2), MMQ_R32(3), MMQ_R32(4), MMQ_R32(5), MMQ_R32(6), MMQ_R32(7),
+          MMQ_R32(8), MMQ_R32(9), MMQ_R32(10), MMQ_R32(11), MMQ_R32(12), MMQ_R32(13), MMQ_R32(14),
+          MMQ_R32(15)
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
         v[i] = __uint_as_float(r[i]);
 }
 

@@ -73,3 +73,53 @@ def untile_rows(buf: np.ndarray, rows_padded: int, n: int, dtype=np.float32):
 
 def is_tf32(a: np.ndarray) -> bool:
     return bool(np.all((a.view(np.uint32) & 0x1FFF) == 0))
+
+
+def compact_plane(typ: str, codes: np.ndarray, rows_padded: int) -> np.ndarray:
+    """The compact code plane documented in include/mmq.h (CW), built from decoded codes
+    [od, id] (q4_K 0..15; q6_K -32..31): uint8 bytes of [row tile][k-block][word][128][16 B]."""
+    od, K = codes.shape
+    v = np.zeros((rows_padded, K), np.uint32)
+    v[:od] = codes.astype(np.int64) + (32 if typ == "q6_K" else 0)
+    nt, nkb = rows_padded // TILE_ROWS, K // TILE_K
+    W = 3 if typ == "q6_K" else 2
+    # v[nt, r, kb, hc, i] for the 32 values i of chunk hc of k-block kb
+    vv = v.reshape(nt, TILE_ROWS, nkb, 2, 32)
+    i = np.arange(32)
+    u, p, h = i // 8, (i % 8) // 2, i % 2
+    out = np.zeros((nt, nkb, W, TILE_ROWS, 4), np.uint32)
+    low = vv & 15
+    for hc in range(2):
+        for uu in range(4):
+            sel = u == uu
+            sh = (4 * p + 16 * h)[sel]
+            out[:, :, hc, :, uu] = np.bitwise_or.reduce(low[:, :, :, hc][..., sel] << sh, axis=-1).transpose(0, 2, 1)
+    if W == 3:
+        high = vv >> 4
+        for hc in range(2):
+            for s in range(2):
+                sel = (u // 2) == s
+                sh = (8 * (u % 2) + 2 * p + 16 * h)[sel]
+                out[:, :, 2, :, 2 * hc + s] = np.bitwise_or.reduce(high[:, :, :, hc][..., sel] << sh,
+                                                                   axis=-1).transpose(0, 2, 1)
+    return out.reshape(-1).view(np.uint8)
+
+
+def scale_plane(rows: np.ndarray, rows_padded: int) -> np.ndarray:
+    """The sub-block scale plane (SC) from per-row bytes [od, nsb, 16]: uint8 bytes of
+    [row tile][super-block][128][16 B], padded rows zero."""
+    od, nsb, _ = rows.shape
+    full = np.zeros((rows_padded, nsb, 16), np.uint8)
+    full[:od] = rows
+    return full.reshape(rows_padded // TILE_ROWS, TILE_ROWS, nsb, 16).transpose(0, 2, 1, 3).reshape(-1)
+
+
+def untile_token_operand(buf: np.ndarray, n: int, K: int):
+    """Few-token operand plane (tq) -> (hi, lo) float16 arrays [n, K]."""
+    nkb = K // TILE_K
+    u16 = np.ascontiguousarray(buf[: nkb * 2 * n * 128]).view(np.uint16).reshape(nkb, 2, n * 64)
+    idx = _IDX[:n]                                           # rows 0..n-1 of the swizzled tile
+    t = u16[:, :, idx]                                       # [nkb, 2, n, 64]
+    hi = t[:, 0].transpose(1, 0, 2).reshape(n, K).view(np.float16)
+    lo = t[:, 1].transpose(1, 0, 2).reshape(n, K).view(np.float16)
+    return hi, lo

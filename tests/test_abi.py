@@ -44,10 +44,17 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
     assert lay["pairs"] == (0, 256 * 16 * 8)
     assert lay["am"] == (256 * 16 * 8, 2 * 2 * 8192)            # 2 token tiles x 2 super-blocks
     assert sc == lay["am"][0] + lay["am"][1]
-    # token counts up to 8 add the int8 code plane after the tiles
-    assert mmq.mmq_act_plane_bytes(5, 512)[0] == 128 * 512 * 2 + 5 * 512
-    assert mmq.mmq_act_plane_bytes(8, 512)[0] == 128 * 512 * 2 + 8 * 512
-    assert mmq.mmq_act_plane_bytes(9, 512)[0] == 128 * 512 * 2
+    # token counts up to 8 add the int8 code plane after the tiles, up to 64 the few-token
+    # operand (8 k-blocks x hi, lo x 16 * ceil(M/16) rows of 128 B) and 1/p (2 x 64 floats)
+    assert mmq.mmq_act_plane_bytes(5, 512) == (128 * 512 * 2 + 5 * 512 + 8 * 2 * 16 * 128,
+                                               128 * 16 * 8 + 2 * 8192 + 2 * 64 * 4)
+    assert mmq.mmq_act_plane_bytes(8, 512)[0] == 128 * 512 * 2 + 8 * 512 + 8 * 2 * 16 * 128
+    assert mmq.mmq_act_plane_bytes(9, 512)[0] == 128 * 512 * 2 + 8 * 2 * 16 * 128
+    assert mmq.mmq_act_plane_bytes(64, 512)[0] == 128 * 512 * 2 + 8 * 2 * 64 * 128
+    assert mmq.mmq_act_plane_bytes(65, 512)[0] == 128 * 512 * 2
+    assert mmq.mmq_act_ft_layout(33, 512) == {"tq": (128 * 512 * 2, 8 * 2 * 48 * 128),
+                                              "ip": (128 * 16 * 8 + 2 * 8192, 2 * 64 * 4)}
+    assert mmq.mmq_act_ft_layout(65, 512) == {"tq": (0, 0), "ip": (0, 0)}
     for t in (mmq.MMQ_Q4_K, mmq.MMQ_Q6_K):
         L = mmq.mmq_packed_weight_layout(t, 4097, 1024)
         Np, nsb = 4224, 4
@@ -57,8 +64,11 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
         assert L["aux"] == (sum(L["sbd"]), Np * nsb * 64)
         assert L["flag"][0] == sum(L["aux"])
         assert L["raw"] == (sum(L["flag"]), 4097 * 4 * (144 if t == mmq.MMQ_Q4_K else 224))
+        words = 2 if t == mmq.MMQ_Q4_K else 3
+        assert L["cw"] == (-(-sum(L["raw"]) // 256) * 256, (Np // 128) * 16 * words * 128 * 16)
+        assert L["sc"] == (sum(L["cw"]), Np * nsb * 16)
         assert all(off % 16 == 0 for off, _ in L.values())
-        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == -(-sum(L["raw"]) // 256) * 256
+        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["sc"])
 
 
 @pytest.mark.parametrize("M,K,err", [(0, 256, 2), (1, 255, 2), (1, 0, 2), (5, 300, 2), (1 << 23, 256, 2)])
@@ -94,10 +104,10 @@ def test_argument_errors_are_synchronous_and_cuda_free(mmq_lib):
     assert lib.mmq_convert_ggml_blocks(7, p16, 4, p16, None) == 1
     assert lib.mmq_convert_ggml_blocks(12, None, 4, p16, None) == 1
     assert lib.mmq_convert_ggml_blocks(14, p16, 4, None, None) == 1
-    # kernel selector: 0 to 3 only (host state, no CUDA call)
-    assert lib.mmq_debug_select_large_m_kernel(4) == 1
+    # kernel selector: 0 to 5 only (host state, no CUDA call)
+    assert lib.mmq_debug_select_large_m_kernel(6) == 1
     assert lib.mmq_debug_select_large_m_kernel(-1) == 1
-    assert lib.mmq_debug_select_large_m_kernel(3) == 0
+    assert lib.mmq_debug_select_large_m_kernel(5) == 0
     assert lib.mmq_debug_select_large_m_kernel(0) == 0
     # wait-timeout injection: limit 1 us .. 2 s when arming; disarming takes any limit
     assert lib.mmq_debug_inject_wait_timeout(0, 999) == 1

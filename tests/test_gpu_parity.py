@@ -16,7 +16,8 @@ import oracle
 import synth
 import quant_int8_mmq_gb300 as mmq
 from tests.encode import encode_q4k_ggml, encode_q6k_ggml
-from tests.planes import is_tf32, padded, untile_codes, untile_pairs, untile_rows, untile_tf32_pair
+from tests.planes import (compact_plane, is_tf32, padded, scale_plane, untile_codes, untile_pairs, untile_rows,
+                          untile_tf32_pair, untile_token_operand)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -105,15 +106,58 @@ def _check_prepass(x, ldx=None):
     assert not hi[M:].any() and not lo[M:].any()
     # M <= 8: the int8 codes after the tiles, each 8-value group in the order (0,2,4,6,1,3,5,7)
     qab = qa.cpu().numpy()
+    ft = mmq.mmq_act_ft_layout(M, K)
     if M <= mmq.SMALL_M:
-        assert qab.size == Mp * K * 2 + M * K
-        i8 = qab[Mp * K * 2:].view(np.int8).reshape(M, K // 8, 8)
+        i8 = qab[Mp * K * 2:Mp * K * 2 + M * K].view(np.int8).reshape(M, K // 8, 8)
         order = np.array([0, 2, 4, 6, 1, 3, 5, 7])
         back = np.empty_like(i8)
         back[:, :, order] = i8
         assert np.array_equal(back.reshape(M, K).astype(np.int64), q.astype(np.int64))
+    assert qab.size == Mp * K * 2 + (M * K if M <= mmq.SMALL_M else 0) + ft["tq"][1]
+    # M <= 64: the few-token operand hi/lo and 1/p, against the header's formula
+    if M <= mmq.FT_MAX_M:
+        n = -(-M // 16) * 16
+        to, tb = ft["tq"]
+        io, ib = ft["ip"]
+        assert to == Mp * K * 2 + (M * K if M <= mmq.SMALL_M else 0) and tb == (K // 64) * 2 * n * 128
+        assert io == lay["am"][0] + lay["am"][1] and ib == (K // 256) * 64 * 4
+        hi, lo = untile_token_operand(qab[to:to + tb], n, K)
+        whi, wlo, wip = ft_operand(q, d, n)
+        assert np.array_equal(hi.view(np.uint16), whi.view(np.uint16))
+        assert np.array_equal(lo.view(np.uint16), wlo.view(np.uint16))
+        ip = scb[io:io + ib].view(np.float32).reshape(K // 256, 64)[:, :n]
+        assert np.array_equal(ip.view(np.uint32), wip.view(np.uint32))
     else:
-        assert qab.size == Mp * K * 2
+        assert ft["tq"][1] == 0 and ft["ip"][1] == 0
+
+
+def ft_operand(q, d, n):
+    """The few-token operand as include/mmq.h defines it, in numpy (float16 arithmetic
+    emulated exactly through float64): per token and super-block p = 2^(P - 127),
+    P = min(260 - E(dmax), 253); s = p*d; s_hi = rn16(s), s_lo = rn16(s - s_hi);
+    hi = rn16(s_hi*q); lo = rn16(rn16(s_hi*q - hi) + s_lo*q).  Rows M..n-1 are zero.
+    Returns (hi, lo float16 [n, K], 1/p float32 [K/256, n])."""
+    M, K = q.shape
+    nsb = K // 256
+    dd = np.zeros((n, K // 32), np.float32)
+    dd[:M] = d
+    qq = np.zeros((n, K), np.float64)
+    qq[:M] = q
+    dmax = dd.reshape(n, nsb, 8).max(axis=2)
+    E = (dmax.view(np.uint32) >> 23) & 0xFF
+    P = np.minimum(260 - E.astype(np.int64), 253).astype(np.uint32)
+    p = (P << 23).view(np.float32)
+    ip = ((254 - P) << 23).astype(np.uint32).view(np.float32)
+    s = (dd.reshape(n, nsb, 8) * p[:, :, None]).astype(np.float32).reshape(n, K // 32)
+    s_hi = s.astype(np.float16)
+    s_lo = (s - s_hi.astype(np.float32)).astype(np.float16)
+    shi = np.repeat(s_hi.astype(np.float64), 32, axis=1)
+    slo = np.repeat(s_lo.astype(np.float64), 32, axis=1)
+    prod = shi * qq
+    hi = prod.astype(np.float16)
+    r = (prod - hi.astype(np.float64)).astype(np.float16)
+    lo = (slo * qq + r.astype(np.float64)).astype(np.float16)
+    return hi, lo, ip.T.copy()
 
 
 @pytest.mark.parametrize("M,K,seed", [(16, 512, 0), (512, 4096, 1), (130, 768, 5), (1, 256, 6), (2047, 1024, 7),
@@ -178,7 +222,7 @@ def test_pack_planes_byte_exact(typ, od, id_):
     pk = packed.cpu().numpy()
     tid = mmq.TYPES[t]
     L = mmq.mmq_packed_weight_layout(tid, od, id_)
-    assert pk.size == -(-sum(L["raw"]) // 256) * 256
+    assert pk.size == sum(L["sc"])
     Np, nsb, nchunk = padded(od), id_ // 256, id_ // 32
     part = {k: pk[o:o + n] for k, (o, n) in L.items()}
     codes = untile_codes(part["codes"], Np, id_)
@@ -223,6 +267,13 @@ def test_pack_planes_byte_exact(typ, od, id_):
     else:
         want = np.concatenate([raw[..., 16:], raw[..., :16]], axis=2)
     assert np.array_equal(rawp, want)
+    # compact codes and sub-block scales of the few-token GEMM (the header's bit map)
+    assert np.array_equal(part["cw"], compact_plane(t, q, Np))
+    if t == "q6_K":
+        rows = sc.view(np.uint8)
+    else:
+        rows = np.concatenate([sc, m], axis=2)
+    assert np.array_equal(part["sc"], scale_plane(rows, Np))
 
 
 # --------------------------------------------------------------------------- dots
@@ -483,20 +534,21 @@ def test_gemm_chunk_kernel_plain_q6k_all_tiles_split(chunk_kernel, M, od, id_):
     assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
 
 
-# --------------------------------------------------------------------------- few-token layout (8 < M <= 64)
+# --------------------------------------------------------------------------- few-token GEMM (8 < M <= 64)
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
 @pytest.mark.parametrize("M", [9, 16, 17, 31, 32, 33, 48, 63, 64])
-def test_gemm_few_token_layout_parity(typ, M):
-    """The chunk kernel with the tokens as the MMA's N (16 * ceil(M / 16) columns):
-    ragged token counts around every multiple of 16, an odd od (ragged last weight
-    tile); 3 weight tiles of 3 super-blocks, so each tile runs on a cluster of 3 CTAs,
-    one super-block each, whose partial sums meet in rank 0."""
+def test_gemm_few_token_parity(typ, M):
+    """The few-token GEMM (compact codes widened in shared memory, tokens as the MMA's N =
+    16 * ceil(M / 16), one TMEM accumulator per super-block): ragged token counts around
+    every multiple of 16, an odd od (ragged last weight tile); 3 weight tiles of 3
+    super-blocks, so each tile runs on a cluster of 3 CTAs, one super-block each, whose
+    partial sums meet in rank 0."""
     t = "q6_K" if typ.startswith("q6_K") else typ
     od, id_ = 259, 768
     raw = _q6_raw(od, id_, od + M, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, od + M)
     x = synth.activations(M, id_, 20 * M + 1)
     Y = _run_gemm(t, raw, x).cpu().numpy()
-    assert "few-token layout" in mmq.mmq_last_path()
+    assert "few-token GEMM" in mmq.mmq_last_path()
     assert "K split: cluster of S=3 CTAs" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
@@ -504,10 +556,9 @@ def test_gemm_few_token_layout_parity(typ, M):
 
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
 @pytest.mark.parametrize("M", [9, 31, 64])
-def test_gemm_few_token_layout_k_halves(typ, M):
-    """Selector 3: the few-token layout without the cluster split.  With 3 weight tiles
-    every tile runs as two K-halves (odd super-block count: 1 and 2) that add into a
-    zeroed Y; bit-identical run to run."""
+def test_gemm_few_token_without_cluster(typ, M):
+    """Selector 3: the few-token GEMM without the cluster split (each CTA takes whole
+    tiles); bit-identical run to run."""
     t = "q6_K" if typ.startswith("q6_K") else typ
     od, id_ = 259, 768
     raw = _q6_raw(od, id_, od + M + 1, True) if t == "q6_K" else synth.q4k_blocks(od, id_, od + M + 1)
@@ -515,7 +566,7 @@ def test_gemm_few_token_layout_k_halves(typ, M):
     mmq.mmq_debug_select_large_m_kernel(3)
     try:
         Y = _run_gemm(t, raw, x).cpu().numpy()
-        assert "K split: two K-halves" in mmq.mmq_last_path()
+        assert "few-token GEMM" in mmq.mmq_last_path() and "K split: none" in mmq.mmq_last_path()
         Y2 = _run_gemm(t, raw, x).cpu().numpy()
     finally:
         mmq.mmq_debug_select_large_m_kernel(0)
@@ -527,20 +578,21 @@ def test_gemm_few_token_layout_k_halves(typ, M):
 _FEW_TOKEN_STACK = [(typ, M, od, id_, split)
                     for typ in ("q4_K", "q6_K", "q6_K_full")
                     for M, od, id_, split in ((31, 4097, 11008, "cluster of S=4"), (64, 11008, 4096, "none"),
-                                              (20, 32000, 4096, "none"))
+                                              (20, 32000, 4096, "none"), (48, 4096, 4096, "cluster of S=4"))
                     if not (typ == "q4_K" and od == 32000)]     # lm_head is q6_K
 
 
 @pytest.mark.parametrize("typ,M,od,id_,split", _FEW_TOKEN_STACK)
-def test_gemm_few_token_layout_stack_shapes(typ, M, od, id_, split):
-    """FFN-down (odd od), FFN-gate and lm_head shapes at decode-tail token counts: many
-    tiles (the persistent rounds and the last-round split) against the oracle, and the
-    result equals the 128-token tile layout's to the tolerance, run to run bit-identical."""
+def test_gemm_few_token_stack_shapes(typ, M, od, id_, split):
+    """FFN-down (odd od), FFN-gate, attention and lm_head shapes at decode-tail token
+    counts: many tiles (persistent rounds, or clusters along K) against the oracle, and
+    the result equals the 128-token chunk kernel's to the tolerance, run to run
+    bit-identical."""
     t = "q6_K" if typ.startswith("q6_K") else typ
     raw = _q6_raw(od, id_, M + 7, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, M + 7)
     x = synth.activations(M, id_, M + 8)
     Y = _run_gemm(t, raw, x).cpu().numpy()
-    assert "few-token layout" in mmq.mmq_last_path()
+    assert "few-token GEMM" in mmq.mmq_last_path()
     assert f"K split: {split}" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
@@ -555,7 +607,7 @@ def test_gemm_few_token_layout_stack_shapes(typ, M, od, id_, split):
     assert_y_close(Y, Yr.astype(np.float64), S)
 
 
-def test_gemm_few_token_layout_row_stride_unaligned():
+def test_gemm_few_token_row_stride_unaligned():
     typ, M, od, id_ = "q4_K", 27, 203, 512
     raw = _raw(typ, od, id_, seed=25)
     x = synth.activations(M, id_, 26)
@@ -564,16 +616,72 @@ def test_gemm_few_token_layout_row_stride_unaligned():
         buf = torch.full((M * ldy + 8,), -7.0, dtype=torch.float32, device=DEV)
         Yv = buf[off:off + M * ldy].view(M, ldy)
         _run_gemm(typ, raw, x, Y=Yv)
-        assert "few-token layout" in mmq.mmq_last_path()
+        assert "few-token GEMM" in mmq.mmq_last_path()
         host = Yv.cpu().numpy()
         assert_y_close(host[:, :od], Yo, S)
         assert np.all(host[:, od:] == -7.0)
         assert np.all(buf[:off].cpu().numpy() == -7.0)
 
 
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
+def test_gemm_few_token_wide_dynamic_range(typ):
+    """The few-token operand is p * d_a * q_a with one power of two p per (token,
+    super-block): chunks scaled by 2^-8 .. 2^8 inside every super-block, 5 % all-zero
+    chunks, whole rows at 1e-20 and 1e20."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    M, od, id_ = 40, 300, 1024
+    rng = np.random.default_rng(95)
+    f = np.exp2(rng.integers(-8, 9, size=(M, id_ // 32))).astype(np.float32)
+    f[rng.random(f.shape) < 0.05] = 0.0
+    x = (synth.activations(M, id_, 96).reshape(M, -1, 32) * f[..., None]).reshape(M, id_)
+    x[0] *= np.float32(1e-20)
+    x[1] *= np.float32(1e20)
+    raw = _q6_raw(od, id_, 97, True) if t == "q6_K" else synth.q4k_blocks(od, id_, 97)
+    Y = _run_gemm(t, raw, x).cpu().numpy()
+    assert "few-token GEMM" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+def test_gemm_few_token_kernel_at_streaming_sizes(typ, M):
+    """Selector 5: the few-token GEMM also for M <= 8 (N = 16)."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    od, id_ = 4097, 1024
+    raw = _q6_raw(od, id_, od + M + 3, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, od + M + 3)
+    x = synth.activations(M, id_, 10 * M + 5)
+    mmq.mmq_debug_select_large_m_kernel(5)
+    try:
+        Y = _run_gemm(t, raw, x).cpu().numpy()
+        assert "few-token GEMM" in mmq.mmq_last_path()
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
+@pytest.mark.parametrize("M,od,id_", [(31, 4097, 11008), (31, 259, 768)])
+def test_gemm_chunk_kernel_few_token_layout(typ, M, od, id_):
+    """Selector 4: the chunk kernel's transposed few-token layout (tokens as N, exact
+    integer dots per chunk), kept for comparison."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    raw = _q6_raw(od, id_, M + 17, True) if t == "q6_K" else synth.q4k_blocks(od, id_, M + 17)
+    x = synth.activations(M, id_, M + 18)
+    mmq.mmq_debug_select_large_m_kernel(4)
+    try:
+        Y = _run_gemm(t, raw, x).cpu().numpy()
+        assert "chunk GEMM, few-token layout" in mmq.mmq_last_path()
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+    Yo, S = oracle_gemm(t, raw, x)
+    assert_y_close(Y, Yo, S)
+
+
 def test_select_large_m_kernel_rejects_other_values():
     with pytest.raises(mmq.MMQError):
-        mmq.mmq_debug_select_large_m_kernel(4)
+        mmq.mmq_debug_select_large_m_kernel(6)
 
 
 # --------------------------------------------------------------------------- weight-streaming path (M <= 8)

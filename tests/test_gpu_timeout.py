@@ -10,7 +10,7 @@ producer leaves one operand fill out (its barrier is never armed and no copy is
 issued) and every wait of that launch gives up after 1 ms.  The kernel then leaves
 its loops, drains its own copies and MMAs, frees TMEM and exits.  Launches that
 split a tile over a CTA cluster are not injected (a cluster barrier has no time
-limit); the injected few-token launch runs without the cluster split.
+limit); injected few-token launches run without the cluster split.
 """
 import numpy as np
 import pytest
@@ -43,8 +43,9 @@ def _raw(typ, od, id_, seed):
     (2, "q6_K", 200, 300, 768, "super-block"),
     (1, "q4_K", 200, 300, 768, "chunk GEMM"),
     (1, "q6_K_full", 200, 300, 768, "chunk GEMM"),
-    (0, "q4_K", 31, 259, 768, "few-token layout"),
-    (0, "q6_K_full", 31, 259, 768, "few-token layout"),
+    (0, "q4_K", 31, 259, 768, "few-token GEMM"),
+    (0, "q6_K_full", 31, 259, 768, "few-token GEMM"),
+    (4, "q4_K", 31, 259, 768, "chunk GEMM, few-token layout"),
 ])
 def test_expired_wait_is_reported_then_cleared(selector, typ, M, od, id_, label):
     t = "q6_K" if typ.startswith("q6_K") else typ
