@@ -208,30 +208,33 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  * The GEMM: Y[t][j] (t < M, j < od, row stride ldy floats) is overwritten with
  * the formula at the top of this file.  packed comes from mmq_pack_weights of
  * the same (type, od, id); qa/scales from mmq_quantize_act with K = id and the
- * same M.  Two tensor-core kernels compute it (mmq_last_path names the one
- * launched; mmq_debug_select_large_m_kernel can force either):
- *  - super-block kernel (scale-folded codes, when its 128 x 256 tiles number at
- *    least the SM count): the activation operand is p*d_a*q_a (p a power of two
- *    per token and super-block) held as an f16 hi + lo pair (about 2^-21
- *    relative per value), times the exact f16 weight codes, summed over a whole
- *    super-block in f32; then d and 1/p are applied per super-block;
- *  - chunk kernel (otherwise): the integer dots run exactly (codes held as f16
+ * same M.  Four kernels compute it (mmq_last_path names the one launched;
+ * mmq_debug_select_large_m_kernel can force a choice):
+ *  - M <= MMQ_SMALL_M (decode and tail shapes), the weight-streaming kernel: the
+ *    RAW plane and the int8 activation plane, exact integer dots on the CUDA
+ *    cores (dp4a), and the scales applied per chunk in the formula's own order
+ *    (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=
+ *    d_a*(d*sc0*I_0 + d*sc1*I_1)), with a fixed reduction order;
+ *  - MMQ_SMALL_M < M <= MMQ_FT_MAX_M, the few-token kernel: the CW codes are
+ *    widened to exact f16 integers (q4_K sc*q; q6_K the two exact tiles
+ *    sc*l/4 and 4*sc*(h-2), l and h the low 4 and high 2 bits of q + 32) in
+ *    tensor memory and contracted on tcgen05 against the tq operand (f16 hi and
+ *    lo of p*d_a*q_a as one 2N-row operand), one f32 accumulator per
+ *    super-block, then d and 1/p applied per super-block; when the weight tiles
+ *    are few, each is split along K over a cluster of up to 8 CTAs whose partial
+ *    sums are added in rank order (deterministic);
+ *  - larger M, the super-block kernel (scale-folded codes, when its 128 x 256
+ *    tiles number at least the SM count): the activation operand p*d_a*q_a as
+ *    an f16 hi + lo pair (about 2^-21 relative per value) times the exact f16
+ *    CODES, summed over a whole super-block in f32, then d and 1/p per
+ *    super-block;
+ *  - otherwise the chunk kernel: the integer dots run exactly (codes held as f16
  *    integers, every partial sum an integer below 2^24 in the f32 accumulator)
  *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
- *    For M <= 64 it runs in a few-token layout: the weight tile is the MMA's A
- *    operand and the tokens its N (M rounded up to 16), the same arithmetic per
- *    element with only the tokens present copied and contracted; when the weight
- *    tiles are few, each is split along K over a cluster of up to 4 CTAs whose
- *    partial sums are added in a fixed order (deterministic).
- * Both: the q4_K min term sum_c (d_a*ssum)*(dmin*m_c) runs as a tf32 hi/lo
- * tensor-core contraction (relative error about 2^-21 per product); Y is
- * deterministic for given inputs and kernel.  Rows t >= M and columns j >= od
- * are never written.  ldy >= od.
- * M <= MMQ_SMALL_M (decode and tail shapes) takes the weight-streaming path
- * instead: the RAW plane and the int8 activation plane, exact integer dots on
- * the CUDA cores (dp4a), and the scales applied per chunk in the formula's own
- * order (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=
- * d_a*(d*sc0*I_0 + d*sc1*I_1)), with a fixed reduction order.
+ * The tile kernels compute the q4_K min term sum_c (d_a*ssum)*(dmin*m_c) as a
+ * tf32 hi/lo tensor-core contraction (relative error about 2^-21 per product).
+ * Y is deterministic for given inputs and kernel.  Rows t >= M and columns
+ * j >= od are never written.  ldy >= od.
  * -------------------------------------------------------------------------- */
 mmq_status mmq_gemm_q6k(const void* packed, int od, int id, const void* qa, const void* scales,
                         int M, float* Y, int ldy, mmq_stream_t s);
@@ -248,15 +251,13 @@ mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, cons
 mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa,
                                const void* scales, int M, float* dots, mmq_stream_t s);
 
-/* Debug/verification: which kernel computes Y for M > MMQ_SMALL_M (process-wide).
- *   0 (default): the super-block kernel for scale-folded codes (q4_K always,
- *      q6_K when every |sc| <= 64) when its 128 x 256 tiles number at least the
- *      SM count, else the chunk kernel; plain q6_K codes: the chunk kernel; the
- *      chunk kernel takes its few-token layout when M <= 64;
- *   1: the chunk kernel for every case, always in its 128-token tile layout;
- *   2: the super-block kernel for every scale-folded case;
- *   3: as 0, but the few-token layout never splits a tile over a CTA cluster
- *      (tiles are split into two K-halves instead when they are few).
+/* Debug/verification: which kernel computes Y (process-wide).
+ *   0 (default): as described above the GEMM calls;
+ *   1: the chunk kernel for every M > MMQ_SMALL_M (128-token tiles);
+ *   2: the super-block kernel for every scale-folded case with M > MMQ_SMALL_M
+ *      (plain-code q6_K: the chunk kernel);
+ *   3: as 0, but the few-token kernel never splits a tile over a CTA cluster;
+ *   4: as 0, but the few-token kernel also for M <= MMQ_SMALL_M.
  * Returns MMQ_ERR_ARG for any other value.  Not thread-safe against GEMM calls
  * in flight on other host threads. */
 mmq_status mmq_debug_select_large_m_kernel(int which);
@@ -286,8 +287,9 @@ const char* mmq_status_string(mmq_status st);
 const char* mmq_last_path(void);
 
 /* Number of kernel launches the library has made in this process (every entry
- * point that launches adds the kernels it launched: prepass 1, repack 3 or 4,
- * GEMM 1, or 2 when the last round's tiles are split and first zeroed). */
+ * point that launches adds the kernels it launched: prepass 1, repack 4 or 5,
+ * GEMM 1, or 2 when the last round's tiles are split and first zeroed, or when a
+ * q6_K super-block launch is followed by the chunk kernel's flag check). */
 unsigned long long mmq_launch_count(void);
 
 /* Library version string. */

@@ -148,7 +148,7 @@ mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int o
         return st;
     const char* label = nullptr;
     const cudaError_t e =
-        (mode == mmq::GEMM_Y && M <= mmq::SMALL_M && mmq::large_m_kernel() != 5)
+        (mode == mmq::GEMM_Y && M <= mmq::SMALL_M && mmq::large_m_kernel() != 4)
             ? mmq::launch_gemm_small(static_cast<int>(t), packed, od, id, qa, scales, M, out, ldy,
                                      reinterpret_cast<cudaStream_t>(s), &label)
             : mmq::launch_gemm(static_cast<int>(t), mode, packed, od, id, qa, scales, M, out, ldy,
@@ -310,7 +310,7 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
 
 mmq_status mmq_debug_select_large_m_kernel(int which)
 {
-    if (which < 0 || which > 5)
+    if (which < 0 || which > 4)
         return MMQ_ERR_ARG;
     mmq::select_large_m_kernel(which);
     return MMQ_OK;

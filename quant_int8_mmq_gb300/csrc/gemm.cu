@@ -39,12 +39,6 @@
 //               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner;
 //               per tile acc -= the q4_K min-term item; store Y (or, for the two
 //               K-halves of a last-round tile, add into a zeroed Y).
-// Few tokens (M <= 64, Y only): the same roles in a transposed layout, with the
-// weight tile as the MMA's A operand on the TMEM lanes and the tokens as N (M rounded
-// up to 16), only those token rows copied, a deeper operand ring (7 stages with 8 KiB
-// token slots) and four 128-column TMEM items; when the weight tiles are few, each runs
-// on a cluster of up to 4 CTAs along K whose partial sums meet in rank 0 through
-// distributed shared memory; see gemm_roles_tc.
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
 // set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing
 // thread's wait + fence + commit cost about 80 cycles on top of a chunk's 128 cycles
@@ -82,11 +76,6 @@ constexpr int PROMO_WARP0 = 4;
 constexpr int NUM_PROMO_WARPS = 8;
 constexpr int COLS_PER_WARP = BN / 2;   // 64
 constexpr uint32_t TMEM_COLS = 512;
-// Few-token layout: up to TC_MAX_M tokens as the MMA's N, TC_COLS accumulator columns
-// per chunk (one per token), each promotion warp taking TC_HALF of them.
-constexpr int TC_MAX_M = 64;
-constexpr int TC_COLS = 64;
-constexpr int TC_HALF = TC_COLS / 2;
 // Register split: the launch gives every thread LAUNCH_REGS; the control warpgroup
 // drops to CTRL_REGS and the two promotion warpgroups grow to PROMO_REGS out of the
 // same pool (the host checks the compiled count before launching).
@@ -130,36 +119,6 @@ static_assert(SMEM_B % 1024 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && S
                   SMEM_BAR % 8 == 0,
               "alignment");
 
-// Shared memory of the few-token layout: a deeper operand ring (activation slots hold
-// only TC_MAX_M rows, 8 KiB) and four 128-column TMEM items instead of two of 256.
-constexpr int TC_STAGES = 7;
-constexpr int TC_ITEMS = 4;
-constexpr uint32_t TC_ITEM_COLS = TMEM_COLS / TC_ITEMS;
-constexpr int TC_A_BYTES = TC_MAX_M * 128;
-constexpr int TC_SMEM_B = 0;
-constexpr int TC_SMEM_A = TC_SMEM_B + TC_STAGES * TILE_BYTES;
-constexpr int TC_SMEM_SB = TC_SMEM_A + TC_STAGES * TC_A_BYTES;
-constexpr int TC_SMEM_BAR = TC_SMEM_SB + SBR * SB_BYTES;
-constexpr int TC_BAR_FULL = 0;
-constexpr int TC_BAR_EMPTY = TC_BAR_FULL + TC_STAGES;
-constexpr int TC_BAR_SBFULL = TC_BAR_EMPTY + TC_STAGES;
-constexpr int TC_BAR_SBEMPTY = TC_BAR_SBFULL + SBR;
-constexpr int TC_BAR_TFULL = TC_BAR_SBEMPTY + SBR;
-constexpr int TC_BAR_TEMPTY = TC_BAR_TFULL + TC_ITEMS;
-constexpr int TC_BAR_DRAIN = TC_BAR_TEMPTY + TC_ITEMS;
-constexpr int TC_NUM_BARS = TC_BAR_DRAIN + 1;
-constexpr int TC_SMEM_TMEMPTR = TC_SMEM_BAR + TC_NUM_BARS * 8;
-constexpr int TC_SMEM_ALLOC = TC_SMEM_TMEMPTR + 16 + 1024;
-static_assert(TC_SMEM_ALLOC <= 227 * 1024, "shared memory budget (few-token layout)");
-static_assert(TC_SMEM_A % 1024 == 0 && TC_A_BYTES % 1024 == 0 && TC_SMEM_SB % 16 == 0 && TC_SMEM_BAR % 8 == 0,
-              "alignment (few-token layout)");
-static_assert(MIN_AM_BYTES <= TC_A_BYTES && MIN_BM_BYTES <= TILE_BYTES, "min-term operands fit a few-token stage");
-static_assert(2 * TC_COLS <= static_cast<int>(TC_ITEM_COLS), "an item holds two chunks (or sub-blocks) of columns");
-// K-slice partial sums of a cluster rank (one float per weight row and token) and, after
-// them, one ok flag per promotion warp, in the rank's idle weight stages.
-constexpr int TC_OKF_OFF = TC_MAX_M * BM * 4;
-static_assert(TC_OKF_OFF + NUM_PROMO_WARPS * 4 <= TC_STAGES * TILE_BYTES,
-              "K-slice partial sums and ok flags fit the idle weight stages");
 
 struct GemmArgs {
     const uint8_t* A;     // activation code tiles      [num_m][nkb][16 KiB]
@@ -179,8 +138,6 @@ struct GemmArgs {
     int vec_store;        // Y is 16-byte aligned and ldy % 4 == 0
     int skip_folded;      // q6_K: return at once when the codes are folded (the
                           // super-block kernel, launched first, has written Y)
-    int n_tok;            // few-token layout: MMA N (M rounded up to 16, <= TC_MAX_M)
-    int kslices;          // few-token layout: CTAs per weight tile (a cluster along K), 1 = none
     unsigned int* err;    // the library's sticky error word
     unsigned long long wait_ns;   // limit of each bounded wait
     int withhold;         // verification: operand fill CTA 0's producer leaves out (-1: none)
@@ -672,387 +629,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
     }
 }
 
-// Few-token layout (SMALL_M < M <= TC_MAX_M): the weight tile is the MMA's A operand,
-// its 128 rows on the TMEM lanes, and the tokens are N (g.n_tok = M rounded up to 16),
-// one accumulator column per token.  Only the first n_tok rows of each activation
-// tile are copied, the MMAs are 128 x n_tok x 16, and each promotion thread owns one
-// weight row and half of the token columns.  The arithmetic is the token-row
-// layout's, element by element: inner += d_a * I' per chunk, acc += d * inner per
-// super-block, acc -= the q4_K min term, in the same order.
-// Work unit u of a few-token launch.  With kslices > 1 the launch is one cluster of
-// kslices CTAs per weight tile; CTA rank r takes super-blocks
-// [r*nsb/kslices, (r+1)*nsb/kslices) and the partial sums meet in rank 0.
-__device__ __forceinline__ Unit tc_unit(const GemmArgs& g, int u, int nsb)
-{
-    if (g.kslices <= 1)
-        return unit_of(g, u, nsb);
-    Unit w;
-    const int r = u % g.kslices;
-    w.m = 0;
-    w.n = u / g.kslices;
-    w.sb0 = r * nsb / g.kslices;
-    w.sb1 = (r + 1) * nsb / g.kslices;
-    w.half = false;
-    return w;
-}
-
-template <int TYPE, bool FOLDED>
-__device__ __forceinline__ void gemm_roles_tc(const GemmArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
-                                              int warp, int lane)
-{
-    constexpr bool Q4 = (TYPE == 12);
-    constexpr uint32_t ITEM_COLS = TC_ITEM_COLS;
-    const int nkb = g.id / BK;
-    const int nsb = g.id / QK_K;
-    const uint32_t a_bytes = static_cast<uint32_t>(g.n_tok) * 128u;  // first n_tok rows of a 128-row tile
-    auto bar = [&](int i) -> uint32_t { return sbase + TC_SMEM_BAR + 8u * static_cast<uint32_t>(i); };
-
-    if (warp < PROMO_WARP0) {
-        if (warp == 0 && lane == 0) {
-            // -------------------------------------------------------- producer
-            RingPos<TC_STAGES> op;
-            RingPos<SBR> sb;
-            uint32_t n_ops = 0, n_sb = 0;
-            constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
-            const uint32_t skip = withheld_fill(g);
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
-                const Unit w = tc_unit(g, u, nsb);
-                const int n = w.n;
-                const uint8_t* Ab = g.A;   // one token tile (num_m == 1)
-                const uint8_t* Bb = g.B + static_cast<size_t>(n) * nkb * TILE_BYTES;
-                for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
-                    if ((kb & 3) == 0) {
-                        const int s = kb >> 2;
-                        if (!ctl_wait(g, bar(TC_BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        fence_proxy_async_smem();
-                        const uint32_t dst = sbase + TC_SMEM_SB + sb.i * SB_BYTES;
-                        const uint32_t fb = bar(TC_BAR_SBFULL + sb.i);
-                        mbar_arrive_expect_tx(fb, sb_tx);
-                        bulk_g2s(dst + SB_SBD_OFF, g.SBD + (static_cast<size_t>(n) * nsb + s) * SB_SBD_BYTES,
-                                 SB_SBD_BYTES, fb);
-                        bulk_g2s(dst + SB_AS_OFF, g.AS + static_cast<size_t>(s) * SB_AS_BYTES, SB_AS_BYTES, fb);
-                        if (!FOLDED) {
-                            bulk_g2s(dst + SB_X_OFF, g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_SC_BYTES,
-                                     SB_SC_BYTES, fb);
-                        }
-                        sb.next();
-                        ++n_sb;
-                    }
-                    if (!ctl_wait(g, bar(TC_BAR_EMPTY + op.i), op.ph ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    if (n_ops == skip) {
-                        op.next();
-                        ++n_ops;
-                        continue;
-                    }
-                    const uint32_t fo = bar(TC_BAR_FULL + op.i);
-                    mbar_arrive_expect_tx(fo, TILE_BYTES + a_bytes);
-                    bulk_g2s(sbase + TC_SMEM_A + op.i * TC_A_BYTES, Ab + static_cast<size_t>(kb) * TILE_BYTES, a_bytes,
-                             fo);
-                    bulk_g2s(sbase + TC_SMEM_B + op.i * TILE_BYTES, Bb + static_cast<size_t>(kb) * TILE_BYTES,
-                             TILE_BYTES, fo);
-                    op.next();
-                    ++n_ops;
-                }
-                if (Q4 && ok) {
-                    for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(g, bar(TC_BAR_EMPTY + op.i), op.ph ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t fo = bar(TC_BAR_FULL + op.i);
-                        mbar_arrive_expect_tx(fo, MIN_AM_BYTES + MIN_BM_BYTES);
-                        bulk_g2s(sbase + TC_SMEM_A + op.i * TC_A_BYTES, g.AM + static_cast<size_t>(s) * MIN_AM_BYTES,
-                                 MIN_AM_BYTES, fo);
-                        bulk_g2s(sbase + TC_SMEM_B + op.i * TILE_BYTES,
-                                 g.AUX + (static_cast<size_t>(n) * nsb + s) * MIN_BM_BYTES, MIN_BM_BYTES, fo);
-                        op.next();
-                        ++n_ops;
-                    }
-                }
-            }
-            for (uint32_t i = (n_ops > TC_STAGES ? n_ops - TC_STAGES : 0); i < n_ops; ++i)
-                if (i != skip)
-                    drain_wait(g, bar(TC_BAR_FULL + i % TC_STAGES), (i / TC_STAGES) & 1u);
-            for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
-                drain_wait(g, bar(TC_BAR_SBFULL + i % SBR), (i / SBR) & 1u);
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
-            const uint32_t idesc = idesc_f16_f32(BM, g.n_tok);
-            const uint32_t idesc_t = idesc_tf32_f32(BM, g.n_tok);
-            RingPos<TC_STAGES> op;
-            RingPos<TC_ITEMS> item;
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
-                const Unit w = tc_unit(g, u, nsb);
-                for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
-                    if (!ctl_wait(g, bar(TC_BAR_FULL + op.i), op.ph)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint64_t w0 = sdesc_k_sw128(sbase + TC_SMEM_B + op.i * TILE_BYTES);  // weights: A
-                    const uint64_t x0 = sdesc_k_sw128(sbase + TC_SMEM_A + op.i * TC_A_BYTES);  // tokens: B
-                    if (FOLDED) {
-                        if (!ctl_wait(g, bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + item.i * ITEM_COLS;
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            umma_f16(d + cc * TC_COLS, w0 + 4u * cc, x0 + 4u * cc, idesc, 0u);
-                            umma_f16(d + cc * TC_COLS, w0 + 4u * cc + 2, x0 + 4u * cc + 2, idesc, 1u);
-                        }
-                        umma_commit(bar(TC_BAR_TFULL + item.i));
-                        item.next();
-                    } else {
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            if (!ctl_wait(g, bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                            umma_f16(d, w0 + 4u * cc, x0 + 4u * cc, idesc, 0u);
-                            umma_f16(d + TC_COLS, w0 + 4u * cc + 2, x0 + 4u * cc + 2, idesc, 0u);
-                            umma_commit(bar(TC_BAR_TFULL + item.i));
-                            item.next();
-                        }
-                        if (!ok)
-                            break;
-                    }
-                    umma_commit(bar(TC_BAR_EMPTY + op.i));
-                    op.next();
-                }
-                if (Q4 && ok) {
-                    if (!ctl_wait(g, bar(TC_BAR_TEMPTY + item.i), item.ph ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                    for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(g, bar(TC_BAR_FULL + op.i), op.ph)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t xm = sbase + TC_SMEM_A + op.i * TC_A_BYTES;
-                        const uint32_t wm = sbase + TC_SMEM_B + op.i * TILE_BYTES;
-                        const uint64_t whi = sdesc_tf32_tile(wm), wlo = sdesc_tf32_tile(wm + TF32_TILE_BYTES);
-                        const uint64_t xhi = sdesc_tf32_tile(xm), xlo = sdesc_tf32_tile(xm + TF32_TILE_BYTES);
-                        umma_tf32(d, whi, xhi, idesc_t, s > w.sb0 ? 1u : 0u);
-                        umma_tf32(d, whi, xlo, idesc_t, 1u);
-                        umma_tf32(d, wlo, xhi, idesc_t, 1u);
-                        umma_commit(bar(TC_BAR_EMPTY + op.i));
-                        op.next();
-                    }
-                    if (!ok)
-                        break;
-                    umma_commit(bar(TC_BAR_TFULL + item.i));
-                    item.next();
-                }
-            }
-            umma_commit(bar(TC_BAR_DRAIN));
-            drain_wait(g, bar(TC_BAR_DRAIN), 0u);
-        }
-        __syncwarp();
-        if (g.kslices > 1) {   // the CTA barrier and the two cluster barriers of the promotion warps
-            named_bar_sync(1, NUM_THREADS);
-            cluster_sync();
-            cluster_sync();
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------------- promotion
-    const int pw = warp - PROMO_WARP0;              // 0..7
-    const int q = warp & 3;                          // TMEM lane quarter: weight rows q*32 .. q*32+31
-    const int t0 = (pw >> 2) * TC_HALF;              // first token column of this warp
-    const int row_in_tile = q * 32 + lane;
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    RingPos<TC_ITEMS> item;
-    RingPos<SBR> sb;
-    auto release = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(bar(TC_BAR_TEMPTY + item.i));
-        item.next();
-    };
-    bool ok = true;
-    const bool clustered = g.kslices > 1;   // then the launch gives this CTA exactly one unit
-    bool had_unit = false;
-    int j = 0;
-    float acc[TC_HALF];
-#pragma unroll
-    for (int t = 0; t < TC_HALF; ++t)
-        acc[t] = 0.0f;
-    for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
-        const Unit w = tc_unit(g, u, nsb);
-        j = w.n * BN + row_in_tile;
-        had_unit = true;
-#pragma unroll
-        for (int t = 0; t < TC_HALF; ++t)
-            acc[t] = 0.0f;
-        for (int s = w.sb0; s < w.sb1; ++s) {
-            const uint8_t* sbe = smem + TC_SMEM_SB + sb.i * SB_BYTES;
-            if (!warp_wait(g, bar(TC_BAR_SBFULL + sb.i), sb.ph)) {
-                ok = false;
-                break;
-            }
-            // token scale pairs {d_a, ssum} of chunk k: tokens t0 .. t0+31 as 16 uint4
-            const uint4* tsc4 = reinterpret_cast<const uint4*>(sbe + SB_AS_OFF);
-            const float dsb = reinterpret_cast<const float*>(sbe + SB_SBD_OFF)[row_in_tile];
-            float inner[TC_HALF];
-#pragma unroll
-            for (int t = 0; t < TC_HALF; ++t)
-                inner[t] = 0.0f;
-            for (int k2 = 0; k2 < 4 && ok; ++k2) {
-                if (FOLDED) {
-                    if (!warp_wait(g, bar(TC_BAR_TFULL + item.i), item.ph)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t col0 = lane_addr + item.i * ITEM_COLS + t0;
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int k = 2 * k2 + cc;
-                        float I[TC_HALF];
-                        tmem_ld32_wait(col0 + cc * TC_COLS, I);
-                        if (cc == 1)
-                            release();
-                        const uint4* ts = tsc4 + (k * BM + t0) / 2;
-#pragma unroll
-                        for (int i = 0; i < TC_HALF / 2; ++i) {
-                            const uint4 v = ts[i];
-                            inner[2 * i] = fmaf(__uint_as_float(v.x), I[2 * i], inner[2 * i]);
-                            inner[2 * i + 1] = fmaf(__uint_as_float(v.z), I[2 * i + 1], inner[2 * i + 1]);
-                        }
-                    }
-                } else {
-                    const float* scp = reinterpret_cast<const float*>(sbe + SB_X_OFF);
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int k = 2 * k2 + cc;
-                        if (!warp_wait(g, bar(TC_BAR_TFULL + item.i), item.ph)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t col0 = lane_addr + item.i * ITEM_COLS + t0;
-                        float h0[TC_HALF], h1[TC_HALF];
-                        tmem_ld32_wait(col0, h0);
-                        tmem_ld32_wait(col0 + TC_COLS, h1);
-                        release();
-                        const float sc0 = scp[(2 * k) * BN + row_in_tile];
-                        const float sc1 = scp[(2 * k + 1) * BN + row_in_tile];
-                        const uint4* ts = tsc4 + (k * BM + t0) / 2;
-#pragma unroll
-                        for (int i = 0; i < TC_HALF / 2; ++i) {
-                            const uint4 v = ts[i];
-                            const float u0 = fmaf(h1[2 * i], sc1, h0[2 * i] * sc0);
-                            const float u1 = fmaf(h1[2 * i + 1], sc1, h0[2 * i + 1] * sc0);
-                            inner[2 * i] = fmaf(__uint_as_float(v.x), u0, inner[2 * i]);
-                            inner[2 * i + 1] = fmaf(__uint_as_float(v.z), u1, inner[2 * i + 1]);
-                        }
-                    }
-                }
-            }
-            if (!ok)
-                break;
-#pragma unroll
-            for (int t = 0; t < TC_HALF; ++t)
-                acc[t] = fmaf(dsb, inner[t], acc[t]);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(TC_BAR_SBEMPTY + sb.i));
-            sb.next();
-        }
-        if (!ok)
-            break;
-        if (Q4) {
-            if (!warp_wait(g, bar(TC_BAR_TFULL + item.i), item.ph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float mn[TC_HALF];
-            tmem_ld32_wait(lane_addr + item.i * ITEM_COLS + t0, mn);
-            release();
-#pragma unroll
-            for (int t = 0; t < TC_HALF; ++t)
-                acc[t] = fmaf(-1.0f, mn[t], acc[t]);
-        }
-        if (!clustered && j < g.od) {
-#pragma unroll
-            for (int t = 0; t < TC_HALF; ++t) {
-                const int tok = t0 + t;
-                if (tok < g.M) {
-                    float* p = g.out + static_cast<size_t>(tok) * g.ldy + j;
-                    if (w.half)
-                        atomicAdd(p, acc[t]);
-                    else
-                        *p = acc[t];
-                }
-            }
-        }
-    }
-    if (clustered) {
-        // The K slices' partial sums meet in rank 0 and are added in rank order (the
-        // result does not depend on scheduling).  The CTA barrier first lets the
-        // producer and the MMA thread finish draining their copies and MMAs, so that the
-        // operand ring is idle before the partial sums overwrite it.  Every rank also
-        // leaves the ok flag of each promotion warp, and rank 0 stores Y only if every
-        // flag of every rank is set.  Every thread passes the CTA barrier and both
-        // cluster barriers, also after an expired wait.
-        const uint32_t rank = cluster_ctarank();
-        float* scratch = reinterpret_cast<float*>(smem + TC_SMEM_B);
-        named_bar_sync(1, NUM_THREADS);
-        if (rank != 0) {
-#pragma unroll
-            for (int t = 0; t < TC_HALF; ++t)
-                scratch[(t0 + t) * BM + row_in_tile] = acc[t];
-        }
-        if (lane == 0)
-            reinterpret_cast<int*>(smem + TC_SMEM_B + TC_OKF_OFF)[pw] = ok ? 1 : 0;
-        cluster_sync();
-        bool all_ok = ok;
-        if (rank == 0) {
-            for (int r = 0; r < g.kslices; ++r) {
-                const uint32_t fbase = cluster_map(sbase + TC_SMEM_B + TC_OKF_OFF, static_cast<uint32_t>(r));
-                for (int w = 0; w < NUM_PROMO_WARPS; ++w)
-                    all_ok = all_ok && ld_cluster_u32(fbase + 4u * static_cast<uint32_t>(w)) != 0u;
-            }
-        }
-        if (rank == 0 && all_ok && had_unit) {
-            for (int r = 1; r < g.kslices; ++r) {
-                const uint32_t rbase = cluster_map(sbase + TC_SMEM_B, static_cast<uint32_t>(r));
-#pragma unroll
-                for (int t = 0; t < TC_HALF; ++t)
-                    acc[t] += ld_cluster_f32(rbase + 4u * static_cast<uint32_t>((t0 + t) * BM + row_in_tile));
-            }
-            if (j < g.od) {
-#pragma unroll
-                for (int t = 0; t < TC_HALF; ++t) {
-                    const int tok = t0 + t;
-                    if (tok < g.M)
-                        g.out[static_cast<size_t>(tok) * g.ldy + j] = acc[t];
-                }
-            }
-        }
-        cluster_sync();
-    }
-}
-
-template <int TYPE, int MODE, bool TC>
+template <int TYPE, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
 {
     if (TYPE == 14 && g.skip_folded && __ldg(g.FLAG) != 0u)
@@ -1064,53 +641,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
     const uint32_t sbase = raw_addr + pad;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // barrier layout of the chosen tile layout
-    constexpr int kBar = TC ? TC_SMEM_BAR : SMEM_BAR;
-    constexpr int kStages = TC ? TC_STAGES : STAGES;
-    constexpr int kFull = TC ? TC_BAR_FULL : BAR_FULL, kEmpty = TC ? TC_BAR_EMPTY : BAR_EMPTY;
-    constexpr int kSbFull = TC ? TC_BAR_SBFULL : BAR_SBFULL, kSbEmpty = TC ? TC_BAR_SBEMPTY : BAR_SBEMPTY;
-    constexpr int kTFull = TC ? TC_BAR_TFULL : BAR_TFULL, kTEmpty = TC ? TC_BAR_TEMPTY : BAR_TEMPTY;
-    constexpr int kDrain = TC ? TC_BAR_DRAIN : BAR_DRAIN;
-    constexpr int kItems = TC ? TC_ITEMS : 4;
-    constexpr int kTmemPtr = TC ? TC_SMEM_TMEMPTR : SMEM_TMEMPTR;
-    auto bar = [&](int i) -> uint32_t { return sbase + kBar + 8u * static_cast<uint32_t>(i); };
+    auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kFull + s), 1);
-            mbar_init(bar(kEmpty + s), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(BAR_FULL + s), 1);
+            mbar_init(bar(BAR_EMPTY + s), 1);
         }
         for (int s = 0; s < SBR; ++s) {
-            mbar_init(bar(kSbFull + s), 1);
-            mbar_init(bar(kSbEmpty + s), NUM_PROMO_WARPS);
+            mbar_init(bar(BAR_SBFULL + s), 1);
+            mbar_init(bar(BAR_SBEMPTY + s), NUM_PROMO_WARPS);
         }
-        for (int k = 0; k < kItems; ++k) {
-            mbar_init(bar(kTFull + k), 1);
-            mbar_init(bar(kTEmpty + k), NUM_PROMO_WARPS);
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(bar(BAR_TFULL + k), 1);
+            mbar_init(bar(BAR_TEMPTY + k), NUM_PROMO_WARPS);
         }
-        mbar_init(bar(kDrain), 1);
+        mbar_init(bar(BAR_DRAIN), 1);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(sbase + kTmemPtr, TMEM_COLS);
+        tmem_alloc(sbase + SMEM_TMEMPTR, TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + kTmemPtr);
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + SMEM_TMEMPTR);
 
-    if constexpr (TC) {
-        if constexpr (TYPE == 14) {
-            if (__ldg(g.FLAG) != 0u)
-                gemm_roles_tc<14, true>(g, smem, sbase, tmem_base, warp, lane);
-            else
-                gemm_roles_tc<14, false>(g, smem, sbase, tmem_base, warp, lane);
-        } else {
-            gemm_roles_tc<12, true>(g, smem, sbase, tmem_base, warp, lane);
-        }
-    } else if constexpr (TYPE == 14) {
+    if constexpr (TYPE == 14) {
         // q6_K codes hold sc*q (one accumulator per chunk) unless some |sc| > 64;
         // the repack recorded which in the flag word (uniform for the launch).
         if (__ldg(g.FLAG) != 0u)
@@ -1143,7 +702,7 @@ __global__ void __launch_bounds__(256) zero_tiles_kernel(float* __restrict__ Y, 
     }
 }
 
-template <int TYPE, int MODE, bool TC = false>
+template <int TYPE, int MODE>
 cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
 {
     static std::atomic<uint64_t> attr_set_mask{0};  // one bit per device ordinal
@@ -1155,74 +714,20 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
     if (!(attr_set_mask.load() & bit)) {
         // The setmaxnreg split draws on the registers the launch reserved; a build
         // that compiled to fewer per thread would make the promotion wait forever.
-        // (The few-token layout does not split registers.)
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm_kernel<TYPE, MODE, TC>);
+        e = cudaFuncGetAttributes(&fa, gemm_kernel<TYPE, MODE>);
         if (e != cudaSuccess)
             return e;
-        if (!TC && fa.numRegs < LAUNCH_REGS)
+        if (fa.numRegs < LAUNCH_REGS)
             return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(gemm_kernel<TYPE, MODE, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TC ? TC_SMEM_ALLOC : SMEM_ALLOC);
+        e = cudaFuncSetAttribute(gemm_kernel<TYPE, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess)
             return e;
         attr_set_mask.fetch_or(bit);
     }
     count_launch();
-    if (TC && a.kslices > 1) {   // one cluster of kslices CTAs per weight tile
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = static_cast<unsigned>(a.kslices);
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = TC_SMEM_ALLOC;
-        cfg.stream = s;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gemm_kernel<TYPE, MODE, TC>, a);
-    }
-    gemm_kernel<TYPE, MODE, TC><<<grid, NUM_THREADS, TC ? TC_SMEM_ALLOC : SMEM_ALLOC, s>>>(a);
+    gemm_kernel<TYPE, MODE><<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(a);
     return cudaGetLastError();
-}
-
-// Clusters of `size` few-token CTAs that can be resident at once on this device (0 if
-// the query fails); cached per type, size and device ordinal.
-template <int TYPE>
-int tc_max_clusters(int size)
-{
-    static std::atomic<int> cache[5][64];   // size 0..4 (2..4 used) x device ordinal
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || size < 2 || size > 4)
-        return 0;
-    const int c = cache[size][dev].load();
-    if (c != 0)
-        return c > 0 ? c : 0;
-    int n = 0;
-    if (cudaFuncSetAttribute(gemm_kernel<TYPE, GEMM_Y, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TC_SMEM_ALLOC) == cudaSuccess) {
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = static_cast<unsigned>(size);
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(size));
-        cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = TC_SMEM_ALLOC;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<TYPE, GEMM_Y, true>, &cfg) != cudaSuccess) {
-            n = 0;
-            cudaGetLastError();   // clear the failed query's error, and only that one
-        }
-    } else {
-        cudaGetLastError();
-    }
-    cache[size][dev].store(n > 0 ? n : -1);
-    return n;
 }
 
 }  // namespace
@@ -1254,9 +759,10 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     e = take_wait_ctl(&wc, &injected);
     if (e != cudaSuccess)
         return e;
-    // Few tokens: the few-token GEMM (compact codes widened in shared memory, one TMEM
-    // accumulator per super-block), unless a tile layout was selected.
-    if (mode == GEMM_Y && M <= FT_MAX_M && (sel == 0 || sel == 3 || sel == 5))
+    // Few tokens: the few-token GEMM (compact codes widened into tensor memory, one TMEM
+    // accumulator per super-block), unless a tile kernel was selected.  No cluster split
+    // under a wait-timeout injection: a cluster barrier has no time limit.
+    if (mode == GEMM_Y && M <= FT_MAX_M && (sel == 0 || sel == 3 || sel == 4))
         return launch_gemm_ft(type, packed, od, id, qa, scales, M, out, ldy, s, wc, !injected && sel != 3,
                               path_label);
     if (sb_first) {
@@ -1297,11 +803,6 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.err = wc.err;
     a.wait_ns = wc.limit_ns;
     a.withhold = wc.withhold_fill;
-    // Few tokens: the tokens become the MMA's N (one accumulator column each) unless the
-    // token-row layout or the super-block kernel was selected.
-    const bool tc = mode == GEMM_Y && !sb_first && sel == 4 && M <= TC_MAX_M;
-    a.n_tok = tc ? ceil_div(M, 16) * 16 : 0;
-    a.kslices = 1;
 
     const int tiles = a.num_m * a.num_n;
     int grid = tiles < nsm ? tiles : nsm;
@@ -1313,29 +814,8 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     // Tiles run as two K-halves added into a zeroed Y (two addends: the order cannot
     // change the sum): every tile when the launch has at most half as many tiles as SMs
     // (decode-tail shapes), else the last round's tiles when they fill at most half.
-    // Few tokens and few weight tiles: one cluster of kslices CTAs per tile, each on a
-    // slice of K (partial sums added in rank order in shared memory), as many CTAs as
-    // the clusters that fit at once allow.
-    // (No cluster split under a wait-timeout injection: a cluster barrier has no time limit.)
-    if (tc && !injected) {
-        const int ts = ceil_div(od, BN);
-        for (int ks = 4; ks >= 2; --ks) {
-            if (nsb < ks || ts * ks > nsm)
-                continue;
-            const int fit = type == 14 ? tc_max_clusters<14>(ks) : tc_max_clusters<12>(ks);
-            if (fit >= ts) {
-                a.kslices = ks;
-                break;
-            }
-        }
-    }
-    if (a.kslices > 1) {
-        a.units = tiles * a.kslices;
-        a.full_units = a.units;
-        grid = a.units;
-    }
     int split = 0;
-    if (mode == GEMM_Y && !sb_first && nsb >= 2 && a.kslices == 1) {
+    if (mode == GEMM_Y && !sb_first && nsb >= 2) {
         if (2 * tiles <= nsm)
             split = tiles;
         else if (tiles > grid && rem > 0 && 2 * rem <= grid)
@@ -1353,40 +833,6 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
             return e;
     }
 
-    if (tc) {
-        if (path_label) {
-            // the K split actually taken: a cluster of S CTAs per tile, two K-halves, or none
-            static const char* const lab[2][5] = {
-                {"q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
-                 "super-block; K split: none",
-                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
-                 "super-block; K split: two K-halves added into a zeroed Y",
-                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
-                 "super-block; K split: cluster of S=2 CTAs",
-                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
-                 "super-block; K split: cluster of S=3 CTAs",
-                 "q4_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on scale-folded exact int codes, tf32 hi/lo min term, f32 d_a per chunk / d per "
-                 "super-block; K split: cluster of S=4 CTAs"},
-                {"q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: none",
-                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: two K-halves added "
-                 "into a zeroed Y",
-                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: cluster of S=2 CTAs",
-                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: cluster of S=3 CTAs",
-                 "q6_K: chunk GEMM, few-token layout (M <= 64): weight tile as the MMA's A, tokens as N, tcgen05.mma "
-                 "kind::f16 on exact int codes, f32 d_a per chunk / d per super-block; K split: cluster of S=4 CTAs"}};
-            *path_label = lab[type == 14 ? 1 : 0][a.kslices > 1 ? a.kslices : (split > 0 ? 1 : 0)];
-        }
-        return type == 14 ? launch_typed<14, GEMM_Y, true>(a, grid, s) : launch_typed<12, GEMM_Y, true>(a, grid, s);
-    }
     if (type == 14) {
         if (path_label)
             *path_label = sb_first

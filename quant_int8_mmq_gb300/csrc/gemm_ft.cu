@@ -41,7 +41,7 @@
 // distributed shared memory, in rank order); 16 warps:
 //   warp 0       producer: compact codes of each stage into a 4-deep ring (bulk copies,
 //                L2 prefetch four stages ahead) and once per super-block the weight d,
-//                the sub-block scales and the tokens' 1/p into a 3-deep ring.
+//                the sub-block scales and the tokens' 1/p into an 8-deep ring.
 //   warp 1       allocates TMEM: 4 accumulator items of 64 columns, 2 weight buffers of
 //                128 columns.
 //   warp 2       producer: the tokens' hi and lo tiles of each super-block (and the q4_K
@@ -79,7 +79,7 @@ constexpr int NUM_PROMO_WARPS = 4;
 constexpr int RAW_STAGES = 4;           // compact-code ring depth (stages)
 constexpr int PF_STAGES = 4;            // L2 prefetch distance of the compact codes, stages
 constexpr int TOK_STAGES = 2;           // token ring depth (super-blocks)
-constexpr int SBR = 3;                  // super-block ring depth
+constexpr int SBR = 8;                  // super-block ring depth (small entries: keeps the code stream ahead of the promotion)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t WBUF_COL0 = 256;     // accumulator items in columns [0, 256), then the two weight buffers
 constexpr uint32_t WBUF_COLS = 128;
@@ -925,22 +925,22 @@ cudaError_t launch_gemm_ft(int type, const void* packed, int od, int id, const v
     e = type == 14 ? launch_ft_nt<14>(a, nsm, allow_cluster, s) : launch_ft_nt<12>(a, nsm, allow_cluster, s);
     if (e == cudaSuccess && path_label) {
         static const char* const lab[2][9] = {
-            {"q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened to sc*q f16 tiles in shared memory, "
+            {"q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened to sc*q f16 tiles in tensor memory, "
              "weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, one TMEM accumulator per "
              "super-block, tf32 hi/lo min term; K split: none",
-             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened in shared memory; K split: cluster of S=2 CTAs",
-             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened in shared memory; K split: cluster of S=3 CTAs",
-             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened in shared memory; K split: cluster of S=4 CTAs",
-             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened in shared memory; K split: cluster of S=6 CTAs",
-             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened in shared memory; K split: cluster of S=8 CTAs"},
+             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=2 CTAs",
+             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=3 CTAs",
+             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=4 CTAs",
+             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=6 CTAs",
+             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=8 CTAs"},
             {"q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened to two exact f16 tiles (sc*l/4, "
-             "4*sc*(h-2)) in shared memory, weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, one "
+             "4*sc*(h-2)) in tensor memory, weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, one "
              "TMEM accumulator per super-block; K split: none",
-             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened in shared memory; K split: cluster of S=2 CTAs",
-             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened in shared memory; K split: cluster of S=3 CTAs",
-             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened in shared memory; K split: cluster of S=4 CTAs",
-             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened in shared memory; K split: cluster of S=6 CTAs",
-             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened in shared memory; K split: cluster of S=8 CTAs"}};
+             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=2 CTAs",
+             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=3 CTAs",
+             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=4 CTAs",
+             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=6 CTAs",
+             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=8 CTAs"}};
         *path_label = lab[type == 14 ? 1 : 0][g_last_kslices > 1 ? g_last_kslices : 0];
     }
     return e;

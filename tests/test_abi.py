@@ -104,10 +104,10 @@ def test_argument_errors_are_synchronous_and_cuda_free(mmq_lib):
     assert lib.mmq_convert_ggml_blocks(7, p16, 4, p16, None) == 1
     assert lib.mmq_convert_ggml_blocks(12, None, 4, p16, None) == 1
     assert lib.mmq_convert_ggml_blocks(14, p16, 4, None, None) == 1
-    # kernel selector: 0 to 5 only (host state, no CUDA call)
-    assert lib.mmq_debug_select_large_m_kernel(6) == 1
+    # kernel selector: 0 to 4 only (host state, no CUDA call)
+    assert lib.mmq_debug_select_large_m_kernel(5) == 1
     assert lib.mmq_debug_select_large_m_kernel(-1) == 1
-    assert lib.mmq_debug_select_large_m_kernel(5) == 0
+    assert lib.mmq_debug_select_large_m_kernel(4) == 0
     assert lib.mmq_debug_select_large_m_kernel(0) == 0
     # wait-timeout injection: limit 1 us .. 2 s when arming; disarming takes any limit
     assert lib.mmq_debug_inject_wait_timeout(0, 999) == 1

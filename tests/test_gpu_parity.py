@@ -646,12 +646,12 @@ def test_gemm_few_token_wide_dynamic_range(typ):
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
 @pytest.mark.parametrize("M", [1, 2, 5, 8])
 def test_gemm_few_token_kernel_at_streaming_sizes(typ, M):
-    """Selector 5: the few-token GEMM also for M <= 8 (N = 16)."""
+    """Selector 4: the few-token GEMM also for M <= 8 (N = 16)."""
     t = "q6_K" if typ.startswith("q6_K") else typ
     od, id_ = 4097, 1024
     raw = _q6_raw(od, id_, od + M + 3, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, od + M + 3)
     x = synth.activations(M, id_, 10 * M + 5)
-    mmq.mmq_debug_select_large_m_kernel(5)
+    mmq.mmq_debug_select_large_m_kernel(4)
     try:
         Y = _run_gemm(t, raw, x).cpu().numpy()
         assert "few-token GEMM" in mmq.mmq_last_path()
@@ -661,27 +661,9 @@ def test_gemm_few_token_kernel_at_streaming_sizes(typ, M):
     assert_y_close(Y, Yo, S)
 
 
-@pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
-@pytest.mark.parametrize("M,od,id_", [(31, 4097, 11008), (31, 259, 768)])
-def test_gemm_chunk_kernel_few_token_layout(typ, M, od, id_):
-    """Selector 4: the chunk kernel's transposed few-token layout (tokens as N, exact
-    integer dots per chunk), kept for comparison."""
-    t = "q6_K" if typ.startswith("q6_K") else typ
-    raw = _q6_raw(od, id_, M + 17, True) if t == "q6_K" else synth.q4k_blocks(od, id_, M + 17)
-    x = synth.activations(M, id_, M + 18)
-    mmq.mmq_debug_select_large_m_kernel(4)
-    try:
-        Y = _run_gemm(t, raw, x).cpu().numpy()
-        assert "chunk GEMM, few-token layout" in mmq.mmq_last_path()
-    finally:
-        mmq.mmq_debug_select_large_m_kernel(0)
-    Yo, S = oracle_gemm(t, raw, x)
-    assert_y_close(Y, Yo, S)
-
-
 def test_select_large_m_kernel_rejects_other_values():
     with pytest.raises(mmq.MMQError):
-        mmq.mmq_debug_select_large_m_kernel(6)
+        mmq.mmq_debug_select_large_m_kernel(5)
 
 
 # --------------------------------------------------------------------------- weight-streaming path (M <= 8)

@@ -45,7 +45,6 @@ def _raw(typ, od, id_, seed):
     (1, "q6_K_full", 200, 300, 768, "chunk GEMM"),
     (0, "q4_K", 31, 259, 768, "few-token GEMM"),
     (0, "q6_K_full", 31, 259, 768, "few-token GEMM"),
-    (4, "q4_K", 31, 259, 768, "chunk GEMM, few-token layout"),
 ])
 def test_expired_wait_is_reported_then_cleared(selector, typ, M, od, id_, label):
     t = "q6_K" if typ.startswith("q6_K") else typ
