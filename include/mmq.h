@@ -188,6 +188,19 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
 mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id,
                             void* packed, mmq_stream_t s);
 
+/* Fused registration of two weights that read the same input ([r58] §5, the fused
+ * FFN gate/up GEMM): packs raw_a (od_a rows) and raw_b (od_b rows), both of type t
+ * and width id, as ONE weight of od = od_a + od_b rows in the layout above, rows
+ * [0, od_a) from raw_a and [od_a, od) from raw_b; the planes equal those of
+ * mmq_pack_weights on the two raw buffers concatenated row-wise, without that copy.
+ * One GEMM on it (mmq_gemm_* with od = od_a + od_b) over one set of activation
+ * planes writes both outputs side by side: Y[t][j] for j < od_a is row j of a,
+ * Y[t][od_a + j] row j of b.  packed must hold mmq_packed_weight_bytes(t, od, id).
+ * MMQ_ERR_SHAPE for od_a or od_b < 1 or a sum over MMQ_MAX_OD; otherwise as
+ * mmq_pack_weights. */
+mmq_status mmq_pack_weights_fused(mmq_type t, const void* raw_a, int od_a, const void* raw_b, int od_b, int id,
+                                  void* packed, mmq_stream_t s);
+
 /* GGUF interop (registration time): nblocks q4_K (144 B) or q6_K (210 B) blocks in
  * the public ggml (llama.cpp) block layout, rewritten into the layout documented
  * above for raw_blocks, so that mmq_pack_weights can take weights read from a GGUF

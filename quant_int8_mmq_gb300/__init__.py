@@ -22,10 +22,10 @@ __all__ = [
     "mmq_act_plane_bytes", "mmq_act_scale_layout", "mmq_act_ft_layout", "mmq_quantize_act",
     "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
-    "mmq_pack_weights", "mmq_convert_ggml_blocks", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
+    "mmq_pack_weights", "mmq_pack_weights_fused", "mmq_convert_ggml_blocks", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
     "mmq_debug_inject_wait_timeout",
     "mmq_get_device_error", "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
-    "quantize_act", "pack_weights", "gemm", "gemm_dots", "TYPES",
+    "quantize_act", "pack_weights", "pack_weights_fused", "gemm", "gemm_dots", "TYPES",
 ]
 
 MMQ_Q4_K = 12
@@ -69,6 +69,7 @@ def load():
             "mmq_act_scale_layout": [I, I, S, S, S, S],
             "mmq_act_ft_layout": [I, I, S, S, S, S],
             "mmq_pack_weights": [I, P, I, I, P, P],
+            "mmq_pack_weights_fused": [I, P, I, P, I, I, P, P],
             "mmq_convert_ggml_blocks": [I, P, ctypes.c_size_t, P, P],
             "mmq_gemm_q6k": [P, I, I, P, P, I, P, I, P],
             "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
@@ -144,6 +145,11 @@ def mmq_act_ft_layout(M, K):
 
 def mmq_pack_weights(t, raw, od, id_, packed, stream=0):
     _check(load().mmq_pack_weights(t, raw, od, id_, packed, stream or None), "mmq_pack_weights")
+
+
+def mmq_pack_weights_fused(t, raw_a, od_a, raw_b, od_b, id_, packed, stream=0):
+    _check(load().mmq_pack_weights_fused(t, raw_a, od_a, raw_b, od_b, id_, packed, stream or None),
+           "mmq_pack_weights_fused")
 
 
 def mmq_convert_ggml_blocks(t, src, nblocks, dst, stream=0):
@@ -274,6 +280,27 @@ def pack_weights(t, raw, od, id_, packed=None, stream=None):
     _require(packed.is_cuda and packed.is_contiguous() and _nbytes(packed) >= nb,
              f"packed must be a contiguous CUDA buffer of at least {nb} bytes")
     mmq_pack_weights(tid, raw.data_ptr(), od, id_, packed.data_ptr(), _stream(stream))
+    return packed
+
+
+def pack_weights_fused(t, raw_a, od_a, raw_b, od_b, id_, packed=None, stream=None):
+    """Two raw weights of one type and width (uint8 CUDA tensors) packed as one weight of
+    od_a + od_b rows (a's rows first); one GEMM on it computes both outputs."""
+    torch = _torch()
+    tid = _type_id(t)
+    for raw, od in ((raw_a, od_a), (raw_b, od_b)):
+        _require(raw.dtype == torch.uint8 and raw.is_contiguous() and raw.is_cuda,
+                 "raw weights must be contiguous uint8 CUDA tensors")
+        _require(raw.numel() == od * (id_ // 256) * BLOCK_BYTES[tid],
+                 f"raw holds {raw.numel()} bytes, {od} x {id_} {t} weights are {od * (id_ // 256) * BLOCK_BYTES[tid]}")
+    _require(raw_a.device == raw_b.device, "both raw weights must be on one device")
+    nb = mmq_packed_weight_bytes(tid, od_a + od_b, id_)
+    if packed is None:
+        packed = torch.empty(nb, dtype=torch.uint8, device=raw_a.device)
+    _require(packed.is_cuda and packed.is_contiguous() and _nbytes(packed) >= nb,
+             f"packed must be a contiguous CUDA buffer of at least {nb} bytes")
+    mmq_pack_weights_fused(tid, raw_a.data_ptr(), od_a, raw_b.data_ptr(), od_b, id_, packed.data_ptr(),
+                           _stream(stream))
     return packed
 
 

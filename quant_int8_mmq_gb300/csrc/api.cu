@@ -271,7 +271,28 @@ mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id, 
     st = check_device();
     if (st != MMQ_OK)
         return st;
-    return from_cuda(mmq::launch_pack(static_cast<int>(t), raw_blocks, od, id, packed,
+    return from_cuda(mmq::launch_pack(static_cast<int>(t), raw_blocks, od, raw_blocks, od, id, packed,
+                                      reinterpret_cast<cudaStream_t>(s)));
+}
+
+mmq_status mmq_pack_weights_fused(mmq_type t, const void* raw_a, int od_a, const void* raw_b, int od_b, int id,
+                                  void* packed, mmq_stream_t s)
+{
+    if (t != MMQ_Q4_K && t != MMQ_Q6_K)
+        return MMQ_ERR_ARG;
+    if (od_a < 1 || od_b < 1 || static_cast<long long>(od_a) + od_b > MMQ_MAX_OD)
+        return MMQ_ERR_SHAPE;
+    mmq_status st = check_weight_shape(t, od_a + od_b, id);
+    if (st != MMQ_OK)
+        return st;
+    if (!raw_a || !raw_b || !packed)
+        return MMQ_ERR_ARG;
+    if (!aligned(packed, 16))
+        return MMQ_ERR_ALIGN;
+    st = check_device();
+    if (st != MMQ_OK)
+        return st;
+    return from_cuda(mmq::launch_pack(static_cast<int>(t), raw_a, od_a, raw_b, od_a + od_b, id, packed,
                                       reinterpret_cast<cudaStream_t>(s)));
 }
 

@@ -193,7 +193,10 @@ cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, cudaSt
 // Each returns cudaSuccess or the launch error; arguments are already validated.
 cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales,
                                 cudaStream_t s);
-cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed, cudaStream_t s);
+// Repack od rows: rows [0, od_a) from raw_a and rows [od_a, od) from raw_b (a fused
+// pack of two weights sharing their input; a plain pack passes od_a = od).
+cudaError_t launch_pack(int type, const void* raw_a, int od_a, const void* raw_b, int od, int id, void* packed,
+                        cudaStream_t s);
 // ggml-layout blocks -> the layout launch_pack reads (src == dst allowed).
 cudaError_t launch_convert_ggml(int type, const void* src, size_t nblocks, void* dst, cudaStream_t s);
 

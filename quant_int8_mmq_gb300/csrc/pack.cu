@@ -70,13 +70,31 @@ __device__ __forceinline__ int q4k_field(const uint8_t* sc12, int f)
     return static_cast<int>(v & 63u);
 }
 
+// The raw blocks of the weight being packed: rows [0, od_a) from a, rows from od_a on
+// from b (a fused pack of two weights that share their input), each row-major with
+// nsb blocks per row; a plain pack has od_a = od.
+struct RawRows {
+    const uint8_t* a;
+    const uint8_t* b;
+    int od_a, nsb, bytes;
+    __device__ __forceinline__ const uint8_t* block(int j, int sb) const
+    {
+        return j < od_a ? a + (static_cast<size_t>(j) * nsb + sb) * bytes
+                        : b + (static_cast<size_t>(j - od_a) * nsb + sb) * bytes;
+    }
+    __device__ __forceinline__ const uint8_t* block(long long linear) const   // row-major block index
+    {
+        return block(static_cast<int>(linear / nsb), static_cast<int>(linear % nsb));
+    }
+};
+
 // q6_K: max |sc| over the tensor -> flag word 1 (atomicMax); word 0 is set later.
-__global__ void q6k_scale_scan(const uint8_t* __restrict__ raw, long long nblocks, unsigned int* flag)
+__global__ void q6k_scale_scan(const RawRows raw, long long nblocks, unsigned int* flag)
 {
     unsigned int mx = 0;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks * 16;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int v = static_cast<int8_t>(raw[(i >> 4) * Q6K_BYTES + 192 + (i & 15)]);
+        const int v = static_cast<int8_t>(raw.block(i >> 4)[192 + (i & 15)]);
         const unsigned int a = static_cast<unsigned int>(v < 0 ? -v : v);
         mx = a > mx ? a : mx;
     }
@@ -88,7 +106,7 @@ __global__ void q6k_scale_scan(const uint8_t* __restrict__ raw, long long nblock
 }
 
 template <int TYPE>
-__global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ raw, int od, int id, int Np,
+__global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, int id, int Np,
                                                    uint8_t* __restrict__ codes, float2* __restrict__ pairs,
                                                    float* __restrict__ sbd, uint8_t* __restrict__ aux,
                                                    unsigned int* __restrict__ flag)
@@ -111,7 +129,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ r
         float2 w = make_float2(0.0f, 0.0f);
         if (j < od) {
             if (TYPE == 14) {  // q6_K
-                const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + sb) * Q6K_BYTES;
+                const uint8_t* b = raw.block(j, sb);
                 const uint8_t* ql = b + 16 * cc;   // values 32cc.. use ql bytes 16cc..16cc+15
                 const uint8_t* qh = b + 128 + 8 * cc;
                 const int s0 = static_cast<int8_t>(b[192 + 2 * cc]);
@@ -140,7 +158,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ r
                         scp[s * TILE_ROWS + r] = static_cast<float>(static_cast<int8_t>(b[192 + s]));
                 }
             } else {  // q4_K
-                const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + sb) * Q4K_BYTES;
+                const uint8_t* b = raw.block(j, sb);
                 const uint8_t* qs = b + 16 + 16 * cc;
                 const int sc = q4k_field(b + 4, cc);
                 const int m = q4k_field(b + 4, 8 + cc);
@@ -194,7 +212,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ r
 //   q4_K in [d 2 | dmin 2 | scales 12 | qs 128]  -> out [qs 128 | d, dmin, scales 16]
 //   q6_K in [ql 128 | qh 64 | scales 16 | d 2]   -> out [the same 210 | zeros 14]
 template <int TYPE>
-__global__ void __launch_bounds__(256) raw_relayout_kernel(const uint8_t* __restrict__ raw, long long nblocks,
+__global__ void __launch_bounds__(256) raw_relayout_kernel(const RawRows raw, long long nblocks,
                                                            uint32_t* __restrict__ out)
 {
     constexpr int IN = (TYPE == 12) ? Q4K_BYTES : Q6K_BYTES;
@@ -204,7 +222,7 @@ __global__ void __launch_bounds__(256) raw_relayout_kernel(const uint8_t* __rest
          w += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long b = w / OUTW;
         const int o = static_cast<int>(w - b * OUTW) * 4;
-        const uint8_t* src = raw + b * IN;
+        const uint8_t* src = raw.block(b);
         uint32_t v = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -232,7 +250,7 @@ __global__ void __launch_bounds__(256) raw_relayout_kernel(const uint8_t* __rest
 //     in bytes 8hc..8hc+7, byte group s = 0, 1 of it holding units u = 2s and 2s + 1
 //     of the chunk, value 8u + 2p + h at bit 8(u - 2s) + 2p + 16h.
 template <int TYPE>
-__global__ void __launch_bounds__(256) compact_kernel(const uint8_t* __restrict__ raw, int od, int id, int Np,
+__global__ void __launch_bounds__(256) compact_kernel(const RawRows raw, int od, int id, int Np,
                                                       uint4* __restrict__ cw, uint4* __restrict__ scp)
 {
     constexpr int W = cw_words(TYPE);
@@ -255,7 +273,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const uint8_t* __restrict_
                 word[w][u] = 0u;
         uint32_t sc4[4] = {0u, 0u, 0u, 0u};
         if (j < od) {
-            const uint8_t* b = raw + (static_cast<size_t>(j) * nsb + sb) * (TYPE == 12 ? Q4K_BYTES : Q6K_BYTES);
+            const uint8_t* b = raw.block(j, sb);
             for (int hc = 0; hc < 2; ++hc) {
                 const int e0 = 64 * (kb & 3) + 32 * hc;      // first value of the chunk in its block
                 for (int i2 = 0; i2 < 32; ++i2) {
@@ -305,8 +323,15 @@ __global__ void __launch_bounds__(256) compact_kernel(const uint8_t* __restrict_
 
 }  // namespace
 
-cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed, cudaStream_t s)
+cudaError_t launch_pack(int type, const void* raw_a, int od_a, const void* raw_b, int od, int id, void* packed,
+                        cudaStream_t s)
 {
+    RawRows rb;
+    rb.a = static_cast<const uint8_t*>(raw_a);
+    rb.b = static_cast<const uint8_t*>(raw_b);
+    rb.od_a = od_a;
+    rb.nsb = id / QK_K;
+    rb.bytes = type == 12 ? Q4K_BYTES : Q6K_BYTES;
     const WeightPlanes wp = weight_planes(type, od, id);
     const int Np = ceil_div(od, TILE_ROWS) * TILE_ROWS;
     const long long total = static_cast<long long>(Np) * (id / CHUNK);
@@ -314,7 +339,6 @@ cudaError_t launch_pack(int type, const void* raw, int od, int id, void* packed,
     if (blocks > 65535LL * 8)
         blocks = 65535LL * 8;
     uint8_t* base = static_cast<uint8_t*>(packed);
-    const uint8_t* rb = static_cast<const uint8_t*>(raw);
     unsigned int* flag = reinterpret_cast<unsigned int*>(base + wp.flag_off);
     cudaError_t e = cudaMemsetAsync(flag, 0, wp.flag_bytes, s);
     if (e != cudaSuccess)

@@ -100,6 +100,12 @@ def test_argument_errors_are_synchronous_and_cuda_free(mmq_lib):
     # bad type id
     assert lib.mmq_pack_weights(7, p16, 8, 256, p16, None) == 1
     assert lib.mmq_debug_gemm_dots(7, p16, 8, 256, p16, p16, 4, p16, None) == 1
+    # fused pack: bad type, empty part, null pointer, misaligned output
+    assert lib.mmq_pack_weights_fused(7, p16, 8, p16, 8, 256, p16, None) == 1
+    assert lib.mmq_pack_weights_fused(12, p16, 0, p16, 8, 256, p16, None) == 2
+    assert lib.mmq_pack_weights_fused(12, p16, 8, p16, 8, 300, p16, None) == 2
+    assert lib.mmq_pack_weights_fused(12, p16, 8, None, 8, 256, p16, None) == 1
+    assert lib.mmq_pack_weights_fused(12, p16, 8, p16, 8, 256, p16 + 8, None) == 3
     # ggml conversion: bad type, null pointers
     assert lib.mmq_convert_ggml_blocks(7, p16, 4, p16, None) == 1
     assert lib.mmq_convert_ggml_blocks(12, None, 4, p16, None) == 1

@@ -276,6 +276,63 @@ def test_pack_planes_byte_exact(typ, od, id_):
     assert np.array_equal(part["sc"], scale_plane(rows, Np))
 
 
+# --------------------------------------------------------------------------- fused two-weight pack
+@pytest.mark.parametrize("typ,od_a,od_b,id_", [("q4_K", 130, 67, 768), ("q6_K", 64, 259, 512), ("q6_K_mixed", 200, 57, 256)])
+def test_pack_fused_equals_pack_of_concatenation(typ, od_a, od_b, id_):
+    """The fused pack reads the two raw weights in place and writes the planes a pack of
+    their row-wise concatenation writes, byte for byte (q6_K_mixed: only the second
+    weight has scales beyond 64, so the fold decision spans both)."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    if typ == "q6_K_mixed":
+        ra, rb = _q6_raw(od_a, id_, 3, False), _q6_raw(od_b, id_, 4, True)
+    else:
+        ra, rb = _raw(t, od_a, id_, seed=5), _raw(t, od_b, id_, seed=6)
+    fused = mmq.pack_weights_fused(t, _to_dev(ra.reshape(-1)), od_a, _to_dev(rb.reshape(-1)), od_b, id_)
+    whole = gpu_pack(t, np.concatenate([ra, rb], axis=0))
+    _sync()
+    f, w = fused.cpu().numpy(), whole.cpu().numpy()
+    for name, (o, n) in mmq.mmq_packed_weight_layout(mmq.TYPES[t], od_a + od_b, id_).items():
+        assert np.array_equal(f[o:o + n], w[o:o + n]), name      # (alignment gaps are never written)
+
+
+@pytest.mark.parametrize("typ,od_a,od_b,id_,M", [("q4_K", 130, 67, 768, 200), ("q4_K", 300, 300, 512, 31),
+                                                ("q6_K", 259, 128, 768, 40), ("q4_K", 130, 67, 768, 3)])
+def test_gemm_fused_weights(typ, od_a, od_b, id_, M):
+    """One GEMM over the fused weight computes both outputs side by side: each part
+    matches the oracle and the separate GEMM of its own weight."""
+    ra, rb = _raw(typ, od_a, id_, seed=od_a + M), _raw(typ, od_b, id_, seed=od_b + M)
+    x = synth.activations(M, id_, seed=M + 9)
+    qa, sc = gpu_quantize(x)
+    fused = mmq.pack_weights_fused(typ, _to_dev(ra.reshape(-1)), od_a, _to_dev(rb.reshape(-1)), od_b, id_)
+    Y = mmq.gemm(typ, fused, od_a + od_b, id_, qa, sc, M)
+    Ya = mmq.gemm(typ, gpu_pack(typ, ra), od_a, id_, qa, sc, M)
+    Yb = mmq.gemm(typ, gpu_pack(typ, rb), od_b, id_, qa, sc, M)
+    _sync()
+    Y = Y.cpu().numpy()
+    for part, raw, Ys in ((Y[:, :od_a], ra, Ya), (Y[:, od_a:], rb, Yb)):
+        Yo, S = oracle_gemm(typ, raw, x)
+        assert_y_close(part, Yo, S)
+        assert_y_close(part, Ys.cpu().numpy().astype(np.float64), S)
+
+
+def test_gemm_fused_ffn_gate_up_at_prompt_length_sampled():
+    """The FFN gate and up weights (11008 x 4096 q4_K each) fused into one 22016-row
+    GEMM at M = 3314 tokens, the launch configuration of the fused bench figure."""
+    M, od, id_ = synth.STACK_M, 11008, 4096
+    ra, rb = synth.q4k_blocks(od, id_, 501), synth.q4k_blocks(od, id_, 502)
+    x = synth.activations(M, id_, 503)
+    qa, sc = gpu_quantize(x)
+    fused = mmq.pack_weights_fused("q4_K", _to_dev(ra.reshape(-1)), od, _to_dev(rb.reshape(-1)), od, id_)
+    Y = mmq.gemm("q4_K", fused, 2 * od, id_, qa, sc, M)
+    _sync()
+    assert "super-block" in mmq.mmq_last_path()
+    Y = Y.cpu().numpy()
+    rows = np.unique(np.r_[0, 127, 128, 3200, M - 1, np.random.default_rng(7).integers(0, M, 3)])
+    for part, raw in ((Y[:, :od], ra), (Y[:, od:], rb)):
+        Yo, S = oracle_gemm("q4_K", raw, x[rows])
+        assert_y_close(part[rows], Yo, S)
+
+
 # --------------------------------------------------------------------------- dots
 @pytest.mark.parametrize("typ", ["q6_K", "q6_K_full", "q4_K"])
 @pytest.mark.parametrize("M,od,id_", [(200, 300, 768), (1, 129, 256), (130, 64, 512), (257, 131, 2048)])
