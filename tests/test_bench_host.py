@@ -1,6 +1,6 @@
 """Host logic of bench.py that needs no GPU: the stack of GEMM shapes it times, the
-fused-pair bookkeeping of --fuse-shared-inputs, and the rule that a committed DRAM-traffic
-figure counts only for the exact kernel source it was captured from."""
+fused-pair bookkeeping of --fuse-shared-inputs, and the rule that committed ncu counters
+count only for the exact kernel sources they were captured from."""
 import hashlib
 import json
 import os
@@ -45,26 +45,32 @@ def test_fused_pairs_keep_every_row_and_seed():
             assert src[f"{layer}.{a}"][2] == src[f"{layer}.{b}"][2] == i
 
 
-def test_traffic_counts_only_for_the_captured_source(tmp_path, monkeypatch):
-    d = json.load(open(os.path.join(ROOT, "profiles", "gemm_traffic.json")))
-    key, want = next(iter(d["per_launch_dram_bytes"].items()))
-    src = os.path.join(ROOT, "quant_int8_mmq_gb300", "csrc", d["source"])
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() == d["source_sha256"]:
-        assert bench.kernel_traffic(key) == want
-    else:
-        assert bench.kernel_traffic(key) is None
-    # a copy of the tree whose kernel source differs by one byte reports no traffic
+def _sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
+def test_counters_count_only_for_the_captured_sources(tmp_path, monkeypatch):
+    d = json.load(open(os.path.join(ROOT, "profiles", "gemm_counters.json")))
+    key, want = next(iter(d["kernels"].items()))
+    srcs = [os.path.join(ROOT, "quant_int8_mmq_gb300", "csrc", n) for n in d["sources"]]
+    fresh = _sha(srcs) == d["sources_sha256"]
+    assert bench.kernel_traffic(key) == (want["dram_bytes"] if fresh else None)
+    # a copy of the tree whose kernel sources differ by one byte reports nothing
     fake = tmp_path / "root"
     (fake / "profiles").mkdir(parents=True)
     (fake / "quant_int8_mmq_gb300" / "csrc").mkdir(parents=True)
-    shutil.copy(os.path.join(ROOT, "profiles", "gemm_traffic.json"), fake / "profiles")
-    body = open(src, "rb").read()
-    (fake / "quant_int8_mmq_gb300" / "csrc" / d["source"]).write_bytes(body + b"\n")
+    shutil.copy(os.path.join(ROOT, "profiles", "gemm_counters.json"), fake / "profiles")
+    for n, src in zip(d["sources"], srcs):
+        shutil.copy(src, fake / "quant_int8_mmq_gb300" / "csrc" / n)
     monkeypatch.setattr(bench, "ROOT", str(fake))
+    assert bench.kernel_traffic(key) == (want["dram_bytes"] if fresh else None)
+    last = fake / "quant_int8_mmq_gb300" / "csrc" / d["sources"][-1]
+    last.write_bytes(last.read_bytes() + b"\n")
     assert bench.kernel_traffic(key) is None
-    (fake / "quant_int8_mmq_gb300" / "csrc" / d["source"]).write_bytes(body)
-    if hashlib.sha256(body).hexdigest() == d["source_sha256"]:
-        assert bench.kernel_traffic(key) == want
+    assert bench.kernel_counters(key) is None
     assert bench.kernel_traffic("no_such_kernel") is None
 
 
