@@ -107,16 +107,18 @@ typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
  *        field of the largest of its 8 chunk scales d, s = p*d (exact),
  *        s_hi = rn_f16(s), s_lo = rn_f16(s - s_hi), and for each code q:
  *        hi = rn_f16(s_hi*q), lo = rn_f16(fma(s_hi, q, -hi) + s_lo*q) (f16 fma);
- *     ip (in scales, after am) f32 1/p at index sb*MMQ_FT_MAX_M + t (t < N).
+ *     ip (in scales, after am) f32 1/p at index sb*MMQ_FT_MAX_M + t (t < N);
+ *     fm (in scales, after ip) f32 ma = d*ssum (one f32 multiply) of chunk c of
+ *        super-block sb at index (sb*MMQ_FT_MAX_M + t)*8 + c % 8 (t < N).
  * -------------------------------------------------------------------------- */
 #define MMQ_SMALL_M 8
 #define MMQ_FT_MAX_M 64
 mmq_status mmq_act_plane_bytes(int M, int K, size_t* qa_bytes, size_t* scale_bytes);
 mmq_status mmq_act_scale_layout(int M, int K, size_t* pair_offset, size_t* pair_bytes,
                                 size_t* am_offset, size_t* am_bytes);
-/* Offsets and sizes of the few-token planes (all four 0 when M > MMQ_FT_MAX_M). */
+/* Offsets and sizes of the few-token planes (all six 0 when M > MMQ_FT_MAX_M). */
 mmq_status mmq_act_ft_layout(int M, int K, size_t* tq_offset, size_t* tq_bytes,
-                             size_t* ip_offset, size_t* ip_bytes);
+                             size_t* ip_offset, size_t* ip_bytes, size_t* fm_offset, size_t* fm_bytes);
 
 /* Quantize x [M][ldx] f32 (row-major, first K values of each row used) per
  * 32-value chunk: d = amax/127 (IEEE f32 division), q = round(x/d) (IEEE f32
@@ -138,7 +140,7 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *   q6_K ((ql[e/2] >> 4*(e%2)) & 15 | ((qh[e/4] >> 2*(e%4)) & 3) << 4) - 32,
  *   q4_K (qs[e/2] >> 4*(e%2)) & 15.  Value e of a q6_K block uses scales[e/16].
  *
- * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds six planes at
+ * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds nine planes at
  * the offsets mmq_packed_weight_layout() returns; Np = 128*ceil(od/128),
  * nkb = id/64, nchunk = id/32, nsb = id/256; rows j >= od are zero:
  *   CODES  Np*id f16 integers in 16384-byte tiles (nt, kb) at (nt*nkb + kb)*16384,
@@ -160,7 +162,7 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *          blocks, row-major: q4_K 144 B [qs[128] | d | dmin | scales[12]],
  *          q6_K 224 B [ql[128] | qh[64] | scales[16] | d | 14 zero bytes].
  *   CW     compact codes for the few-token GEMM, which widens them to f16 in
- *          shared memory: per (nt, kb) W = 2 (q4_K) or 3 (q6_K) words of 16 bytes
+ *          tensor memory: per (nt, kb) W = 2 (q4_K) or 3 (q6_K) words of 16 bytes
  *          per row, word-major: word w of row r at ((nt*nkb + kb)*W + w)*2048 + r*16.
  *          Words 0, 1 hold chunk 2*kb + w: the 4-bit code (q4_K) or the low 4 bits
  *          of q + 32 (q6_K) of value 8u + 2p + h of the chunk (u, p = 0..3, h = 0,1)
@@ -169,6 +171,8 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *          8u + 2p + h of the chunk in word 2hc + u/2 at bit 8(u%2) + 2p + 16h.
  *   SC     sub-block scales per (nt, sb): 16 bytes per row at ((nt*nsb + sb)*128 + r)*16:
  *          q4_K the six-bit sc_0..sc_7 then m_0..m_7, one per byte; q6_K scales[16].
+ *   DM     q4_K: f32 dmin per (row, super-block) at index ((j/128)*nsb + sb)*128 + j%128
+ *          (the few-token GEMM's min-term factor); q6_K: empty.
  * -------------------------------------------------------------------------- */
 typedef enum {
     MMQ_PLANE_CODES = 0,
@@ -179,7 +183,8 @@ typedef enum {
     MMQ_PLANE_RAW = 5,
     MMQ_PLANE_CW = 6,
     MMQ_PLANE_SC = 7,
-    MMQ_NUM_WEIGHT_PLANES = 8
+    MMQ_PLANE_DM = 8,
+    MMQ_NUM_WEIGHT_PLANES = 9
 } mmq_weight_plane;
 
 mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes);

@@ -67,7 +67,7 @@ def load():
             "mmq_packed_weight_bytes": [I, I, I, S],
             "mmq_packed_weight_layout": [I, I, I, S, S],
             "mmq_act_scale_layout": [I, I, S, S, S, S],
-            "mmq_act_ft_layout": [I, I, S, S, S, S],
+            "mmq_act_ft_layout": [I, I, S, S, S, S, S, S],
             "mmq_pack_weights": [I, P, I, I, P, P],
             "mmq_pack_weights_fused": [I, P, I, P, I, I, P, P],
             "mmq_convert_ggml_blocks": [I, P, ctypes.c_size_t, P, P],
@@ -116,7 +116,7 @@ def mmq_packed_weight_bytes(t, od, id_):
     return b.value
 
 
-PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw", "cw", "sc")
+PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw", "cw", "sc", "dm")
 SMALL_M = 8          # token counts up to this take the weight-streaming path
 FT_MAX_M = 64        # token counts up to this take the few-token GEMM (and get its planes)
 
@@ -137,10 +137,10 @@ def mmq_act_scale_layout(M, K):
 
 
 def mmq_act_ft_layout(M, K):
-    """{"tq": (offset, size), "ip": (offset, size)} of the few-token planes (sizes 0 when M > 64)."""
-    v = [ctypes.c_size_t() for _ in range(4)]
+    """{"tq", "ip", "fm": (offset, size)} of the few-token planes (sizes 0 when M > 64)."""
+    v = [ctypes.c_size_t() for _ in range(6)]
     _check(load().mmq_act_ft_layout(M, K, *[ctypes.byref(x) for x in v]), "mmq_act_ft_layout")
-    return {"tq": (v[0].value, v[1].value), "ip": (v[2].value, v[3].value)}
+    return {"tq": (v[0].value, v[1].value), "ip": (v[2].value, v[3].value), "fm": (v[4].value, v[5].value)}
 
 
 def mmq_pack_weights(t, raw, od, id_, packed, stream=0):

@@ -224,15 +224,17 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
     sizes[MMQ_PLANE_RAW] = w.raw_bytes;
     offsets[MMQ_PLANE_CW] = w.cw_off;
     sizes[MMQ_PLANE_CW] = w.cw_bytes;
+    offsets[MMQ_PLANE_DM] = w.dm_off;
+    sizes[MMQ_PLANE_DM] = w.dm_bytes;
     offsets[MMQ_PLANE_SC] = w.sc_off;
     sizes[MMQ_PLANE_SC] = w.sc_bytes;
     return MMQ_OK;
 }
 
 mmq_status mmq_act_ft_layout(int M, int K, size_t* tq_offset, size_t* tq_bytes, size_t* ip_offset,
-                             size_t* ip_bytes)
+                             size_t* ip_bytes, size_t* fm_offset, size_t* fm_bytes)
 {
-    if (!tq_offset || !tq_bytes || !ip_offset || !ip_bytes)
+    if (!tq_offset || !tq_bytes || !ip_offset || !ip_bytes || !fm_offset || !fm_bytes)
         return MMQ_ERR_ARG;
     if (M < 1 || M > MMQ_MAX_M || !valid_k(K))
         return MMQ_ERR_SHAPE;
@@ -241,6 +243,8 @@ mmq_status mmq_act_ft_layout(int M, int K, size_t* tq_offset, size_t* tq_bytes, 
     *tq_bytes = p.tq_bytes;
     *ip_offset = p.ip_bytes ? p.ip_off : 0;
     *ip_bytes = p.ip_bytes;
+    *fm_offset = p.fm_bytes ? p.fm_off : 0;
+    *fm_bytes = p.fm_bytes;
     return MMQ_OK;
 }
 

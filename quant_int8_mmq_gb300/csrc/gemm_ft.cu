@@ -6,19 +6,27 @@
 // operands swapped, so that the weight rows fill the 128 TMEM lanes and the tokens are
 // the MMA's N (16 * ceil(M/16) columns):
 //
-//   D[j,t] = sum_{k in sb} W[j,k] * (hi[t,k] + lo[t,k])      (tcgen05 kind::f16, f32 TMEM)
-//   Y[t,j] = sum_sb d_sb[j] * D[j,t] * (1/p[t,sb])  -  sum_c (d_a*ssum)[t,c] * (dmin*m)[j,c]
+//   D[j,t] = sum_{k in stage} W[j,k] * (hi[t,k] + lo[t,k])      (tcgen05 kind::f16, f32 TMEM)
+//   Y[t,j] = sum_sb d_sb[j] * (sum of the super-block's stage D[j,t]) * (1/p[t,sb])
+//            -  sum_sb sum_c dmin_sb[j] * m_c[j] * (d_a*ssum)[t,c]            (q4_K)
 //
 // hi + lo = p * d_a * q_a is the activation operand the prepass writes for few tokens
 // (about 21 significant bits per value, p a power of two per token and super-block);
 // W is the integer-scaled weight code, exact in f16:
 //   q4_K: W = sc_c * q                           (|W| <= 945, one tile)
-//   q6_K: W = (sc * l) / 4  +  4 * sc * (h - 2)  (two tiles; l, h the low 4 and high 2
-//         bits of q + 32; sc * l / 4 is a quarter-integer below 480 in magnitude and
-//         4 sc (h - 2) an integer of at most 1024, both exact for any int8 sc), so the
-//         sum of the two tiles is sc * q / 4 and the promotion uses 4/p.
+//   q6_K whose every |sc| <= 64 (the packed flag says so):
+//         W = sc * q = sc * l + 16 sc (h - 2)    (|W| <= 2048, one tile; l, h the low 4
+//         and high 2 bits of q + 32, each term exact and so is their f16 sum)
+//   q6_K otherwise:
+//         W = (sc * l) / 4  +  4 * sc * (h - 2)  (two tiles; sc * l / 4 is a quarter-integer
+//         below 480 in magnitude and 4 sc (h - 2) an integer of at most 1024, both exact
+//         for any int8 sc), so the sum of the two tiles is sc * q / 4 and the promotion
+//         uses 4/p.
 // Every product W * hi, W * lo is exact; the roundings are the split of the activation
-// operand, the f32 sums and the promotion (the 1e-5 bound on Y holds with margin).
+// operand, the f32 sums and the promotion (the 1e-5 bound on Y holds with margin).  The
+// q4_K min term is a contraction over only 8 chunks per super-block: the promotion
+// threads take it on the CUDA cores (8 f32 FMAs per token and super-block), off the
+// tensor pipe.
 //
 // The weights come from the compact code plane (0.5 B per value for q4_K, 0.75 for
 // q6_K) and are widened to f16 by converter warps, the unpacking of "r56 - q6_K A-side
@@ -30,31 +38,33 @@
 // memory (tcgen05.st), where the MMA reads its A operand; only the compact codes and
 // the tokens pass through shared memory.
 //
-// Synchronisation is the cost at these sizes (each mbarrier hand-off between roles
-// costs a few hundred cycles whatever the stage carries), so a stage is large: one
-// super-block of q4_K or half a super-block of q6_K (128 TMEM columns of weights,
-// double-buffered), the tokens of a whole super-block arrive in one bulk copy, and one
-// MMA covers the hi and the lo rows of the tokens.
+// At these N an MMA costs the issuing thread a fixed ~50 ns whatever its width, and
+// MMAs from different threads into different accumulators overlap on the tensor
+// pipe, so two warps issue: stage g (a super-block, or for two-tile q6_K half of one)
+// goes to issuer g % 2, into its own accumulator item; the promotion adds the items
+// of a super-block.  A stage is large because each mbarrier hand-off between roles
+// costs a few hundred cycles whatever the stage carries: 128 TMEM columns of widened
+// weights (double-buffered), the tokens of a whole super-block in one bulk copy, and
+// one MMA covering the hi and the lo rows of the tokens.
 //
 // One CTA per SM, persistent over 128-row weight tiles (or, when the tiles are few,
 // one cluster of S CTAs per tile along K whose partial sums meet in rank 0 through
 // distributed shared memory, in rank order); 16 warps:
-//   warp 0       producer: compact codes of each stage into a 4-deep ring (bulk copies,
-//                L2 prefetch four stages ahead) and once per super-block the weight d,
-//                the sub-block scales and the tokens' 1/p into an 8-deep ring.
-//   warp 1       allocates TMEM: 4 accumulator items of 64 columns, 2 weight buffers of
-//                128 columns.
-//   warp 2       producer: the tokens' hi and lo tiles of each super-block (and the q4_K
-//                min-term operands) into a 2-deep ring.
-//   warp 3       MMA issuer: per stage the MMAs 128 x 2N x 16 (A = weights from TMEM, B =
-//                the N hi and N lo token rows from shared memory in one operand; q6_K two
-//                weight tiles) into the super-block's item, and for q4_K the min term
-//                (tf32 hi/lo, three MMAs per super-block) per unit.
+//   warp 0       producer: compact codes of each stage into a ring (bulk copies, L2
+//                prefetch four stages ahead) and once per super-block the weight d, the
+//                sub-block scales, the tokens' 1/p and (q4_K) the weight dmin and the
+//                tokens' d_a*ssum into a ring.
+//   warp 1       allocates TMEM (accumulator items in columns [0, 256), two weight
+//                buffers of 128 columns), then issues the odd stages.
+//   warp 2       producer: the tokens' hi and lo tiles of each super-block into a 2-deep
+//                ring.
+//   warp 3       issues the even stages: 128 x 2N x 16 MMAs (A = weights from TMEM, B =
+//                the N hi and N lo token rows from shared memory in one operand).
 //   warps 4-11   converters: thread (row r, half h of the stage) widens its values into
-//                the weight buffer and the warp signals the issuer.
+//                the weight buffer and the warp signals the issuers.
 //   warps 12-15  promotion: thread = weight row (its TMEM lane), every token: per
-//                super-block one TMEM load, acc += d * (D * 1/p); per unit acc -= min
-//                term; store Y.
+//                super-block its stage items' TMEM loads, acc += d * (D * 1/p), and for
+//                q4_K acc -= dmin * sum_c m_c * (d_a*ssum)_c; store Y.
 //
 // Every mbarrier wait is bounded; on expiry the kernel sets the library's error word,
 // every role leaves its loop, waits (bounded) for its own copies and MMAs in flight,
@@ -76,14 +86,14 @@ constexpr int CONV_WARP0 = 4;
 constexpr int NUM_CONV_WARPS = 8;
 constexpr int PROMO_WARP0 = 12;
 constexpr int NUM_PROMO_WARPS = 4;
-constexpr int RAW_STAGES = 4;           // compact-code ring depth (stages)
+constexpr int NUM_ISSUERS = 2;          // warp 3: even stages, warp 1: odd stages
 constexpr int PF_STAGES = 4;            // L2 prefetch distance of the compact codes, stages
 constexpr int TOK_STAGES = 2;           // token ring depth (super-blocks)
-constexpr int SBR = 8;                  // super-block ring depth (small entries: keeps the code stream ahead of the promotion)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t WBUF_COL0 = 256;     // accumulator items in columns [0, 256), then the two weight buffers
 constexpr uint32_t WBUF_COLS = 128;
 constexpr int MAX_CLUSTER = 8;
+constexpr int SMEM_BUDGET = 227 * 1024 - 2048;   // rings; the rest: barriers, TMEM address, alignment slack
 static_assert(WBUF_COL0 + 2 * WBUF_COLS <= TMEM_COLS, "TMEM budget");
 // Accumulator items: one MMA covers the hi and the lo token rows (N = 2 x 16*NT columns:
 // W*hi in the first half, W*lo in the second), 64 or 128 columns per item.
@@ -92,27 +102,36 @@ __host__ __device__ constexpr uint32_t item_cols_of(int nt) { return nt <= 2 ? 6
 // K split of the most recent launch from this thread (for its path label).
 thread_local int g_last_kslices = 1;
 
-// Super-block ring entry: weight d of the 128 rows, their 16 sub-block scale bytes, and
-// 1/p of the FT_MAX_M tokens.
+// Super-block ring entry: weight d of the 128 rows, their 16 sub-block scale bytes, 1/p
+// of the FT_MAX_M tokens, and for q4_K the rows' dmin and the tokens' 8 values d_a*ssum.
 constexpr int SB_SBD_OFF = 0;
 constexpr int SB_SC_OFF = SB_SBD_OFF + BM * 4;
 constexpr int SB_IP_OFF = SB_SC_OFF + BM * SC_ROW_BYTES;
-constexpr int SB_BYTES = SB_IP_OFF + FT_MAX_M * 4;
-// q4_K min-term operands of one super-block in a token slot: weight tf32 hi/lo tiles,
-// then the tokens'.
-constexpr int MIN_SB_BYTES = 4 * TF32_TILE_BYTES;
+constexpr int SB_DM_OFF = SB_IP_OFF + FT_MAX_M * 4;
+constexpr int SB_FM_OFF = SB_DM_OFF + BM * 4;
+__host__ __device__ constexpr int sb_bytes_of(int type) { return type == 12 ? SB_FM_OFF + FT_MAX_M * 32 : SB_DM_OFF; }
 
-template <int TYPE, int NT>
+// ONE: one weight tile per k-block (q4_K always; q6_K when its codes fold); else two.
+template <int TYPE, int NT, bool ONE>
 struct Cfg {
     static constexpr int N = 16 * NT;
+    static constexpr int TILES = ONE ? 1 : 2;
     static constexpr int ITEMS = items_of(NT);
     static constexpr uint32_t ITEM_COLS = item_cols_of(NT);
     static_assert(ITEMS * ITEM_COLS == WBUF_COL0 && 2 * N <= static_cast<int>(ITEM_COLS), "items");
-    static constexpr int KPS = (TYPE == 12) ? 4 : 2;                 // k-blocks per stage
+    static_assert(TYPE == 14 || ONE, "q4_K has one tile");
+    static constexpr int KPS = ONE ? 4 : 2;                          // k-blocks per stage
     static constexpr int SPS = 4 / KPS;                              // stages per super-block
+    static_assert(KPS * 32 * TILES == static_cast<int>(WBUF_COLS), "a stage fills one weight buffer");
     static constexpr int RAW_BYTES = KPS * cw_kblock_bytes(TYPE);    // compact codes of a stage
     static constexpr int TOK_KB_BYTES = 2 * N * 128;                 // hi rows, lo rows of a k-block
     static constexpr int TOK_SLOT = 4 * TOK_KB_BYTES;                // a super-block of tokens
+    static constexpr int SB_BYTES = sb_bytes_of(TYPE);
+    static constexpr int SBR = TYPE == 12 ? 6 : 8;                   // super-block ring depth
+    static constexpr int FIXED = TOK_STAGES * TOK_SLOT + SBR * SB_BYTES;
+    static constexpr int RAW_FIT = (SMEM_BUDGET - FIXED) / RAW_BYTES;
+    static constexpr int RAW_STAGES = RAW_FIT > 4 ? 4 : RAW_FIT;     // compact-code ring depth
+    static_assert(RAW_STAGES >= 2, "shared memory budget");
     static constexpr int SMEM_TOK = 0;
     static constexpr int SMEM_RAW = SMEM_TOK + TOK_STAGES * TOK_SLOT;
     static constexpr int SMEM_SB = SMEM_RAW + RAW_STAGES * RAW_BYTES;
@@ -133,23 +152,33 @@ struct Cfg {
     static constexpr int SMEM_ALLOC = SMEM_TMEMPTR + 16 + 1024;      // slack for 1024-byte alignment
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(TOK_SLOT % 1024 == 0 && TOK_KB_BYTES % 1024 == 0 && SMEM_RAW % 16 == 0 &&
-                      RAW_BYTES % 16 == 0 && SMEM_SB % 16 == 0 && SMEM_BAR % 8 == 0,
+                      RAW_BYTES % 16 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && SMEM_BAR % 8 == 0,
                   "alignment");
-    static_assert(MIN_SB_BYTES <= TOK_SLOT, "min-term operands fit a token slot");
     // cluster K split: partial sums (rows x FT_MAX_M tokens) and the promotion warps' ok
     // flags, in the idle token and compact rings
     static constexpr int OKF_OFF = BM * FT_MAX_M * 4;
     static_assert(OKF_OFF + NUM_PROMO_WARPS * 4 <= SMEM_SB, "partial sums fit the idle rings");
 };
 
+// Dynamic shared memory of a launch: the larger of the q6_K layouts (the kernel picks
+// one from the packed flag).
+template <int TYPE, int NT>
+constexpr int smem_alloc_of()
+{
+    return TYPE == 12 ? Cfg<12, NT, true>::SMEM_ALLOC
+                      : (Cfg<14, NT, true>::SMEM_ALLOC > Cfg<14, NT, false>::SMEM_ALLOC ? Cfg<14, NT, true>::SMEM_ALLOC
+                                                                                       : Cfg<14, NT, false>::SMEM_ALLOC);
+}
+
 struct FtArgs {
     const uint8_t* CW;    // compact codes        [num_n][nkb][words][128][16 B]
     const uint8_t* SC;    // sub-block scales     [num_n][nsb][128][16 B]
     const uint8_t* SBD;   // weight d             [num_n][nsb][128] f32
-    const uint8_t* AUX;   // q4_K min-term tiles  [num_n][nsb][hi 4 KiB, lo 4 KiB]
+    const uint8_t* DM;    // q4_K weight dmin     [num_n][nsb][128] f32
+    const unsigned int* FLAG;   // q6_K: word 0 = 1 if every |sc| <= 64
     const uint8_t* TQ;    // token hi/lo tiles    [nkb][hi n_tok rows | lo n_tok rows][128 B]
     const uint8_t* IP;    // token 1/p            [nsb][FT_MAX_M] f32
-    const uint8_t* AM;    // token min-term tiles [nsb][hi 4 KiB, lo 4 KiB] (token tile 0)
+    const uint8_t* FM;    // token d_a*ssum       [nsb][FT_MAX_M][8] f32
     float* Y;
     int ldy;
     int M, od, id;
@@ -265,16 +294,33 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Folded q6_K (one tile): sc * q = 4 * (sc * l / 4) + 16 sc (h - 2), from the two-tile
+// terms a = sc * l / 4 (widen_q6_lo) and b = 16 sc (h - 2) (widen_q6_hi with 16 sc / 4^p):
+// one f16x2 fma per pair, exact because the result is an integer of at most 2048.
+__device__ __forceinline__ uint4 fold_q6(uint4 a, uint4 b)
+{
+    const __half2 four = __float2half2_rn(4.0f);
+    uint4 o;
+    o.x = h2u(__hfma2(u2h(a.x), four, u2h(b.x)));
+    o.y = h2u(__hfma2(u2h(a.y), four, u2h(b.y)));
+    o.z = h2u(__hfma2(u2h(a.z), four, u2h(b.z)));
+    o.w = h2u(__hfma2(u2h(a.w), four, u2h(b.w)));
+    return o;
+}
+
 // Work unit u: weight tile n and its super-block range; stage st of the unit covers
-// k-blocks [4*sb0 + st*KPS, +KPS).
-template <int TYPE, int NT>
+// k-blocks [4*sb0 + st*KPS, +KPS).  Stages are numbered across the CTA's units (g);
+// stage g goes to issuer g % 2 and accumulator item g % ITEMS, its super-block's
+// tokens to slot (g / SPS) % 2.
+template <int TYPE, int NT, bool ONE>
 __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
                                          int warp, int lane)
 {
-    using C = Cfg<TYPE, NT>;
+    using C = Cfg<TYPE, NT, ONE>;
     constexpr bool Q4 = (TYPE == 12);
     constexpr int N = C::N;
     constexpr int KPS = C::KPS;
+    constexpr int SPS = C::SPS;
     const int nkb = g.id / TILE_K;
     const int nsb = g.id / QK_K;
     auto bar = [&](int i) -> uint32_t { return sbase + C::SMEM_BAR + 8u * static_cast<uint32_t>(i); };
@@ -283,31 +329,36 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     if (warp < CONV_WARP0) {
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ producer: compact codes, super-block entries
-            RingPos<RAW_STAGES> rp;
-            RingPos<SBR> sp;
+            RingPos<C::RAW_STAGES> rp;
+            RingPos<C::SBR> sp;
             uint32_t n_raw = 0, n_sb = 0;
             const uint32_t skip = (blockIdx.x == 0 && g.withhold >= 0) ? static_cast<uint32_t>(g.withhold) : ~0u;
+            constexpr uint32_t SB_TX = BM * 4 + BM * SC_ROW_BYTES + FT_MAX_M * 4 + (Q4 ? BM * 4 + N * 32 : 0);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
                 const uint8_t* cwb = g.CW + (static_cast<size_t>(w.n) * nkb + 4 * w.sb0) * cw_kblock_bytes(TYPE);
-                const int nst = (w.sb1 - w.sb0) * C::SPS;
+                const int nst = (w.sb1 - w.sb0) * SPS;
                 bulk_prefetch_l2(cwb, static_cast<uint32_t>(min(PF_STAGES, nst) * C::RAW_BYTES));
                 for (int st = 0; st < nst; ++st) {
-                    if (st % C::SPS == 0) {
-                        const int s = w.sb0 + st / C::SPS;
+                    if (st % SPS == 0) {
+                        const int s = w.sb0 + st / SPS;
                         if (!ctl_wait(g, bar(C::BAR_SBEMPTY + sp.i), sp.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_smem();   // after the consumers' ordinary loads
-                        const uint32_t dst = sbase + C::SMEM_SB + sp.i * SB_BYTES;
+                        const uint32_t dst = sbase + C::SMEM_SB + sp.i * C::SB_BYTES;
                         const uint32_t fb = bar(C::BAR_SBFULL + sp.i);
-                        mbar_arrive_expect_tx(fb, BM * 4 + BM * SC_ROW_BYTES + FT_MAX_M * 4);
+                        mbar_arrive_expect_tx(fb, SB_TX);
                         const size_t ts = static_cast<size_t>(w.n) * nsb + s;
                         bulk_g2s(dst + SB_SBD_OFF, g.SBD + ts * (BM * 4), BM * 4, fb);
                         bulk_g2s(dst + SB_SC_OFF, g.SC + ts * (BM * SC_ROW_BYTES), BM * SC_ROW_BYTES, fb);
                         bulk_g2s(dst + SB_IP_OFF, g.IP + static_cast<size_t>(s) * (FT_MAX_M * 4), FT_MAX_M * 4, fb);
+                        if (Q4) {
+                            bulk_g2s(dst + SB_DM_OFF, g.DM + ts * (BM * 4), BM * 4, fb);
+                            bulk_g2s(dst + SB_FM_OFF, g.FM + static_cast<size_t>(s) * (FT_MAX_M * 32), N * 32, fb);
+                        }
                         sp.next();
                         ++n_sb;
                     }
@@ -331,92 +382,58 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                     ++n_raw;
                 }
             }
-            for (uint32_t i = (n_raw > RAW_STAGES ? n_raw - RAW_STAGES : 0); i < n_raw; ++i)
+            for (uint32_t i = (n_raw > C::RAW_STAGES ? n_raw - C::RAW_STAGES : 0); i < n_raw; ++i)
                 if (i != skip)
-                    drain_wait(g, bar(C::BAR_RFULL + i % RAW_STAGES), (i / RAW_STAGES) & 1u);
-            for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
-                drain_wait(g, bar(C::BAR_SBFULL + i % SBR), (i / SBR) & 1u);
-        } else if (warp == 3 && lane == 0) {
-            // ------------------------------------------------ MMA issuer
+                    drain_wait(g, bar(C::BAR_RFULL + i % C::RAW_STAGES), (i / C::RAW_STAGES) & 1u);
+            for (uint32_t i = (n_sb > C::SBR ? n_sb - C::SBR : 0); i < n_sb; ++i)
+                drain_wait(g, bar(C::BAR_SBFULL + i % C::SBR), (i / C::SBR) & 1u);
+        } else if ((warp == 3 || warp == 1) && lane == 0) {
+            // ------------------------------------------------ MMA issuers: stage g with g % 2 == e
+            const uint32_t e = warp == 3 ? 0u : 1u;
             constexpr uint32_t idesc = idesc_f16_f32(BM, 2 * N);   // hi and lo token rows at once
-            constexpr uint32_t idesc_t = idesc_tf32_acc32(BM, N);
-            RingPos<2> ab;
-            RingPos<TOK_STAGES> tp;
-            RingPos<C::ITEMS> it;
+            uint32_t gs = 0;                                        // stage number across units
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
-                const int nst = (w.sb1 - w.sb0) * C::SPS;
-                for (int st = 0; st < nst; ++st) {
-                    const int sst = st % C::SPS;
-                    if (sst == 0 && (!ctl_wait(g, bar(C::BAR_TEMPTY + it.i), it.ph ^ 1u) ||
-                                     !ctl_wait(g, bar(C::BAR_TKFULL + tp.i), tp.ph))) {
-                        ok = false;
-                        break;
-                    }
-                    if (!ctl_wait(g, bar(C::BAR_WCONV + ab.i), ab.ph)) {
+                const int nst = (w.sb1 - w.sb0) * SPS;
+                for (int st = 0; st < nst; ++st, ++gs) {
+                    if ((gs & 1u) != e)
+                        continue;
+                    const uint32_t item = gs % C::ITEMS, iph = (gs / C::ITEMS) & 1u;
+                    const uint32_t sg = gs / SPS;                     // super-block number across units
+                    const uint32_t slot = sg % TOK_STAGES, tph = (sg / TOK_STAGES) & 1u;
+                    if (!ctl_wait(g, bar(C::BAR_TEMPTY + item), iph ^ 1u) ||
+                        !ctl_wait(g, bar(C::BAR_TKFULL + slot), tph) ||
+                        !ctl_wait(g, bar(C::BAR_WCONV + e), (gs >> 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem_base + it.i * C::ITEM_COLS;
-                    const uint32_t wa = tmem_base + WBUF_COL0 + ab.i * WBUF_COLS;
-                    const uint32_t tk = sbase + C::SMEM_TOK + tp.i * C::TOK_SLOT;
+                    const uint32_t d = tmem_base + item * C::ITEM_COLS;
+                    const uint32_t wa = tmem_base + WBUF_COL0 + e * WBUF_COLS;
+                    const uint32_t tk = sbase + C::SMEM_TOK + slot * C::TOK_SLOT;
+                    const int sst = static_cast<int>(gs % SPS);       // stage within its super-block
 #pragma unroll
                     for (int k = 0; k < KPS; ++k) {
-                        const int kbs = sst * KPS + k;          // k-block of the super-block
                         // the k-block's 2N token rows: N of hi, then N of lo
-                        const uint64_t bt = sdesc_k_sw128(tk + kbs * C::TOK_KB_BYTES);
+                        const uint64_t bt = sdesc_k_sw128(tk + (sst * KPS + k) * C::TOK_KB_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {       // 16 values per step
-                            const uint32_t acol = (Q4 ? 32u * kbs : 32u * k) + 8u * kk;
-                            umma_f16_ts(d, wa + acol, bt + 2u * kk, idesc, (kbs | kk) ? 1u : 0u);
-                            if (!Q4)
+                            const uint32_t acol = 32u * k + 8u * kk;
+                            umma_f16_ts(d, wa + acol, bt + 2u * kk, idesc, (k | kk) ? 1u : 0u);
+                            if (!ONE)
                                 umma_f16_ts(d, wa + 64u + acol, bt + 2u * kk, idesc, 1u);
                         }
                     }
-                    umma_commit(bar(C::BAR_AEMPTY + ab.i));
-                    ab.next();
-                    if (sst == C::SPS - 1) {
-                        umma_commit(bar(C::BAR_TKEMPTY + tp.i));
-                        umma_commit(bar(C::BAR_TFULL + it.i));
-                        tp.next();
-                        it.next();
-                    }
-                }
-                if (Q4 && ok) {
-                    // the unit's min term
-                    if (!ctl_wait(g, bar(C::BAR_TEMPTY + it.i), it.ph ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t d = tmem_base + it.i * C::ITEM_COLS;
-                    for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(g, bar(C::BAR_TKFULL + tp.i), tp.ph)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t wm = sbase + C::SMEM_TOK + tp.i * C::TOK_SLOT;
-                        const uint32_t xm = wm + 2 * TF32_TILE_BYTES;
-                        const uint64_t whi = sdesc_tf32_core(wm), wlo = sdesc_tf32_core(wm + TF32_TILE_BYTES);
-                        const uint64_t xhi = sdesc_tf32_core(xm), xlo = sdesc_tf32_core(xm + TF32_TILE_BYTES);
-                        umma_tf32_ss(d, whi, xhi, idesc_t, (s > w.sb0) ? 1u : 0u);
-                        umma_tf32_ss(d, whi, xlo, idesc_t, 1u);
-                        umma_tf32_ss(d, wlo, xhi, idesc_t, 1u);
-                        umma_commit(bar(C::BAR_TKEMPTY + tp.i));
-                        tp.next();
-                    }
-                    if (!ok)
-                        break;
-                    umma_commit(bar(C::BAR_TFULL + it.i));
-                    it.next();
+                    umma_commit(bar(C::BAR_AEMPTY + e));
+                    umma_commit(bar(C::BAR_TFULL + item));
+                    umma_commit(bar(C::BAR_TKEMPTY + slot));
                 }
             }
-            umma_commit(bar(C::BAR_DRAIN));           // every MMA issued so far has completed
+            umma_commit(bar(C::BAR_DRAIN));           // every MMA this thread issued has completed
             drain_wait(g, bar(C::BAR_DRAIN), 0u);
         } else if (warp == 2 && lane == 0) {
-            // ------------------------------------------------ producer: token tiles, min-term operands
+            // ------------------------------------------------ producer: token tiles
             RingPos<TOK_STAGES> tp;
             uint32_t n_t = 0;
             bool ok = true;
@@ -433,23 +450,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                              g.TQ + static_cast<size_t>(4 * s) * C::TOK_KB_BYTES, C::TOK_SLOT, fb);
                     tp.next();
                     ++n_t;
-                }
-                if (Q4 && ok) {
-                    for (int s = w.sb0; s < w.sb1; ++s) {
-                        if (!ctl_wait(g, bar(C::BAR_TKEMPTY + tp.i), tp.ph ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t dst = sbase + C::SMEM_TOK + tp.i * C::TOK_SLOT;
-                        const uint32_t fb = bar(C::BAR_TKFULL + tp.i);
-                        mbar_arrive_expect_tx(fb, MIN_SB_BYTES);
-                        bulk_g2s(dst, g.AUX + (static_cast<size_t>(w.n) * nsb + s) * (2 * TF32_TILE_BYTES),
-                                 2 * TF32_TILE_BYTES, fb);
-                        bulk_g2s(dst + 2 * TF32_TILE_BYTES, g.AM + static_cast<size_t>(s) * (2 * TF32_TILE_BYTES),
-                                 2 * TF32_TILE_BYTES, fb);
-                        tp.next();
-                        ++n_t;
-                    }
                 }
             }
             for (uint32_t i = (n_t > TOK_STAGES ? n_t - TOK_STAGES : 0); i < n_t; ++i)
@@ -471,39 +471,43 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
         const int r = q * 32 + lane;                  // weight row of the tile
         const int h = cwarp >> 2;                     // half of the stage
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        RingPos<RAW_STAGES> rp;
-        RingPos<SBR> sp;
+        RingPos<C::RAW_STAGES> rp;
+        RingPos<C::SBR> sp;
         RingPos<2> ab;              // weight buffer
         bool ok = true;
         for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
             const Unit w = unit_of(g, u, nsb);
-            const int nst = (w.sb1 - w.sb0) * C::SPS;
+            const int nst = (w.sb1 - w.sb0) * SPS;
             for (int st = 0; st < nst; ++st) {
-                const int sst = st % C::SPS;               // stage within its super-block
+                const int sst = st % SPS;                  // stage within its super-block
                 if (sst == 0 && !warp_wait(g, bar(C::BAR_SBFULL + sp.i), sp.ph)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* scr = smem + C::SMEM_SB + sp.i * SB_BYTES + SB_SC_OFF + r * SC_ROW_BYTES;
+                const uint8_t* scr = smem + C::SMEM_SB + sp.i * C::SB_BYTES + SB_SC_OFF + r * SC_ROW_BYTES;
                 if (!warp_wait(g, bar(C::BAR_RFULL + rp.i), rp.ph)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* raw = smem + C::SMEM_RAW + rp.i * C::RAW_BYTES;
-                uint4 xw[4];
-                uint4 hw = make_uint4(0u, 0u, 0u, 0u);
+                // this half's words: q4_K the 4 chunks of k-blocks 2h, 2h+1; q6_K two-tile the
+                // 2 nibble words and the high word of k-block h; q6_K one-tile those of k-blocks
+                // 2h and 2h+1
+                constexpr int NW = Q4 ? 4 : (ONE ? 6 : 3);
+                uint4 xw[NW];
                 if (Q4) {
-                    // chunks j = 0..3 of this half: k-block 2h + j/2 of the stage, word j % 2
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         xw[j] = *reinterpret_cast<const uint4*>(raw + (2 * h + (j >> 1)) * cw_kblock_bytes(TYPE) +
                                                                 ((j & 1) * BM + r) * 16);
                 } else {
-                    // k-block h of the stage: nibble words of its two chunks, then the high-bit word
-                    const uint8_t* kb = raw + h * cw_kblock_bytes(TYPE);
-                    xw[0] = *reinterpret_cast<const uint4*>(kb + r * 16);
-                    xw[1] = *reinterpret_cast<const uint4*>(kb + (BM + r) * 16);
-                    hw = *reinterpret_cast<const uint4*>(kb + (2 * BM + r) * 16);
+#pragma unroll
+                    for (int b = 0; b < NW / 3; ++b) {
+                        const uint8_t* kb = raw + ((NW / 3) * h + b) * cw_kblock_bytes(TYPE);
+#pragma unroll
+                        for (int wd = 0; wd < 3; ++wd)
+                            xw[3 * b + wd] = *reinterpret_cast<const uint4*>(kb + (wd * BM + r) * 16);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -527,28 +531,42 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                         tmem_st16(wcol + 64 * h + 16 * j, o);
                     }
                 } else {
-                    const uint32_t hs[4] = {hw.x, hw.y, hw.z, hw.w};
 #pragma unroll
-                    for (int cw = 0; cw < 2; ++cw) {               // the k-block's two chunks
-                        const int cc = 2 * (2 * sst + h) + cw;      // chunk of the super-block
-                        const uint32_t xs[4] = {xw[cw].x, xw[cw].y, xw[cw].z, xw[cw].w};
-                        uint4 oa[4], ob[4];
+                    for (int b = 0; b < NW / 3; ++b) {
+                        const int kbs = ONE ? 2 * h + b : 2 * sst + h;     // k-block of the super-block
+                        const int kcol = ONE ? 32 * (2 * h + b) : 32 * h;  // its columns in the buffer
+                        const uint32_t hs[4] = {xw[3 * b + 2].x, xw[3 * b + 2].y, xw[3 * b + 2].z, xw[3 * b + 2].w};
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {     // 16-value sub-blocks
-                            const float sc = static_cast<float>(static_cast<int8_t>(scr[2 * cc + half]));
-                            const __half2 c1 = __float2half2_rn(sc * 0.25f), a1 = __float2half2_rn(-256.0f * sc);
-                            const __half2 c16 = __float2half2_rn(sc * 0.015625f), a16 = __float2half2_rn(-16.0f * sc);
-                            const __half2 m[4] = {__float2half2_rn(4.0f * sc), __float2half2_rn(sc),
-                                                  __float2half2_rn(0.25f * sc), __float2half2_rn(0.0625f * sc)};
+                        for (int cw = 0; cw < 2; ++cw) {               // the k-block's two chunks
+                            const int cc = 2 * kbs + cw;               // chunk of the super-block
+                            const uint32_t xs[4] = {xw[3 * b + cw].x, xw[3 * b + cw].y, xw[3 * b + cw].z,
+                                                    xw[3 * b + cw].w};
+                            uint4 oa[4], ob[4];
 #pragma unroll
-                            for (int v = 0; v < 2; ++v) {
-                                const int uu = 2 * half + v;
-                                oa[uu] = widen_q6_lo(xs[uu], c1, a1, c16, a16);
-                                ob[uu] = widen_q6_hi(hs[2 * cw + half] >> (8 * v), m);
+                            for (int half = 0; half < 2; ++half) {     // 16-value sub-blocks
+                                const float sc = static_cast<float>(static_cast<int8_t>(scr[2 * cc + half]));
+                                const __half2 c1 = __float2half2_rn(sc * 0.25f), a1 = __float2half2_rn(-256.0f * sc);
+                                const __half2 c16 = __float2half2_rn(sc * 0.015625f),
+                                              a16 = __float2half2_rn(-16.0f * sc);
+                                const float hsc = ONE ? 4.0f * sc : sc;   // one tile: 16 sc (h - 2)
+                                const __half2 m[4] = {__float2half2_rn(4.0f * hsc), __float2half2_rn(hsc),
+                                                      __float2half2_rn(0.25f * hsc), __float2half2_rn(0.0625f * hsc)};
+#pragma unroll
+                                for (int v = 0; v < 2; ++v) {
+                                    const int uu = 2 * half + v;
+                                    oa[uu] = widen_q6_lo(xs[uu], c1, a1, c16, a16);
+                                    ob[uu] = widen_q6_hi(hs[2 * cw + half] >> (8 * v), m);
+                                }
+                            }
+                            if (ONE) {
+                                const uint4 o[4] = {fold_q6(oa[0], ob[0]), fold_q6(oa[1], ob[1]),
+                                                    fold_q6(oa[2], ob[2]), fold_q6(oa[3], ob[3])};
+                                tmem_st16(wcol + kcol + 16 * cw, o);
+                            } else {
+                                tmem_st16(wcol + kcol + 16 * cw, oa);
+                                tmem_st16(wcol + 64 + kcol + 16 * cw, ob);
                             }
                         }
-                        tmem_st16(wcol + 32 * h + 16 * cw, oa);
-                        tmem_st16(wcol + 64 + 32 * h + 16 * cw, ob);
                     }
                 }
                 tmem_wait_st();
@@ -557,7 +575,7 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                 if (lane == 0)
                     mbar_arrive(bar(C::BAR_WCONV + ab.i));
                 ab.next();
-                if (sst == C::SPS - 1) {
+                if (sst == SPS - 1) {
                     if (lane == 0)
                         mbar_arrive(bar(C::BAR_SBEMPTY + sp.i));
                     sp.next();
@@ -576,9 +594,9 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     const int q = warp & 3;                              // TMEM lane quarter
     const int row = q * 32 + lane;                       // weight row of the tile
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    constexpr float IPS = Q4 ? 1.0f : 4.0f;              // q6_K tiles hold sc * q / 4
+    constexpr float IPS = ONE ? 1.0f : 4.0f;             // two q6_K tiles hold sc * q / 4
     RingPos<C::ITEMS> it;
-    RingPos<SBR> sp;
+    RingPos<C::SBR> sp;
     bool ok = true, had_unit = false;
     int n_tile = 0;
     float acc[N];
@@ -597,24 +615,43 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                 ok = false;
                 break;
             }
-            const uint8_t* sbe = smem + C::SMEM_SB + sp.i * SB_BYTES;
+            const uint8_t* sbe = smem + C::SMEM_SB + sp.i * C::SB_BYTES;
             const float dsb = reinterpret_cast<const float*>(sbe + SB_SBD_OFF)[row];
             const float4* ip4 = reinterpret_cast<const float4*>(sbe + SB_IP_OFF);
-            if (!warp_wait(g, bar(C::BAR_TFULL + it.i), it.ph)) {
+            // the super-block's SPS stage items: it, it + 1 (mod ITEMS)
+            uint32_t ii[SPS];
+            bool got = true;
+#pragma unroll
+            for (int k = 0; k < SPS; ++k) {
+                ii[k] = it.i;
+                got = got && warp_wait(g, bar(C::BAR_TFULL + it.i), it.ph);
+                it.next();
+            }
+            if (!got) {
                 ok = false;
                 break;
             }
             tc_fence_after();
 #pragma unroll
             for (int gq = 0; gq < NT; ++gq) {
-                float Dh[16], Dl[16];      // W*hi and W*lo of tokens 16gq .. 16gq+15
-                tmem_ld16_wait(lane_addr + it.i * C::ITEM_COLS + 16 * gq, Dh);
-                tmem_ld16_wait(lane_addr + it.i * C::ITEM_COLS + N + 16 * gq, Dl);
+                float Dt[16];              // sum over the stages of W*hi + W*lo, tokens 16gq ..
+#pragma unroll
+                for (int k = 0; k < SPS; ++k) {
+                    float Dh[16], Dl[16];
+                    tmem_ld16_wait(lane_addr + ii[k] * C::ITEM_COLS + 16 * gq, Dh);
+                    tmem_ld16_wait(lane_addr + ii[k] * C::ITEM_COLS + N + 16 * gq, Dl);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        Dt[e] = k == 0 ? __fadd_rn(Dh[e], Dl[e]) : __fadd_rn(Dt[e], __fadd_rn(Dh[e], Dl[e]));
+                }
                 if (gq == NT - 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar(C::BAR_TEMPTY + it.i));
+                    if (lane == 0) {
+#pragma unroll
+                        for (int k = 0; k < SPS; ++k)
+                            mbar_arrive(bar(C::BAR_TEMPTY + ii[k]));
+                    }
                 }
 #pragma unroll
                 for (int i4 = 0; i4 < 4; ++i4) {
@@ -623,12 +660,34 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int t = 16 * gq + 4 * i4 + e;
-                        const float Dt = __fadd_rn(Dh[4 * i4 + e], Dl[4 * i4 + e]);
-                        acc[t] = fmaf(dsb, __fmul_rn(Dt, ipa[e] * IPS), acc[t]);
+                        acc[t] = fmaf(dsb, __fmul_rn(Dt[4 * i4 + e], ipa[e] * IPS), acc[t]);
                     }
                 }
             }
-            it.next();
+            if (Q4) {
+                // min term: acc -= sum_c (dmin * m_c) * (d_a * ssum)_c
+                const float dmin = reinterpret_cast<const float*>(sbe + SB_DM_OFF)[row];
+                const uint2 mw = *reinterpret_cast<const uint2*>(sbe + SB_SC_OFF + row * SC_ROW_BYTES + 8);
+                float dmn[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    dmn[c] = -__fmul_rn(dmin, static_cast<float>(((c < 4 ? mw.x : mw.y) >> (8 * (c & 3))) & 0xFFu));
+                const float4* fm = reinterpret_cast<const float4*>(sbe + SB_FM_OFF);
+#pragma unroll
+                for (int t = 0; t < N; ++t) {
+                    const float4 a = fm[2 * t], b = fm[2 * t + 1];
+                    float v = acc[t];
+                    v = fmaf(dmn[0], a.x, v);
+                    v = fmaf(dmn[1], a.y, v);
+                    v = fmaf(dmn[2], a.z, v);
+                    v = fmaf(dmn[3], a.w, v);
+                    v = fmaf(dmn[4], b.x, v);
+                    v = fmaf(dmn[5], b.y, v);
+                    v = fmaf(dmn[6], b.z, v);
+                    v = fmaf(dmn[7], b.w, v);
+                    acc[t] = v;
+                }
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(C::BAR_SBEMPTY + sp.i));
@@ -636,28 +695,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
         }
         if (!ok)
             break;
-        if (Q4) {
-            if (!warp_wait(g, bar(C::BAR_TFULL + it.i), it.ph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int gq = 0; gq < NT; ++gq) {
-                float D[16];
-                tmem_ld16_wait(lane_addr + it.i * C::ITEM_COLS + 16 * gq, D);
-                if (gq == NT - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar(C::BAR_TEMPTY + it.i));
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    acc[16 * gq + e] = fmaf(-1.0f, D[e], acc[16 * gq + e]);
-            }
-            it.next();
-        }
         if (!clustered) {
             const int j = w.n * BM + row;
             if (j < g.od) {
@@ -670,7 +707,7 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     }
     if (clustered) {
         // The K slices' partial sums meet in rank 0 and are added in rank order.  The CTA
-        // barrier lets the producers and the MMA issuer finish draining their copies and
+        // barrier lets the producers and the MMA issuers finish draining their copies and
         // MMAs first, so the rings are idle when the partial sums overwrite them.  Each
         // rank leaves one ok flag per promotion warp; rank 0 stores Y only if all are set.
         const uint32_t rank = cluster_ctarank();
@@ -711,33 +748,26 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     }
 }
 
-template <int TYPE, int NT>
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
+// Barrier set-up, TMEM, the roles, TMEM release, for one layout.
+template <int TYPE, int NT, bool ONE>
+__device__ __forceinline__ void ft_body(const FtArgs& g, uint8_t* smem, uint32_t sbase, int warp, int lane)
 {
-    using C = Cfg<TYPE, NT>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
-    uint8_t* smem = smem_raw + pad;
-    const uint32_t sbase = raw_addr + pad;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    using C = Cfg<TYPE, NT, ONE>;
     auto bar = [&](int i) -> uint32_t { return sbase + C::SMEM_BAR + 8u * static_cast<uint32_t>(i); };
-
     if (threadIdx.x == 0) {
-        for (int s = 0; s < RAW_STAGES; ++s) {
+        for (int s = 0; s < C::RAW_STAGES; ++s) {
             mbar_init(bar(C::BAR_RFULL + s), 1);
             mbar_init(bar(C::BAR_REMPTY + s), NUM_CONV_WARPS);
         }
         for (int s = 0; s < TOK_STAGES; ++s) {
             mbar_init(bar(C::BAR_TKFULL + s), 1);
-            mbar_init(bar(C::BAR_TKEMPTY + s), 1);
+            mbar_init(bar(C::BAR_TKEMPTY + s), C::SPS);          // one commit per stage of the super-block
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::BAR_AEMPTY + s), 1);
             mbar_init(bar(C::BAR_WCONV + s), NUM_CONV_WARPS);
         }
-        for (int s = 0; s < SBR; ++s) {
+        for (int s = 0; s < C::SBR; ++s) {
             mbar_init(bar(C::BAR_SBFULL + s), 1);
             mbar_init(bar(C::BAR_SBEMPTY + s), NUM_CONV_WARPS + NUM_PROMO_WARPS);
         }
@@ -745,7 +775,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
             mbar_init(bar(C::BAR_TFULL + k), 1);
             mbar_init(bar(C::BAR_TEMPTY + k), NUM_PROMO_WARPS);
         }
-        mbar_init(bar(C::BAR_DRAIN), 1);
+        mbar_init(bar(C::BAR_DRAIN), NUM_ISSUERS);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -761,13 +791,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
     // the kernel ahead on the stream (the prepass) writes the token planes; the weight
     // planes are registration-time data
     grid_dep_wait();
-    ft_roles<TYPE, NT>(g, smem, sbase, tmem_base, warp, lane);
+    ft_roles<TYPE, NT, ONE>(g, smem, sbase, tmem_base, warp, lane);
 
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int TYPE, int NT>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if constexpr (TYPE == 12) {
+        ft_body<12, NT, true>(g, smem, sbase, warp, lane);
+    } else {
+        // the packed flag (registration-time data, uniform for the launch) says whether
+        // every sub-block scale fits the one-tile form
+        if (__ldg(g.FLAG) != 0u)
+            ft_body<14, NT, true>(g, smem, sbase, warp, lane);
+        else
+            ft_body<14, NT, false>(g, smem, sbase, warp, lane);
     }
 }
 
@@ -783,7 +835,7 @@ cudaError_t set_smem_attr()
     if (attr_set_mask.load() & bit)
         return cudaSuccess;
     e = cudaFuncSetAttribute(gemm_ft_kernel<TYPE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<TYPE, NT>::SMEM_ALLOC);
+                             smem_alloc_of<TYPE, NT>());
     if (e != cudaSuccess)
         return e;
     attr_set_mask.fetch_or(bit);
@@ -812,7 +864,7 @@ int max_clusters(int size)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(size));
         cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = Cfg<TYPE, NT>::SMEM_ALLOC;
+        cfg.dynamicSmemBytes = smem_alloc_of<TYPE, NT>();
         cfg.attrs = at;
         cfg.numAttrs = 1;
         if (cudaOccupancyMaxActiveClusters(&n, gemm_ft_kernel<TYPE, NT>, &cfg) != cudaSuccess) {
@@ -863,7 +915,7 @@ cudaError_t launch_ft_typed(FtArgs a, int nsm, bool allow_cluster, cudaStream_t 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = Cfg<TYPE, NT>::SMEM_ALLOC;
+    cfg.dynamicSmemBytes = smem_alloc_of<TYPE, NT>();
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = na;
@@ -906,10 +958,11 @@ cudaError_t launch_gemm_ft(int type, const void* packed, int od, int id, const v
     a.CW = pk + wp.cw_off;
     a.SC = pk + wp.sc_off;
     a.SBD = pk + wp.sbd_off;
-    a.AUX = pk + wp.aux_off;
+    a.DM = pk + wp.dm_off;
+    a.FLAG = reinterpret_cast<const unsigned int*>(pk + wp.flag_off);
     a.TQ = static_cast<const uint8_t*>(qa) + ap.tq_off;
     a.IP = sc + ap.ip_off;
-    a.AM = sc + ap.am_off;
+    a.FM = sc + ap.fm_off;
     a.Y = Y;
     a.ldy = ldy;
     a.M = M;
@@ -926,21 +979,21 @@ cudaError_t launch_gemm_ft(int type, const void* packed, int od, int id, const v
     if (e == cudaSuccess && path_label) {
         static const char* const lab[2][9] = {
             {"q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened to sc*q f16 tiles in tensor memory, "
-             "weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, one TMEM accumulator per "
-             "super-block, tf32 hi/lo min term; K split: none",
-             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=2 CTAs",
-             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=3 CTAs",
-             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=4 CTAs",
-             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=6 CTAs",
-             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory; K split: cluster of S=8 CTAs"},
-            {"q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened to two exact f16 tiles (sc*l/4, "
-             "4*sc*(h-2)) in tensor memory, weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, one "
-             "TMEM accumulator per super-block; K split: none",
-             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=2 CTAs",
-             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=3 CTAs",
-             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=4 CTAs",
-             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=6 CTAs",
-             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory; K split: cluster of S=8 CTAs"}};
+             "weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, two MMA issuers with one TMEM "
+             "accumulator per stage, min term on the CUDA cores; K split: none",
+             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=2 CTAs",
+             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=3 CTAs",
+             "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=4 CTAs",
+             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=6 CTAs",
+             "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=8 CTAs"},
+            {"q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened in tensor memory to one sc*q f16 tile "
+             "(every |sc| <= 64) or two exact tiles (sc*l/4, 4*sc*(h-2)), weights as the MMA's A, token operand "
+             "p*d_a*q_a as f16 hi+lo as N, two MMA issuers with one TMEM accumulator per stage; K split: none",
+             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=2 CTAs",
+             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=3 CTAs",
+             "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=4 CTAs",
+             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=6 CTAs",
+             "", "q6_K: few-token GEMM (M <= 64): compact 6-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=8 CTAs"}};
         *path_label = lab[type == 14 ? 1 : 0][g_last_kslices > 1 ? g_last_kslices : 0];
     }
     return e;

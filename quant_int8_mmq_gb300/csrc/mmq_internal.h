@@ -52,8 +52,9 @@ __host__ __device__ constexpr int small_pos(int k)   // byte position of value k
 // prepass writes as well: per 64-value k-block, the FT_N = 16*ceil(M/16) token rows of
 // hi = rn_f16(s_hi*q) then of lo = rn_f16(s_hi*q - hi + s_lo*q) (s = p*d, split into
 // two f16 values s_hi + s_lo; p a power of two per token and super-block), in the
-// 128-byte-swizzled operand layout (row t at t*128); and 1/p per (super-block, token),
-// FT_MAX_M entries per super-block.
+// 128-byte-swizzled operand layout (row t at t*128); 1/p per (super-block, token),
+// FT_MAX_M entries per super-block; and the q4_K min-term operand ma = d*ssum per
+// (super-block, token, chunk of the super-block), 8 f32 per token.
 constexpr int FT_MAX_M = 64;   // MMQ_FT_MAX_M
 __host__ __device__ constexpr int ft_n(int M) { return ((M + 15) / 16) * 16; }
 
@@ -65,7 +66,8 @@ struct ActPlanes {       // layout of mmq_quantize_act's outputs
     size_t pair_off, pair_bytes;   // {f32 d, i32 ssum} per (token, chunk)
     size_t am_off, am_bytes;       // tf32 hi/lo tiles of d*ssum per (token tile, super-block)
     size_t ip_off, ip_bytes;       // M <= FT_MAX_M: f32 1/p [K/256][FT_MAX_M], else 0
-    size_t scale_bytes;            // pairs + am + 1/p
+    size_t fm_off, fm_bytes;       // M <= FT_MAX_M: f32 d*ssum [K/256][FT_MAX_M][8], else 0
+    size_t scale_bytes;            // pairs + am + 1/p + d*ssum
 };
 inline ActPlanes act_planes(int M, int K)
 {
@@ -83,7 +85,9 @@ inline ActPlanes act_planes(int M, int K)
     a.am_bytes = Mp / TILE_ROWS * static_cast<size_t>(K / QK_K) * 2 * TF32_TILE_BYTES;
     a.ip_off = a.am_off + a.am_bytes;
     a.ip_bytes = (M <= FT_MAX_M) ? static_cast<size_t>(K / QK_K) * FT_MAX_M * 4 : 0;
-    a.scale_bytes = a.ip_off + a.ip_bytes;
+    a.fm_off = a.ip_off + a.ip_bytes;
+    a.fm_bytes = (M <= FT_MAX_M) ? static_cast<size_t>(K / QK_K) * FT_MAX_M * 8 * 4 : 0;
+    a.scale_bytes = a.fm_off + a.fm_bytes;
     return a;
 }
 
@@ -116,6 +120,7 @@ struct WeightPlanes {    // layout of mmq_pack_weights' output
     size_t raw_off, raw_bytes;     // re-laid raw blocks [od][id/256]
     size_t cw_off, cw_bytes;       // compact codes [row tile][k-block][word][128][16 B]
     size_t sc_off, sc_bytes;       // sub-block scales [row tile][super-block][128][16 B]
+    size_t dm_off, dm_bytes;       // q4_K: f32 dmin per (row, super-block) [row tile][super-block][128]; q6_K: 0
     size_t total;
 };
 inline WeightPlanes weight_planes(int type, int od, int id)
@@ -139,7 +144,9 @@ inline WeightPlanes weight_planes(int type, int od, int id)
     w.cw_bytes = (Np / TILE_ROWS) * static_cast<size_t>(id / TILE_K) * cw_kblock_bytes(type);
     w.sc_off = w.cw_off + w.cw_bytes;
     w.sc_bytes = Np * nsb * SC_ROW_BYTES;
-    w.total = w.sc_off + w.sc_bytes;
+    w.dm_off = w.sc_off + w.sc_bytes;
+    w.dm_bytes = type == 12 ? Np * nsb * 4 : 0;
+    w.total = w.dm_off + w.dm_bytes;
     return w;
 }
 

@@ -23,6 +23,8 @@
 //         q6_K: the 16 int8 sub-block scales as f32 per (row, super-block), used
 //               when the codes are not folded.
 //  flag   q6_K: word 0 = 1 if the codes are folded, word 1 = max |sc|.
+//  dm     q4_K: f32 dmin per (row, super-block), the factor of the few-token GEMM's
+//         min term (which multiplies it by m_c on the fly).
 //  raw    the raw blocks re-laid for 16-byte loads by the weight-streaming path
 //         (few tokens): codes first, then the scale bytes; q4_K keeps 144 bytes,
 //         q6_K is padded with zeros to 224.
@@ -109,7 +111,7 @@ template <int TYPE>
 __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, int id, int Np,
                                                    uint8_t* __restrict__ codes, float2* __restrict__ pairs,
                                                    float* __restrict__ sbd, uint8_t* __restrict__ aux,
-                                                   unsigned int* __restrict__ flag)
+                                                   float* __restrict__ dm, unsigned int* __restrict__ flag)
 {
     const int nchunk = id / CHUNK;
     const int nkb = id / TILE_K;
@@ -171,8 +173,10 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
                 const float dmin = load_f16_bytes(b + 2);
                 const float dmn = __fmul_rn(dmin, static_cast<float>(m));
                 w = make_float2(__fmul_rn(d, static_cast<float>(sc)), dmn);
-                if (cc == 0)
+                if (cc == 0) {
                     sbd[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = d;
+                    dm[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = dmin;
+                }
                 const float hi = tf32_rna(dmn);
                 const float lo = __fsub_rn(dmn, hi);  // <= 6 significant bits: exact in tf32
                 uint8_t* t0 = aux + (static_cast<size_t>(nt) * nsb + sb) * (2 * TF32_TILE_BYTES);
@@ -193,6 +197,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
                         scp[s * TILE_ROWS + r] = 0.0f;
                 }
             } else {
+                if (cc == 0)
+                    dm[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = 0.0f;
                 uint8_t* t0 = aux + (static_cast<size_t>(nt) * nsb + sb) * (2 * TF32_TILE_BYTES);
                 *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, cc)) = 0.0f;
                 *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, cc)) = 0.0f;
@@ -354,11 +360,13 @@ cudaError_t launch_pack(int type, const void* raw_a, int od_a, const void* raw_b
         q6k_scale_scan<<<static_cast<unsigned>(sblocks), 256, 0, s>>>(rb, nblocks, flag);
         count_launch();
         pack_kernel<14><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
-                                                                        sbd, base + wp.aux_off, flag);
+                                                                        sbd, base + wp.aux_off, nullptr, flag);
     } else {
         count_launch();
         pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
-                                                                        sbd, base + wp.aux_off, flag);
+                                                                        sbd, base + wp.aux_off,
+                                                                        reinterpret_cast<float*>(base + wp.dm_off),
+                                                                        flag);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess)

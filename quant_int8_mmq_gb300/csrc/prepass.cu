@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                                                            int Mp, int vec4, uint16_t* __restrict__ qa,
                                                            uint2* __restrict__ scales, uint8_t* __restrict__ am,
                                                            int8_t* __restrict__ qa8, uint8_t* __restrict__ tq,
-                                                           float* __restrict__ ip, int ftn)
+                                                           float* __restrict__ ip, float* __restrict__ fm, int ftn)
 {
     // x may come from the kernel ahead, and qa / scales may still be read by it.
     grid_dep_wait();
@@ -236,6 +236,8 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                 uint8_t* t0 = am + (static_cast<size_t>(mt) * nsb + sb) * (2 * TF32_TILE_BYTES);
                 *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = hi;
                 *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = lo;
+                if (fm != nullptr && t < ftn)
+                    fm[(static_cast<size_t>(sb) * FT_MAX_M + t) * 8 + (c & 7)] = ma;
             }
         }
     }
@@ -266,7 +268,8 @@ cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa,
         static_cast<uint16_t*>(qa), reinterpret_cast<uint2*>(sc + ap.pair_off), sc + ap.am_off,
         ap.i8_bytes ? reinterpret_cast<int8_t*>(static_cast<uint8_t*>(qa) + ap.i8_off) : nullptr,
         ap.tq_bytes ? static_cast<uint8_t*>(qa) + ap.tq_off : nullptr,
-        ap.ip_bytes ? reinterpret_cast<float*>(sc + ap.ip_off) : nullptr, ap.tq_bytes ? ft_n(M) : 0);
+        ap.ip_bytes ? reinterpret_cast<float*>(sc + ap.ip_off) : nullptr,
+        ap.fm_bytes ? reinterpret_cast<float*>(sc + ap.fm_off) : nullptr, ap.tq_bytes ? ft_n(M) : 0);
 }
 
 }  // namespace mmq

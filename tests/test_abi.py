@@ -47,14 +47,15 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
     # token counts up to 8 add the int8 code plane after the tiles, up to 64 the few-token
     # operand (8 k-blocks x hi, lo x 16 * ceil(M/16) rows of 128 B) and 1/p (2 x 64 floats)
     assert mmq.mmq_act_plane_bytes(5, 512) == (128 * 512 * 2 + 5 * 512 + 8 * 2 * 16 * 128,
-                                               128 * 16 * 8 + 2 * 8192 + 2 * 64 * 4)
+                                               128 * 16 * 8 + 2 * 8192 + 2 * 64 * 4 + 2 * 64 * 8 * 4)
     assert mmq.mmq_act_plane_bytes(8, 512)[0] == 128 * 512 * 2 + 8 * 512 + 8 * 2 * 16 * 128
     assert mmq.mmq_act_plane_bytes(9, 512)[0] == 128 * 512 * 2 + 8 * 2 * 16 * 128
     assert mmq.mmq_act_plane_bytes(64, 512)[0] == 128 * 512 * 2 + 8 * 2 * 64 * 128
     assert mmq.mmq_act_plane_bytes(65, 512)[0] == 128 * 512 * 2
     assert mmq.mmq_act_ft_layout(33, 512) == {"tq": (128 * 512 * 2, 8 * 2 * 48 * 128),
-                                              "ip": (128 * 16 * 8 + 2 * 8192, 2 * 64 * 4)}
-    assert mmq.mmq_act_ft_layout(65, 512) == {"tq": (0, 0), "ip": (0, 0)}
+                                              "ip": (128 * 16 * 8 + 2 * 8192, 2 * 64 * 4),
+                                              "fm": (128 * 16 * 8 + 2 * 8192 + 2 * 64 * 4, 2 * 64 * 8 * 4)}
+    assert mmq.mmq_act_ft_layout(65, 512) == {"tq": (0, 0), "ip": (0, 0), "fm": (0, 0)}
     for t in (mmq.MMQ_Q4_K, mmq.MMQ_Q6_K):
         L = mmq.mmq_packed_weight_layout(t, 4097, 1024)
         Np, nsb = 4224, 4
@@ -67,8 +68,9 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
         words = 2 if t == mmq.MMQ_Q4_K else 3
         assert L["cw"] == (-(-sum(L["raw"]) // 256) * 256, (Np // 128) * 16 * words * 128 * 16)
         assert L["sc"] == (sum(L["cw"]), Np * nsb * 16)
+        assert L["dm"] == (sum(L["sc"]), Np * nsb * 4 if t == mmq.MMQ_Q4_K else 0)
         assert all(off % 16 == 0 for off, _ in L.values())
-        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["sc"])
+        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["dm"])
 
 
 @pytest.mark.parametrize("M,K,err", [(0, 256, 2), (1, 255, 2), (1, 0, 2), (5, 300, 2), (1 << 23, 256, 2)])

@@ -119,8 +119,15 @@ def _check_prepass(x, ldx=None):
         n = -(-M // 16) * 16
         to, tb = ft["tq"]
         io, ib = ft["ip"]
+        fo, fb = ft["fm"]
         assert to == Mp * K * 2 + (M * K if M <= mmq.SMALL_M else 0) and tb == (K // 64) * 2 * n * 128
         assert io == lay["am"][0] + lay["am"][1] and ib == (K // 256) * 64 * 4
+        assert fo == io + ib and fb == (K // 256) * 64 * 8 * 4
+        # the q4_K min-term operand d * ssum (one f32 multiply) per (super-block, token, chunk)
+        fm = scb[fo:fo + fb].view(np.float32).reshape(K // 256, 64, 8)[:, :n]
+        wfm = np.zeros((n, K // 32), np.float32)
+        wfm[:M] = (d * s.astype(np.float32)).astype(np.float32)
+        assert np.array_equal(fm.view(np.uint32), wfm.reshape(n, K // 256, 8).transpose(1, 0, 2).view(np.uint32))
         hi, lo = untile_token_operand(qab[to:to + tb], n, K)
         whi, wlo, wip = ft_operand(q, d, n)
         assert np.array_equal(hi.view(np.uint16), whi.view(np.uint16))
@@ -128,7 +135,7 @@ def _check_prepass(x, ldx=None):
         ip = scb[io:io + ib].view(np.float32).reshape(K // 256, 64)[:, :n]
         assert np.array_equal(ip.view(np.uint32), wip.view(np.uint32))
     else:
-        assert ft["tq"][1] == 0 and ft["ip"][1] == 0
+        assert ft["tq"][1] == 0 and ft["ip"][1] == 0 and ft["fm"][1] == 0
 
 
 def ft_operand(q, d, n):
@@ -222,7 +229,7 @@ def test_pack_planes_byte_exact(typ, od, id_):
     pk = packed.cpu().numpy()
     tid = mmq.TYPES[t]
     L = mmq.mmq_packed_weight_layout(tid, od, id_)
-    assert pk.size == sum(L["sc"])
+    assert pk.size == sum(L["dm"])
     Np, nsb, nchunk = padded(od), id_ // 256, id_ // 32
     part = {k: pk[o:o + n] for k, (o, n) in L.items()}
     codes = untile_codes(part["codes"], Np, id_)
@@ -254,6 +261,8 @@ def test_pack_planes_byte_exact(typ, od, id_):
         # hi + lo reproduces dmn = dmin * m_c exactly (f64 sum of two tf32 values)
         assert np.array_equal(hi[:od].astype(np.float64) + lo[:od].astype(np.float64), wb.astype(np.float64))
         assert not hi[od:].any() and not lo[od:].any()
+        dm = untile_rows(part["dm"], Np, nsb)
+        assert np.array_equal(dm[:od].view(np.uint32), dmin.view(np.uint32)) and not dm[od:].view(np.uint32).any()
     assert np.array_equal(codes[:od], want_codes)
     assert np.array_equal(a[:od].view(np.uint32), wa.view(np.uint32))
     assert np.array_equal(b[:od].view(np.uint32), wb.view(np.uint32))
