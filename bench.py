@@ -776,6 +776,10 @@ def run_ours(args, world, rank, local):
     if counters:
         roof["ncu"] = {k: v for k, v in counters.items() if k != "dram_bytes"}
 
+    classes = {k: {"launches": cls_n[k], "us_per_launch": cls_time[k] / cls_n[k] * 1e6,
+                   "tflops_int8_equiv": cls_flops[k] / cls_time[k] / 1e12,
+                   "frac_of_bf16_sustained": cls_flops[k] / cls_time[k] / 1e12 / peak,
+                   "share_of_step": cls_time[k] / t} for k in sorted(cls_time, key=cls_time.get, reverse=True)}
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 operands: exact int weight codes x activations p*d_a*q_a as f16 hi+lo -> f32",
@@ -786,6 +790,7 @@ def run_ours(args, world, rank, local):
             "gemm_share_of_step": gemm_time / t,
             "gemm_only_tok_s": world * M * args.steps / gemm_time,
             "roofline": roof,
+            "gemm_classes": classes,
             "gpu_launches": launches,
             "path": mmq.mmq_last_path()}
     if probe.get("int8_mma_sync_tops"):

@@ -234,23 +234,28 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *    (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=
  *    d_a*(d*sc0*I_0 + d*sc1*I_1)), with a fixed reduction order;
  *  - MMQ_SMALL_M < M <= MMQ_FT_MAX_M, the few-token kernel: the CW codes are
- *    widened to exact f16 integers (q4_K sc*q; q6_K the two exact tiles
- *    sc*l/4 and 4*sc*(h-2), l and h the low 4 and high 2 bits of q + 32) in
- *    tensor memory and contracted on tcgen05 against the tq operand (f16 hi and
- *    lo of p*d_a*q_a as one 2N-row operand), one f32 accumulator per
- *    super-block, then d and 1/p applied per super-block; when the weight tiles
- *    are few, each is split along K over a cluster of up to 8 CTAs whose partial
- *    sums are added in rank order (deterministic);
+ *    widened to exact f16 integers (q4_K sc*q; q6_K sc*q when FLAG says every
+ *    |scales[i]| <= 64, else the two exact tiles sc*l/4 and 4*sc*(h-2), l and h
+ *    the low 4 and high 2 bits of q + 32) in tensor memory and contracted on
+ *    tcgen05 against the tq operand (f16 hi and lo of p*d_a*q_a as one 2N-row
+ *    operand), one f32 accumulator per stage, then d and 1/p applied per
+ *    super-block; the q4_K min term sum_c (dmin*m_c)*(d_a*ssum) in f32 FMAs from
+ *    DM, SC and fm; when the weight tiles are few, each is split along K over a
+ *    cluster of up to 8 CTAs whose partial sums are added in rank order
+ *    (deterministic);
  *  - larger M, the super-block kernel (scale-folded codes, when its 128 x 256
  *    tiles number at least the SM count): the activation operand p*d_a*q_a as
  *    an f16 hi + lo pair (about 2^-21 relative per value) times the exact f16
  *    CODES, summed over a whole super-block in f32, then d and 1/p per
- *    super-block;
+ *    super-block.  When the last round of tiles fills at most half the SMs (or
+ *    all tiles do), those tiles run as two K-halves added into Y after a zeroing
+ *    kernel, 0 + a + b, the same in either order;
  *  - otherwise the chunk kernel: the integer dots run exactly (codes held as f16
  *    integers, every partial sum an integer below 2^24 in the f32 accumulator)
  *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
- * The tile kernels compute the q4_K min term sum_c (d_a*ssum)*(dmin*m_c) as a
- * tf32 hi/lo tensor-core contraction (relative error about 2^-21 per product).
+ * The super-block and chunk kernels compute the q4_K min term sum_c
+ * (d_a*ssum)*(dmin*m_c) as a tf32 hi/lo tensor-core contraction (relative error
+ * about 2^-21 per product).
  * Y is deterministic for given inputs and kernel.  Rows t >= M and columns
  * j >= od are never written.  ldy >= od.
  * -------------------------------------------------------------------------- */
@@ -306,8 +311,8 @@ const char* mmq_last_path(void);
 
 /* Number of kernel launches the library has made in this process (every entry
  * point that launches adds the kernels it launched: prepass 1, repack 4 or 5,
- * GEMM 1, or 2 when the last round's tiles are split and first zeroed, or when a
- * q6_K super-block launch is followed by the chunk kernel's flag check). */
+ * GEMM 1, or 2 when K-half tiles are first zeroed, or when a q6_K
+ * super-block launch is followed by the chunk kernel's flag check). */
 unsigned long long mmq_launch_count(void);
 
 /* Library version string. */

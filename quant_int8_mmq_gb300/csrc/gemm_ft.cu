@@ -93,6 +93,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t WBUF_COL0 = 256;     // accumulator items in columns [0, 256), then the two weight buffers
 constexpr uint32_t WBUF_COLS = 128;
 constexpr int MAX_CLUSTER = 8;
+static_assert(MAX_CLUSTER * NUM_PROMO_WARPS <= 32, "one lane per rank flag");
 constexpr int SMEM_BUDGET = 227 * 1024 - 2048;   // rings; the rest: barriers, TMEM address, alignment slack
 static_assert(WBUF_COL0 + 2 * WBUF_COLS <= TMEM_COLS, "TMEM budget");
 // Accumulator items: one MMA covers the hi and the lo token rows (N = 2 x 16*NT columns:
@@ -347,7 +348,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                             ok = false;
                             break;
                         }
-                        fence_proxy_async_smem();   // after the consumers' ordinary loads
                         const uint32_t dst = sbase + C::SMEM_SB + sp.i * C::SB_BYTES;
                         const uint32_t fb = bar(C::BAR_SBFULL + sp.i);
                         mbar_arrive_expect_tx(fb, SB_TX);
@@ -373,7 +373,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                         ++n_raw;
                         continue;
                     }
-                    fence_proxy_async_smem();
                     const uint32_t fb = bar(C::BAR_RFULL + rp.i);
                     mbar_arrive_expect_tx(fb, C::RAW_BYTES);
                     bulk_g2s(sbase + C::SMEM_RAW + rp.i * C::RAW_BYTES, cwb + static_cast<size_t>(st) * C::RAW_BYTES,
@@ -638,8 +637,8 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
 #pragma unroll
                 for (int k = 0; k < SPS; ++k) {
                     float Dh[16], Dl[16];
-                    tmem_ld16_wait(lane_addr + ii[k] * C::ITEM_COLS + 16 * gq, Dh);
-                    tmem_ld16_wait(lane_addr + ii[k] * C::ITEM_COLS + N + 16 * gq, Dl);
+                    tmem_ld16x2_wait(lane_addr + ii[k] * C::ITEM_COLS + 16 * gq,
+                                     lane_addr + ii[k] * C::ITEM_COLS + N + 16 * gq, Dh, Dl);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         Dt[e] = k == 0 ? __fadd_rn(Dh[e], Dl[e]) : __fadd_rn(Dt[e], __fadd_rn(Dh[e], Dl[e]));
@@ -722,18 +721,25 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
             reinterpret_cast<int*>(smem + C::SMEM_TOK + C::OKF_OFF)[q] = ok ? 1 : 0;
         cluster_sync();
         if (rank == 0) {
-            bool all_ok = ok && had_unit;
-            for (int rr = 0; rr < g.kslices; ++rr) {
-                const uint32_t fbase = cluster_map(sbase + C::SMEM_TOK + C::OKF_OFF, static_cast<uint32_t>(rr));
-                for (int w4 = 0; w4 < NUM_PROMO_WARPS; ++w4)
-                    all_ok = all_ok && ld_cluster_u32(fbase + 4u * static_cast<uint32_t>(w4)) != 0u;
-            }
+            // every rank's flags at once: lane l reads flag l % 4 of rank l / 4 (S * 4 <= 32)
+            uint32_t f = 1u;
+            if (lane < g.kslices * NUM_PROMO_WARPS)
+                f = ld_cluster_u32(cluster_map(sbase + C::SMEM_TOK + C::OKF_OFF, static_cast<uint32_t>(lane >> 2)) +
+                                   4u * static_cast<uint32_t>(lane & 3));
+            const bool all_ok = __all_sync(0xffffffffu, f != 0u) && ok && had_unit;
             if (all_ok) {
                 for (int rr = 1; rr < g.kslices; ++rr) {
                     const uint32_t rbase = cluster_map(sbase + C::SMEM_TOK, static_cast<uint32_t>(rr));
 #pragma unroll
-                    for (int t = 0; t < N; ++t)
-                        acc[t] += ld_cluster_f32(rbase + 4u * static_cast<uint32_t>(t * BM + row));
+                    for (int t0 = 0; t0 < N; t0 += 16) {
+                        float v[16];        // 16 loads in flight before their sums
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            v[t] = ld_cluster_f32(rbase + 4u * static_cast<uint32_t>((t0 + t) * BM + row));
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            acc[t0 + t] += v[t];
+                    }
                 }
                 const int j = n_tile * BM + row;
                 if (j < g.od) {

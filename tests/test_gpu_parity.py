@@ -525,6 +525,23 @@ def test_gemm_last_round_split_parity(typ):
     assert_y_close(Y, Yo, S)
 
 
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
+def test_gemm_third_round_halves_parity(typ):
+    """Super-block kernel: 8 x 40 = 320 tiles on 152 SMs leave 16 tiles for a third
+    round, which run as two K-halves each (one super-block apiece) added into a zeroed
+    Y after two whole rounds; ragged M (last tile 104 tokens) and od (last tile 216
+    rows); bitwise the same on a second run."""
+    M, od, id_ = 1000, 10200, 512
+    raw = _q6_raw(od, id_, 45, False) if typ == "q6_K" else synth.q4k_blocks(od, id_, 45)
+    x = synth.activations(M, id_, 46)
+    Y = _run_gemm(typ, raw, x).cpu().numpy()
+    assert "super-block" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(typ, raw, x)
+    assert_y_close(Y, Yo, S)
+    again = _run_gemm(typ, raw, x).cpu().numpy()
+    assert np.array_equal(Y.view(np.uint32), again.view(np.uint32))
+
+
 def test_gemm_last_round_split_deterministic():
     raw = synth.q4k_blocks(5100, 512, 43)
     x = synth.activations(1024, 512, 44)
