@@ -348,6 +348,9 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                             ok = false;
                             break;
                         }
+                        // consumers read the entry with ordinary loads; the bulk copy that
+                        // refills it is ordered after them only through this proxy fence
+                        fence_proxy_async_smem();
                         const uint32_t dst = sbase + C::SMEM_SB + sp.i * C::SB_BYTES;
                         const uint32_t fb = bar(C::BAR_SBFULL + sp.i);
                         mbar_arrive_expect_tx(fb, SB_TX);
@@ -373,6 +376,7 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                         ++n_raw;
                         continue;
                     }
+                    fence_proxy_async_smem();
                     const uint32_t fb = bar(C::BAR_RFULL + rp.i);
                     mbar_arrive_expect_tx(fb, C::RAW_BYTES);
                     bulk_g2s(sbase + C::SMEM_RAW + rp.i * C::RAW_BYTES, cwb + static_cast<size_t>(st) * C::RAW_BYTES,
