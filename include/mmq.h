@@ -140,14 +140,15 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *   q6_K ((ql[e/2] >> 4*(e%2)) & 15 | ((qh[e/4] >> 2*(e%4)) & 3) << 4) - 32,
  *   q4_K (qs[e/2] >> 4*(e%2)) & 15.  Value e of a q6_K block uses scales[e/16].
  *
- * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds nine planes at
+ * packed (caller-owned, mmq_packed_weight_bytes() bytes) holds ten planes at
  * the offsets mmq_packed_weight_layout() returns; Np = 128*ceil(od/128),
  * nkb = id/64, nchunk = id/32, nsb = id/256; rows j >= od are zero:
  *   CODES  Np*id f16 integers in 16384-byte tiles (nt, kb) at (nt*nkb + kb)*16384,
  *          row r / value k at byte r*128 + (((k/8) ^ (r%8))*16) + (k%8)*2.
- *          The integer sub-block scale is folded into the code where the product
- *          is an exact f16 integer: q4_K sc_c*q (|.| <= 945); q6_K sc*q when every
- *          |scales[i]| of the tensor is <= 64 (|.| <= 2048), else the plain code q.
+ *          The integer sub-block scale is folded into the code, exactly: q4_K
+ *          sc_c*q (|.| <= 945); q6_K sc*q when every |scales[i]| of the tensor is
+ *          <= 64 (|.| <= 2048), else sc*l with l = (q + 32) & 15 (|.| <= 1920) and
+ *          the second tile in CODES2.
  *   PAIRS  Np*nchunk entries of two floats, entry (j, c) at index
  *          ((j/128)*nchunk + c)*128 + j%128:
  *            q6_K {d*scales[2*(c%8)], d*scales[2*(c%8)+1]}
@@ -156,7 +157,8 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *   AUX    per (row tile nt, super-block sb) an 8192-byte block at (nt*nsb + sb)*8192:
  *            q4_K: dmn = dmin*m_c split exactly into tf32 hi + lo; the hi tile then
  *                  the lo tile, row r / chunk k at (r/8)*256 + (k/4)*128 + (r%8)*16 + (k%4)*4;
- *            q6_K: the 16 scales as f32, scale s of row r at byte (s*128 + r)*4.
+ *            q6_K: the 16 scales as f32, scale s of row r at byte (s*128 + r)*4
+ *                  (kept for read-back; no kernel reads it).
  *   FLAG   q6_K: uint32 word 0 = 1 if CODES are folded, word 1 = max |scales[i]|.
  *   RAW    the raw blocks re-laid for the weight-streaming GEMM, od rows x nsb
  *          blocks, row-major: q4_K 144 B [qs[128] | d | dmin | scales[12]],
@@ -173,6 +175,10 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *          q4_K the six-bit sc_0..sc_7 then m_0..m_7, one per byte; q6_K scales[16].
  *   DM     q4_K: f32 dmin per (row, super-block) at index ((j/128)*nsb + sb)*128 + j%128
  *          (the few-token GEMM's min-term factor); q6_K: empty.
+ *   CODES2 q6_K: Np*id f16 values in the CODES tile layout, 16*sc*(h - 2) with
+ *          h = (q + 32) >> 4 (a multiple of 16 of magnitude <= 4096, exact) when
+ *          CODES holds sc*l, so that CODES + CODES2 = sc*q; zero when CODES is
+ *          folded; q4_K: empty.
  * -------------------------------------------------------------------------- */
 typedef enum {
     MMQ_PLANE_CODES = 0,
@@ -184,7 +190,8 @@ typedef enum {
     MMQ_PLANE_CW = 6,
     MMQ_PLANE_SC = 7,
     MMQ_PLANE_DM = 8,
-    MMQ_NUM_WEIGHT_PLANES = 9
+    MMQ_PLANE_CODES2 = 9,
+    MMQ_NUM_WEIGHT_PLANES = 10
 } mmq_weight_plane;
 
 mmq_status mmq_packed_weight_bytes(mmq_type t, int od, int id, size_t* bytes);
@@ -243,15 +250,16 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *    DM, SC and fm; when the weight tiles are few, each is split along K over a
  *    cluster of up to 8 CTAs whose partial sums are added in rank order
  *    (deterministic);
- *  - larger M, the super-block kernel (scale-folded codes, when its 128 x 256
- *    tiles number at least the SM count): the activation operand p*d_a*q_a as
- *    an f16 hi + lo pair (about 2^-21 relative per value) times the exact f16
- *    CODES, summed over a whole super-block in f32, then d and 1/p per
- *    super-block.  When the last round of tiles fills at most half the SMs (or
+ *  - larger M, the super-block kernel (when its 128 x 256 tiles number at least
+ *    the SM count): the activation operand p*d_a*q_a as an f16 hi + lo pair
+ *    (about 2^-21 relative per value) times the exact f16 CODES (and CODES2 for
+ *    two-tile q6_K, a second pair of MMAs into the same accumulator), summed over
+ *    a whole super-block in f32, then d and 1/p per super-block.  When the last round of tiles fills at most half the SMs (or
  *    all tiles do), those tiles run as two K-halves added into Y after a zeroing
  *    kernel, 0 + a + b, the same in either order;
- *  - otherwise the chunk kernel: the integer dots run exactly (codes held as f16
- *    integers, every partial sum an integer below 2^24 in the f32 accumulator)
+ *  - otherwise the chunk kernel: the integer dots sum_chunk (sc*q)*q_a run
+ *    exactly (codes held as f16 integers, two-tile q6_K as two MMAs per 16
+ *    values, every partial sum an integer below 2^24 in the f32 accumulator)
  *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
  * The super-block and chunk kernels compute the q4_K min term sum_c
  * (d_a*ssum)*(dmin*m_c) as a tf32 hi/lo tensor-core contraction (relative error
@@ -268,17 +276,15 @@ mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, cons
  * contraction) writes the raw integer dots it accumulates instead of Y, as f32
  * values holding the exact integers, at dots[(t*od + j)*nsub + s]:
  *   q4_K: nsub = id/32, s = chunk c: sc_c * sum(q * q_a)
- *   q6_K folded codes: nsub = id/32, s = chunk c: sc0*I_0 + sc1*I_1
- *   q6_K plain codes:  nsub = id/16, s = 16-value sub-block: I_s = sum(q * q_a)
- * (I_s the per-sub-block dot).  Size the buffer for id/16 per (t, j) for q6_K. */
+ *   q6_K: nsub = id/32, s = chunk c: sc0*I_0 + sc1*I_1
+ * (I_h = sum(q * q_a) over the chunk's 16-value half h; |value| < 2^24). */
 mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa,
                                const void* scales, int M, float* dots, mmq_stream_t s);
 
 /* Debug/verification: which kernel computes Y (process-wide).
  *   0 (default): as described above the GEMM calls;
  *   1: the chunk kernel for every M > MMQ_SMALL_M (128-token tiles);
- *   2: the super-block kernel for every scale-folded case with M > MMQ_SMALL_M
- *      (plain-code q6_K: the chunk kernel);
+ *   2: the super-block kernel for every M > MMQ_SMALL_M;
  *   3: as 0, but the few-token kernel never splits a tile over a CTA cluster;
  *   4: as 0, but the few-token kernel also for M <= MMQ_SMALL_M.
  * Returns MMQ_ERR_ARG for any other value.  Not thread-safe against GEMM calls
@@ -311,8 +317,7 @@ const char* mmq_last_path(void);
 
 /* Number of kernel launches the library has made in this process (every entry
  * point that launches adds the kernels it launched: prepass 1, repack 4 or 5,
- * GEMM 1, or 2 when K-half tiles are first zeroed, or when a q6_K
- * super-block launch is followed by the chunk kernel's flag check). */
+ * GEMM 1, or 2 when K-half tiles are first zeroed). */
 unsigned long long mmq_launch_count(void);
 
 /* Library version string. */

@@ -116,7 +116,7 @@ def mmq_packed_weight_bytes(t, od, id_):
     return b.value
 
 
-PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw", "cw", "sc", "dm")
+PLANES = ("codes", "pairs", "sbd", "aux", "flag", "raw", "cw", "sc", "dm", "codes2")
 SMALL_M = 8          # token counts up to this take the weight-streaming path
 FT_MAX_M = 64        # token counts up to this take the few-token GEMM (and get its planes)
 
@@ -320,12 +320,12 @@ def gemm(t, packed, od, id_, qa, scales, M, Y=None, stream=None):
 
 
 def gemm_dots(t, packed, od, id_, qa, scales, M, stream=None):
-    """Raw integer dots from the GEMM kernel as a flat f32 buffer of M*od*nsub values
-    (nsub = id/32, or id/16 for q6_K tensors with plain codes; see include/mmq.h)."""
+    """Raw integer dots from the GEMM kernel as a flat f32 buffer of M*od*(id/32)
+    values, one per (token, row, chunk); see include/mmq.h."""
     torch = _torch()
     tid = _type_id(t)
     _check_gemm_buffers(tid, packed, od, id_, qa, scales, M)
-    nsub = id_ // 16 if tid == MMQ_Q6_K else id_ // 32
+    nsub = id_ // 32
     dots = torch.full((M * od * nsub,), float("nan"), dtype=torch.float32, device=packed.device)
     mmq_debug_gemm_dots(tid, packed.data_ptr(), od, id_, qa.data_ptr(), scales.data_ptr(), M, dots.data_ptr(),
                         _stream(stream))

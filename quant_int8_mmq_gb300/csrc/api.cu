@@ -226,6 +226,8 @@ mmq_status mmq_packed_weight_layout(mmq_type t, int od, int id, size_t offsets[M
     sizes[MMQ_PLANE_CW] = w.cw_bytes;
     offsets[MMQ_PLANE_DM] = w.dm_off;
     sizes[MMQ_PLANE_DM] = w.dm_bytes;
+    offsets[MMQ_PLANE_CODES2] = w.code2_off;
+    sizes[MMQ_PLANE_CODES2] = w.code2_bytes;
     offsets[MMQ_PLANE_SC] = w.sc_off;
     sizes[MMQ_PLANE_SC] = w.sc_bytes;
     return MMQ_OK;

@@ -5,8 +5,10 @@
 //         I' = sum over the chunk of (sc_c * q) * q_a   (integer; sc folded into the codes)
 //         ma = d_a * ssum, dmn = dmin * m_c
 //   q6_K: Y = sum_sb d_sb * sum_{c in sb} d_a[t,c] * I'[t,j,c]
-//         I' = sum of (sc * q) * q_a over the chunk when the codes are folded, else
-//         sc0 * I_0 + sc1 * I_1 from one accumulator per 16-value sub-block.
+//         I' = sum of (sc * q) * q_a over the chunk: one MMA per 16 values on the
+//         folded codes sc * q, or, when some |sc| > 64, two on the exact tiles sc * l
+//         and 16 sc (h - 2) whose sum is sc * q (l, h the low 4 and high 2 bits of
+//         q + 32) into the same accumulator.
 // This is the q6_K/q4_K formula with the integer sub-block scale moved into the
 // integer dot and the f16 super-block scale factored out of the chunk sum; every
 // dot is an exact integer below 2^24.  The q4_K min term is a contraction over
@@ -19,17 +21,16 @@
 // and one 64-column chunk load in registers:
 //   warp 0      producer: cp.async.bulk copies (no multicast) of the pre-swizzled
 //               f16 operand tiles into a STAGES-deep ring, and once per super-block
-//               the token scales of its 8 chunks, the weight d and (plain-code q6_K)
-//               the sub-block scales into an SBR ring; for q4_K, after a tile's last
+//               the token scales of its 8 chunks and the weight d into an SBR ring
+//               (two weight tiles per stage for two-tile q6_K); for q4_K, after a tile's last
 //               k-block, the min-term operands of every super-block through the
 //               operand ring; completion on mbarriers.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::f16 (f16-held
 //               integer codes, f32 accumulate) into two 256-column TMEM items that are
-//               synchronised as units: with folded codes an item is one 64-value
-//               k-block (its two chunks' accumulators side by side), so the issuing
-//               thread waits, fences and commits once per two chunks; with plain
-//               q6_K codes an item is one chunk (two 16-value sub-block
-//               accumulators).  q4_K: the min term sum_c (d_a*ssum)(dmin*m) carries
+//               synchronised as units: an item is one 64-value k-block (its two
+//               chunks' accumulators side by side), so the issuing thread waits,
+//               fences and commits once per two chunks.  q4_K: the min term
+//               sum_c (d_a*ssum)(dmin*m) carries
 //               no per-super-block factor, so it is one kind::tf32 contraction per
 //               tile (three MMAs per super-block, hi/lo split) into one item after the
 //               tile's last k-block.
@@ -85,23 +86,22 @@ constexpr int PROMO_REGS = 224;
 static_assert(CTRL_REGS * 128 + PROMO_REGS * 256 <= LAUNCH_REGS * NUM_THREADS, "register split");
 
 // One super-block ring entry: weight d per row, the token scale pairs of the
-// super-block's 8 chunks, then q4_K min-term operands or plain-code q6_K scales.
+// super-block's 8 chunks.
 constexpr int SB_SBD_OFF = 0;
 constexpr int SB_SBD_BYTES = BN * 4;
 constexpr int SB_AS_OFF = SB_SBD_OFF + SB_SBD_BYTES;
 constexpr int SB_AS_BYTES = 8 * BM * 8;            // {d, ssum} x 8 chunks x 128 tokens
-constexpr int SB_X_OFF = SB_AS_OFF + SB_AS_BYTES;
-constexpr int SB_SC_BYTES = 16 * BN * 4;           // plain-code q6_K: sub-block scales
-constexpr int SB_BYTES = SB_X_OFF + SB_SC_BYTES;
+constexpr int SB_BYTES = SB_AS_OFF + SB_AS_BYTES;
 // q4_K min-term operands per super-block (token hi, lo tiles; weight hi, lo tiles),
 // streamed through the operand ring after a tile's last k-block.
 constexpr int MIN_AM_BYTES = 2 * TF32_TILE_BYTES;
 constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;
 static_assert(MIN_AM_BYTES <= TILE_BYTES && MIN_BM_BYTES <= TILE_BYTES, "min-term operands fit a stage");
 
+constexpr int B_STAGE = 2 * TILE_BYTES;          // one weight tile, or the two exact q6_K tiles
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * TILE_BYTES;
-constexpr int SMEM_SB = SMEM_B + STAGES * TILE_BYTES;
+constexpr int SMEM_SB = SMEM_B + STAGES * B_STAGE;
 constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
 constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = BAR_FULL + STAGES;
@@ -115,8 +115,7 @@ constexpr int SMEM_TMEMPTR = SMEM_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_TMEMPTR + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;    // slack for 1024-byte alignment
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-static_assert(SMEM_B % 1024 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && SB_X_OFF % 16 == 0 &&
-                  SMEM_BAR % 8 == 0,
+static_assert(SMEM_B % 1024 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && SMEM_BAR % 8 == 0,
               "alignment");
 
 
@@ -125,8 +124,9 @@ struct GemmArgs {
     const uint8_t* AS;    // token scale pairs          [num_m][nchunk][128] x {f32 d, i32 ssum}
     const uint8_t* AM;    // token min-term tiles       [num_m][nsb][hi 4 KiB, lo 4 KiB]
     const uint8_t* B;     // weight code tiles          [num_n][nkb][16 KiB]
+    const uint8_t* B2;    // q6_K second code tiles     [num_n][nkb][16 KiB] (two-tile codes)
     const uint8_t* SBD;   // weight d per super-block   [num_n][nsb][128] f32
-    const uint8_t* AUX;   // q4_K min-term tiles [num_n][nsb][8 KiB]; q6_K scales [num_n][nsb][16][128]
+    const uint8_t* AUX;   // q4_K min-term tiles [num_n][nsb][8 KiB]
     const unsigned int* FLAG;
     float* out;           // Y [M][ldy], or the dot dump [M][od][nsub]
     int ldy;
@@ -136,8 +136,6 @@ struct GemmArgs {
     int full_units;       // units below this are whole tiles
     int nsb_half;         // split units: super-blocks [0, nsb_half) and [nsb_half, nsb)
     int vec_store;        // Y is 16-byte aligned and ldy % 4 == 0
-    int skip_folded;      // q6_K: return at once when the codes are folded (the
-                          // super-block kernel, launched first, has written Y)
     unsigned int* err;    // the library's sticky error word
     unsigned long long wait_ns;   // limit of each bounded wait
     int withhold;         // verification: operand fill CTA 0's producer leaves out (-1: none)
@@ -255,16 +253,16 @@ struct RingPos {
 };
 
 // The three roles of one CTA.  TYPE 12 = q4_K, 14 = q6_K; MODE GEMM_Y or GEMM_DOTS;
-// FOLDED = the codes carry the integer sub-block scale (one accumulator per chunk).
-template <int TYPE, int MODE, bool FOLDED>
+// TILES = 1 (codes sc * q) or 2 (q6_K with some |sc| > 64: tiles sc * l and
+// 16 sc (h - 2), two MMAs per 16 values into the same accumulator).
+template <int TYPE, int MODE, int TILES>
 __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
                                            int warp, int lane)
 {
     constexpr bool Q4 = (TYPE == 12);
-    // TMEM holds two 256-column items, synchronised as units: folded codes, one 64-value
-    // k-block (its two chunks' accumulators side by side); plain q6_K codes, one chunk
-    // (its two 16-value sub-block accumulators side by side); q4_K's min term takes an
-    // item of its own per super-block.
+    // TMEM holds two 256-column items, synchronised as units: one 64-value k-block (its
+    // two chunks' accumulators side by side); q4_K's min term takes an item of its own
+    // per tile.
     constexpr uint32_t ITEM_COLS = 2 * BN;
     const int nkb = g.id / BK;
     const int nchunk = g.id / CHUNK;
@@ -280,7 +278,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             RingPos<STAGES> op;
             RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sb = 0;  // fills issued on each ring
-            constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES + (FOLDED ? 0 : SB_SC_BYTES);
+            constexpr uint32_t sb_tx = SB_SBD_BYTES + SB_AS_BYTES;
             const uint32_t skip = withheld_fill(g);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
@@ -288,6 +286,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                 const int m = w.m, n = w.n;
                 const uint8_t* Ab = g.A + static_cast<size_t>(m) * nkb * TILE_BYTES;
                 const uint8_t* Bb = g.B + static_cast<size_t>(n) * nkb * TILE_BYTES;
+                const uint8_t* B2b = (TILES == 2) ? g.B2 + static_cast<size_t>(n) * nkb * TILE_BYTES : nullptr;
                 const uint8_t* ASb = g.AS + static_cast<size_t>(m) * nchunk * BM * 8;
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {  // a new super-block
@@ -305,10 +304,6 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         bulk_g2s(dst + SB_SBD_OFF, g.SBD + (static_cast<size_t>(n) * nsb + s) * SB_SBD_BYTES,
                                  SB_SBD_BYTES, fb);
                         bulk_g2s(dst + SB_AS_OFF, ASb + static_cast<size_t>(s) * SB_AS_BYTES, SB_AS_BYTES, fb);
-                        if (!FOLDED) {
-                            bulk_g2s(dst + SB_X_OFF, g.AUX + (static_cast<size_t>(n) * nsb + s) * SB_SC_BYTES,
-                                     SB_SC_BYTES, fb);
-                        }
                         sb.next();
                         ++n_sb;
                     }
@@ -322,11 +317,14 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         continue;
                     }
                     const uint32_t fo = bar(BAR_FULL + op.i);
-                    mbar_arrive_expect_tx(fo, 2 * TILE_BYTES);
+                    mbar_arrive_expect_tx(fo, (1 + TILES) * TILE_BYTES);
                     bulk_g2s(sbase + SMEM_A + op.i * TILE_BYTES, Ab + static_cast<size_t>(kb) * TILE_BYTES,
                              TILE_BYTES, fo);
-                    bulk_g2s(sbase + SMEM_B + op.i * TILE_BYTES, Bb + static_cast<size_t>(kb) * TILE_BYTES,
+                    bulk_g2s(sbase + SMEM_B + op.i * B_STAGE, Bb + static_cast<size_t>(kb) * TILE_BYTES,
                              TILE_BYTES, fo);
+                    if (TILES == 2)
+                        bulk_g2s(sbase + SMEM_B + op.i * B_STAGE + TILE_BYTES,
+                                 B2b + static_cast<size_t>(kb) * TILE_BYTES, TILE_BYTES, fo);
                     op.next();
                     ++n_ops;
                 }
@@ -342,7 +340,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         mbar_arrive_expect_tx(fo, MIN_AM_BYTES + MIN_BM_BYTES);
                         bulk_g2s(sbase + SMEM_A + op.i * TILE_BYTES,
                                  g.AM + (static_cast<size_t>(m) * nsb + s) * MIN_AM_BYTES, MIN_AM_BYTES, fo);
-                        bulk_g2s(sbase + SMEM_B + op.i * TILE_BYTES,
+                        bulk_g2s(sbase + SMEM_B + op.i * B_STAGE,
                                  g.AUX + (static_cast<size_t>(n) * nsb + s) * MIN_BM_BYTES, MIN_BM_BYTES, fo);
                         op.next();
                         ++n_ops;
@@ -370,41 +368,28 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         break;
                     }
                     const uint64_t a0 = sdesc_k_sw128(sbase + SMEM_A + op.i * TILE_BYTES);
-                    const uint64_t b0 = sdesc_k_sw128(sbase + SMEM_B + op.i * TILE_BYTES);
+                    const uint64_t b0 = sdesc_k_sw128(sbase + SMEM_B + op.i * B_STAGE);
+                    const uint64_t b1 = sdesc_k_sw128(sbase + SMEM_B + op.i * B_STAGE + TILE_BYTES);
                     // K advance inside the 128-byte swizzled rows: 32 bytes per 16 values
                     // (the descriptor's address field counts 16-byte units).
-                    if (FOLDED) {
-                        // one item per k-block: one wait, one fence, one commit for two chunks
-                        if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + item.i * ITEM_COLS;
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            umma_f16(d + cc * BN, a0 + 4u * cc, b0 + 4u * cc, idesc, 0u);
-                            umma_f16(d + cc * BN, a0 + 4u * cc + 2, b0 + 4u * cc + 2, idesc, 1u);
-                        }
-                        umma_commit(bar(BAR_TFULL + item.i));
-                        item.next();
-                    } else {
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                            umma_f16(d, a0 + 4u * cc, b0 + 4u * cc, idesc, 0u);
-                            umma_f16(d + BN, a0 + 4u * cc + 2, b0 + 4u * cc + 2, idesc, 0u);
-                            umma_commit(bar(BAR_TFULL + item.i));
-                            item.next();
-                        }
-                        if (!ok)
-                            break;
+                    // one item per k-block: one wait, one fence, one commit for two chunks
+                    if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + item.i * ITEM_COLS;
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        umma_f16(d + cc * BN, a0 + 4u * cc, b0 + 4u * cc, idesc, 0u);
+                        umma_f16(d + cc * BN, a0 + 4u * cc + 2, b0 + 4u * cc + 2, idesc, 1u);
+                        if (TILES == 2) {
+                            umma_f16(d + cc * BN, a0 + 4u * cc, b1 + 4u * cc, idesc, 1u);
+                            umma_f16(d + cc * BN, a0 + 4u * cc + 2, b1 + 4u * cc + 2, idesc, 1u);
+                        }
+                    }
+                    umma_commit(bar(BAR_TFULL + item.i));
+                    item.next();
                     umma_commit(bar(BAR_EMPTY + op.i));  // operand stage free once these MMAs finish
                     op.next();
                 }
@@ -424,7 +409,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         }
                         tc_fence_after();
                         const uint32_t am = sbase + SMEM_A + op.i * TILE_BYTES;
-                        const uint32_t bm = sbase + SMEM_B + op.i * TILE_BYTES;
+                        const uint32_t bm = sbase + SMEM_B + op.i * B_STAGE;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
                         umma_tf32(d, ahi, bhi, idesc_t, s > w.sb0 ? 1u : 0u);
@@ -484,80 +469,32 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
             for (int i = 0; i < COLS_PER_WARP / 2; ++i)
                 inner[i] = make_float2(0.0f, 0.0f);
             for (int k2 = 0; k2 < 4 && ok; ++k2) {             // the super-block's four k-blocks
-                if (FOLDED) {
-                    if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t col0 = lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP;
+                if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col0 = lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int k = 2 * k2 + cc;
-                        const int c = 8 * s + k;                // chunk index along id
-                        float I[COLS_PER_WARP];
-                        tmem_ld64_wait(col0 + cc * BN, I);
-                        if (cc == 1)
-                            release();                          // both chunks are in registers
-                        if (MODE == GEMM_Y) {
-                            const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
-                            const float2 da2 = make_float2(da, da);
-#pragma unroll
-                            for (int i = 0; i < COLS_PER_WARP / 2; ++i)
-                                inner[i] = ffma2(da2, make_float2(I[2 * i], I[2 * i + 1]), inner[i]);
-                        } else if (row < g.M) {
-#pragma unroll
-                            for (int i = 0; i < COLS_PER_WARP; ++i) {
-                                const int j = jb + i;
-                                if (j < g.od)
-                                    g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] = I[i];
-                            }
-                        }
-                    }
-                } else {
-                    // q6_K with plain codes: one item per chunk, one accumulator per 16-value
-                    // sub-block, I' = sc0 * I_0 + sc1 * I_1 (exact: |I'| < 2^24).
-                    const float* scp = reinterpret_cast<const float*>(sbe + SB_X_OFF);
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int k = 2 * k2 + cc;
-                        const int c = 8 * s + k;
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int k = 2 * k2 + cc;
+                    const int c = 8 * s + k;                    // chunk index along id
+                    float I[COLS_PER_WARP];
+                    tmem_ld64_wait(col0 + cc * BN, I);
+                    if (cc == 1)
+                        release();                              // both chunks are in registers
+                    if (MODE == GEMM_Y) {
                         const float da = __uint_as_float(tsc[k * BM + row_in_tile].x);
                         const float2 da2 = make_float2(da, da);
-                        const int s0 = 2 * k;
-                        if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t col0 = lane_addr + item.i * ITEM_COLS + hc * COLS_PER_WARP;
 #pragma unroll
-                        for (int p = 0; p < COLS_PER_WARP / 8; ++p) {
-                            float h0[8], h1[8];
-                            tmem_ld8x2_wait(col0 + p * 8, col0 + BN + p * 8, h0, h1);
-                            if (p == COLS_PER_WARP / 8 - 1)
-                                release();
-                            if (MODE == GEMM_DOTS) {
-                                if (row < g.M) {
+                        for (int i = 0; i < COLS_PER_WARP / 2; ++i)
+                            inner[i] = ffma2(da2, make_float2(I[2 * i], I[2 * i + 1]), inner[i]);
+                    } else if (row < g.M) {
 #pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        const int j = jb + p * 8 + i;
-                                        if (j < g.od) {
-                                            float* dst = g.out + (static_cast<size_t>(row) * g.od + j) * (2 * nchunk);
-                                            dst[2 * c] = h0[i];
-                                            dst[2 * c + 1] = h1[i];
-                                        }
-                                    }
-                                }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 8; i += 2) {
-                                    const int col = hc * COLS_PER_WARP + p * 8 + i;
-                                    const float u0 = fmaf(h1[i], scp[(s0 + 1) * BN + col], h0[i] * scp[s0 * BN + col]);
-                                    const float u1 =
-                                        fmaf(h1[i + 1], scp[(s0 + 1) * BN + col + 1], h0[i + 1] * scp[s0 * BN + col + 1]);
-                                    inner[p * 4 + i / 2] = ffma2(da2, make_float2(u0, u1), inner[p * 4 + i / 2]);
-                                }
-                            }
+                        for (int i = 0; i < COLS_PER_WARP; ++i) {
+                            const int j = jb + i;
+                            if (j < g.od)
+                                g.out[(static_cast<size_t>(row) * g.od + j) * nchunk + c] = I[i];
                         }
                     }
                 }
@@ -632,8 +569,6 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
 template <int TYPE, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
 {
-    if (TYPE == 14 && g.skip_folded && __ldg(g.FLAG) != 0u)
-        return;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -670,14 +605,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + SMEM_TMEMPTR);
 
     if constexpr (TYPE == 14) {
-        // q6_K codes hold sc*q (one accumulator per chunk) unless some |sc| > 64;
+        // q6_K codes hold sc*q in one tile unless some |sc| > 64 (then two exact tiles);
         // the repack recorded which in the flag word (uniform for the launch).
         if (__ldg(g.FLAG) != 0u)
-            gemm_roles<14, MODE, true>(g, smem, sbase, tmem_base, warp, lane);
+            gemm_roles<14, MODE, 1>(g, smem, sbase, tmem_base, warp, lane);
         else
-            gemm_roles<14, MODE, false>(g, smem, sbase, tmem_base, warp, lane);
+            gemm_roles<14, MODE, 2>(g, smem, sbase, tmem_base, warp, lane);
     } else {
-        gemm_roles<12, MODE, true>(g, smem, sbase, tmem_base, warp, lane);
+        gemm_roles<12, MODE, 1>(g, smem, sbase, tmem_base, warp, lane);
     }
 
     tc_fence_before();
@@ -747,10 +682,9 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    // Y of scale-folded codes goes to the super-block kernel when its 128 x 256 tiles
-    // fill every SM at least once (fewer, larger tiles lose more to idle SMs than the
-    // faster contraction wins back); for q6_K the chunk kernel is launched after it
-    // and runs only when the codes are plain.
+    // Y goes to the super-block kernel when its 128 x 256 tiles fill every SM at least
+    // once (fewer, larger tiles lose more to idle SMs than the faster contraction wins
+    // back), else to this chunk kernel; both read the one- or two-tile q6_K codes.
     const int sel = g_large_m_kernel.load();
     const bool sb_fills = static_cast<long long>(ceil_div(M, BM)) * ceil_div(od, 2 * BN) >= nsm;
     const bool sb_first = mode == GEMM_Y && (sel == 2 || (sel == 0 && sb_fills));
@@ -767,17 +701,14 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
                               path_label);
     if (sb_first) {
         e = launch_gemm_sb(type, packed, od, id, qa, scales, M, out, ldy, s, wc);
-        // the chunk kernel launched after it (q6_K) only reads the flag or runs plain codes
-        wc.withhold_fill = -1;
-        wc.limit_ns = WAIT_LIMIT_NS;
-        if (e != cudaSuccess)
-            return e;
-        if (type == 12) {
-            if (path_label)
-                *path_label = "q4_K: super-block tcgen05 GEMM, 128x256 tiles, activation operand p*d_a*q_a split "
-                              "f16 hi+lo in shared memory, one TMEM accumulator per super-block, tf32 hi/lo min term";
-            return cudaSuccess;
-        }
+        if (e == cudaSuccess && path_label)
+            *path_label = type == 12
+                              ? "q4_K: super-block tcgen05 GEMM, 128x256 tiles, activation operand p*d_a*q_a split "
+                                "f16 hi+lo in shared memory, one TMEM accumulator per super-block, tf32 hi/lo min term"
+                              : "q6_K: super-block tcgen05 GEMM, 128x256 tiles, activation operand p*d_a*q_a split "
+                                "f16 hi+lo in shared memory, one TMEM accumulator per super-block; codes sc*q in one "
+                                "f16 tile (every |sc| <= 64) or two exact tiles sc*l and 16*sc*(h-2)";
+        return e;
     }
     const WeightPlanes wp = weight_planes(type, od, id);
     const ActPlanes ap = act_planes(M, id);
@@ -788,6 +719,7 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.AS = sc + ap.pair_off;
     a.AM = sc + ap.am_off;
     a.B = pk + wp.code_off;
+    a.B2 = pk + wp.code2_off;
     a.SBD = pk + wp.sbd_off;
     a.AUX = pk + wp.aux_off;
     a.FLAG = reinterpret_cast<const unsigned int*>(pk + wp.flag_off);
@@ -799,7 +731,6 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     a.num_m = ceil_div(M, BM);
     a.num_n = ceil_div(od, BN);
     a.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (ldy & 3) == 0) ? 1 : 0;
-    a.skip_folded = sb_first ? 1 : 0;
     a.err = wc.err;
     a.wait_ns = wc.limit_ns;
     a.withhold = wc.withhold_fill;
@@ -835,12 +766,9 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
 
     if (type == 14) {
         if (path_label)
-            *path_label = sb_first
-                              ? "q6_K: super-block tcgen05 GEMM on scale-folded codes (128x256 tiles, activation "
-                                "operand split f16 hi+lo), else the chunk GEMM on plain codes (per-sub-block TMEM "
-                                "accumulators, f32 d_a per chunk)"
-                              : "q6_K: chunk GEMM, tcgen05.mma kind::f16 128x128x16 on exact int codes, two 256-column "
-                                "TMEM items, f32 d_a per chunk / d per super-block";
+            *path_label = "q6_K: chunk GEMM, tcgen05.mma kind::f16 128x128x16 on exact int codes (sc*q in one f16 "
+                          "tile, or two exact tiles sc*l and 16*sc*(h-2)), two 256-column TMEM items, f32 d_a per "
+                          "chunk / d per super-block";
         return mode == GEMM_Y ? launch_typed<14, GEMM_Y>(a, grid, s) : launch_typed<14, GEMM_DOTS>(a, grid, s);
     }
     if (path_label)

@@ -64,7 +64,6 @@ namespace {
 
 constexpr int BM = 128;               // tokens per tile (TMEM lanes, MMA M)
 constexpr int BN = 256;               // weight rows per tile (MMA N): two 128-row tiles
-constexpr int STAGES = 3;             // operand ring depth
 constexpr int SBR = 3;                // super-block ring depth
 constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
@@ -89,7 +88,6 @@ static_assert(CTRL_REGS * 128 + CONV_REGS * 128 + PROMO_REGS * 256 <= LAUNCH_REG
 constexpr int ST_A = 0;
 constexpr int ST_LO = TILE_BYTES;
 constexpr int ST_B = 2 * TILE_BYTES;
-constexpr int STAGE_BYTES = 4 * TILE_BYTES;
 constexpr int MIN_AM_BYTES = 2 * TF32_TILE_BYTES;      // token hi, lo
 constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;      // per 128-row weight tile: hi, lo
 // Min-term super-blocks per stage: a stage of one super-block holds only 384 cycles of
@@ -108,26 +106,36 @@ constexpr int SB_IP_BYTES = BM * 4;
 constexpr int SB_COPY_BYTES = SB_SBD_BYTES + SB_AS_BYTES;
 constexpr int SB_BYTES = SB_IP_OFF + SB_IP_BYTES;
 
-constexpr int SMEM_ST = 0;
-constexpr int SMEM_SB = SMEM_ST + STAGES * STAGE_BYTES;
-constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
-constexpr int BAR_FULL = 0;                      // the stage's activation (or min-term token) tile
-constexpr int BAR_FULLB = BAR_FULL + STAGES;     // the stage's weight tiles
-constexpr int BAR_CONV = BAR_FULLB + STAGES;
-constexpr int BAR_EMPTY = BAR_CONV + STAGES;
-constexpr int BAR_SBFULL = BAR_EMPTY + STAGES;
-constexpr int BAR_SBEMPTY = BAR_SBFULL + SBR;
-constexpr int BAR_IPREADY = BAR_SBEMPTY + SBR;
-constexpr int BAR_TFULL = BAR_IPREADY + SBR;
-constexpr int BAR_TEMPTY = BAR_TFULL + 2;
-constexpr int BAR_DRAIN = BAR_TEMPTY + 2;
-constexpr int NUM_BARS = BAR_DRAIN + 1;
-constexpr int SMEM_TMEMPTR = SMEM_BAR + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_TMEMPTR + 16;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;    // slack for 1024-byte alignment
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-static_assert(STAGE_BYTES % 1024 == 0 && SMEM_SB % 1024 == 0 && SB_BYTES % 16 == 0 && SMEM_BAR % 8 == 0,
-              "alignment");
+// Shared-memory plan of a launch, by the number of exact weight tiles per k-block:
+// TILES = 1 (codes sc * q): 3 stages of [A | lo | B n0 | B n1]; TILES = 2 (q6_K with
+// some |sc| > 64: tiles sc * l and 16 sc (h - 2)): 2 stages of [A | lo | B n0 | B n1 |
+// B2 n0 | B2 n1].
+template <int TILES>
+struct SbL {
+    static constexpr int STAGES = TILES == 1 ? 3 : 2;         // operand ring depth
+    static constexpr int STAGE_BYTES = (2 + 2 * TILES) * TILE_BYTES;
+    static constexpr int SMEM_ST = 0;
+    static constexpr int SMEM_SB = SMEM_ST + STAGES * STAGE_BYTES;
+    static constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
+    static constexpr int BAR_FULL = 0;                      // the stage's activation (or min-term token) tile
+    static constexpr int BAR_FULLB = BAR_FULL + STAGES;     // the stage's weight tiles
+    static constexpr int BAR_CONV = BAR_FULLB + STAGES;
+    static constexpr int BAR_EMPTY = BAR_CONV + STAGES;
+    static constexpr int BAR_SBFULL = BAR_EMPTY + STAGES;
+    static constexpr int BAR_SBEMPTY = BAR_SBFULL + SBR;
+    static constexpr int BAR_IPREADY = BAR_SBEMPTY + SBR;
+    static constexpr int BAR_TFULL = BAR_IPREADY + SBR;
+    static constexpr int BAR_TEMPTY = BAR_TFULL + 2;
+    static constexpr int BAR_DRAIN = BAR_TEMPTY + 2;
+    static constexpr int NUM_BARS = BAR_DRAIN + 1;
+    static constexpr int SMEM_TMEMPTR = SMEM_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_USED = SMEM_TMEMPTR + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;    // slack for 1024-byte alignment
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    static_assert(STAGE_BYTES % 1024 == 0 && SMEM_SB % 1024 == 0 && SB_BYTES % 16 == 0 && SMEM_BAR % 8 == 0,
+                  "alignment");
+};
+constexpr int SMEM_ALLOC = SbL<1>::SMEM_ALLOC > SbL<2>::SMEM_ALLOC ? SbL<1>::SMEM_ALLOC : SbL<2>::SMEM_ALLOC;
 static_assert(MIN_PER_STAGE * MIN_AM_BYTES <= TILE_BYTES && MIN_PER_STAGE * 2 * MIN_BM_BYTES <= 2 * TILE_BYTES,
               "min-term operands fit a stage");
 
@@ -136,6 +144,7 @@ struct SbArgs {
     const uint8_t* AS;    // token scale pairs          [num_m][nchunk][128] x {f32 d, i32 ssum}
     const uint8_t* AM;    // token min-term tiles       [num_m][nsb][hi 4 KiB, lo 4 KiB]
     const uint8_t* B;     // weight code tiles          [num_n128][nkb][16 KiB]
+    const uint8_t* B2;    // q6_K second code tiles     [num_n128][nkb][16 KiB] (two-tile codes)
     const uint8_t* SBD;   // weight d per super-block   [num_n128][nsb][128] f32
     const uint8_t* AUX;   // q4_K min-term tiles        [num_n128][nsb][hi 4 KiB, lo 4 KiB]
     const unsigned int* FLAG;
@@ -292,21 +301,22 @@ __device__ __forceinline__ void split_pair(uint32_t cbits, __half2 s_hi, __half2
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-template <int TYPE>
+template <int TYPE, int TILES>
 __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
                                          int warp, int lane)
 {
+    using L = SbL<TILES>;
     constexpr bool Q4 = (TYPE == 12);
     const int nkb = g.id / TILE_K;
     const int nchunk = g.id / CHUNK;
     const int nsb = g.id / QK_K;
-    auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
+    auto bar = [&](int i) -> uint32_t { return sbase + L::SMEM_BAR + 8u * static_cast<uint32_t>(i); };
 
     if (warp < CONV_WARP0) {
         regs_shrink<CTRL_REGS>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------------ producer
-            RingPos<STAGES> op;
+            RingPos<L::STAGES> op;
             RingPos<SBR> sb;
             uint32_t n_ops = 0, n_sb = 0;
             // verification only: the fill of this CTA that is left out (never armed,
@@ -321,6 +331,8 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 const uint8_t* Ab = g.A + static_cast<size_t>(m) * nkb * TILE_BYTES;
                 const uint8_t* B0 = g.B + static_cast<size_t>(n0) * nkb * TILE_BYTES;
                 const uint8_t* B1 = g.B + static_cast<size_t>(n1) * nkb * TILE_BYTES;
+                const uint8_t* B20 = TILES == 2 ? g.B2 + static_cast<size_t>(n0) * nkb * TILE_BYTES : nullptr;
+                const uint8_t* B21 = TILES == 2 ? g.B2 + static_cast<size_t>(n1) * nkb * TILE_BYTES : nullptr;
                 const uint8_t* ASb = g.AS + static_cast<size_t>(m) * nchunk * BM * 8;
                 if (Q4) {
                     // the tile's min-term operands, consumed after its last k-block
@@ -333,13 +345,13 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     if ((kb & 3) == 0) {
                         const int s = kb >> 2;
-                        if (!ctl_wait(g, bar(BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(L::BAR_SBEMPTY + sb.i), sb.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_smem();   // after the consumers' ordinary loads
-                        const uint32_t dst = sbase + SMEM_SB + sb.i * SB_BYTES;
-                        const uint32_t fb = bar(BAR_SBFULL + sb.i);
+                        const uint32_t dst = sbase + L::SMEM_SB + sb.i * SB_BYTES;
+                        const uint32_t fb = bar(L::BAR_SBFULL + sb.i);
                         mbar_arrive_expect_tx(fb, SB_COPY_BYTES);
                         bulk_g2s(dst + SB_SBD_OFF, g.SBD + (static_cast<size_t>(n0) * nsb + s) * 512, 512, fb);
                         bulk_g2s(dst + SB_SBD_OFF + 512, g.SBD + (static_cast<size_t>(n1) * nsb + s) * 512, 512, fb);
@@ -347,7 +359,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         sb.next();
                         ++n_sb;
                     }
-                    if (!ctl_wait(g, bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(L::BAR_EMPTY + op.i), op.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
@@ -357,22 +369,30 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         continue;
                     }
                     fence_proxy_async_smem();       // after the converter's ordinary stores
-                    const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
+                    const uint32_t st = sbase + L::SMEM_ST + op.i * L::STAGE_BYTES;
                     // the activation tile completes on its own barrier so that the converter
                     // starts while the weight tiles are still in flight
-                    const uint32_t fo = bar(BAR_FULL + op.i), fw = bar(BAR_FULLB + op.i);
+                    const uint32_t fo = bar(L::BAR_FULL + op.i), fw = bar(L::BAR_FULLB + op.i);
                     const size_t ko = static_cast<size_t>(kb) * TILE_BYTES;
                     mbar_arrive_expect_tx(fo, TILE_BYTES);
                     bulk_g2s(st + ST_A, Ab + ko, TILE_BYTES, fo);
-                    mbar_arrive_expect_tx(fw, 2 * TILE_BYTES);
+                    mbar_arrive_expect_tx(fw, 2 * TILES * TILE_BYTES);
                     bulk_g2s(st + ST_B, B0 + ko, TILE_BYTES, fw);
                     bulk_g2s(st + ST_B + TILE_BYTES, B1 + ko, TILE_BYTES, fw);
-                    if (kb + STAGES < 4 * w.sb1) {
+                    if (TILES == 2) {
+                        bulk_g2s(st + ST_B + 2 * TILE_BYTES, B20 + ko, TILE_BYTES, fw);
+                        bulk_g2s(st + ST_B + 3 * TILE_BYTES, B21 + ko, TILE_BYTES, fw);
+                    }
+                    if (kb + L::STAGES < 4 * w.sb1) {
                         // warm L2 with the tiles of the k-block this stage takes next
                         // (measured: about 3.5 % off the launch)
-                        const size_t kp = static_cast<size_t>(kb + STAGES) * TILE_BYTES;
+                        const size_t kp = static_cast<size_t>(kb + L::STAGES) * TILE_BYTES;
                         bulk_prefetch_l2(B0 + kp, TILE_BYTES);
                         bulk_prefetch_l2(B1 + kp, TILE_BYTES);
+                        if (TILES == 2) {
+                            bulk_prefetch_l2(B20 + kp, TILE_BYTES);
+                            bulk_prefetch_l2(B21 + kp, TILE_BYTES);
+                        }
                         bulk_prefetch_l2(Ab + kp, TILE_BYTES);
                     }
                     op.next();
@@ -384,13 +404,13 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     // at ST_B + e * 16 KiB
                     for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
                         const int ne = min(MIN_PER_STAGE, w.sb1 - s);
-                        if (!ctl_wait(g, bar(BAR_EMPTY + op.i), op.ph ^ 1u)) {
+                        if (!ctl_wait(g, bar(L::BAR_EMPTY + op.i), op.ph ^ 1u)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_smem();
-                        const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
-                        const uint32_t fo = bar(BAR_FULL + op.i), fw = bar(BAR_FULLB + op.i);
+                        const uint32_t st = sbase + L::SMEM_ST + op.i * L::STAGE_BYTES;
+                        const uint32_t fo = bar(L::BAR_FULL + op.i), fw = bar(L::BAR_FULLB + op.i);
                         mbar_arrive_expect_tx(fo, ne * MIN_AM_BYTES);
                         bulk_g2s(st + ST_A, g.AM + (static_cast<size_t>(m) * nsb + s) * MIN_AM_BYTES,
                                  ne * MIN_AM_BYTES, fo);
@@ -409,66 +429,71 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     }
                 }
             }
-            for (uint32_t i = (n_ops > STAGES ? n_ops - STAGES : 0); i < n_ops; ++i) {
+            for (uint32_t i = (n_ops > L::STAGES ? n_ops - L::STAGES : 0); i < n_ops; ++i) {
                 if (i == skip)
                     continue;
-                drain_wait(g, bar(BAR_FULL + i % STAGES), (i / STAGES) & 1u);
-                drain_wait(g, bar(BAR_FULLB + i % STAGES), (i / STAGES) & 1u);
+                drain_wait(g, bar(L::BAR_FULL + i % L::STAGES), (i / L::STAGES) & 1u);
+                drain_wait(g, bar(L::BAR_FULLB + i % L::STAGES), (i / L::STAGES) & 1u);
             }
             for (uint32_t i = (n_sb > SBR ? n_sb - SBR : 0); i < n_sb; ++i)
-                drain_wait(g, bar(BAR_SBFULL + i % SBR), (i / SBR) & 1u);
+                drain_wait(g, bar(L::BAR_SBFULL + i % SBR), (i / SBR) & 1u);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_t = idesc_tf32(BM, BN);
-            RingPos<STAGES> op;
+            RingPos<L::STAGES> op;
             RingPos<2> item;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
                 for (int kb = 4 * w.sb0; kb < 4 * w.sb1; ++kb) {
                     const int k2 = kb & 3;
-                    if (k2 == 0 && !ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                    if (k2 == 0 && !ctl_wait(g, bar(L::BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    if (!ctl_wait(g, bar(BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(BAR_FULLB + op.i), op.ph)) {
+                    if (!ctl_wait(g, bar(L::BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(L::BAR_FULLB + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
+                    const uint32_t st = sbase + L::SMEM_ST + op.i * L::STAGE_BYTES;
                     const uint64_t ah = sdesc_k_sw128(st + ST_A);
                     const uint64_t al = sdesc_k_sw128(st + ST_LO);
                     const uint64_t b = sdesc_k_sw128(st + ST_B);
+                    const uint64_t b2 = sdesc_k_sw128(st + ST_B + 2 * TILE_BYTES);
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
                     // 16 values per step: +32 bytes (two 16-byte units) inside the swizzled rows
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         umma_f16(d, ah + 2u * kk, b + 2u * kk, idesc, (k2 | kk) ? 1u : 0u);
                         umma_f16(d, al + 2u * kk, b + 2u * kk, idesc, 1u);
+                        if (TILES == 2) {   // the second exact tile: sc*l + 16 sc (h - 2) = sc*q
+                            umma_f16(d, ah + 2u * kk, b2 + 2u * kk, idesc, 1u);
+                            umma_f16(d, al + 2u * kk, b2 + 2u * kk, idesc, 1u);
+                        }
                     }
-                    umma_commit(bar(BAR_EMPTY + op.i));
+                    umma_commit(bar(L::BAR_EMPTY + op.i));
                     op.next();
                     if (k2 == 3) {
-                        umma_commit(bar(BAR_TFULL + item.i));
+                        umma_commit(bar(L::BAR_TFULL + item.i));
                         item.next();
                     }
                 }
                 if (Q4 && ok) {
-                    if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
+                    if (!ctl_wait(g, bar(L::BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
                     for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
                         const int ne = min(MIN_PER_STAGE, w.sb1 - s);
-                        if (!ctl_wait(g, bar(BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(BAR_FULLB + op.i), op.ph)) {
+                        if (!ctl_wait(g, bar(L::BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(L::BAR_FULLB + op.i), op.ph)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t st = sbase + SMEM_ST + op.i * STAGE_BYTES;
+                        const uint32_t st = sbase + L::SMEM_ST + op.i * L::STAGE_BYTES;
                         for (int e = 0; e < ne; ++e) {
                             const uint32_t aa = st + ST_A + e * MIN_AM_BYTES;
                             const uint32_t bb = st + ST_B + e * 2 * MIN_BM_BYTES;
@@ -478,17 +503,17 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                             mma_tf32(d, ahi, blo, idesc_t, 1u);
                             mma_tf32(d, alo, bhi, idesc_t, 1u);
                         }
-                        umma_commit(bar(BAR_EMPTY + op.i));
+                        umma_commit(bar(L::BAR_EMPTY + op.i));
                         op.next();
                     }
                     if (!ok)
                         break;
-                    umma_commit(bar(BAR_TFULL + item.i));
+                    umma_commit(bar(L::BAR_TFULL + item.i));
                     item.next();
                 }
             }
-            umma_commit(bar(BAR_DRAIN));
-            drain_wait(g, bar(BAR_DRAIN), 0u);
+            umma_commit(bar(L::BAR_DRAIN));
+            drain_wait(g, bar(L::BAR_DRAIN), 0u);
         }
         __syncwarp();
         return;
@@ -500,17 +525,17 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
         const int r = (warp - CONV_WARP0) * 32 + lane;    // token row of the tile
         const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
-        RingPos<STAGES> op;
+        RingPos<L::STAGES> op;
         RingPos<SBR> sb;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
             const Unit w = unit_of(g, u, nsb);
             for (int s = w.sb0; ok && s < w.sb1; ++s) {
-                if (!warp_wait(g, bar(BAR_SBFULL + sb.i), sb.ph)) {
+                if (!warp_wait(g, bar(L::BAR_SBFULL + sb.i), sb.ph)) {
                     ok = false;
                     break;
                 }
-                const uint2* pr = reinterpret_cast<const uint2*>(smem + SMEM_SB + sb.i * SB_BYTES + SB_AS_OFF);
+                const uint2* pr = reinterpret_cast<const uint2*>(smem + L::SMEM_SB + sb.i * SB_BYTES + SB_AS_OFF);
                 float da[8];
                 float dmax = 0.0f;
 #pragma unroll
@@ -524,17 +549,17 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 for (int k = 0; k < 8; ++k)
                     da[k] *= p;                   // s = d_a * p, exact
                 // 1/p (exact) for the promotion warps
-                reinterpret_cast<float*>(smem + SMEM_SB + sb.i * SB_BYTES + SB_IP_OFF)[r] =
+                reinterpret_cast<float*>(smem + L::SMEM_SB + sb.i * SB_BYTES + SB_IP_OFF)[r] =
                     __uint_as_float((254u - pf) << 23);
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(BAR_IPREADY + sb.i));
-                    mbar_arrive(bar(BAR_SBEMPTY + sb.i));
+                    mbar_arrive(bar(L::BAR_IPREADY + sb.i));
+                    mbar_arrive(bar(L::BAR_SBEMPTY + sb.i));
                 }
                 sb.next();
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) {
-                    if (!warp_wait(g, bar(BAR_FULL + op.i), op.ph)) {
+                    if (!warp_wait(g, bar(L::BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
@@ -547,7 +572,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         shi[cc] = __half2half2(hh);
                         slo[cc] = __half2half2(__float2half_rn(sk - __half2float(hh)));
                     }
-                    uint8_t* st = smem + SMEM_ST + op.i * STAGE_BYTES;
+                    uint8_t* st = smem + L::SMEM_ST + op.i * L::STAGE_BYTES;
                     // all eight 16-byte groups of the row first (one shared-memory
                     // latency per k-block), then convert and store
                     uint4 c[8];
@@ -569,20 +594,20 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                     fence_proxy_async_smem();           // ordinary stores -> tensor-core reads
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(bar(BAR_CONV + op.i));
+                        mbar_arrive(bar(L::BAR_CONV + op.i));
                     op.next();
                 }
             }
             if (Q4 && ok) {
                 // min-term stages pass through unchanged
                 for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
-                    if (!warp_wait(g, bar(BAR_FULL + op.i), op.ph)) {
+                    if (!warp_wait(g, bar(L::BAR_FULL + op.i), op.ph)) {
                         ok = false;
                         break;
                     }
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(bar(BAR_CONV + op.i));
+                        mbar_arrive(bar(L::BAR_CONV + op.i));
                     op.next();
                 }
             }
@@ -623,11 +648,11 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             float ip[2][2] = {{-1.0f, -1.0f}, {-1.0f, -1.0f}};
             const float2* d2 = nullptr;
             if (!min_item) {
-                if (!warp_wait(g, bar(BAR_SBFULL + sb.i), sb.ph) || !warp_wait(g, bar(BAR_IPREADY + sb.i), sb.ph)) {
+                if (!warp_wait(g, bar(L::BAR_SBFULL + sb.i), sb.ph) || !warp_wait(g, bar(L::BAR_IPREADY + sb.i), sb.ph)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* sbe = smem + SMEM_SB + sb.i * SB_BYTES;
+                const uint8_t* sbe = smem + L::SMEM_SB + sb.i * SB_BYTES;
                 const float* ipr = reinterpret_cast<const float*>(sbe + SB_IP_OFF);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -636,7 +661,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         ip[h][rho] = ipr[q * 32 + 16 * h + 8 * rho + quad];
                 d2 = reinterpret_cast<const float2*>(sbe + SB_SBD_OFF) + hc * (COLS_PER_WARP / 2) + qi;
             }
-            if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
+            if (!warp_wait(g, bar(L::BAR_TFULL + item.i), item.ph)) {
                 ok = false;
                 break;
             }
@@ -652,7 +677,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
-                            mbar_arrive(bar(BAR_TEMPTY + item.i));
+                            mbar_arrive(bar(L::BAR_TEMPTY + item.i));
                         item.next();
                     }
 #pragma unroll
@@ -672,7 +697,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
             if (!min_item) {
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(BAR_SBEMPTY + sb.i));
+                    mbar_arrive(bar(L::BAR_SBEMPTY + sb.i));
                 sb.next();
             }
         }
@@ -716,13 +741,55 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
     }
 }
 
+// Barrier set-up, TMEM, the roles, TMEM release, for one shared-memory plan.
+template <int TYPE, int TILES>
+__device__ __forceinline__ void sb_body(const SbArgs& g, uint8_t* smem, uint32_t sbase, int warp, int lane)
+{
+    using L = SbL<TILES>;
+    auto bar = [&](int i) -> uint32_t { return sbase + L::SMEM_BAR + 8u * static_cast<uint32_t>(i); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::STAGES; ++s) {
+            mbar_init(bar(L::BAR_FULL + s), 1);
+            mbar_init(bar(L::BAR_FULLB + s), 1);
+            mbar_init(bar(L::BAR_CONV + s), NUM_CONV_WARPS);
+            mbar_init(bar(L::BAR_EMPTY + s), 1);
+        }
+        for (int s = 0; s < SBR; ++s) {
+            mbar_init(bar(L::BAR_SBFULL + s), 1);
+            mbar_init(bar(L::BAR_SBEMPTY + s), NUM_CONV_WARPS + NUM_PROMO_WARPS);
+            mbar_init(bar(L::BAR_IPREADY + s), NUM_CONV_WARPS);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bar(L::BAR_TFULL + k), 1);
+            mbar_init(bar(L::BAR_TEMPTY + k), NUM_PROMO_WARPS);
+        }
+        mbar_init(bar(L::BAR_DRAIN), 1);
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::SMEM_TMEMPTR, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::SMEM_TMEMPTR);
+
+    sb_roles<TYPE, TILES>(g, smem, sbase, tmem_base, warp, lane);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 template <int TYPE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_sb_kernel(const SbArgs g)
 {
-    // q6_K codes without the folded sub-block scale (some |sc| > 64) are left to the
-    // chunk-granular kernel, launched after this one; the flag is uniform.
-    if (TYPE == 14 && __ldg(g.FLAG) == 0u)
-        return;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -730,44 +797,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_sb_kernel(const SbArgs g)
     const uint32_t sbase = raw_addr + pad;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    auto bar = [&](int i) -> uint32_t { return sbase + SMEM_BAR + 8u * static_cast<uint32_t>(i); };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(BAR_FULL + s), 1);
-            mbar_init(bar(BAR_FULLB + s), 1);
-            mbar_init(bar(BAR_CONV + s), NUM_CONV_WARPS);
-            mbar_init(bar(BAR_EMPTY + s), 1);
-        }
-        for (int s = 0; s < SBR; ++s) {
-            mbar_init(bar(BAR_SBFULL + s), 1);
-            mbar_init(bar(BAR_SBEMPTY + s), NUM_CONV_WARPS + NUM_PROMO_WARPS);
-            mbar_init(bar(BAR_IPREADY + s), NUM_CONV_WARPS);
-        }
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(bar(BAR_TFULL + k), 1);
-            mbar_init(bar(BAR_TEMPTY + k), NUM_PROMO_WARPS);
-        }
-        mbar_init(bar(BAR_DRAIN), 1);
-        fence_barrier_init();
-        fence_proxy_async_smem();
-    }
-    if (warp == 1) {
-        tmem_alloc(sbase + SMEM_TMEMPTR, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + SMEM_TMEMPTR);
-
-    sb_roles<TYPE>(g, smem, sbase, tmem_base, warp, lane);
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (TYPE == 14) {
+        // q6_K codes hold sc*q in one tile unless some |sc| > 64 (then two exact tiles);
+        // the repack recorded which in the flag word (uniform for the launch).
+        if (__ldg(g.FLAG) != 0u)
+            sb_body<14, 1>(g, smem, sbase, warp, lane);
+        else
+            sb_body<14, 2>(g, smem, sbase, warp, lane);
+    } else {
+        sb_body<12, 1>(g, smem, sbase, warp, lane);
     }
 }
 
@@ -827,6 +865,7 @@ cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const v
     a.AS = sc + ap.pair_off;
     a.AM = sc + ap.am_off;
     a.B = pk + wp.code_off;
+    a.B2 = pk + wp.code2_off;
     a.SBD = pk + wp.sbd_off;
     a.AUX = pk + wp.aux_off;
     a.FLAG = reinterpret_cast<const unsigned int*>(pk + wp.flag_off);

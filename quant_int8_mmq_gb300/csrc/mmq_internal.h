@@ -121,6 +121,7 @@ struct WeightPlanes {    // layout of mmq_pack_weights' output
     size_t cw_off, cw_bytes;       // compact codes [row tile][k-block][word][128][16 B]
     size_t sc_off, sc_bytes;       // sub-block scales [row tile][super-block][128][16 B]
     size_t dm_off, dm_bytes;       // q4_K: f32 dmin per (row, super-block) [row tile][super-block][128]; q6_K: 0
+    size_t code2_off, code2_bytes; // q6_K: second f16 tile 16*sc*(h-2) of unfolded codes (zero when folded); q4_K: 0
     size_t total;
 };
 inline WeightPlanes weight_planes(int type, int od, int id)
@@ -146,7 +147,9 @@ inline WeightPlanes weight_planes(int type, int od, int id)
     w.sc_bytes = Np * nsb * SC_ROW_BYTES;
     w.dm_off = w.sc_off + w.sc_bytes;
     w.dm_bytes = type == 12 ? Np * nsb * 4 : 0;
-    w.total = w.dm_off + w.dm_bytes;
+    w.code2_off = w.dm_off + w.dm_bytes;
+    w.code2_bytes = type == 14 ? Np * static_cast<size_t>(id) * 2 : 0;
+    w.total = w.code2_off + w.code2_bytes;
     return w;
 }
 

@@ -3,11 +3,13 @@
 // Raw q6_K / q4_K super-blocks -> the planes the GEMM streams (rows >= od zero):
 //  codes  f16 integer codes in the tensor-core operand tile layout (128 weight
 //         rows x 64 values, 128-byte swizzle) with the integer sub-block scale
-//         folded in where the product stays an exact f16 integer:
-//           q4_K: sc_c * q  (|.| <= 63 * 15 = 945, always folded)
-//           q6_K: sc * q    when every |sc| of the tensor is <= 64 (|.| <= 2048),
-//                 else the plain code q (the GEMM then keeps one accumulator per
-//                 16-value sub-block)
+//         folded in, exactly:
+//           q4_K: sc_c * q  (|.| <= 63 * 15 = 945)
+//           q6_K: sc * q    when every |sc| of the tensor is <= 64 (|.| <= 2048);
+//                 else sc * l, l the low 4 bits of q + 32 (|.| <= 1920), and
+//  codes2 (q6_K) the second tile 16 * sc * (h - 2), h the high 2 bits of q + 32
+//         (a multiple of 16 of magnitude <= 4096, exact), so that
+//         codes + codes2 = sc * (l + 16 (h - 2)) = sc * q; zero when folded
 //  pairs  tile-major f32 scale pairs per (row, chunk), built the way the W_dsc
 //         plane is ("r56 - q6_K A-side bundle ...", §2.2 and §2.3): exact f16 -> f32
 //         and int -> f32 conversions and exactly one f32 multiply (__fmul_rn, never
@@ -109,7 +111,8 @@ __global__ void q6k_scale_scan(const RawRows raw, long long nblocks, unsigned in
 
 template <int TYPE>
 __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, int id, int Np,
-                                                   uint8_t* __restrict__ codes, float2* __restrict__ pairs,
+                                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ codes2,
+                                                   float2* __restrict__ pairs,
                                                    float* __restrict__ sbd, uint8_t* __restrict__ aux,
                                                    float* __restrict__ dm, unsigned int* __restrict__ flag)
 {
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
         const int sb = c >> 3;
         const int nt = j / TILE_ROWS, r = j % TILE_ROWS;
         uint32_t h2[16];            // 32 codes as 16 f16 pairs
+        uint32_t g2[16];            // q6_K second tile (zero unless unfolded)
         float2 w = make_float2(0.0f, 0.0f);
         if (j < od) {
             if (TYPE == 14) {  // q6_K
@@ -141,14 +145,17 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
                     const int e0 = 2 * p, e1 = 2 * p + 1;  // values 32cc+e0, 32cc+e1
                     const unsigned lo = ql[p];
                     const unsigned hb = qh[p >> 1];
-                    int u0 = static_cast<int>((lo & 15u) | (((hb >> (2 * (e0 & 3))) & 3u) << 4)) - 32;
-                    int u1 = static_cast<int>((lo >> 4) | (((hb >> (2 * (e1 & 3))) & 3u) << 4)) - 32;
+                    const int l0 = static_cast<int>(lo & 15u), l1 = static_cast<int>(lo >> 4);
+                    const int hh0 = static_cast<int>((hb >> (2 * (e0 & 3))) & 3u);
+                    const int hh1 = static_cast<int>((hb >> (2 * (e1 & 3))) & 3u);
+                    const int sc = p < 8 ? s0 : s1;  // values 0..15 of the chunk use s0
                     if (fold) {
-                        const int sc = p < 8 ? s0 : s1;  // values 0..15 of the chunk use s0
-                        u0 *= sc;
-                        u1 *= sc;
+                        h2[p] = half2_bits(sc * (l0 + 16 * hh0 - 32), sc * (l1 + 16 * hh1 - 32));
+                        g2[p] = 0u;
+                    } else {
+                        h2[p] = half2_bits(sc * l0, sc * l1);
+                        g2[p] = half2_bits(16 * sc * (hh0 - 2), 16 * sc * (hh1 - 2));
                     }
-                    h2[p] = half2_bits(u0, u1);
                 }
                 const float d = load_f16_bytes(b + 208);
                 w = make_float2(__fmul_rn(d, static_cast<float>(s0)), __fmul_rn(d, static_cast<float>(s1)));
@@ -168,6 +175,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
                 for (int p = 0; p < 16; ++p) {
                     const unsigned v = qs[p];
                     h2[p] = half2_bits(sc * static_cast<int>(v & 15u), sc * static_cast<int>(v >> 4));
+                    g2[p] = 0u;
                 }
                 const float d = load_f16_bytes(b + 0);
                 const float dmin = load_f16_bytes(b + 2);
@@ -186,7 +194,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
         } else {
 #pragma unroll
             for (int p = 0; p < 16; ++p)
-                h2[p] = 0u;
+                h2[p] = g2[p] = 0u;
             if (cc == 0)
                 sbd[(static_cast<size_t>(nt) * nsb + sb) * TILE_ROWS + r] = 0.0f;
             if (TYPE == 14) {
@@ -210,6 +218,13 @@ __global__ void __launch_bounds__(256) pack_kernel(const RawRows raw, int od, in
         for (int u = 0; u < 4; ++u)  // four 16-byte units of 8 codes each
             *reinterpret_cast<uint4*>(tile + tile_byte(r, k0 + 8 * u)) =
                 make_uint4(h2[4 * u], h2[4 * u + 1], h2[4 * u + 2], h2[4 * u + 3]);
+        if (TYPE == 14) {
+            uint8_t* tile2 = codes2 + (static_cast<size_t>(nt) * nkb + kb) * TILE_BYTES;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(tile2 + tile_byte(r, k0 + 8 * u)) =
+                    make_uint4(g2[4 * u], g2[4 * u + 1], g2[4 * u + 2], g2[4 * u + 3]);
+        }
         pairs[(static_cast<size_t>(nt) * nchunk + c) * TILE_ROWS + r] = w;
     }
 }
@@ -359,12 +374,13 @@ cudaError_t launch_pack(int type, const void* raw_a, int od_a, const void* raw_b
         count_launch();
         q6k_scale_scan<<<static_cast<unsigned>(sblocks), 256, 0, s>>>(rb, nblocks, flag);
         count_launch();
-        pack_kernel<14><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
-                                                                        sbd, base + wp.aux_off, nullptr, flag);
+        pack_kernel<14><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off,
+                                                                        base + wp.code2_off, pairs, sbd,
+                                                                        base + wp.aux_off, nullptr, flag);
     } else {
         count_launch();
-        pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, pairs,
-                                                                        sbd, base + wp.aux_off,
+        pack_kernel<12><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rb, od, id, Np, base + wp.code_off, nullptr,
+                                                                        pairs, sbd, base + wp.aux_off,
                                                                         reinterpret_cast<float*>(base + wp.dm_off),
                                                                         flag);
     }

@@ -69,8 +69,9 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
         assert L["cw"] == (-(-sum(L["raw"]) // 256) * 256, (Np // 128) * 16 * words * 128 * 16)
         assert L["sc"] == (sum(L["cw"]), Np * nsb * 16)
         assert L["dm"] == (sum(L["sc"]), Np * nsb * 4 if t == mmq.MMQ_Q4_K else 0)
+        assert L["codes2"] == (sum(L["dm"]), Np * 1024 * 2 if t == mmq.MMQ_Q6_K else 0)
         assert all(off % 16 == 0 for off, _ in L.values())
-        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["dm"])
+        assert mmq.mmq_packed_weight_bytes(t, 4097, 1024) == sum(L["codes2"])
 
 
 @pytest.mark.parametrize("M,K,err", [(0, 256, 2), (1, 255, 2), (1, 0, 2), (5, 300, 2), (1 << 23, 256, 2)])

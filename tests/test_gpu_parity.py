@@ -229,7 +229,7 @@ def test_pack_planes_byte_exact(typ, od, id_):
     pk = packed.cpu().numpy()
     tid = mmq.TYPES[t]
     L = mmq.mmq_packed_weight_layout(tid, od, id_)
-    assert pk.size == sum(L["dm"])
+    assert pk.size == sum(L["codes2"])
     Np, nsb, nchunk = padded(od), id_ // 256, id_ // 32
     part = {k: pk[o:o + n] for k, (o, n) in L.items()}
     codes = untile_codes(part["codes"], Np, id_)
@@ -244,7 +244,15 @@ def test_pack_planes_byte_exact(typ, od, id_):
         flag = part["flag"].view(np.uint32)
         assert flag[0] == int(folded) and flag[1] == maxsc
         assert folded == (typ == "q6_K")
-        want_codes = q * scale_e if folded else q
+        # two exact tiles when unfolded: sc * l and 16 * sc * (h - 2), l and h the low 4
+        # and high 2 bits of q + 32
+        l, h = (q + 32) & 15, (q + 32) >> 4
+        want_codes = q * scale_e if folded else scale_e * l
+        want_codes2 = np.zeros_like(q) if folded else 16 * scale_e * (h - 2)
+        codes2 = untile_codes(part["codes2"], Np, id_)
+        assert np.array_equal(codes2[:od], want_codes2) and not codes2[od:].any()
+        if not folded:       # the two tiles add up to the folded code sc * q
+            assert np.array_equal(codes[:od] + codes2[:od], q * scale_e)
         dsc = oracle.scale_planes_q6k(raw)
         wa, wb = dsc[..., 0], dsc[..., 1]
         # sub-block scales as f32, [row tile][sb][16][128]
@@ -366,13 +374,14 @@ def test_gemm_dots_bit_exact(typ, M, od, id_):
     else:
         I = oracle.dots_q6k(raw, q).astype(np.int64)                       # [M, od, 2*nchunk]
         _, scf = oracle.fields_q6k(raw)
-        if typ == "q6_K":                                                  # folded: sc0*I0 + sc1*I1
+        if typ == "q6_K":                                                  # one tile: sc0*I0 + sc1*I1
             s16 = scf.reshape(od, 2 * nchunk).astype(np.int64)[None]
             want = (I * s16).reshape(M, od, nchunk, 2).sum(-1)
             got = got[: M * od * nchunk].reshape(M, od, nchunk)
-        else:                                                              # plain codes: per sub-block
-            want = I
-            got = got.reshape(M, od, 2 * nchunk)
+        else:                                                              # two exact tiles: the same sums
+            s16 = scf.reshape(od, 2 * nchunk).astype(np.int64)[None]
+            want = (I * s16).reshape(M, od, nchunk, 2).sum(-1)
+            got = got[: M * od * nchunk].reshape(M, od, nchunk)
     assert np.array_equal(got, want.astype(np.float64))
 
 
@@ -512,15 +521,14 @@ def test_gemm_deterministic(y_kernel):
 def test_gemm_last_round_split_parity(typ):
     """Super-block kernel: 8 x 20 = 160 tiles of 128 x 256 on 152 SMs, the 8 tiles of the
     last round run as two K-halves that add into a zeroed Y (odd super-block count:
-    halves of 1 and 2); ragged od (last tile 236 rows).  q6_K_full (plain codes) takes
-    the chunk kernel: 8 x 40 = 320 tiles of 128 x 128, 16 split."""
+    halves of 1 and 2); ragged od (last tile 236 rows); q6_K_full runs its two exact
+    tiles per k-block."""
     t = "q6_K" if typ.startswith("q6_K") else typ
     M, od, id_ = 1024, 5100, 768
     raw = _q6_raw(od, id_, 41, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, 41)
     x = synth.activations(M, id_, 42)
     Y = _run_gemm(t, raw, x).cpu().numpy()
-    want = "chunk GEMM on plain codes" if typ == "q6_K_full" else "super-block"
-    assert want in mmq.mmq_last_path()
+    assert "super-block" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
 
@@ -593,8 +601,8 @@ def chunk_kernel():
     ("q4_K", 40, 200, 256),       # one super-block per row
 ])
 def test_gemm_chunk_kernel_y_parity(chunk_kernel, typ, M, od, id_):
-    """Y from the chunk-granular kernel (every case when selected; otherwise it serves
-    plain-code q6_K only)."""
+    """Y from the chunk-granular kernel (every case when selected; otherwise the tile
+    counts too small for the super-block kernel)."""
     raw = _raw(typ, od, id_, seed=od + M)
     x = synth.activations(M, id_, seed=M + 5)
     Y = _run_gemm(typ, raw, x).cpu().numpy()
@@ -604,8 +612,8 @@ def test_gemm_chunk_kernel_y_parity(chunk_kernel, typ, M, od, id_):
 
 
 @pytest.mark.parametrize("M,od,id_", [(40, 300, 768), (31, 4097, 1024)])
-def test_gemm_chunk_kernel_plain_q6k_all_tiles_split(chunk_kernel, M, od, id_):
-    """Plain-code q6_K (|sc| up to 127) on the chunk kernel with few tiles: every tile
+def test_gemm_chunk_kernel_two_tile_q6k_all_tiles_split(chunk_kernel, M, od, id_):
+    """Two-tile q6_K (|sc| up to 128) on the chunk kernel with few tiles: every tile
     runs as two K-halves added into a zeroed Y."""
     raw = _q6_raw(od, id_, od + 3, True)
     x = synth.activations(M, id_, seed=M + 6)
