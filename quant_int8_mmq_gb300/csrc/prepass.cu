@@ -39,20 +39,76 @@ __device__ __forceinline__ float quant_one(float x, float d)
     return fminf(fmaxf(r, -127.0f), 127.0f) + 0.0f;    // + 0: code 0 is +0, never -0
 }
 
-// The same quotient with the chunk's divisor shared: rd = 1/d correctly rounded
-// (once per chunk), then Markstein's correction step (P. Markstein, "Computation of
-// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
-// 1990): q0 = RN(x * rd) is within one ulp of x/d, e = x - d * q0 is exact as one
-// FMA, and RN(q0 + e * rd) is the correctly rounded quotient RN(x/d) when rd =
-// RN(1/d) and nothing overflows or underflows, which the caller guarantees by using
-// this only for d in [2^-100, 2^100].  The rounding to an integer is unchanged, and
-// no clamp is needed: for finite x with |x| <= amax and d = RN(amax/127) normal,
-// |x/d| <= 127 (1 + 2^-23), so RN(x/d) rounds to at most 127 in magnitude.
-__device__ __forceinline__ float quant_one_shared(float x, float d, float rd)
+// Packed pairs of f32 (the f32x2 arithmetic of sm_100-class SMs: one instruction for two
+// IEEE round-to-nearest operations, each rounded as its scalar form would be).
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
 {
-    const float q0 = __fmul_rn(x, rd);
-    const float e = __fmaf_rn(-q0, d, x);
-    return roundf(__fmaf_rn(e, rd, q0)) + 0.0f;        // + 0: code 0 is +0, never -0
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+// Round half away from zero of |y| < 2^23 as trunc(y + sign(y) * (1/2 - 2^-25)): below a
+// tie the sum stays under the next integer (its distance to it is at least one ulp of y
+// plus 2^-25, while the rounding moves it by at most half an ulp), at a tie or above it
+// reaches the next integer (n + 1 - 2^-25 rounds up, to even at n + 1 = 1), and the
+// truncation then gives the rounded value; -0 is left as -0.
+__device__ __forceinline__ float round_away_small(float y)
+{
+    const float c = __uint_as_float((__float_as_uint(y) & 0x80000000u) | 0x3EFFFFFFu);
+    return truncf(__fadd_rn(y, c));
+}
+
+// Eight codes of one chunk with the chunk's divisor shared, two values per instruction:
+// rd = 1/d correctly rounded (once per chunk), then Markstein's correction step (P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34, 1990): q0 = RN(x * rd) is within one ulp of x/d,
+// e = x - d * q0 is exact as one FMA, and RN(q0 + e * rd) is the correctly rounded
+// quotient RN(x/d) when rd = RN(1/d) and nothing overflows or underflows, which the
+// caller guarantees by using this only for d in [2^-100, 2^100].  No clamp is needed:
+// for finite x with |x| <= amax and d = RN(amax/127) normal, |x/d| <= 127 (1 + 2^-23),
+// so the rounded quotient is at most 127 in magnitude.  q is left as integer-valued
+// floats with code 0 as +0.
+__device__ __forceinline__ void quant8_shared(const float (&v)[8], float d, float rd, float (&q)[8])
+{
+    const uint64_t rd2 = f2_pack(rd, rd), nd2 = f2_pack(-d, -d), zero2 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint64_t x2 = f2_pack(v[2 * i], v[2 * i + 1]);
+        const uint64_t q0 = f2_mul(x2, rd2);
+        const uint64_t e = f2_fma(q0, nd2, x2);       // x - d * q0, exact
+        const uint64_t y = f2_fma(e, rd2, q0);        // RN(x / d)
+        const uint64_t r = f2_add(f2_pack(round_away_small(f2_lo(y)), round_away_small(f2_hi(y))), zero2);
+        q[2 * i] = f2_lo(r);
+        q[2 * i + 1] = f2_hi(r);
+    }
+}
+
+// Sum of eight integer-valued floats (exact: |sum| <= 1016).
+__device__ __forceinline__ float sum8(const float (&q)[8])
+{
+    const uint64_t a = f2_add(f2_pack(q[0], q[1]), f2_pack(q[2], q[3]));
+    const uint64_t b = f2_add(f2_pack(q[4], q[5]), f2_pack(q[6], q[7]));
+    const uint64_t c = f2_add(a, b);
+    return __fadd_rn(f2_lo(c), f2_hi(c));
 }
 
 __device__ __forceinline__ float tf32_rna(float v)
@@ -162,9 +218,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
             // evaluated next to the shared-reciprocal one)
             float q[8];
             if (shared) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    q[i] = quant_one_shared(v[i], d, rd);
+                quant8_shared(v, d, rd, q);
             } else if (d != 0.0f) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -174,10 +228,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                 for (int i = 0; i < 8; ++i)
                     q[i] = 0.0f;
             }
-            float sf = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                sf += q[i];
+            float sf = sum8(q);
             sf += __shfl_xor_sync(0xffffffffu, sf, 1);
             sf += __shfl_xor_sync(0xffffffffu, sf, 2);
             const int s = static_cast<int>(sf);
