@@ -698,6 +698,23 @@ def test_gemm_few_token_stack_shapes(typ, M, od, id_, split):
     assert_y_close(Y, Yr.astype(np.float64), S)
 
 
+@pytest.mark.parametrize("M,od,id_", [(24, 32001, 512), (32, 20000, 256)])
+def test_gemm_few_token_min_term_across_units(M, od, id_):
+    """q4_K at N = 32 (min term on the tensor core, one TMEM accumulator per issuer per
+    unit): more weight tiles than SMs, so CTAs take several units in turn and each
+    accumulator is handed back by the promotion before the next unit overwrites it;
+    with id = 256 every unit is one super-block and the units of a CTA alternate
+    between the two issuers.  Bit-identical run to run."""
+    raw = synth.q4k_blocks(od, id_, M + od)
+    x = synth.activations(M, id_, M + 3)
+    Y = _run_gemm("q4_K", raw, x).cpu().numpy()
+    assert "few-token GEMM" in mmq.mmq_last_path() and "K split: none" in mmq.mmq_last_path()
+    Yo, S = oracle_gemm("q4_K", raw, x)
+    assert_y_close(Y, Yo, S)
+    Y2 = _run_gemm("q4_K", raw, x).cpu().numpy()
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+
+
 def test_gemm_few_token_row_stride_unaligned():
     typ, M, od, id_ = "q4_K", 27, 203, 512
     raw = _raw(typ, od, id_, seed=25)
