@@ -235,19 +235,24 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  * the same (type, od, id); qa/scales from mmq_quantize_act with K = id and the
  * same M.  Four kernels compute it (mmq_last_path names the one launched;
  * mmq_debug_select_large_m_kernel can force a choice):
- *  - M <= MMQ_SMALL_M (decode and tail shapes), the weight-streaming kernel: the
+ *  - M <= MMQ_SMALL_M (decode and tail shapes), the weight-streaming kernel,
+ *    except where the few-token kernel below is faster (measured crossovers,
+ *    w = od*id: q4_K with w >= 2^24 and M >= 7, or w >= 2^25 and M >= 6; q6_K
+ *    with w >= 2^25 and M = 8, or w >= 3*2^25 and M >= 6): the
  *    RAW plane and the int8 activation plane, exact integer dots on the CUDA
  *    cores (dp4a), and the scales applied per chunk in the formula's own order
  *    (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=
  *    d_a*(d*sc0*I_0 + d*sc1*I_1)), with a fixed reduction order;
- *  - MMQ_SMALL_M < M <= MMQ_FT_MAX_M, the few-token kernel: the CW codes are
+ *  - otherwise for M <= MMQ_FT_MAX_M, the few-token kernel: the CW codes are
  *    widened to exact f16 integers (q4_K sc*q; q6_K sc*q when FLAG says every
  *    |scales[i]| <= 64, else the two exact tiles sc*l/4 and 4*sc*(h-2), l and h
  *    the low 4 and high 2 bits of q + 32) in tensor memory and contracted on
  *    tcgen05 against the tq operand (f16 hi and lo of p*d_a*q_a as one 2N-row
  *    operand), one f32 accumulator per stage, then d and 1/p applied per
- *    super-block; the q4_K min term sum_c (dmin*m_c)*(d_a*ssum) in f32 FMAs from
- *    DM, SC and fm; when the weight tiles are few, each is split along K over a
+ *    super-block; the q4_K min term sum_c (dmin*m_c)*(d_a*ssum) from DM, SC and,
+ *    for 17 <= M <= 32, the am plane as a tf32 hi/lo tensor-core contraction
+ *    (dmin*m_c split exactly in the kernel; hi*hi + hi*lo + lo*hi), else from fm
+ *    in f32 FMAs; when the weight tiles are few, each is split along K over a
  *    cluster of up to 8 CTAs whose partial sums are added in rank order
  *    (deterministic);
  *  - larger M, the super-block kernel (when its 128 x 256 tiles number at least

@@ -129,6 +129,22 @@ mmq_status check_weight_shape(mmq_type t, int od, int id)
     return MMQ_OK;
 }
 
+// Token counts up to MMQ_SMALL_M go to the weight-streaming kernel, whose cost grows with
+// M (its integer dots are issue-bound), unless the weight is large enough that the
+// few-token kernel, whose cost hardly depends on M, is faster.  The crossovers were
+// measured on GB300 over q4_K 4096x4096 / 11008x4096 and q6_K 4096x4096 / 4097x11008 /
+// 32000x4096 at M = 2..8.
+bool takes_streaming_path(mmq_type t, int od, int id, int M)
+{
+    if (M > mmq::SMALL_M)
+        return false;
+    const long long w = static_cast<long long>(od) * id;
+    constexpr long long W24 = 1ll << 24, W25 = 1ll << 25;
+    if (t == MMQ_Q4_K)
+        return !(w >= W24 && (M >= 7 || (M >= 6 && w >= W25)));
+    return !((w >= W25 && M >= 8) || (w >= 3 * W25 && M >= 6));
+}
+
 mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int od, int id, const void* qa,
                        const void* scales, int M, float* out, int ldy, mmq_stream_t s)
 {
@@ -148,7 +164,7 @@ mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int o
         return st;
     const char* label = nullptr;
     const cudaError_t e =
-        (mode == mmq::GEMM_Y && M <= mmq::SMALL_M && mmq::large_m_kernel() != 4)
+        (mode == mmq::GEMM_Y && takes_streaming_path(t, od, id, M) && mmq::large_m_kernel() != 4)
             ? mmq::launch_gemm_small(static_cast<int>(t), packed, od, id, qa, scales, M, out, ldy,
                                      reinterpret_cast<cudaStream_t>(s), &label)
             : mmq::launch_gemm(static_cast<int>(t), mode, packed, od, id, qa, scales, M, out, ldy,

@@ -790,12 +790,29 @@ def test_gemm_streaming_parity(typ, M, od, id_):
 
 @pytest.mark.parametrize("M", [8, 9])
 def test_gemm_streaming_boundary(M):
-    """M = 8 streams the weights, M = 9 takes the tile GEMM: both match the oracle."""
+    """M = 8 streams the weights (a small weight), M = 9 takes the tile GEMM: both match
+    the oracle."""
     raw = synth.q4k_blocks(257, 2048, 31)
     x = synth.activations(M, 2048, 32)
     Y = _run_gemm("q4_K", raw, x).cpu().numpy()
     assert ("weight-streaming" in mmq.mmq_last_path()) == (M <= mmq.SMALL_M)
     Yo, S = oracle_gemm("q4_K", raw, x)
+    assert_y_close(Y, Yo, S)
+
+
+@pytest.mark.parametrize("typ,od,id_,M,path", [
+    ("q4_K", 11008, 4096, 5, "weight-streaming"), ("q4_K", 11008, 4096, 6, "few-token GEMM"),
+    ("q4_K", 4096, 4096, 6, "weight-streaming"), ("q4_K", 4096, 4096, 7, "few-token GEMM"),
+    ("q6_K", 4097, 11008, 7, "weight-streaming"), ("q6_K", 4097, 11008, 8, "few-token GEMM")])
+def test_gemm_small_m_routing_at_the_crossovers(typ, od, id_, M, path):
+    """Up to 8 tokens the weight-streaming kernel runs unless the weight is large enough for
+    the few-token kernel to be faster (the header's measured crossovers): either way Y
+    matches the oracle at the full shape."""
+    raw = synth.blocks(typ, od, id_, M + 40)
+    x = synth.activations(M, id_, M + 41)
+    Y = _run_gemm(typ, raw, x).cpu().numpy()
+    assert path in mmq.mmq_last_path()
+    Yo, S = oracle_gemm(typ, raw, x)
     assert_y_close(Y, Yo, S)
 
 
