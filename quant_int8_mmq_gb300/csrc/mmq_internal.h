@@ -38,7 +38,7 @@ __host__ __device__ constexpr int tf32_tile_byte(int r, int k)
 }
 constexpr int TF32_TILE_BYTES = 128 * 8 * 4;
 
-// Token counts up to SMALL_M may take the weight-streaming path; for them the prepass
+// Token counts up to SMALL_M take the weight-streaming path; for them the prepass
 // also writes int8 codes, row-major, each group of 8 values stored in the order
 // (0,2,4,6,1,3,5,7) so that a word of low (or high) weight nibbles meets the four
 // activation codes it multiplies.
