@@ -937,8 +937,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
     if constexpr (TYPE == 12) {
         ft_body<12, NT, true>(g, smem, sbase, warp, lane);
     } else {
-        // the packed flag (registration-time data, uniform for the launch) says whether
-        // every sub-block scale fits the one-tile form
+        // the packed flag (uniform for the launch) says whether every sub-block scale
+        // fits the one-tile form; it is read only once the kernel ahead, which may be the
+        // repack that wrote it, has completed
+        grid_dep_wait();
         if (__ldg(g.FLAG) != 0u)
             ft_body<14, NT, true>(g, smem, sbase, warp, lane);
         else

@@ -777,6 +777,12 @@ __device__ __forceinline__ void sb_body(const SbArgs& g, uint8_t* smem, uint32_t
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + L::SMEM_TMEMPTR);
 
+    // A dependent launch: the set-up above may overlap the kernel ahead on the stream (the
+    // prepass that writes the activation planes, or a kernel still reading Y); nothing is
+    // read or written in global memory before it has completed.  The next kernel may be
+    // scheduled as this grid's CTAs finish.
+    grid_dep_wait();
+    grid_dep_launch();
     sb_roles<TYPE, TILES>(g, smem, sbase, tmem_base, warp, lane);
 
     tc_fence_before();
@@ -799,7 +805,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_sb_kernel(const SbArgs g)
     const int lane = threadIdx.x & 31;
     if constexpr (TYPE == 14) {
         // q6_K codes hold sc*q in one tile unless some |sc| > 64 (then two exact tiles);
-        // the repack recorded which in the flag word (uniform for the launch).
+        // the repack recorded which in the flag word (uniform for the launch).  The flag
+        // is read only once the kernel ahead, which may be the repack, has completed.
+        grid_dep_wait();
         if (__ldg(g.FLAG) != 0u)
             sb_body<14, 1>(g, smem, sbase, warp, lane);
         else
@@ -847,8 +855,8 @@ cudaError_t launch_sb_typed(const SbArgs& a, int grid, cudaStream_t s)
         attr_set_mask.fetch_or(bit);
     }
     count_launch();
-    gemm_sb_kernel<TYPE><<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent_smem(gemm_sb_kernel<TYPE>, dim3(static_cast<unsigned>(grid)), dim3(NUM_THREADS),
+                                 static_cast<size_t>(SMEM_ALLOC), s, a);
 }
 
 }  // namespace

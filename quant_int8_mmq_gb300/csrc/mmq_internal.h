@@ -185,7 +185,8 @@ void arm_wait_injection(int fill, unsigned long long limit_ns);
 // it touches memory that an earlier kernel may write (only an L2 prefetch may precede
 // the wait).  Returns the launch error.
 template <typename... P, typename... A>
-cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, cudaStream_t s, A&&... args)
+cudaError_t launch_dependent_smem(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                  A&&... args)
 {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -193,11 +194,16 @@ cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, cudaSt
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, cudaStream_t s, A&&... args)
+{
+    return launch_dependent_smem(kernel, grid, block, 0, s, std::forward<A>(args)...);
 }
 
 // Each returns cudaSuccess or the launch error; arguments are already validated.

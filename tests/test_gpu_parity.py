@@ -550,6 +550,47 @@ def test_gemm_third_round_halves_parity(typ):
     assert np.array_equal(Y.view(np.uint32), again.view(np.uint32))
 
 
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
+def test_superblock_back_to_back_calls_share_buffers(typ):
+    """Prepass and super-block GEMM calls queued on one stream with no synchronisation in
+    between, all through the same activation planes, and the last two GEMMs writing the
+    same Y.  Both are dependent launches: a GEMM's set-up overlaps the prepass ahead of
+    it, a prepass may start while the GEMM ahead still runs.  Each result must still be
+    the oracle's for its own inputs (no prepass overwrites planes a GEMM still reads, no
+    GEMM reads planes before its prepass wrote them, the later Y is the one left).  The
+    second weight is packed right before its first GEMM, so the flag and planes a GEMM
+    reads come from the kernel just ahead of it there."""
+    od, id_ = 4096, 512
+    raws = [_raw(typ, od, id_, seed=930 + i) for i in range(2)]
+    Ms = [1300, 1420, 1290, 1350]
+    xs = [synth.activations(M, id_, seed=940 + i) for i, M in enumerate(Ms)]
+    xd = [_to_dev(x) for x in xs]
+    qb, sb = mmq.mmq_act_plane_bytes(max(Ms), id_)
+    qa = torch.empty(qb, dtype=torch.uint8, device=DEV)
+    sc = torch.empty(sb, dtype=torch.uint8, device=DEV)
+    shared = torch.full((max(Ms), od), float("nan"), dtype=torch.float32, device=DEV)
+    packs = [gpu_pack(typ, raws[0]), None]
+    _sync()
+    outs = []
+    for i, x in enumerate(xd):
+        M = x.shape[0]
+        mmq.quantize_act(x, qa, sc)
+        if packs[i % 2] is None:
+            packs[i % 2] = gpu_pack(typ, raws[i % 2])
+        Y = shared[:M] if i >= len(xd) - 2 else None
+        outs.append(mmq.gemm(typ, packs[i % 2], od, id_, qa, sc, M, Y=Y))
+        assert "super-block" in mmq.mmq_last_path()
+    _sync()
+    assert mmq.mmq_get_device_error() == 0
+    for i, (x, Y) in enumerate(zip(xs, outs)):
+        if i == len(xs) - 2:
+            continue   # overwritten by the last call
+        Yo, S = oracle_gemm(typ, raws[i % 2], x)
+        assert_y_close(Y.cpu().numpy(), Yo, S)
+    # rows past the last two calls' M were never written
+    assert np.isnan(shared[max(Ms[-2:]):].cpu().numpy()).all()
+
+
 def test_gemm_last_round_split_deterministic():
     raw = synth.q4k_blocks(5100, 512, 43)
     x = synth.activations(1024, 512, 44)
