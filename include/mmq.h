@@ -164,13 +164,13 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  *          blocks, row-major: q4_K 144 B [qs[128] | d | dmin | scales[12]],
  *          q6_K 224 B [ql[128] | qh[64] | scales[16] | d | 14 zero bytes].
  *   CW     compact codes for the few-token GEMM, which widens them to f16 in
- *          tensor memory: per (nt, kb) W = 2 (q4_K) or 3 (q6_K) words of 16 bytes
+ *          tensor memory: per (nt, kb) W = 2 (q4_K) or 4 (q6_K) words of 16 bytes
  *          per row, word-major: word w of row r at ((nt*nkb + kb)*W + w)*2048 + r*16.
- *          Words 0, 1 hold chunk 2*kb + w: the 4-bit code (q4_K) or the low 4 bits
- *          of q + 32 (q6_K) of value 8u + 2p + h of the chunk (u, p = 0..3, h = 0,1)
- *          at bit 4p + 16h of its 32-bit word u.  q6_K word 2 holds the high 2 bits
- *          of q + 32: chunk hc (0, 1) in its 32-bit words 2hc and 2hc + 1, value
- *          8u + 2p + h of the chunk in word 2hc + u/2 at bit 8(u%2) + 2p + 16h.
+ *          q4_K: word w holds chunk 2*kb + w, the 4-bit code of value 8u + 2p + h
+ *          of the chunk (u, p = 0..3, h = 0,1) at bit 4p + 16h of its 32-bit word u.
+ *          q6_K: word w holds the 16 values of sub-block w of the k-block, one byte
+ *          4*(q + 32) each, value 4u + o (u, o = 0..3) at byte 2*(o & 1) + (o >> 1)
+ *          of its 32-bit word u.
  *   SC     sub-block scales per (nt, sb): 16 bytes per row at ((nt*nsb + sb)*128 + r)*16:
  *          q4_K the six-bit sc_0..sc_7 then m_0..m_7, one per byte; q6_K scales[16].
  *   DM     q4_K: f32 dmin per (row, super-block) at index ((j/128)*nsb + sb)*128 + j%128
@@ -238,7 +238,7 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *  - M <= MMQ_SMALL_M (decode and tail shapes), the weight-streaming kernel,
  *    except where the few-token kernel below is faster (measured crossovers,
  *    w = od*id: q4_K with w >= 2^24 and M >= 7, or w >= 2^25 and M >= 6; q6_K
- *    with w >= 2^25 and M = 8, or w >= 3*2^25 and M >= 6): the
+ *    with w >= 2^25 and M >= 6, or w >= 3*2^25 and M >= 5): the
  *    RAW plane and the int8 activation plane, exact integer dots on the CUDA
  *    cores (dp4a), and the scales applied per chunk in the formula's own order
  *    (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=

@@ -142,7 +142,7 @@ bool takes_streaming_path(mmq_type t, int od, int id, int M)
     constexpr long long W24 = 1ll << 24, W25 = 1ll << 25;
     if (t == MMQ_Q4_K)
         return !(w >= W24 && (M >= 7 || (M >= 6 && w >= W25)));
-    return !((w >= W25 && M >= 8) || (w >= 3 * W25 && M >= 6));
+    return !((w >= W25 && M >= 6) || (w >= 3 * W25 && M >= 5));
 }
 
 mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int od, int id, const void* qa,

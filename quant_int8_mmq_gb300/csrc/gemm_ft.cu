@@ -15,10 +15,11 @@
 // W is the integer-scaled weight code, exact in f16:
 //   q4_K: W = sc_c * q                           (|W| <= 945, one tile)
 //   q6_K whose every |sc| <= 64 (the packed flag says so):
-//         W = sc * q = sc * l + 16 sc (h - 2)    (|W| <= 2048, one tile; l, h the low 4
-//         and high 2 bits of q + 32, each term exact and so is their f16 sum)
+//         W = sc * q                             (|W| <= 2048, one tile, one fma from
+//         1024 + 4 (q + 32))
 //   q6_K otherwise:
-//         W = (sc * l) / 4  +  4 * sc * (h - 2)  (two tiles; sc * l / 4 is a quarter-integer
+//         W = (sc * l) / 4  +  4 * sc * (h - 2)  (two tiles, l and h the low 4 and high 2
+//         bits of q + 32; sc * l / 4 is a quarter-integer
 //         below 480 in magnitude and 4 sc (h - 2) an integer of at most 1024, both exact
 //         for any int8 sc), so the sum of the two tiles is sc * q / 4 and the promotion
 //         uses 4/p.
@@ -32,8 +33,9 @@
 // issuer for the whole unit.  Otherwise the promotion threads take it on the CUDA
 // cores (8 f32 FMAs per token and super-block).
 //
-// The weights come from the compact code plane (0.5 B per value for q4_K, 0.75 for
-// q6_K) and are widened to f16 by converter warps, the unpacking of "r56 - q6_K A-side
+// The weights come from the compact code plane (0.5 B per value for q4_K, 1 for q6_K:
+// one byte 4 (q + 32), which a mask alone puts under the exponent) and are widened to
+// f16 by converter warps, the unpacking of "r56 - q6_K A-side
 // bundle ..." §1 / "r58 - q4_K BT spec ..." §3.2 done in the GEMM instead of at
 // registration.  Each f16 pair comes from one 32-bit word with a mask, an OR of the
 // exponent of 1024 (0x6400, so the field lands in the mantissa: 1024 + field) and one
@@ -281,23 +283,35 @@ __device__ __forceinline__ uint4 widen_q4(uint32_t x, __half2 c1, __half2 a1, __
     return o;
 }
 
-// q6_K tile A: (sc * l) / 4 of one unit from the nibble word (l = low 4 bits of q + 32):
-// fma(1024 + l, sc/4, -256 sc) and fma(1024 + 16 l, sc/64, -16 sc).
-__device__ __forceinline__ uint4 widen_q6_lo(uint32_t x, __half2 c1, __half2 a1, __half2 c16, __half2 a16)
+// q6_K, one sub-block word x (16 values, byte 4 (q + 32) each, values 4u + {0, 1} at
+// bytes 0, 2 and 4u + {2, 3} at bytes 1, 3 of 32-bit word u): the mask puts 4 (q + 32)
+// under the exponent of 1024, so each f16 lane is 1024 + 4 (q + 32), exactly.
+//   one tile (every |sc| <= 64): fma(1024 + 4 (q + 32), sc/4, -288 sc) = sc * q
+//     (|sc q| <= 2048: exact; 288 sc is 9 * 32 * sc, exact);
+//   two tiles: the low 4 bits l alone give fma(1024 + 4 l, sc/16, -64 sc) = sc * l / 4
+//     (a quarter-integer below 480) and the high 2 bits h alone give
+//     fma(1024 + 64 h, sc/16, -72 sc) = 4 sc (h - 2); both exact for any int8 sc.
+__device__ __forceinline__ uint32_t q6_pair(uint32_t w, uint32_t mask, __half2 c, __half2 a)
 {
-    return widen_q4(x, c1, a1, c16, a16);
+    return h2u(__hfma2(u2h(lop_or(w, mask)), c, a));
 }
-
-// q6_K tile B: 4 sc (h - 2) of one unit from its 2-bit fields (pair p at bits 2p and
-// 16 + 2p of g): (1024 + 4^p h) - (1024 + 2 * 4^p) = 4^p (h - 2), times 4 sc / 4^p.
-__device__ __forceinline__ uint4 widen_q6_hi(uint32_t g, const __half2 (&m)[4])
+__device__ __forceinline__ void widen_q6_one(uint4 x, __half2 c, __half2 a, uint4& o0, uint4& o1)
 {
-    uint4 o;
-    o.x = h2u(__hmul2(__hadd2(u2h(lop_or(g, 0x00030003u)), __float2half2_rn(-1026.0f)), m[0]));
-    o.y = h2u(__hmul2(__hadd2(u2h(lop_or(g, 0x000C000Cu)), __float2half2_rn(-1032.0f)), m[1]));
-    o.z = h2u(__hmul2(__hadd2(u2h(lop_or(g, 0x00300030u)), __float2half2_rn(-1056.0f)), m[2]));
-    o.w = h2u(__hmul2(__hadd2(u2h(lop_or(g, 0x00C000C0u)), __float2half2_rn(-1152.0f)), m[3]));
-    return o;
+    constexpr uint32_t Q = 0x00FC00FCu;
+    o0 = make_uint4(q6_pair(x.x, Q, c, a), q6_pair(x.x >> 8, Q, c, a), q6_pair(x.y, Q, c, a),
+                    q6_pair(x.y >> 8, Q, c, a));
+    o1 = make_uint4(q6_pair(x.z, Q, c, a), q6_pair(x.z >> 8, Q, c, a), q6_pair(x.w, Q, c, a),
+                    q6_pair(x.w >> 8, Q, c, a));
+}
+__device__ __forceinline__ void widen_q6_two(uint4 x, __half2 c, __half2 al, __half2 ah, uint4& l0, uint4& l1,
+                                             uint4& h0, uint4& h1)
+{
+    constexpr uint32_t L = 0x003C003Cu, H = 0x00C000C0u;
+    const uint32_t w[8] = {x.x, x.x >> 8, x.y, x.y >> 8, x.z, x.z >> 8, x.w, x.w >> 8};
+    l0 = make_uint4(q6_pair(w[0], L, c, al), q6_pair(w[1], L, c, al), q6_pair(w[2], L, c, al), q6_pair(w[3], L, c, al));
+    l1 = make_uint4(q6_pair(w[4], L, c, al), q6_pair(w[5], L, c, al), q6_pair(w[6], L, c, al), q6_pair(w[7], L, c, al));
+    h0 = make_uint4(q6_pair(w[0], H, c, ah), q6_pair(w[1], H, c, ah), q6_pair(w[2], H, c, ah), q6_pair(w[3], H, c, ah));
+    h1 = make_uint4(q6_pair(w[4], H, c, ah), q6_pair(w[5], H, c, ah), q6_pair(w[6], H, c, ah), q6_pair(w[7], H, c, ah));
 }
 
 // Four f16 pairs (one 8-value unit) from each of 4 uint4: 16 TMEM columns of one lane.
@@ -323,20 +337,6 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-// Folded q6_K (one tile): sc * q = 4 * (sc * l / 4) + 16 sc (h - 2), from the two-tile
-// terms a = sc * l / 4 (widen_q6_lo) and b = 16 sc (h - 2) (widen_q6_hi with 16 sc / 4^p):
-// one f16x2 fma per pair, exact because the result is an integer of at most 2048.
-__device__ __forceinline__ uint4 fold_q6(uint4 a, uint4 b)
-{
-    const __half2 four = __float2half2_rn(4.0f);
-    uint4 o;
-    o.x = h2u(__hfma2(u2h(a.x), four, u2h(b.x)));
-    o.y = h2u(__hfma2(u2h(a.y), four, u2h(b.y)));
-    o.z = h2u(__hfma2(u2h(a.z), four, u2h(b.z)));
-    o.w = h2u(__hfma2(u2h(a.w), four, u2h(b.w)));
-    return o;
 }
 
 // Work unit u: weight tile n and its super-block range; stage st of the unit covers
@@ -556,9 +556,8 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                 }
                 const uint8_t* raw = smem + C::SMEM_RAW + rp.i * C::RAW_BYTES;
                 // this half's words: q4_K the 4 chunks of k-blocks 2h, 2h+1; q6_K two-tile the
-                // 2 nibble words and the high word of k-block h; q6_K one-tile those of k-blocks
-                // 2h and 2h+1
-                constexpr int NW = Q4 ? 4 : (ONE ? 6 : 3);
+                // 4 sub-block words of k-block h; q6_K one-tile those of k-blocks 2h and 2h+1
+                constexpr int NW = Q4 ? 4 : (ONE ? 8 : 4);
                 uint4 xw[NW];
                 if (Q4) {
 #pragma unroll
@@ -567,11 +566,11 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                                                                 ((j & 1) * BM + r) * 16);
                 } else {
 #pragma unroll
-                    for (int b = 0; b < NW / 3; ++b) {
-                        const uint8_t* kb = raw + ((NW / 3) * h + b) * cw_kblock_bytes(TYPE);
+                    for (int b = 0; b < NW / 4; ++b) {
+                        const uint8_t* kb = raw + ((NW / 4) * h + b) * cw_kblock_bytes(TYPE);
 #pragma unroll
-                        for (int wd = 0; wd < 3; ++wd)
-                            xw[3 * b + wd] = *reinterpret_cast<const uint4*>(kb + (wd * BM + r) * 16);
+                        for (int wd = 0; wd < 4; ++wd)
+                            xw[4 * b + wd] = *reinterpret_cast<const uint4*>(kb + (wd * BM + r) * 16);
                     }
                 }
                 __syncwarp();
@@ -618,40 +617,29 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                     }
                 } else {
 #pragma unroll
-                    for (int b = 0; b < NW / 3; ++b) {
+                    for (int b = 0; b < NW / 4; ++b) {
                         const int kbs = ONE ? 2 * h + b : 2 * sst + h;     // k-block of the super-block
                         const int kcol = ONE ? 32 * (2 * h + b) : 32 * h;  // its columns in the buffer
-                        const uint32_t hs[4] = {xw[3 * b + 2].x, xw[3 * b + 2].y, xw[3 * b + 2].z, xw[3 * b + 2].w};
 #pragma unroll
                         for (int cw = 0; cw < 2; ++cw) {               // the k-block's two chunks
                             const int cc = 2 * kbs + cw;               // chunk of the super-block
-                            const uint32_t xs[4] = {xw[3 * b + cw].x, xw[3 * b + cw].y, xw[3 * b + cw].z,
-                                                    xw[3 * b + cw].w};
                             uint4 oa[4], ob[4];
 #pragma unroll
                             for (int half = 0; half < 2; ++half) {     // 16-value sub-blocks
                                 const float sc = static_cast<float>(static_cast<int8_t>(scr[2 * cc + half]));
-                                const __half2 c1 = __float2half2_rn(sc * 0.25f), a1 = __float2half2_rn(-256.0f * sc);
-                                const __half2 c16 = __float2half2_rn(sc * 0.015625f),
-                                              a16 = __float2half2_rn(-16.0f * sc);
-                                const float hsc = ONE ? 4.0f * sc : sc;   // one tile: 16 sc (h - 2)
-                                const __half2 m[4] = {__float2half2_rn(4.0f * hsc), __float2half2_rn(hsc),
-                                                      __float2half2_rn(0.25f * hsc), __float2half2_rn(0.0625f * hsc)};
-#pragma unroll
-                                for (int v = 0; v < 2; ++v) {
-                                    const int uu = 2 * half + v;
-                                    oa[uu] = widen_q6_lo(xs[uu], c1, a1, c16, a16);
-                                    ob[uu] = widen_q6_hi(hs[2 * cw + half] >> (8 * v), m);
+                                const uint4 x = xw[4 * b + 2 * cw + half];
+                                if (ONE) {
+                                    widen_q6_one(x, __float2half2_rn(0.25f * sc), __float2half2_rn(-288.0f * sc),
+                                                 oa[2 * half], oa[2 * half + 1]);
+                                } else {
+                                    widen_q6_two(x, __float2half2_rn(0.0625f * sc), __float2half2_rn(-64.0f * sc),
+                                                 __float2half2_rn(-72.0f * sc), oa[2 * half], oa[2 * half + 1],
+                                                 ob[2 * half], ob[2 * half + 1]);
                                 }
                             }
-                            if (ONE) {
-                                const uint4 o[4] = {fold_q6(oa[0], ob[0]), fold_q6(oa[1], ob[1]),
-                                                    fold_q6(oa[2], ob[2]), fold_q6(oa[3], ob[3])};
-                                tmem_st16(wcol + kcol + 16 * cw, o);
-                            } else {
-                                tmem_st16(wcol + kcol + 16 * cw, oa);
+                            tmem_st16(wcol + kcol + 16 * cw, oa);
+                            if (!ONE)
                                 tmem_st16(wcol + 64 + kcol + 16 * cw, ob);
-                            }
                         }
                     }
                 }

@@ -98,13 +98,13 @@ constexpr int RAW4_BYTES = 144;
 constexpr int RAW6_BYTES = 224;
 __host__ __device__ constexpr int raw_block_bytes(int type) { return type == 12 ? RAW4_BYTES : RAW6_BYTES; }
 
-// Compact code plane (the few-token GEMM's weight operand, widened to f16 in shared
+// Compact code plane (the few-token GEMM's weight operand, widened to f16 in tensor
 // memory): per (128-row tile, 64-value k-block) CW_WORDS 16-byte words per row, stored
 // word-major ([word][row][16 B]) so that the 128 rows of one word are 2048 contiguous
-// bytes.  q4_K: words 0, 1 = the 4-bit codes of the k-block's two chunks; q6_K: words
-// 0, 1 = the low 4 bits of q + 32 of the two chunks, word 2 = the high 2 bits of all 64
-// values.  Bit positions: see pack.cu.
-__host__ __device__ constexpr int cw_words(int type) { return type == 12 ? 2 : 3; }
+// bytes.  q4_K: words 0, 1 = the 4-bit codes of the k-block's two chunks; q6_K: word w
+// = the 16 values of sub-block w of the k-block, one byte 4 (q + 32) each.  Bit and
+// byte positions: see pack.cu.
+__host__ __device__ constexpr int cw_words(int type) { return type == 12 ? 2 : 4; }
 __host__ __device__ constexpr int cw_kblock_bytes(int type) { return cw_words(type) * TILE_ROWS * 16; }
 // Sub-block scale plane: per (128-row tile, super-block) 16 bytes per row, [row][16 B]:
 // q4_K the 8 six-bit scales sc_c then the 8 mins m_c (one byte each); q6_K the 16 int8

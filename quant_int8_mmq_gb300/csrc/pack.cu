@@ -264,12 +264,13 @@ __global__ void __launch_bounds__(256) raw_relayout_kernel(const RawRows raw, lo
 // j, k-block kb), the rows of a tile on consecutive threads.  Bit positions are chosen
 // so that the GEMM's converter turns each 32-bit word into f16 pairs with a mask and
 // an OR of the exponent 0x6400 (1024 + the field), no per-value shifts:
-//   nibble word (q4_K code q; q6_K the low 4 bits of q + 32) of a 32-value chunk:
-//     value 8u + 2p + h (u, p = 0..3, h = 0, 1) at bit 4p + 16h of byte group u
-//     (bytes 4u..4u+3);
-//   q6_K high word (the high 2 bits of q + 32 for the k-block's 64 values): chunk hc
-//     in bytes 8hc..8hc+7, byte group s = 0, 1 of it holding units u = 2s and 2s + 1
-//     of the chunk, value 8u + 2p + h at bit 8(u - 2s) + 2p + 16h.
+//   q4_K nibble word (code q) of a 32-value chunk: value 8u + 2p + h (u, p = 0..3,
+//     h = 0, 1) at bit 4p + 16h of byte group u (bytes 4u..4u+3);
+//   q6_K word of a 16-value sub-block: one byte 4 (q + 32) per value (the six-bit code
+//     at bits 2..7, so that 1024 + 4 (q + 32) is exact), value 4u + o (u, o = 0..3) in
+//     32-bit word u at byte 2 (o & 1) + (o >> 1): bytes 0, 2 hold values 4u, 4u + 1 and
+//     bytes 1, 3 values 4u + 2, 4u + 3, each pair one mask (or a shift and a mask) away
+//     from its f16x2 form.
 template <int TYPE>
 __global__ void __launch_bounds__(256) compact_kernel(const RawRows raw, int od, int id, int Np,
                                                       uint4* __restrict__ cw, uint4* __restrict__ scp)
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const RawRows raw, int od,
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 word[w][u] = 0u;
+        static_assert(TYPE == 12 || W == 4, "q6_K: one word per 16-value sub-block");
         uint32_t sc4[4] = {0u, 0u, 0u, 0u};
         if (j < od) {
             const uint8_t* b = raw.block(j, sb);
@@ -299,18 +301,16 @@ __global__ void __launch_bounds__(256) compact_kernel(const RawRows raw, int od,
                 const int e0 = 64 * (kb & 3) + 32 * hc;      // first value of the chunk in its block
                 for (int i2 = 0; i2 < 32; ++i2) {
                     const int e = e0 + i2;
-                    const int u = i2 >> 3, pp = (i2 & 7) >> 1, h = i2 & 1;
-                    uint32_t lo4, hi2 = 0u;
-                    if (TYPE == 12) {
-                        lo4 = (b[16 + e / 2] >> (4 * (e & 1))) & 15u;
+                    if constexpr (TYPE == 12) {
+                        const int u = i2 >> 3, pp = (i2 & 7) >> 1, h = i2 & 1;
+                        const uint32_t lo4 = (b[16 + e / 2] >> (4 * (e & 1))) & 15u;
+                        word[hc][u] |= lo4 << (4 * pp + 16 * h);
                     } else {
-                        lo4 = (b[e / 2] >> (4 * (e & 1))) & 15u;
-                        hi2 = (b[128 + e / 4] >> (2 * (e & 3))) & 3u;
-                    }
-                    word[hc][u] |= lo4 << (4 * pp + 16 * h);
-                    if constexpr (TYPE == 14) {
-                        const int sgrp = u >> 1;                  // byte group of the high word
-                        word[2][2 * hc + sgrp] |= hi2 << (8 * (u - 2 * sgrp) + 2 * pp + 16 * h);
+                        const uint32_t lo4 = (b[e / 2] >> (4 * (e & 1))) & 15u;
+                        const uint32_t hi2 = (b[128 + e / 4] >> (2 * (e & 3))) & 3u;
+                        const int i16 = i2 & 15, o = i16 & 3;      // value 4 u6 + o of the sub-block
+                        const int u6 = i16 >> 2, byte = 2 * (o & 1) + (o >> 1);
+                        word[2 * hc + (i2 >> 4)][u6] |= (4u * (lo4 | (hi2 << 4))) << (8 * byte);
                     }
                 }
             }

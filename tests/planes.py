@@ -82,26 +82,25 @@ def compact_plane(typ: str, codes: np.ndarray, rows_padded: int) -> np.ndarray:
     v = np.zeros((rows_padded, K), np.uint32)
     v[:od] = codes.astype(np.int64) + (32 if typ == "q6_K" else 0)
     nt, nkb = rows_padded // TILE_ROWS, K // TILE_K
-    W = 3 if typ == "q6_K" else 2
+    if typ == "q6_K":
+        # word w = sub-block w of the k-block (16 values), value 4u + o in 32-bit word u at
+        # byte 2 (o & 1) + (o >> 1), holding 4 (q + 32)
+        vv = (4 * v).reshape(nt, TILE_ROWS, nkb, 4, 4, 4)          # [nt, r, kb, w, u, o]
+        byte_of_o = np.array([0, 2, 1, 3])
+        b = np.zeros((nt, TILE_ROWS, nkb, 4, 4, 4), np.uint8)
+        b[..., byte_of_o] = vv.astype(np.uint8)
+        return np.ascontiguousarray(b.transpose(0, 2, 3, 1, 4, 5)).reshape(-1)
+    W = 2
     # v[nt, r, kb, hc, i] for the 32 values i of chunk hc of k-block kb
     vv = v.reshape(nt, TILE_ROWS, nkb, 2, 32)
     i = np.arange(32)
     u, p, h = i // 8, (i % 8) // 2, i % 2
     out = np.zeros((nt, nkb, W, TILE_ROWS, 4), np.uint32)
-    low = vv & 15
     for hc in range(2):
         for uu in range(4):
             sel = u == uu
             sh = (4 * p + 16 * h)[sel]
-            out[:, :, hc, :, uu] = np.bitwise_or.reduce(low[:, :, :, hc][..., sel] << sh, axis=-1).transpose(0, 2, 1)
-    if W == 3:
-        high = vv >> 4
-        for hc in range(2):
-            for s in range(2):
-                sel = (u // 2) == s
-                sh = (8 * (u % 2) + 2 * p + 16 * h)[sel]
-                out[:, :, 2, :, 2 * hc + s] = np.bitwise_or.reduce(high[:, :, :, hc][..., sel] << sh,
-                                                                   axis=-1).transpose(0, 2, 1)
+            out[:, :, hc, :, uu] = np.bitwise_or.reduce(vv[:, :, :, hc][..., sel] << sh, axis=-1).transpose(0, 2, 1)
     return out.reshape(-1).view(np.uint8)
 
 

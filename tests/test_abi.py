@@ -65,7 +65,7 @@ def test_size_queries_follow_the_documented_layout(mmq_lib):
         assert L["aux"] == (sum(L["sbd"]), Np * nsb * 64)
         assert L["flag"][0] == sum(L["aux"])
         assert L["raw"] == (sum(L["flag"]), 4097 * 4 * (144 if t == mmq.MMQ_Q4_K else 224))
-        words = 2 if t == mmq.MMQ_Q4_K else 3
+        words = 2 if t == mmq.MMQ_Q4_K else 4          # q4_K: 4-bit codes; q6_K: one byte per value
         assert L["cw"] == (-(-sum(L["raw"]) // 256) * 256, (Np // 128) * 16 * words * 128 * 16)
         assert L["sc"] == (sum(L["cw"]), Np * nsb * 16)
         assert L["dm"] == (sum(L["sc"]), Np * nsb * 4 if t == mmq.MMQ_Q4_K else 0)
