@@ -922,6 +922,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
     const uint32_t sbase = raw_addr + pad;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // The next kernel on the stream may be scheduled as SMs free up (it waits for this
+    // grid to complete before it touches memory).  For q6_K, while the kernel ahead of
+    // this one finishes, warm L2 with this CTA's first weights: the compact codes of its
+    // first two super-blocks and the first super-block's scales (a prefetch changes no
+    // value; measured: q6_K 4097x11008 -8 %, while for q4_K it made no difference and
+    // cost the 48-token form registers).
+    grid_dep_launch();
+    if (TYPE == 14 && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < g.units) {
+        const int nsb = g.id / QK_K;
+        const Unit w = unit_of(g, static_cast<int>(blockIdx.x), nsb);
+        const size_t ts = static_cast<size_t>(w.n) * nsb + w.sb0;
+        const int nkb = g.id / TILE_K;
+        const uint32_t cw_sb = 4u * static_cast<uint32_t>(cw_kblock_bytes(TYPE));
+        bulk_prefetch_l2(g.CW + (static_cast<size_t>(w.n) * nkb + 4 * w.sb0) * cw_kblock_bytes(TYPE),
+                         (w.sb1 - w.sb0 > 1 ? 2u : 1u) * cw_sb);
+        bulk_prefetch_l2(g.SC + ts * (BM * SC_ROW_BYTES), BM * SC_ROW_BYTES);
+        bulk_prefetch_l2(g.SBD + ts * (BM * 4), BM * 4);
+    }
     if constexpr (TYPE == 12) {
         ft_body<12, NT, true>(g, smem, sbase, warp, lane);
     } else {
