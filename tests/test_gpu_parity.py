@@ -756,6 +756,43 @@ def test_gemm_few_token_min_term_across_units(M, od, id_):
     assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
 
 
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
+def test_few_token_back_to_back_calls_share_buffers(typ):
+    """Prepass and few-token GEMM calls queued on one stream with no synchronisation, all
+    through the same activation planes, the last two GEMMs writing the same Y.  The GEMM
+    lets the next kernel be scheduled at its start (that kernel waits for it before it
+    touches memory); each result must still be the oracle's for its own inputs."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    od, id_ = 2100, 1024
+    raws = [_q6_raw(od, id_, 960 + i, True) if t == "q6_K" else _raw(t, od, id_, seed=960 + i) for i in range(2)]
+    packs = [gpu_pack(t, r) for r in raws]
+    Ms = [31, 12, 40, 20, 17]
+    xs = [synth.activations(M, id_, seed=970 + i) for i, M in enumerate(Ms)]
+    xd = [_to_dev(x) for x in xs]
+    qb, sb = mmq.mmq_act_plane_bytes(max(Ms), id_)
+    qa = torch.empty(qb, dtype=torch.uint8, device=DEV)
+    sc = torch.empty(sb, dtype=torch.uint8, device=DEV)
+    shared = torch.full((max(Ms), od), float("nan"), dtype=torch.float32, device=DEV)
+    _sync()
+    outs = []
+    for i, x in enumerate(xd):
+        M = x.shape[0]
+        mmq.quantize_act(x, qa, sc)
+        Y = shared[:M] if i >= len(xd) - 2 else None
+        outs.append(mmq.gemm(t, packs[i % 2], od, id_, qa, sc, M, Y=Y))
+        assert "few-token GEMM" in mmq.mmq_last_path()
+    _sync()
+    assert mmq.mmq_get_device_error() == 0
+    for i, (x, Y) in enumerate(zip(xs, outs)):
+        if i == len(xs) - 2:
+            continue   # overwritten by the last call
+        Yo, S = oracle_gemm(t, raws[i % 2], x)
+        assert_y_close(Y.cpu().numpy(), Yo, S)
+    # rows the last call (M = 17) did not write still hold the one before it (M = 20)
+    Yo, S = oracle_gemm(t, raws[(len(xs) - 2) % 2], xs[-2])
+    assert_y_close(shared[17:20].cpu().numpy(), Yo[17:], S[17:])
+
+
 def test_gemm_few_token_row_stride_unaligned():
     typ, M, od, id_ = "q4_K", 27, 203, 512
     raw = _raw(typ, od, id_, seed=25)
