@@ -923,12 +923,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ft_kernel(const FtArgs g)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // The next kernel on the stream may be scheduled as SMs free up (it waits for this
-    // grid to complete before it touches memory).  For q6_K, while the kernel ahead of
-    // this one finishes, warm L2 with this CTA's first weights: the compact codes of its
-    // first two super-blocks and the first super-block's scales (a prefetch changes no
-    // value; measured: q6_K 4097x11008 -8 %, while for q4_K it made no difference and
-    // cost the 48-token form registers).
-    grid_dep_launch();
+    // grid to complete before it touches memory), for q6_K and for clustered launches;
+    // and while the kernel ahead of this one finishes, a q6_K CTA warms L2 with its first
+    // weights: the compact codes of its first two super-blocks and the first super-
+    // block's scales (a prefetch changes no value).  Measured back to back: q6_K
+    // 4097x11008 -8 %, q4_K 4096x4096 (clusters) -3 %; the early trigger made the
+    // unclustered q4_K 11008x4096 at 40-64 tokens 4-7 % slower, and the q4_K prefetch
+    // made no difference.
+    if (TYPE == 14 || g.kslices > 1)
+        grid_dep_launch();
     if (TYPE == 14 && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < g.units) {
         const int nsb = g.id / QK_K;
         const Unit w = unit_of(g, static_cast<int>(blockIdx.x), nsb);
