@@ -109,7 +109,7 @@ typedef enum { MMQ_Q4_K = 12, MMQ_Q6_K = 14 } mmq_type;
  *        hi = rn_f16(s_hi*q), lo = rn_f16(fma(s_hi, q, -hi) + s_lo*q) (f16 fma);
  *     ip (in scales, after am) f32 1/p at index sb*MMQ_FT_MAX_M + t (t < N);
  *     fm (in scales, after ip) f32 ma = d*ssum (one f32 multiply) of chunk c of
- *        super-block sb at index (sb*MMQ_FT_MAX_M + t)*8 + c % 8 (t < N).
+ *        super-block sb at index (sb*8 + c % 8)*MMQ_FT_MAX_M + t (t < N).
  * -------------------------------------------------------------------------- */
 #define MMQ_SMALL_M 8
 #define MMQ_FT_MAX_M 64

@@ -204,7 +204,7 @@ struct FtArgs {
     const unsigned int* FLAG;   // q6_K: word 0 = 1 if every |sc| <= 64
     const uint8_t* TQ;    // token hi/lo tiles    [nkb][hi n_tok rows | lo n_tok rows][128 B]
     const uint8_t* IP;    // token 1/p            [nsb][FT_MAX_M] f32
-    const uint8_t* FM;    // token d_a*ssum       [nsb][FT_MAX_M][8] f32
+    const uint8_t* FM;    // token d_a*ssum       [nsb][8][FT_MAX_M] f32
     const uint8_t* AM;    // token min-term tiles [nsb][tf32 hi tile | tf32 lo tile] (token tile 0)
     float* Y;
     int ldy;
@@ -261,6 +261,18 @@ __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask)   // (x & 
     return (x & mask) | 0x64006400u;
 }
 __device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<const uint32_t*>(&v); }
+// (x, y) = fma(m, (fx, fy), (x, y)) as one f32x2 instruction: two IEEE fmas.
+__device__ __forceinline__ void ffma2(float& x, float& y, float m, float fx, float fy)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %2};\n\t"
+        "mov.b64 c, {%3, %4};\n\t"
+        "fma.rn.f32x2 a, b, c, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(m), "f"(fx), "f"(fy));
+}
 __device__ __forceinline__ float tf32_rna(float v)
 {
     uint32_t r;
@@ -365,7 +377,7 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
             uint32_t n_raw = 0, n_sb = 0;
             const uint32_t skip = (blockIdx.x == 0 && g.withhold >= 0) ? static_cast<uint32_t>(g.withhold) : ~0u;
             constexpr uint32_t SB_TX =
-                BM * 4 + BM * SC_ROW_BYTES + FT_MAX_M * 4 + (Q4 ? BM * 4 + (C::MIN_TC ? 2 : 1) * N * 32 : 0);
+                BM * 4 + BM * SC_ROW_BYTES + FT_MAX_M * 4 + (Q4 ? BM * 4 + (C::MIN_TC ? 2 * N * 32 : FT_MAX_M * 32) : 0);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
@@ -397,7 +409,9 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                                 bulk_g2s(dst + SB_AM_OFF, am, N * 32, fb);
                                 bulk_g2s(dst + SB_AM_OFF + N * 32, am + TF32_TILE_BYTES, N * 32, fb);
                             } else {
-                                bulk_g2s(dst + SB_FM_OFF, g.FM + static_cast<size_t>(s) * (FT_MAX_M * 32), N * 32, fb);
+                                // [chunk][FT_MAX_M tokens]: the whole super-block's 2 KB
+                                bulk_g2s(dst + SB_FM_OFF, g.FM + static_cast<size_t>(s) * (FT_MAX_M * 32), FT_MAX_M * 32,
+                                         fb);
                             }
                         }
                         sp.next();
@@ -753,20 +767,17 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     dmn[c] = -__fmul_rn(dmin, static_cast<float>(((c < 4 ? mw.x : mw.y) >> (8 * (c & 3))) & 0xFFu));
-                const float4* fm = reinterpret_cast<const float4*>(sbe + SB_FM_OFF);
+                // chunk-major d_a*ssum: four tokens per load, two per f32x2 fma (each token's
+                // sum still runs over c = 0..7 in order)
+                const float* fmc = reinterpret_cast<const float*>(sbe + SB_FM_OFF);
 #pragma unroll
-                for (int t = 0; t < N; ++t) {
-                    const float4 a = fm[2 * t], b = fm[2 * t + 1];
-                    float v = acc[t];
-                    v = fmaf(dmn[0], a.x, v);
-                    v = fmaf(dmn[1], a.y, v);
-                    v = fmaf(dmn[2], a.z, v);
-                    v = fmaf(dmn[3], a.w, v);
-                    v = fmaf(dmn[4], b.x, v);
-                    v = fmaf(dmn[5], b.y, v);
-                    v = fmaf(dmn[6], b.z, v);
-                    v = fmaf(dmn[7], b.w, v);
-                    acc[t] = v;
+                for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                    for (int t = 0; t < N; t += 4) {
+                        const float4 f = *reinterpret_cast<const float4*>(fmc + c * FT_MAX_M + t);
+                        ffma2(acc[t], acc[t + 1], dmn[c], f.x, f.y);
+                        ffma2(acc[t + 2], acc[t + 3], dmn[c], f.z, f.w);
+                    }
                 }
             }
             __syncwarp();

@@ -66,7 +66,7 @@ struct ActPlanes {       // layout of mmq_quantize_act's outputs
     size_t pair_off, pair_bytes;   // {f32 d, i32 ssum} per (token, chunk)
     size_t am_off, am_bytes;       // tf32 hi/lo tiles of d*ssum per (token tile, super-block)
     size_t ip_off, ip_bytes;       // M <= FT_MAX_M: f32 1/p [K/256][FT_MAX_M], else 0
-    size_t fm_off, fm_bytes;       // M <= FT_MAX_M: f32 d*ssum [K/256][FT_MAX_M][8], else 0
+    size_t fm_off, fm_bytes;       // M <= FT_MAX_M: f32 d*ssum [K/256][8][FT_MAX_M], else 0
     size_t scale_bytes;            // pairs + am + 1/p + d*ssum
 };
 inline ActPlanes act_planes(int M, int K)

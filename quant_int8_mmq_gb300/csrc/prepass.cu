@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                 *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = hi;
                 *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = lo;
                 if (fm != nullptr && t < ftn)
-                    fm[(static_cast<size_t>(sb) * FT_MAX_M + t) * 8 + (c & 7)] = ma;
+                    fm[(static_cast<size_t>(sb) * 8 + (c & 7)) * FT_MAX_M + t] = ma;
             }
         }
     }

@@ -123,11 +123,11 @@ def _check_prepass(x, ldx=None):
         assert to == Mp * K * 2 + (M * K if M <= mmq.SMALL_M else 0) and tb == (K // 64) * 2 * n * 128
         assert io == lay["am"][0] + lay["am"][1] and ib == (K // 256) * 64 * 4
         assert fo == io + ib and fb == (K // 256) * 64 * 8 * 4
-        # the q4_K min-term operand d * ssum (one f32 multiply) per (super-block, token, chunk)
-        fm = scb[fo:fo + fb].view(np.float32).reshape(K // 256, 64, 8)[:, :n]
+        # the q4_K min-term operand d * ssum (one f32 multiply) per (super-block, chunk, token)
+        fm = scb[fo:fo + fb].view(np.float32).reshape(K // 256, 8, 64)[:, :, :n]     # [sb][chunk][token]
         wfm = np.zeros((n, K // 32), np.float32)
         wfm[:M] = (d * s.astype(np.float32)).astype(np.float32)
-        assert np.array_equal(fm.view(np.uint32), wfm.reshape(n, K // 256, 8).transpose(1, 0, 2).view(np.uint32))
+        assert np.array_equal(fm.view(np.uint32), wfm.reshape(n, K // 256, 8).transpose(1, 2, 0).view(np.uint32))
         hi, lo = untile_token_operand(qab[to:to + tb], n, K)
         whi, wlo, wip = ft_operand(q, d, n)
         assert np.array_equal(hi.view(np.uint16), whi.view(np.uint16))
