@@ -261,7 +261,29 @@ __device__ __forceinline__ uint32_t lop_or(uint32_t x, uint32_t mask)   // (x & 
     return (x & mask) | 0x64006400u;
 }
 __device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<const uint32_t*>(&v); }
-// (x, y) = fma(m, (fx, fy), (x, y)) as one f32x2 instruction: two IEEE fmas.
+// Pairs of f32 as one f32x2 instruction each (two IEEE operations, each rounded as its
+// scalar form): (x, y) = (a, b) + (c, d); (x, y) = (a, b) * (c, d); and below
+// (x, y) = fma(m, (fx, fy), (x, y)).
+__device__ __forceinline__ void fadd2(float& x, float& y, float a, float b, float c, float d)
+{
+    asm("{\n\t.reg .b64 p, q;\n\t"
+        "mov.b64 p, {%2, %3};\n\t"
+        "mov.b64 q, {%4, %5};\n\t"
+        "add.rn.f32x2 p, p, q;\n\t"
+        "mov.b64 {%0, %1}, p;\n\t}"
+        : "=f"(x), "=f"(y)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+}
+__device__ __forceinline__ void fmul2(float& x, float& y, float a, float b, float c, float d)
+{
+    asm("{\n\t.reg .b64 p, q;\n\t"
+        "mov.b64 p, {%2, %3};\n\t"
+        "mov.b64 q, {%4, %5};\n\t"
+        "mul.rn.f32x2 p, p, q;\n\t"
+        "mov.b64 {%0, %1}, p;\n\t}"
+        : "=f"(x), "=f"(y)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+}
 __device__ __forceinline__ void ffma2(float& x, float& y, float m, float fx, float fy)
 {
     asm("{\n\t.reg .b64 a, b, c;\n\t"
@@ -736,8 +758,16 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                     tmem_ld16x2_wait(lane_addr + ii[k] * C::ITEM_COLS + 16 * gq,
                                      lane_addr + ii[k] * C::ITEM_COLS + N + 16 * gq, Dh, Dl);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        Dt[e] = k == 0 ? __fadd_rn(Dh[e], Dl[e]) : __fadd_rn(Dt[e], __fadd_rn(Dh[e], Dl[e]));
+                    for (int e = 0; e < 16; e += 2) {
+                        float s0, s1;
+                        fadd2(s0, s1, Dh[e], Dh[e + 1], Dl[e], Dl[e + 1]);
+                        if (k == 0) {
+                            Dt[e] = s0;
+                            Dt[e + 1] = s1;
+                        } else {
+                            fadd2(Dt[e], Dt[e + 1], Dt[e], Dt[e + 1], s0, s1);
+                        }
+                    }
                 }
                 if (gq == NT - 1) {
                     tc_fence_before();
@@ -753,9 +783,11 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                     const float4 ipv = ip4[4 * gq + i4];
                     const float ipa[4] = {ipv.x, ipv.y, ipv.z, ipv.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 4; e += 2) {
                         const int t = 16 * gq + 4 * i4 + e;
-                        acc[t] = fmaf(dsb, __fmul_rn(Dt[4 * i4 + e], ipa[e] * IPS), acc[t]);
+                        float p0, p1;
+                        fmul2(p0, p1, Dt[4 * i4 + e], Dt[4 * i4 + e + 1], ipa[e] * IPS, ipa[e + 1] * IPS);
+                        ffma2(acc[t], acc[t + 1], dsb, p0, p1);
                     }
                 }
             }
