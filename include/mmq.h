@@ -249,10 +249,9 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *    the low 4 and high 2 bits of q + 32) in tensor memory and contracted on
  *    tcgen05 against the tq operand (f16 hi and lo of p*d_a*q_a as one 2N-row
  *    operand), one f32 accumulator per stage, then d and 1/p applied per
- *    super-block; the q4_K min term sum_c (dmin*m_c)*(d_a*ssum) from DM, SC and,
- *    for 17 <= M <= 32, the am plane as a tf32 hi/lo tensor-core contraction
- *    (dmin*m_c split exactly in the kernel; hi*hi + hi*lo + lo*hi), else from fm
- *    in f32 FMAs; when the weight tiles are few, each is split along K over a
+ *    super-block; the q4_K min term sum_c (dmin*m_c)*(d_a*ssum) from DM, SC and
+ *    fm in f32 FMAs (each token's sum over c = 0..7 in order); when the weight
+ *    tiles are few, each is split along K over a
  *    cluster of up to 8 CTAs whose partial sums are added in rank order
  *    (deterministic);
  *  - larger M, the super-block kernel (when its 128 x 256 tiles number at least

@@ -25,13 +25,10 @@
 //         uses 4/p.
 // Every product W * hi, W * lo is exact; the roundings are the split of the activation
 // operand, the f32 sums and the promotion (the 1e-5 bound on Y holds with margin).  The
-// q4_K min term is a contraction over only 8 chunks per super-block.  At N = 32 it runs
-// on the tensor core as in the super-block kernel: the converters write the weight
-// rows' dmn = dmin * m_c as exact tf32 hi + lo into a shared-memory tile, the tokens'
-// d_a*ssum hi + lo rows come from the prepass's min-term plane, and three kind::tf32
-// MMAs per super-block (hi*hi, hi*lo, lo*hi) accumulate into one TMEM accumulator per
-// issuer for the whole unit.  Otherwise the promotion threads take it on the CUDA
-// cores (8 f32 FMAs per token and super-block).
+// q4_K min term is a contraction over only 8 chunks per super-block: the promotion
+// threads take it on the CUDA cores, two tokens per f32x2 FMA against the chunk-major
+// d_a*ssum values the prepass wrote (a tf32 hi/lo tensor-core form, as in the
+// super-block kernel, was slower here once the FMAs were paired).
 //
 // The weights come from the compact code plane (0.5 B per value for q4_K, 1 for q6_K:
 // one byte 4 (q + 32), which a mask alone puts under the exponent) and are widened to
@@ -70,8 +67,7 @@
 //                the weight buffer and the warp signals the issuers.
 //   warps 12-15  promotion: thread = weight row (its TMEM lane), every token: per
 //                super-block its stage items' TMEM loads, acc += d * (D * 1/p), and for
-//                q4_K acc -= dmin * sum_c m_c * (d_a*ssum)_c (or, at N = 32, once per
-//                unit, the two min-term accumulators); store Y.
+//                q4_K acc -= dmin * sum_c m_c * (d_a*ssum)_c; store Y.
 //
 // Every mbarrier wait is bounded; on expiry the kernel sets the library's error word,
 // every role leaves its loop, waits (bounded) for its own copies and MMAs in flight,
@@ -111,15 +107,13 @@ __host__ __device__ constexpr uint32_t item_cols_of(int nt) { return nt <= 2 ? 6
 thread_local int g_last_kslices = 1;
 
 // Super-block ring entry: weight d of the 128 rows, their 16 sub-block scale bytes, 1/p
-// of the FT_MAX_M tokens, and for q4_K the rows' dmin and either the tokens' 8 values
-// d_a*ssum (FM, min term on the CUDA cores) or the first N rows of the tokens' tf32
-// hi and lo min-term tiles (AM, min term on the tensor core; N = 32: 2 x N x 32 B).
+// of the FT_MAX_M tokens, and for q4_K the rows' dmin and the tokens' 8 values d_a*ssum
+// per chunk ([chunk][FT_MAX_M tokens]).
 constexpr int SB_SBD_OFF = 0;
 constexpr int SB_SC_OFF = SB_SBD_OFF + BM * 4;
 constexpr int SB_IP_OFF = SB_SC_OFF + BM * SC_ROW_BYTES;
 constexpr int SB_DM_OFF = SB_IP_OFF + FT_MAX_M * 4;
 constexpr int SB_FM_OFF = SB_DM_OFF + BM * 4;
-constexpr int SB_AM_OFF = SB_FM_OFF;
 __host__ __device__ constexpr int sb_bytes_of(int type) { return type == 12 ? SB_FM_OFF + FT_MAX_M * 32 : SB_DM_OFF; }
 
 // ONE: one weight tile per k-block (q4_K always; q6_K when its codes fold); else two.
@@ -127,19 +121,9 @@ template <int TYPE, int NT, bool ONE>
 struct Cfg {
     static constexpr int N = 16 * NT;
     static constexpr int TILES = ONE ? 1 : 2;
-    // q4_K with N = 32: the min term sum_c dmn[j,c] * (d_a*ssum)[t,c] runs on the tensor
-    // core (kind::tf32, hi/lo operands, K = 8) into one TMEM accumulator per issuer that
-    // spans the whole unit, read once by the promotion; three accumulator items leave
-    // room for the two accumulators in front of the weight buffers.  (At N = 16 the
-    // 8 FMAs per token and super-block on the CUDA cores cost less than the three MMAs
-    // per stage and the smaller item ring; N > 32 leaves no TMEM for the accumulators.)
-    static constexpr bool MIN_TC = TYPE == 12 && NT == 2;
-    static constexpr int ITEMS = MIN_TC ? 3 : items_of(NT);
+    static constexpr int ITEMS = items_of(NT);
     static constexpr uint32_t ITEM_COLS = item_cols_of(NT);
-    static constexpr uint32_t MIN_COL0 = ITEMS * ITEM_COLS;          // min-term accumulators, N columns each
-    static_assert(ITEMS * ITEM_COLS + (MIN_TC ? 2 * N : 0) <= WBUF_COL0 && 2 * N <= static_cast<int>(ITEM_COLS),
-                  "items");
-    static_assert(!MIN_TC || 2 * N * 32 <= FT_MAX_M * 32, "min-term token rows fit the entry");
+    static_assert(ITEMS * ITEM_COLS == WBUF_COL0 && 2 * N <= static_cast<int>(ITEM_COLS), "items");
     static_assert(TYPE == 14 || ONE, "q4_K has one tile");
     static constexpr int KPS = ONE ? 4 : 2;                          // k-blocks per stage
     static constexpr int SPS = 4 / KPS;                              // stages per super-block
@@ -149,17 +133,14 @@ struct Cfg {
     static constexpr int TOK_SLOT = 4 * TOK_KB_BYTES;                // a super-block of tokens
     static constexpr int SB_BYTES = sb_bytes_of(TYPE);
     static constexpr int SBR = TYPE == 12 ? 6 : 8;                   // super-block ring depth
-    static constexpr int DMN_SLOT = 2 * TF32_TILE_BYTES;              // weight-side min-term tiles: hi, lo
-    static constexpr int DMN_BYTES = MIN_TC ? 2 * DMN_SLOT : 0;       // one per weight buffer
-    static constexpr int FIXED = TOK_STAGES * TOK_SLOT + SBR * SB_BYTES + DMN_BYTES;
+    static constexpr int FIXED = TOK_STAGES * TOK_SLOT + SBR * SB_BYTES;
     static constexpr int RAW_FIT = (SMEM_BUDGET - FIXED) / RAW_BYTES;
     static constexpr int RAW_STAGES = RAW_FIT > 4 ? 4 : RAW_FIT;     // compact-code ring depth
     static_assert(RAW_STAGES >= 2, "shared memory budget");
     static constexpr int SMEM_TOK = 0;
     static constexpr int SMEM_RAW = SMEM_TOK + TOK_STAGES * TOK_SLOT;
     static constexpr int SMEM_SB = SMEM_RAW + RAW_STAGES * RAW_BYTES;
-    static constexpr int SMEM_DMN = SMEM_SB + SBR * SB_BYTES;
-    static constexpr int SMEM_BAR = SMEM_DMN + DMN_BYTES;
+    static constexpr int SMEM_BAR = SMEM_SB + SBR * SB_BYTES;
     static constexpr int BAR_RFULL = 0;
     static constexpr int BAR_REMPTY = BAR_RFULL + RAW_STAGES;
     static constexpr int BAR_TKFULL = BAR_REMPTY + RAW_STAGES;
@@ -171,14 +152,12 @@ struct Cfg {
     static constexpr int BAR_TFULL = BAR_SBEMPTY + SBR;
     static constexpr int BAR_TEMPTY = BAR_TFULL + ITEMS;
     static constexpr int BAR_DRAIN = BAR_TEMPTY + ITEMS;
-    static constexpr int BAR_MEMPTY = BAR_DRAIN + 1;                  // min-term accumulator e read
-    static constexpr int NUM_BARS = BAR_MEMPTY + 2;
+    static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr int SMEM_TMEMPTR = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_ALLOC = SMEM_TMEMPTR + 16 + 1024;      // slack for 1024-byte alignment
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(TOK_SLOT % 1024 == 0 && TOK_KB_BYTES % 1024 == 0 && SMEM_RAW % 16 == 0 &&
-                      RAW_BYTES % 16 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && SMEM_DMN % 16 == 0 &&
-                      SMEM_BAR % 8 == 0 && SB_AM_OFF % 16 == 0,
+                      RAW_BYTES % 16 == 0 && SMEM_SB % 16 == 0 && SB_BYTES % 16 == 0 && SMEM_BAR % 8 == 0,
                   "alignment");
     // cluster K split: partial sums (rows x FT_MAX_M tokens) and the promotion warps' ok
     // flags, in the idle token and compact rings
@@ -205,7 +184,6 @@ struct FtArgs {
     const uint8_t* TQ;    // token hi/lo tiles    [nkb][hi n_tok rows | lo n_tok rows][128 B]
     const uint8_t* IP;    // token 1/p            [nsb][FT_MAX_M] f32
     const uint8_t* FM;    // token d_a*ssum       [nsb][8][FT_MAX_M] f32
-    const uint8_t* AM;    // token min-term tiles [nsb][tf32 hi tile | tf32 lo tile] (token tile 0)
     float* Y;
     int ldy;
     int M, od, id;
@@ -294,12 +272,6 @@ __device__ __forceinline__ void ffma2(float& x, float& y, float m, float fx, flo
         "mov.b64 {%0, %1}, a;\n\t}"
         : "+f"(x), "+f"(y)
         : "f"(m), "f"(fx), "f"(fy));
-}
-__device__ __forceinline__ float tf32_rna(float v)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
 }
 __device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<const __half2*>(&v); }
 
@@ -398,8 +370,7 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
             RingPos<C::SBR> sp;
             uint32_t n_raw = 0, n_sb = 0;
             const uint32_t skip = (blockIdx.x == 0 && g.withhold >= 0) ? static_cast<uint32_t>(g.withhold) : ~0u;
-            constexpr uint32_t SB_TX =
-                BM * 4 + BM * SC_ROW_BYTES + FT_MAX_M * 4 + (Q4 ? BM * 4 + (C::MIN_TC ? 2 * N * 32 : FT_MAX_M * 32) : 0);
+            constexpr uint32_t SB_TX = BM * 4 + BM * SC_ROW_BYTES + FT_MAX_M * 4 + (Q4 ? BM * 4 + FT_MAX_M * 32 : 0);
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
@@ -425,16 +396,9 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                         bulk_g2s(dst + SB_IP_OFF, g.IP + static_cast<size_t>(s) * (FT_MAX_M * 4), FT_MAX_M * 4, fb);
                         if (Q4) {
                             bulk_g2s(dst + SB_DM_OFF, g.DM + ts * (BM * 4), BM * 4, fb);
-                            if (C::MIN_TC) {
-                                // rows 0..N-1 of the hi and the lo tile are their first N*32 bytes
-                                const uint8_t* am = g.AM + static_cast<size_t>(s) * (2 * TF32_TILE_BYTES);
-                                bulk_g2s(dst + SB_AM_OFF, am, N * 32, fb);
-                                bulk_g2s(dst + SB_AM_OFF + N * 32, am + TF32_TILE_BYTES, N * 32, fb);
-                            } else {
-                                // [chunk][FT_MAX_M tokens]: the whole super-block's 2 KB
-                                bulk_g2s(dst + SB_FM_OFF, g.FM + static_cast<size_t>(s) * (FT_MAX_M * 32), FT_MAX_M * 32,
-                                         fb);
-                            }
+                            // [chunk][FT_MAX_M tokens]: the whole super-block's 2 KB
+                            bulk_g2s(dst + SB_FM_OFF, g.FM + static_cast<size_t>(s) * (FT_MAX_M * 32), FT_MAX_M * 32,
+                                     fb);
                         }
                         sp.next();
                         ++n_sb;
@@ -468,14 +432,11 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
             // ------------------------------------------------ MMA issuers: stage g with g % 2 == e
             const uint32_t e = warp == 3 ? 0u : 1u;
             constexpr uint32_t idesc = idesc_f16_f32(BM, 2 * N);   // hi and lo token rows at once
-            constexpr uint32_t idesc_m = idesc_tf32_acc32(BM, N);  // min term: tokens once
             uint32_t gs = 0;                                        // stage number across units
-            uint32_t mu = 0;                                        // units this issuer's min term took
             bool ok = true;
             for (int u = blockIdx.x; ok && u < g.units; u += gridDim.x) {
                 const Unit w = unit_of(g, u, nsb);
                 const int nst = (w.sb1 - w.sb0) * SPS;
-                bool mfirst = true;
                 for (int st = 0; st < nst; ++st, ++gs) {
                     if ((gs & 1u) != e)
                         continue;
@@ -504,27 +465,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                             if (!ONE)
                                 umma_f16_ts(d, wa + 64u + acol, bt + 2u * kk, idesc, 1u);
                         }
-                    }
-                    if constexpr (C::MIN_TC) {
-                        // min term of the stage's super-block: dmn (hi, lo) x the tokens' d_a*ssum
-                        // (hi, lo), dropping lo x lo, into this issuer's accumulator for the unit;
-                        // its first use in a unit waits until the promotion has read the last one
-                        if (mfirst && !ctl_wait(g, bar(C::BAR_MEMPTY + e), (mu & 1u) ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t ent = sbase + C::SMEM_SB + (sg % C::SBR) * C::SB_BYTES + SB_AM_OFF;
-                        const uint32_t dt = sbase + C::SMEM_DMN + e * C::DMN_SLOT;
-                        const uint64_t ahi = sdesc_tf32_core(dt), alo = sdesc_tf32_core(dt + TF32_TILE_BYTES);
-                        const uint64_t bhi = sdesc_tf32_core(ent), blo = sdesc_tf32_core(ent + N * 32);
-                        const uint32_t dmt = tmem_base + C::MIN_COL0 + e * N;
-                        umma_tf32_ss(dmt, ahi, bhi, idesc_m, mfirst ? 0u : 1u);
-                        umma_tf32_ss(dmt, ahi, blo, idesc_m, 1u);
-                        umma_tf32_ss(dmt, alo, bhi, idesc_m, 1u);
-                        if (mfirst)
-                            ++mu;
-                        mfirst = false;
                     }
                     umma_commit(bar(C::BAR_AEMPTY + e));
                     umma_commit(bar(C::BAR_TFULL + item));
@@ -630,27 +570,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                                             widen_q4(xw[j].z, c1, a1, c16, a16), widen_q4(xw[j].w, c1, a1, c16, a16)};
                         tmem_st16(wcol + 64 * h + 16 * j, o);
                     }
-                    if constexpr (C::MIN_TC) {
-                        // row r of the weight-side min-term tile of this buffer: dmn = dmin * m_c
-                        // (exact in f32), half 0 writes tf32 hi = rna(dmn), half 1 lo = dmn - hi
-                        // (at most 6 significant bits: exact); the MMA reads it through the
-                        // async proxy
-                        const float dmin =
-                            reinterpret_cast<const float*>(smem + C::SMEM_SB + sp.i * C::SB_BYTES + SB_DM_OFF)[r];
-                        const uint2 mw = *reinterpret_cast<const uint2*>(scr + 8);
-                        float v[8];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float dmn =
-                                __fmul_rn(dmin, static_cast<float>(((c < 4 ? mw.x : mw.y) >> (8 * (c & 3))) & 0xFFu));
-                            const float hi = tf32_rna(dmn);
-                            v[c] = h == 0 ? hi : __fsub_rn(dmn, hi);
-                        }
-                        uint8_t* dt = smem + C::SMEM_DMN + ab.i * C::DMN_SLOT + h * TF32_TILE_BYTES;
-                        *reinterpret_cast<float4*>(dt + tf32_tile_byte(r, 0)) = make_float4(v[0], v[1], v[2], v[3]);
-                        *reinterpret_cast<float4*>(dt + tf32_tile_byte(r, 4)) = make_float4(v[4], v[5], v[6], v[7]);
-                        fence_proxy_async_smem();
-                    }
                 } else {
 #pragma unroll
                     for (int b = 0; b < NW / 4; ++b) {
@@ -709,7 +628,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     RingPos<C::SBR> sp;
     bool ok = true, had_unit = false;
     int n_tile = 0;
-    uint32_t pgs = 0;                                    // stage number at the unit's start
     float acc[N];
 #pragma unroll
     for (int t = 0; t < N; ++t)
@@ -718,12 +636,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
         const Unit w = unit_of(g, u, nsb);
         n_tile = w.n;
         had_unit = true;
-        const int nst = (w.sb1 - w.sb0) * SPS;
-        // the issuers whose min-term accumulator this unit used (issuer e takes the stages
-        // with global number = e mod 2)
-        const bool use0 = nst >= 2 || (nst == 1 && (pgs & 1u) == 0u);
-        const bool use1 = nst >= 2 || (nst == 1 && (pgs & 1u) == 1u);
-        pgs += static_cast<uint32_t>(nst);
 #pragma unroll
         for (int t = 0; t < N; ++t)
             acc[t] = 0.0f;
@@ -791,7 +703,7 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
                     }
                 }
             }
-            if (Q4 && !C::MIN_TC) {
+            if (Q4) {
                 // min term: acc -= sum_c (dmin * m_c) * (d_a * ssum)_c
                 const float dmin = reinterpret_cast<const float*>(sbe + SB_DM_OFF)[row];
                 const uint2 mw = *reinterpret_cast<const uint2*>(sbe + SB_SC_OFF + row * SC_ROW_BYTES + 8);
@@ -819,27 +731,6 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
         }
         if (!ok)
             break;
-        if constexpr (C::MIN_TC) {
-            // min term of the whole unit: the two issuers' accumulators (every MMA that
-            // feeds them completed before the stage items above were committed)
-            tc_fence_after();
-#pragma unroll
-            for (int gq = 0; gq < NT; ++gq) {
-                float m0[16], m1[16];
-                tmem_ld16x2_wait(lane_addr + C::MIN_COL0 + 16 * gq, lane_addr + C::MIN_COL0 + N + 16 * gq, m0, m1);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    acc[16 * gq + e] -= __fadd_rn(use0 ? m0[e] : 0.0f, use1 ? m1[e] : 0.0f);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (use0)
-                    mbar_arrive(bar(C::BAR_MEMPTY + 0));
-                if (use1)
-                    mbar_arrive(bar(C::BAR_MEMPTY + 1));
-            }
-        }
         if (!clustered) {
             const int j = w.n * BM + row;
             if (j < g.od) {
@@ -928,8 +819,6 @@ __device__ __forceinline__ void ft_body(const FtArgs& g, uint8_t* smem, uint32_t
             mbar_init(bar(C::BAR_TEMPTY + k), NUM_PROMO_WARPS);
         }
         mbar_init(bar(C::BAR_DRAIN), NUM_ISSUERS);
-        mbar_init(bar(C::BAR_MEMPTY + 0), NUM_PROMO_WARPS);
-        mbar_init(bar(C::BAR_MEMPTY + 1), NUM_PROMO_WARPS);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -1140,7 +1029,6 @@ cudaError_t launch_gemm_ft(int type, const void* packed, int od, int id, const v
     a.TQ = static_cast<const uint8_t*>(qa) + ap.tq_off;
     a.IP = sc + ap.ip_off;
     a.FM = sc + ap.fm_off;
-    a.AM = sc + ap.am_off;
     a.Y = Y;
     a.ldy = ldy;
     a.M = M;
@@ -1158,7 +1046,7 @@ cudaError_t launch_gemm_ft(int type, const void* packed, int od, int id, const v
         static const char* const lab[2][9] = {
             {"q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened to sc*q f16 tiles in tensor memory, "
              "weights as the MMA's A, token operand p*d_a*q_a as f16 hi+lo as N, two MMA issuers with one TMEM "
-             "accumulator per stage, min term on the tensor core (tf32 hi/lo) at N = 32, else on the CUDA cores; "
+             "accumulator per stage, min term on the CUDA cores in f32x2 pairs; "
              "K split: none",
              "", "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=2 CTAs",
              "q4_K: few-token GEMM (M <= 64): compact 4-bit codes widened into tensor memory, two MMA issuers; K split: cluster of S=3 CTAs",

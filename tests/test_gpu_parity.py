@@ -741,11 +741,10 @@ def test_gemm_few_token_stack_shapes(typ, M, od, id_, split):
 
 @pytest.mark.parametrize("M,od,id_", [(24, 32001, 512), (32, 20000, 256)])
 def test_gemm_few_token_min_term_across_units(M, od, id_):
-    """q4_K at N = 32 (min term on the tensor core, one TMEM accumulator per issuer per
-    unit): more weight tiles than SMs, so CTAs take several units in turn and each
-    accumulator is handed back by the promotion before the next unit overwrites it;
-    with id = 256 every unit is one super-block and the units of a CTA alternate
-    between the two issuers.  Bit-identical run to run."""
+    """q4_K at N = 32 with more weight tiles than SMs: CTAs take several units in turn,
+    and the min term's chunk-major d_a*ssum values and the accumulator items are reused
+    from unit to unit; with id = 256 every unit is one super-block and the units of a
+    CTA alternate between the two issuers.  Bit-identical run to run."""
     raw = synth.q4k_blocks(od, id_, M + od)
     x = synth.activations(M, id_, M + 3)
     Y = _run_gemm("q4_K", raw, x).cpu().numpy()
