@@ -133,6 +133,11 @@ mmq_status mmq_quantize_act(const float* x, int M, int K, int ldx,
  * so one tile's window is contiguous; [r58] §5 names the same plane for q4_K;
  * [r56] §1 and [r58] §3.2: codes unpacked once at registration).
  *
+ * For q6_K the pack calls then read FLAG word 0 back to the host and return only
+ * when the stream has finished the pack (not while the stream is being captured
+ * into a graph); the GEMM calls on that buffer use it to choose their kernel.  The
+ * choice affects the speed only: every kernel reads FLAG itself.
+ *
  * raw_blocks: od rows x id/256 super-blocks, row-major, 210 B (q6_K: ql[128]@0,
  *   qh[64]@128, int8 scales[16]@192, f16 d@208) or 144 B (q4_K: f16 d@0,
  *   f16 dmin@2, scales[12]@4 = 16 six-bit fields little-endian, fields 0..7 the
@@ -254,8 +259,11 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *    tiles are few, each is split along K over a
  *    cluster of up to 8 CTAs whose partial sums are added in rank order
  *    (deterministic);
- *  - larger M, the super-block kernel (when its 128 x 256 tiles number at least
- *    the SM count): the activation operand p*d_a*q_a as an f16 hi + lo pair
+ *  - larger M, the super-block kernel or the chunk kernel below, whichever a
+ *    round-count cost model of both, fitted to GB300 timings, expects to finish
+ *    first (mmq_debug_route gives the choice; q6_K whose registration found the
+ *    codes in two tiles always takes the chunk kernel).  The super-block kernel:
+ *    the activation operand p*d_a*q_a as an f16 hi + lo pair
  *    (about 2^-21 relative per value) times the exact f16 CODES (and CODES2 for
  *    two-tile q6_K, a second pair of MMAs into the same accumulator), summed over
  *    a whole super-block in f32, then d and 1/p per super-block.  When the last round of tiles fills at most half the SMs (or
@@ -284,6 +292,14 @@ mmq_status mmq_gemm_q4k(const void* packed, int od, int id, const void* qa, cons
  * (I_h = sum(q * q_a) over the chunk's 16-value half h; |value| < 2^24). */
 mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, const void* qa,
                                const void* scales, int M, float* dots, mmq_stream_t s);
+
+/* Debug/verification, host logic only (no CUDA call): the kernel the default
+ * selection of mmq_gemm_* gives for (t, od, id, M) on a device with nsm SMs, for
+ * q6_K codes folded (fold = 1), in two tiles (0) or of unknown state (-1, taken as
+ * folded; q4_K ignores fold): *kernel = 0 weight-streaming, 1 chunk, 2 super-block,
+ * 3 few-token.  MMQ_ERR_ARG for a null kernel, nsm < 1 or fold outside -1..1;
+ * otherwise the shape errors of the GEMM calls. */
+mmq_status mmq_debug_route(mmq_type t, int od, int id, int M, int fold, int nsm, int* kernel);
 
 /* Debug/verification: which kernel computes Y (process-wide).
  *   0 (default): as described above the GEMM calls;

@@ -23,7 +23,7 @@ __all__ = [
     "mmq_packed_weight_bytes",
     "mmq_packed_weight_layout",
     "mmq_pack_weights", "mmq_pack_weights_fused", "mmq_convert_ggml_blocks", "mmq_gemm_q6k", "mmq_gemm_q4k", "mmq_debug_gemm_dots", "mmq_debug_select_large_m_kernel",
-    "mmq_debug_inject_wait_timeout",
+    "mmq_debug_inject_wait_timeout", "mmq_debug_route", "ROUTES",
     "mmq_get_device_error", "mmq_status_string", "mmq_last_path", "mmq_version", "mmq_launch_count",
     "quantize_act", "pack_weights", "pack_weights_fused", "gemm", "gemm_dots", "TYPES",
 ]
@@ -75,6 +75,7 @@ def load():
             "mmq_gemm_q4k": [P, I, I, P, P, I, P, I, P],
             "mmq_debug_gemm_dots": [I, P, I, I, P, P, I, P, P],
             "mmq_debug_select_large_m_kernel": [I],
+            "mmq_debug_route": [I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)],
             "mmq_debug_inject_wait_timeout": [I, ctypes.c_ulonglong],
             "mmq_get_device_error": [P],
         }
@@ -171,6 +172,18 @@ def mmq_debug_gemm_dots(t, packed, od, id_, qa, scales, M, dots, stream=0):
 
 def mmq_debug_select_large_m_kernel(which: int):
     _check(load().mmq_debug_select_large_m_kernel(which), "mmq_debug_select_large_m_kernel")
+
+
+ROUTES = {0: "weight-streaming", 1: "chunk", 2: "super-block", 3: "few-token"}
+
+
+def mmq_debug_route(t, od: int, id_: int, M: int, fold: int = 1, nsm: int = 152) -> str:
+    """The kernel the default selection gives (t, od, id, M) on a device with nsm SMs,
+    for q6_K codes folded (fold 1), in two tiles (0) or of unknown state (-1); host
+    logic only, no CUDA call."""
+    out = ctypes.c_int(-1)
+    _check(load().mmq_debug_route(TYPES.get(t, t), od, id_, M, fold, nsm, ctypes.byref(out)), "mmq_debug_route")
+    return ROUTES[out.value]
 
 
 def mmq_debug_inject_wait_timeout(fill: int, limit_ns: int = 0):

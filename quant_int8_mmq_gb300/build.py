@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmmq_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["api.cu", "prepass.cu", "pack.cu", "ggml.cu", "gemm.cu", "gemm_sb.cu", "gemm_small.cu", "gemm_ft.cu"]
+SOURCES = ["api.cu", "prepass.cu", "pack.cu", "ggml.cu", "gemm.cu", "gemm_sb.cu", "gemm_small.cu", "gemm_ft.cu", "route.cu"]
 PEAKS_SRC = "peaks.cu"
 PEAKS_EXE = os.path.join(BUILD_DIR, "mmq_peaks")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

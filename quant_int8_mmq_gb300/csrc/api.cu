@@ -9,6 +9,7 @@
 
 #include "mmq.h"
 #include "mmq_internal.h"
+#include "route.h"
 
 namespace mmq {
 namespace {
@@ -119,6 +120,34 @@ mmq_status check_device()
 }
 
 mmq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MMQ_OK : MMQ_ERR_CUDA; }
+
+// After a pack: for q6_K, read the fold flag (FLAG word 0) back once, so that GEMM
+// calls on this buffer choose their kernel without a device read.  The read waits for
+// the stream.  While the stream is being captured into a graph nothing is read and any
+// earlier record for the address is dropped (GEMMs then take the codes as folded).
+cudaError_t note_fold_state(mmq_type t, const void* packed, int od, int id, cudaStream_t s)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || t != MMQ_Q6_K)
+        return e;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess)
+        return e;
+    if (cap != cudaStreamCaptureStatusNone) {
+        mmq::note_packed(dev, packed, static_cast<int>(t), od, id, -1);
+        return cudaSuccess;
+    }
+    const mmq::WeightPlanes wp = mmq::weight_planes(static_cast<int>(t), od, id);
+    uint32_t flag = 0;
+    e = cudaMemcpyAsync(&flag, static_cast<const uint8_t*>(packed) + wp.flag_off, sizeof(flag),
+                        cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    mmq::note_packed(dev, packed, static_cast<int>(t), od, id, e == cudaSuccess ? (flag != 0 ? 1 : 0) : -1);
+    return e;
+}
 
 mmq_status check_weight_shape(mmq_type t, int od, int id)
 {
@@ -293,8 +322,11 @@ mmq_status mmq_pack_weights(mmq_type t, const void* raw_blocks, int od, int id, 
     st = check_device();
     if (st != MMQ_OK)
         return st;
-    return from_cuda(mmq::launch_pack(static_cast<int>(t), raw_blocks, od, raw_blocks, od, id, packed,
-                                      reinterpret_cast<cudaStream_t>(s)));
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    cudaError_t e = mmq::launch_pack(static_cast<int>(t), raw_blocks, od, raw_blocks, od, id, packed, cs);
+    if (e == cudaSuccess)
+        e = note_fold_state(t, packed, od, id, cs);
+    return from_cuda(e);
 }
 
 mmq_status mmq_pack_weights_fused(mmq_type t, const void* raw_a, int od_a, const void* raw_b, int od_b, int id,
@@ -314,8 +346,11 @@ mmq_status mmq_pack_weights_fused(mmq_type t, const void* raw_a, int od_a, const
     st = check_device();
     if (st != MMQ_OK)
         return st;
-    return from_cuda(mmq::launch_pack(static_cast<int>(t), raw_a, od_a, raw_b, od_a + od_b, id, packed,
-                                      reinterpret_cast<cudaStream_t>(s)));
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    cudaError_t e = mmq::launch_pack(static_cast<int>(t), raw_a, od_a, raw_b, od_a + od_b, id, packed, cs);
+    if (e == cudaSuccess)
+        e = note_fold_state(t, packed, od_a + od_b, id, cs);
+    return from_cuda(e);
 }
 
 mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, void* dst, mmq_stream_t s)
@@ -349,6 +384,24 @@ mmq_status mmq_debug_gemm_dots(mmq_type t, const void* packed, int od, int id, c
                                int M, float* dots, mmq_stream_t s)
 {
     return gemm_common(t, mmq::GEMM_DOTS, packed, od, id, qa, scales, M, dots, od, s);
+}
+
+mmq_status mmq_debug_route(mmq_type t, int od, int id, int M, int fold, int nsm, int* kernel)
+{
+    mmq_status st = check_weight_shape(t, od, id);
+    if (st != MMQ_OK)
+        return st;
+    if (!kernel || nsm < 1 || fold < -1 || fold > 1)
+        return MMQ_ERR_ARG;
+    if (M < 1 || M > MMQ_MAX_M)
+        return MMQ_ERR_SHAPE;
+    if (takes_streaming_path(t, od, id, M))
+        *kernel = 0;
+    else if (M <= MMQ_FT_MAX_M)
+        *kernel = 3;
+    else
+        *kernel = mmq::prefer_superblock(static_cast<int>(t), od, id, M, nsm, t == MMQ_Q6_K ? fold : 1) ? 2 : 1;
+    return MMQ_OK;
 }
 
 mmq_status mmq_debug_select_large_m_kernel(int which)

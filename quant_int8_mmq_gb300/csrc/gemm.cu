@@ -61,6 +61,7 @@
 #include <atomic>
 
 #include "mmq_internal.h"
+#include "route.h"
 #include "ptx.cuh"
 
 namespace mmq {
@@ -682,12 +683,15 @@ cudaError_t launch_gemm(int type, GemmMode mode, const void* packed, int od, int
     e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    // Y goes to the super-block kernel when its 128 x 256 tiles fill every SM at least
-    // once (fewer, larger tiles lose more to idle SMs than the faster contraction wins
-    // back), else to this chunk kernel; both read the one- or two-tile q6_K codes.
+    // Y goes to the super-block kernel or to this chunk kernel by a round-count cost
+    // model of both (two-tile q6_K always here); both read the one- or two-tile q6_K
+    // codes, so the fold state recorded at registration only steers the speed.
     const int sel = g_large_m_kernel.load();
-    const bool sb_fills = static_cast<long long>(ceil_div(M, BM)) * ceil_div(od, 2 * BN) >= nsm;
-    const bool sb_first = mode == GEMM_Y && (sel == 2 || (sel == 0 && sb_fills));
+    const bool sb_first =
+        mode == GEMM_Y &&
+        (sel == 2 || (sel == 0 && M > FT_MAX_M &&
+                      prefer_superblock(type, od, id, M, nsm,
+                                        type == 14 ? packed_fold_state(dev, packed, type, od, id) : 1)));
     WaitCtl wc;
     bool injected = false;
     e = take_wait_ctl(&wc, &injected);

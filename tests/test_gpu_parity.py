@@ -342,7 +342,7 @@ def test_gemm_fused_ffn_gate_up_at_prompt_length_sampled():
     fused = mmq.pack_weights_fused("q4_K", _to_dev(ra.reshape(-1)), od, _to_dev(rb.reshape(-1)), od, id_)
     Y = mmq.gemm("q4_K", fused, 2 * od, id_, qa, sc, M)
     _sync()
-    assert "super-block" in mmq.mmq_last_path()
+    assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
     Y = Y.cpu().numpy()
     rows = np.unique(np.r_[0, 127, 128, 3200, M - 1, np.random.default_rng(7).integers(0, M, 3)])
     for part, raw in ((Y[:, :od], ra), (Y[:, od:], rb)):
@@ -389,7 +389,7 @@ def test_gemm_dots_bit_exact(typ, M, od, id_):
 @pytest.fixture(params=["auto", "super-block"])
 def y_kernel(request):
     """Y through the default kernel choice, and through the super-block kernel forced
-    (the default takes it only when its 128 x 256 tiles fill the GPU)."""
+    (the default takes it where its cost model expects it to finish first)."""
     mmq.mmq_debug_select_large_m_kernel(0 if request.param == "auto" else 2)
     yield request.param
     mmq.mmq_debug_select_large_m_kernel(0)
@@ -397,7 +397,7 @@ def y_kernel(request):
 
 def _check_label(typ, y_kernel, M):
     if y_kernel == "super-block" and M > mmq.SMALL_M:
-        assert "super-block" in mmq.mmq_last_path()
+        assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
 
 
 def _run_gemm(typ, raw, x, Y=None):
@@ -517,8 +517,15 @@ def test_gemm_deterministic(y_kernel):
 
 
 # --------------------------------------------------------------------------- last-round K split
+@pytest.fixture
+def superblock_kernel():
+    mmq.mmq_debug_select_large_m_kernel(2)
+    yield
+    mmq.mmq_debug_select_large_m_kernel(0)
+
+
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K", "q6_K_full"])
-def test_gemm_last_round_split_parity(typ):
+def test_gemm_last_round_split_parity(superblock_kernel, typ):
     """Super-block kernel: 8 x 20 = 160 tiles of 128 x 256 on 152 SMs, the 8 tiles of the
     last round run as two K-halves that add into a zeroed Y (odd super-block count:
     halves of 1 and 2); ragged od (last tile 236 rows); q6_K_full runs its two exact
@@ -528,13 +535,13 @@ def test_gemm_last_round_split_parity(typ):
     raw = _q6_raw(od, id_, 41, typ == "q6_K_full") if t == "q6_K" else synth.q4k_blocks(od, id_, 41)
     x = synth.activations(M, id_, 42)
     Y = _run_gemm(t, raw, x).cpu().numpy()
-    assert "super-block" in mmq.mmq_last_path()
+    assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(t, raw, x)
     assert_y_close(Y, Yo, S)
 
 
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
-def test_gemm_third_round_halves_parity(typ):
+def test_gemm_third_round_halves_parity(superblock_kernel, typ):
     """Super-block kernel: 8 x 40 = 320 tiles on 152 SMs leave 16 tiles for a third
     round, which run as two K-halves each (one super-block apiece) added into a zeroed
     Y after two whole rounds; ragged M (last tile 104 tokens) and od (last tile 216
@@ -543,7 +550,7 @@ def test_gemm_third_round_halves_parity(typ):
     raw = _q6_raw(od, id_, 45, False) if typ == "q6_K" else synth.q4k_blocks(od, id_, 45)
     x = synth.activations(M, id_, 46)
     Y = _run_gemm(typ, raw, x).cpu().numpy()
-    assert "super-block" in mmq.mmq_last_path()
+    assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
     Yo, S = oracle_gemm(typ, raw, x)
     assert_y_close(Y, Yo, S)
     again = _run_gemm(typ, raw, x).cpu().numpy()
@@ -551,7 +558,7 @@ def test_gemm_third_round_halves_parity(typ):
 
 
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
-def test_superblock_back_to_back_calls_share_buffers(typ):
+def test_superblock_back_to_back_calls_share_buffers(superblock_kernel, typ):
     """Prepass and super-block GEMM calls queued on one stream with no synchronisation in
     between, all through the same activation planes, and the last two GEMMs writing the
     same Y.  Both are dependent launches: a GEMM's set-up overlaps the prepass ahead of
@@ -579,7 +586,7 @@ def test_superblock_back_to_back_calls_share_buffers(typ):
             packs[i % 2] = gpu_pack(typ, raws[i % 2])
         Y = shared[:M] if i >= len(xd) - 2 else None
         outs.append(mmq.gemm(typ, packs[i % 2], od, id_, qa, sc, M, Y=Y))
-        assert "super-block" in mmq.mmq_last_path()
+        assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
     _sync()
     assert mmq.mmq_get_device_error() == 0
     for i, (x, Y) in enumerate(zip(xs, outs)):
@@ -622,7 +629,7 @@ def _dynamic_range_cases(x, od, id_):
     for typ in ("q4_K", "q6_K"):
         raw = _raw(typ, od, id_, seed=93)
         Y = _run_gemm(typ, raw, x).cpu().numpy()
-        assert "super-block" in mmq.mmq_last_path()
+        assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
         Yo, S = oracle_gemm(typ, raw, x)
         assert_y_close(Y, Yo, S)
 
@@ -1016,3 +1023,63 @@ def test_ggml_weights_end_to_end(typ, M, od, id_):
     _sync()
     Yo, S = oracle_gemm(typ, raw, x)
     assert_y_close(Y.cpu().numpy(), Yo, S)
+
+
+# --------------------------------------------------------------------------- default kernel choice
+def _route_of(path):
+    # the chunk kernel's label ends in "d per super-block": test it first
+    for key, name in (("chunk GEMM", "chunk"), ("super-block tcgen05 GEMM", "super-block"),
+                      ("few-token GEMM", "few-token"), ("weight-streaming", "weight-streaming")):
+        if key in path:
+            return name
+    raise AssertionError(path)
+
+
+def _sampled_rows_close(typ, raw, x, Y, rows):
+    Yo, S = oracle_gemm(typ, raw, x[rows])
+    assert_y_close(Y[rows], Yo, S)
+
+
+@pytest.mark.parametrize("typ,od,id_,M", [
+    ("q4_K", 4096, 4096, 1024),       # super-block: 128 tiles of 128 x 256, fewer than the SMs
+    ("q4_K", 4096, 4096, 512),        # chunk
+    ("q6_K", 4096, 4096, 1024),       # super-block (folded codes)
+    ("q6_K_full", 4096, 4096, 1024),  # chunk (two tiles, recorded at registration)
+    ("q6_K", 4097, 11008, 1152),      # chunk: 153 super-block tiles leave one for a second round
+    ("q6_K_full", 4097, 2048, 300),
+])
+def test_gemm_takes_the_routed_kernel(typ, od, id_, M):
+    """A call with the default selection runs the kernel mmq_debug_route names for this
+    device and the fold state the pack recorded, and Y is the oracle's on sampled tokens."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    full = typ.endswith("full")
+    raw = _q6_raw(od, id_, 77, full) if t == "q6_K" else synth.q4k_blocks(od, id_, 77)
+    x = synth.activations(M, id_, 78)
+    Y = _run_gemm(t, raw, x).cpu().numpy()
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _route_of(mmq.mmq_last_path()) == mmq.mmq_debug_route(t, od, id_, M, 0 if full else 1, nsm)
+    _sampled_rows_close(t, raw, x, Y, [0, 1, M // 2, M - 1])
+
+
+def test_gemm_on_an_unrecorded_buffer_routes_as_folded_and_stays_exact():
+    """A copy of a packed two-tile q6_K weight has no registration record, so the call
+    takes the codes as folded (the super-block kernel here) and that kernel, reading the
+    flag itself, still runs the two exact tiles: Y equals the recorded buffer's (chunk
+    kernel) within the bound, and the oracle's on sampled tokens."""
+    od, id_, M = 4096, 4096, 1024
+    raw = _q6_raw(od, id_, 79, True)
+    x = synth.activations(M, id_, 80)
+    qa, sc = gpu_quantize(x)
+    packed = gpu_pack("q6_K", raw)
+    Ya = mmq.gemm("q6_K", packed, od, id_, qa, sc, M)
+    _sync()
+    assert _route_of(mmq.mmq_last_path()) == "chunk"
+    copy = packed.clone()
+    Yb = mmq.gemm("q6_K", copy, od, id_, qa, sc, M)
+    _sync()
+    assert _route_of(mmq.mmq_last_path()) == "super-block"
+    Ya, Yb = Ya.cpu().numpy(), Yb.cpu().numpy()
+    rows = [0, 513, M - 1]
+    _sampled_rows_close("q6_K", raw, x, Ya, rows)
+    _sampled_rows_close("q6_K", raw, x, Yb, rows)
+    assert np.max(np.abs(Ya - Yb)) <= 2e-5 * np.max(np.abs(Ya))

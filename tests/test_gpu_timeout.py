@@ -39,8 +39,8 @@ def _raw(typ, od, id_, seed):
 
 
 @pytest.mark.parametrize("selector,typ,M,od,id_,label", [
-    (2, "q4_K", 200, 300, 768, "super-block"),
-    (2, "q6_K", 200, 300, 768, "super-block"),
+    (2, "q4_K", 200, 300, 768, "super-block tcgen05 GEMM"),
+    (2, "q6_K", 200, 300, 768, "super-block tcgen05 GEMM"),
     (1, "q4_K", 200, 300, 768, "chunk GEMM"),
     (1, "q6_K_full", 200, 300, 768, "chunk GEMM"),
     (0, "q4_K", 31, 259, 768, "few-token GEMM"),
