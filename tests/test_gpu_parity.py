@@ -1083,3 +1083,20 @@ def test_gemm_on_an_unrecorded_buffer_routes_as_folded_and_stays_exact():
     _sampled_rows_close("q6_K", raw, x, Ya, rows)
     _sampled_rows_close("q6_K", raw, x, Yb, rows)
     assert np.max(np.abs(Ya - Yb)) <= 2e-5 * np.max(np.abs(Ya))
+
+
+def test_repacking_a_buffer_updates_its_route():
+    """Packing other q6_K weights into the same buffer replaces its record: two-tile codes
+    send the call to the chunk kernel, folded codes packed over them to the super-block
+    kernel, and back; every Y is the oracle's on sampled tokens."""
+    od, id_, M = 4096, 4096, 1024
+    x = synth.activations(M, id_, 83)
+    qa, sc = gpu_quantize(x)
+    buf = None
+    for full, want in ((True, "chunk"), (False, "super-block"), (True, "chunk")):
+        raw = _q6_raw(od, id_, 84 + int(full), full)
+        buf = mmq.pack_weights("q6_K", _to_dev(raw.reshape(-1)), od, id_, packed=buf)
+        Y = mmq.gemm("q6_K", buf, od, id_, qa, sc, M)
+        _sync()
+        assert _route_of(mmq.mmq_last_path()) == want
+        _sampled_rows_close("q6_K", raw, x, Y.cpu().numpy(), [0, M - 1])
