@@ -558,6 +558,46 @@ def exact_path_case(lib, packed, qa, sc, xh, stream, M, peaks):
     return out
 
 
+def q6k_full_range_cases(lib, dev, stream, M, xh, xf, qa, sc, peaks, min_bytes=300e6):
+    """The stack's q6_K shapes with sub-block scales over the whole int8 range, as a
+    quantizer that maps each super-block's largest scale to +-127 makes them (no tensor
+    folds into one f16 tile): per shape the default choice, steered by the fold state the
+    pack recorded (the chunk kernel), beside the super-block kernel forced, at the prompt
+    length over rotated weight copies (at least 300 MB, more than L2)."""
+    import torch
+    import quant_int8_mmq_gb300 as mmq
+    out = []
+    for od, id_, x in ((4096, 11008, xf), (4096, 4096, xh), (32000, 4096, xh)):
+        lib.mmq_quantize_act(x.data_ptr(), M, id_, id_, qa.data_ptr(), sc.data_ptr(), stream.cuda_stream)
+        nb = mmq.mmq_packed_weight_bytes(mmq.MMQ_Q6_K, od, id_)
+        pks = []
+        for c in range(max(2, int(-(-min_bytes // nb)))):
+            raw = torch.from_numpy(synth.q6k_blocks(od, id_, 7100 + c, sc_lo=-128, sc_hi=127).reshape(-1)).to(dev)
+            pks.append(mmq.pack_weights("q6_K", raw, od, id_))
+            del raw
+        Y = torch.empty((M, od), dtype=torch.float32, device=dev)
+        calls = [(lambda s, p=p: lib.mmq_gemm_q6k(p.data_ptr(), od, id_, qa.data_ptr(), sc.data_ptr(), M,
+                                                  Y.data_ptr(), od, s)) for p in pks]
+        case = {"shape": f"q6_K {od}x{id_}", "M": M, "weight_copies": len(pks)}
+        for key, sel in (("default", 0), ("super_block_forced", 2)):
+            mmq.mmq_debug_select_large_m_kernel(sel)
+            try:
+                calls[0](stream.cuda_stream)
+                torch.cuda.synchronize()
+                label = mmq.mmq_last_path()
+                t = graph_time(calls, stream, 4 * len(calls))
+            finally:
+                mmq.mmq_debug_select_large_m_kernel(0)
+            tf = 2.0 * M * od * id_ / t / 1e12
+            case[key] = {"us": t * 1e6, "tflops_int8_equiv": tf, "frac": tf / peaks["bf16_tflops_sustained"],
+                         "path": label.split(":")[1].split("(")[0].split(",")[0].strip() if ":" in label else label}
+        out.append(case)
+        del pks, calls, Y
+    if mmq.mmq_get_device_error() != 0:
+        raise RuntimeError("device error in the full-range q6_K cases")
+    return {"scales": "q6_K sub-block scales U[-128,127]: two exact tiles per k-block", "cases": out}
+
+
 def fused_pair_cases(lib, dev, stream, M, xh, qa, sc, copies=2):
     """q+k and gate+up of one layer as one GEMM over a fused packed weight (one weight
     pass, one launch) against the two GEMMs on the same quantised activations."""
@@ -810,6 +850,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and side:
         line["exact_path"] = exact_path_case(lib, packed, qa, sc, xh, stream, M, peaks)
         line["fused_shared_inputs"] = fused_pair_cases(lib, dev, stream, M, xh, qa, sc)
+        line["q6k_full_range"] = q6k_full_range_cases(lib, dev, stream, M, xh, xf, qa, sc, peaks)
         line["small_m"] = small_m_cases(lib, dev, stream, peaks)
         if not args.no_configs:
             import oracle
