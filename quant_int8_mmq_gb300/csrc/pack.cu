@@ -236,7 +236,6 @@ template <int TYPE>
 __global__ void __launch_bounds__(256) raw_relayout_kernel(const RawRows raw, long long nblocks,
                                                            uint32_t* __restrict__ out)
 {
-    constexpr int IN = (TYPE == 12) ? Q4K_BYTES : Q6K_BYTES;
     constexpr int OUTW = raw_block_bytes(TYPE) / 4;
     const long long words = nblocks * OUTW;
     for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < words;
