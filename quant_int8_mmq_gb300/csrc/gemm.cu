@@ -95,6 +95,9 @@ constexpr int SB_AS_BYTES = 8 * BM * 8;            // {d, ssum} x 8 chunks x 128
 constexpr int SB_BYTES = SB_AS_OFF + SB_AS_BYTES;
 // q4_K min-term operands per super-block (token hi, lo tiles; weight hi, lo tiles),
 // streamed through the operand ring after a tile's last k-block.
+// q4_K min term: super-blocks per TMEM item (one f32 subtraction by the promotion each);
+// shapes with id <= 64 * 256 take one item per tile.
+constexpr int MIN_GROUP_SB = 64;
 constexpr int MIN_AM_BYTES = 2 * TF32_TILE_BYTES;
 constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;
 static_assert(MIN_AM_BYTES <= TILE_BYTES && MIN_BM_BYTES <= TILE_BYTES, "min-term operands fit a stage");
@@ -394,16 +397,18 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     umma_commit(bar(BAR_EMPTY + op.i));  // operand stage free once these MMAs finish
                     op.next();
                 }
-                if (Q4 && ok) {
-                    // Min-term contraction of the whole tile, sum over chunks of
-                    // (d_a*ssum)(dmin*m), one super-block (8 chunks, hi/lo split) per stage
-                    // into one item, consumed by the promotion once per tile.
+                // Min-term contraction of the tile, sum over chunks of (d_a*ssum)(dmin*m),
+                // one super-block (8 chunks, hi/lo split) per stage, into one item per
+                // MIN_GROUP_SB super-blocks that the promotion subtracts in f32: the tensor
+                // core's own accumulation then never chains more than 3 * MIN_GROUP_SB MMAs.
+                for (int g0 = w.sb0; Q4 && ok && g0 < w.sb1; g0 += MIN_GROUP_SB) {
+                    const int g1 = min(g0 + MIN_GROUP_SB, w.sb1);
                     if (!ctl_wait(g, bar(BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                    for (int s = w.sb0; s < w.sb1; ++s) {
+                    for (int s = g0; s < g1; ++s) {
                         if (!ctl_wait(g, bar(BAR_FULL + op.i), op.ph)) {
                             ok = false;
                             break;
@@ -413,7 +418,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                         const uint32_t bm = sbase + SMEM_B + op.i * B_STAGE;
                         const uint64_t ahi = sdesc_tf32_tile(am), alo = sdesc_tf32_tile(am + TF32_TILE_BYTES);
                         const uint64_t bhi = sdesc_tf32_tile(bm), blo = sdesc_tf32_tile(bm + TF32_TILE_BYTES);
-                        umma_tf32(d, ahi, bhi, idesc_t, s > w.sb0 ? 1u : 0u);
+                        umma_tf32(d, ahi, bhi, idesc_t, s > g0 ? 1u : 0u);
                         umma_tf32(d, ahi, blo, idesc_t, 1u);
                         umma_tf32(d, alo, bhi, idesc_t, 1u);
                         umma_commit(bar(BAR_EMPTY + op.i));
@@ -519,8 +524,8 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
         }
         if (!ok)
             break;
-        if (Q4) {
-            // acc -= the tile's min term, one item per tile
+        // acc -= the tile's min term, one item per MIN_GROUP_SB super-blocks
+        for (int g0 = w.sb0; Q4 && g0 < w.sb1; g0 += MIN_GROUP_SB) {
             if (!warp_wait(g, bar(BAR_TFULL + item.i), item.ph)) {
                 ok = false;
                 break;
@@ -535,6 +540,8 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& g, uint8_t* smem, uin
                     acc[i] = ffma2(make_float2(-1.0f, -1.0f), make_float2(mn[2 * i], mn[2 * i + 1]), acc[i]);
             }
         }
+        if (!ok)
+            break;
         if (MODE == GEMM_Y && row < g.M) {
             float* yrow = g.out + static_cast<size_t>(row) * g.ldy;
 #pragma unroll

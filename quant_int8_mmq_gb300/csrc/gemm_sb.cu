@@ -93,6 +93,12 @@ constexpr int MIN_BM_BYTES = 2 * TF32_TILE_BYTES;      // per 128-row weight til
 // Min-term super-blocks per stage: a stage of one super-block holds only 384 cycles of
 // tensor work, too little to cover the copy latency of the next.
 constexpr int MIN_PER_STAGE = 2;
+// Min-term super-blocks per TMEM item, each subtracted by the promotion in f32, so that the
+// tensor core's own accumulation never chains more than 3 * MIN_GROUP_SB MMAs; shapes with
+// id <= 64 * 256 take one item per tile.  A multiple of MIN_PER_STAGE: no stage straddles
+// two items.
+constexpr int MIN_GROUP_SB = 64;
+static_assert(MIN_GROUP_SB % MIN_PER_STAGE == 0, "min-term groups hold whole stages");
 
 // One super-block entry: weight d of the 256 rows, then {d, ssum} of the 8 chunks
 // for the 128 tokens ([chunk][token]) (both copied in), then 1/p per token (written
@@ -480,14 +486,15 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                         item.next();
                     }
                 }
-                if (Q4 && ok) {
+                for (int g0 = w.sb0; Q4 && ok && g0 < w.sb1; g0 += MIN_GROUP_SB) {
+                    const int g1 = min(g0 + MIN_GROUP_SB, w.sb1);
                     if (!ctl_wait(g, bar(L::BAR_TEMPTY + item.i), item.ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t d = tmem_base + item.i * ITEM_COLS;
-                    for (int s = w.sb0; s < w.sb1; s += MIN_PER_STAGE) {
-                        const int ne = min(MIN_PER_STAGE, w.sb1 - s);
+                    for (int s = g0; s < g1; s += MIN_PER_STAGE) {
+                        const int ne = min(MIN_PER_STAGE, g1 - s);
                         if (!ctl_wait(g, bar(L::BAR_CONV + op.i), op.ph) || !ctl_wait(g, bar(L::BAR_FULLB + op.i), op.ph)) {
                             ok = false;
                             break;
@@ -499,7 +506,7 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                             const uint32_t bb = st + ST_B + e * 2 * MIN_BM_BYTES;
                             const uint64_t ahi = sdesc_tf32(aa), alo = sdesc_tf32(aa + TF32_TILE_BYTES);
                             const uint64_t bhi = sdesc_tf32(bb), blo = sdesc_tf32(bb + 2 * TF32_TILE_BYTES);
-                            mma_tf32(d, ahi, bhi, idesc_t, (s + e > w.sb0) ? 1u : 0u);
+                            mma_tf32(d, ahi, bhi, idesc_t, (s + e > g0) ? 1u : 0u);
                             mma_tf32(d, ahi, blo, idesc_t, 1u);
                             mma_tf32(d, alo, bhi, idesc_t, 1u);
                         }
@@ -641,10 +648,11 @@ __device__ __forceinline__ void sb_roles(const SbArgs& g, uint8_t* smem, uint32_
                 for (int n = 0; n < 16; ++n)
                     acc[h][rho][n] = make_float2(0.0f, 0.0f);
         // One item per super-block: acc += d_sb * (D / p); for q4_K one more item per
-        // tile, the min term, taken with d = 1 and 1/p = -1 (acc -= min term).
-        const int s_end = Q4 ? w.sb1 + 1 : w.sb1;
+        // MIN_GROUP_SB super-blocks of the tile, the min term, taken with d = 1 and
+        // 1/p = -1 (acc -= min term).
+        const int s_end = Q4 ? w.sb1 + (w.sb1 - w.sb0 + MIN_GROUP_SB - 1) / MIN_GROUP_SB : w.sb1;
         for (int s = w.sb0; s < s_end; ++s) {
-            const bool min_item = Q4 && s == w.sb1;
+            const bool min_item = Q4 && s >= w.sb1;
             float ip[2][2] = {{-1.0f, -1.0f}, {-1.0f, -1.0f}};
             const float2* d2 = nullptr;
             if (!min_item) {

@@ -1100,3 +1100,88 @@ def test_repacking_a_buffer_updates_its_route():
         _sync()
         assert _route_of(mmq.mmq_last_path()) == want
         _sampled_rows_close("q6_K", raw, x, Y.cpu().numpy(), [0, M - 1])
+
+
+# --------------------------------------------------------------------------- maximum sizes
+def _rows_of(Y, rows):
+    return Y[torch.tensor(rows, device=Y.device)].cpu().numpy()
+
+
+@pytest.mark.parametrize("selector", [0, 1])
+def test_gemm_output_beyond_2_31_elements(selector):
+    """Y with more than 2^31 elements (65 600 x 32 800, row stride od + 8): the stores of
+    the last tokens sit past every 32-bit element offset.  The default choice (super-block
+    kernel) and the chunk kernel; sampled tokens against the oracle, the padding columns
+    untouched."""
+    M, od, id_ = 65600, 32800, 256
+    ldy = od + 8
+    assert M * ldy > 2 ** 31
+    raw = synth.q4k_blocks(od, id_, 301)
+    x = synth.activations(M, id_, 302)
+    qa, sc = gpu_quantize(x)
+    packed = gpu_pack("q4_K", raw)
+    buf = torch.full((M, ldy), float("nan"), dtype=torch.float32, device=DEV)
+    mmq.mmq_debug_select_large_m_kernel(selector)
+    try:
+        mmq.gemm("q4_K", packed, od, id_, qa, sc, M, Y=buf[:, :od])
+        _sync()
+        assert _route_of(mmq.mmq_last_path()) == ("chunk" if selector == 1 else "super-block")
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+    rows = [0, 1, 32768, M - 2, M - 1]
+    got = _rows_of(buf, rows)
+    assert np.isnan(got[:, od:]).all()
+    Yo, S = oracle_gemm("q4_K", raw, x[rows])
+    assert_y_close(got[:, :od], Yo, S)
+    del buf
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("typ", ["q4_K", "q6_K_full"])
+def test_gemm_at_the_largest_k(typ):
+    """id = MMQ_MAX_ID (2^20 values, 4096 super-blocks per row) with a ragged od of 130:
+    the weight-streaming (3 tokens), few-token (31, K split over a cluster) and tile (70,
+    both tile kernels) kernels, sampled tokens against the oracle.  Here |Y| is about
+    130 times smaller than the sum of |terms| (2^20 random terms cancel), so the normwise
+    bound is the demanding one: it failed (1.45e-5) while the tile kernels accumulated
+    the q4_K min term of a whole 2^20-value row in one tensor-core chain of 12 288 tf32
+    MMAs, and holds now that a chain covers at most 64 super-blocks."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    od, id_ = 130, 1 << 20
+    raw = _q6_raw(od, id_, 303, True) if t == "q6_K" else synth.q4k_blocks(od, id_, 303)
+    packed = gpu_pack(t, raw)
+    for M, sel, want in ((3, 0, "weight-streaming"), (31, 0, "few-token"), (70, 1, "chunk"),
+                         (70, 2, "super-block")):
+        x = synth.activations(M, id_, 304 + M)
+        qa, sc = gpu_quantize(x)
+        mmq.mmq_debug_select_large_m_kernel(sel)
+        try:
+            Y = mmq.gemm(t, packed, od, id_, qa, sc, M)
+            _sync()
+        finally:
+            mmq.mmq_debug_select_large_m_kernel(0)
+        assert _route_of(mmq.mmq_last_path()) == want
+        rows = [0, M - 1]
+        Yo, S = oracle_gemm(t, raw, x[rows])
+        assert_y_close(_rows_of(Y, rows), Yo, S)
+        del qa, sc, Y
+
+
+def test_gemm_at_the_largest_od():
+    """od = MMQ_MAX_OD (2^22 weight rows) at id = 256: the weight-streaming kernel at 2
+    tokens (2^20 CTAs of 4 rows), the few-token kernel at 40 (32 768 row tiles on a
+    persistent grid) and a tile kernel at 70; sampled tokens against the oracle."""
+    od, id_ = 1 << 22, 256
+    raw = synth.q4k_blocks(od, id_, 305)
+    packed = gpu_pack("q4_K", raw)
+    for M in (2, 40, 70):
+        x = synth.activations(M, id_, 306 + M)
+        qa, sc = gpu_quantize(x)
+        Y = mmq.gemm("q4_K", packed, od, id_, qa, sc, M)
+        _sync()
+        rows = [0, M - 1]
+        Yo, S = oracle_gemm("q4_K", raw, x[rows])
+        assert_y_close(_rows_of(Y, rows), Yo, S)
+        del qa, sc, Y
+    del packed
+    torch.cuda.empty_cache()
