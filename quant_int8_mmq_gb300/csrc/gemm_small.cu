@@ -87,7 +87,13 @@ __device__ __forceinline__ void q6k_group(uint32_t ql_word, uint32_t h16, uint32
     odd = __vsub4(qo, 0x20202020u);
 }
 
-template <int TYPE, int MT, int R, int WARPS = small_warps(TYPE, MT), int THREADS = WARPS * 32>
+// q4_K at 5 to 8 tokens forms each row's scale products and int8 code words once per
+// chunk rather than once per token.  Measured on GB300 (weights streamed from HBM) over
+// ten q4_K shapes: 1-8 % faster at 5 tokens (one shape, 32000x4096, 2 % slower); at 3-4
+// tokens the change went either way by shape (-26 % to +17 %), and q6_K was 0-7 % slower
+// at every token count, so those keep the per-token form.
+template <int TYPE, int MT, int R, int WARPS = small_warps(TYPE, MT), int THREADS = WARPS * 32,
+          bool HOIST = (TYPE == 12 && MT == 8)>
 __global__ void __launch_bounds__(THREADS) gemm_small_kernel(const uint8_t* __restrict__ raw, int od, int id,
                                                              const int8_t* __restrict__ qa8,
                                                              const uint2* __restrict__ pairs, int M,
@@ -151,6 +157,71 @@ __global__ void __launch_bounds__(THREADS) gemm_small_kernel(const uint8_t* __re
             const int cc = c & 7;
             const uint4(&w0)[R] = w0u[u];
             const uint4(&w1)[R] = w1u[u];
+            if constexpr (HOIST) {
+                // each row's scale products and int8 code words once per chunk, then every
+                // token against them (the same operations per (row, token) as below)
+                float s0[R], s1[R];
+                uint32_t qa_[R][4], qb_[R][4];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (TYPE == 12) {
+                        const uint4 meta = w1[r];
+                        const float d = f16_bits_to_f32(meta.x), dmin = f16_bits_to_f32(meta.x >> 16);
+                        s0[r] = __fmul_rn(d, static_cast<float>(q4k_field6(meta.y, meta.z, meta.w, cc)));
+                        s1[r] = __fmul_rn(dmin, static_cast<float>(q4k_field6(meta.y, meta.z, meta.w, 8 + cc)));
+                        const uint32_t qw[4] = {w0[r].x, w0[r].y, w0[r].z, w0[r].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            qa_[r][i] = qw[i] & 0x0F0F0F0Fu;
+                            qb_[r][i] = (qw[i] >> 4) & 0x0F0F0F0Fu;
+                        }
+                    } else {
+                        const float d = f16_bits_to_f32(w1[r].w);
+                        s0[r] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w1[r].z & 0xFFu)));
+                        s1[r] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>((w1[r].z >> 8) & 0xFFu)));
+                        q6k_group(w0[r].x, w1[r].x & 0xFFFFu, qa_[r][0], qb_[r][0]);
+                        q6k_group(w0[r].y, w1[r].x >> 16, qa_[r][1], qb_[r][1]);
+                        q6k_group(w0[r].z, w1[r].y & 0xFFFFu, qa_[r][2], qb_[r][2]);
+                        q6k_group(w0[r].w, w1[r].y >> 16, qa_[r][3], qb_[r][3]);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (t >= M)
+                        break;
+                    const uint4* ap = reinterpret_cast<const uint4*>(qa8 + static_cast<size_t>(t) * id + c * CHUNK);
+                    const uint4 v0 = __ldg(ap), v1 = __ldg(ap + 1);
+                    const uint32_t a[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    const uint2 pr = __ldg(pairs + static_cast<size_t>(c) * TILE_ROWS + t);
+                    const float da = __uint_as_float(pr.x);
+                    const float ma = __fmul_rn(da, static_cast<float>(static_cast<int>(pr.y)));
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (TYPE == 12) {
+                            int I = 0;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                I = __dp4a(static_cast<int>(qa_[r][i]), static_cast<int>(a[2 * i]), I);
+                                I = __dp4a(static_cast<int>(qb_[r][i]), static_cast<int>(a[2 * i + 1]), I);
+                            }
+                            acc[r][t] = fmaf(da, __fmul_rn(s0[r], static_cast<float>(I)), acc[r][t]);
+                            acc[r][t] = fmaf(-ma, s1[r], acc[r][t]);
+                        } else {
+                            int I0 = 0, I1 = 0;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                I0 = __dp4a(static_cast<int>(qa_[r][i]), static_cast<int>(a[2 * i]), I0);
+                                I0 = __dp4a(static_cast<int>(qb_[r][i]), static_cast<int>(a[2 * i + 1]), I0);
+                                I1 = __dp4a(static_cast<int>(qa_[r][2 + i]), static_cast<int>(a[4 + 2 * i]), I1);
+                                I1 = __dp4a(static_cast<int>(qb_[r][2 + i]), static_cast<int>(a[4 + 2 * i + 1]), I1);
+                            }
+                            const float v = fmaf(s1[r], static_cast<float>(I1), __fmul_rn(s0[r], static_cast<float>(I0)));
+                            acc[r][t] = fmaf(da, v, acc[r][t]);
+                        }
+                    }
+                }
+                continue;
+            }
             // per token: its 8 code words of this chunk, d_a and d_a * ssum, against every row
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
