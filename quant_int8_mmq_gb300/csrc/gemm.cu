@@ -31,14 +31,14 @@
 //               chunks' accumulators side by side), so the issuing thread waits,
 //               fences and commits once per two chunks.  q4_K: the min term
 //               sum_c (d_a*ssum)(dmin*m) carries
-//               no per-super-block factor, so it is one kind::tf32 contraction per
-//               tile (three MMAs per super-block, hi/lo split) into one item after the
-//               tile's last k-block.
+//               no per-super-block factor, so it is a kind::tf32 contraction after the
+//               tile's last k-block (three MMAs per super-block, hi/lo split) into one
+//               item per MIN_GROUP_SB super-blocks.
 //   warps 2-3   idle (they only lend their registers).
 //   warps 4-11  promotion: each owns one TMEM lane quarter (warp % 4) and 64 of the
 //               128 columns; per item: wait, tcgen05.ld of its chunks, one release,
 //               inner += d_a * I' (packed f32x2 FMAs); per super-block acc += d * inner;
-//               per tile acc -= the q4_K min-term item; store Y (or, for the two
+//               per tile acc -= the q4_K min-term items; store Y (or, for the two
 //               K-halves of a last-round tile, add into a zeroed Y).
 // Per-chunk scaling forces one TMEM round trip per 32-value chunk; what it costs is
 // set by the synchronisation, not the tensor pipe.  Measured on GB300, the issuing

@@ -19,7 +19,7 @@
 // (token, super-block) from the largest d_a so that 127 * max d_a * p <= 2^14:
 // hi stays finite and lo stays out of the f16 subnormal range for every value
 // within 2^17 of the super-block's largest.  The q4_K min term is the same tf32
-// hi/lo contraction over chunks as in gemm.cu, once per tile.
+// hi/lo contraction over chunks as in gemm.cu, per tile in items of 64 super-blocks.
 //
 // One CTA per SM, persistent over 128-token x 256-row tiles (N = 256: two 128-row
 // weight tiles side by side); 16 warps in four warpgroups:
@@ -43,7 +43,7 @@
 //   warps 8-15  promotion: each owns one TMEM lane quarter (warp % 4) and 128 of the
 //               256 columns; per super-block: wait, four tcgen05.ld (16x256b shape,
 //               64 columns), release, acc += d_sb * (D / p); per tile acc -= the q4_K
-//               min term; store Y (or, for K-halves, add into a zeroed Y) as float2,
+//               min-term items; store Y (or, for K-halves, add into a zeroed Y) as float2,
 //               whole 32-byte sectors per quad.
 // The synchronisation count per tensor-core FLOP is 8x lower than in gemm.cu and
 // the promotion does one FMA pair per accumulator element per super-block rather
