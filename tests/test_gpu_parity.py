@@ -1185,3 +1185,79 @@ def test_gemm_at_the_largest_od():
         del qa, sc, Y
     del packed
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- graphs and concurrency
+def test_prepass_and_gemms_replay_from_a_cuda_graph():
+    """Prepass + GEMM calls captured once into a CUDA graph (the launches carry no host
+    state that goes stale) and replayed over new activations written into the captured
+    input buffer: every replay gives the oracle's Y for the activations of that replay, on
+    the super-block (q4_K 11008 x 4096, M = 300), few-token (q6_K, M = 40) and
+    weight-streaming (q4_K, M = 3) kernels."""
+    cases = [("q4_K", 11008, 4096, 300), ("q6_K", 4097, 1024, 40), ("q4_K", 2048, 512, 3)]
+    dev = torch.device(DEV)
+    s = torch.cuda.Stream(dev)
+    bufs = []
+    for i, (t, od, id_, M) in enumerate(cases):
+        raw = _raw(t, od, id_, seed=400 + i)
+        packed = gpu_pack(t, raw)
+        xb = torch.zeros((M, id_), dtype=torch.float32, device=dev)
+        qb, sb = mmq.mmq_act_plane_bytes(M, id_)
+        qa = torch.empty(qb, dtype=torch.uint8, device=dev)
+        sc = torch.empty(sb, dtype=torch.uint8, device=dev)
+        Y = torch.empty((M, od), dtype=torch.float32, device=dev)
+        bufs.append((t, od, id_, M, raw, packed, xb, qa, sc, Y))
+    _sync()
+
+    def step(stream):
+        for t, od, id_, M, raw, packed, xb, qa, sc, Y in bufs:
+            mmq.quantize_act(xb, qa, sc, stream=stream)
+            mmq.gemm(t, packed, od, id_, qa, sc, M, Y=Y, stream=stream)
+
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        step(s)                                   # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    torch.cuda.synchronize()
+    for rep in range(2):
+        xs = []
+        for i, (t, od, id_, M, raw, packed, xb, qa, sc, Y) in enumerate(bufs):
+            x = synth.activations(M, id_, seed=410 + 10 * rep + i)
+            xb.copy_(torch.from_numpy(x))
+            xs.append(x)
+        torch.cuda.synchronize()
+        g.replay()
+        _sync()
+        for (t, od, id_, M, raw, packed, xb, qa, sc, Y), x in zip(bufs, xs):
+            rows = sorted({0, M // 2, M - 1})
+            Yo, S = oracle_gemm(t, raw, x[rows])
+            assert_y_close(_rows_of(Y, rows), Yo, S)
+
+
+def test_gemms_on_two_streams_at_once():
+    """Two GEMMs launched back to back on two streams with no synchronisation between
+    them (persistent grids that compete for the SMs; a few-token cluster launch beside a
+    super-block launch): both results are the oracle's, and no wait expires."""
+    dev = torch.device(DEV)
+    cases = [("q4_K", 11008, 4096, 700), ("q6_K", 4097, 2048, 31)]
+    prepared = []
+    for i, (t, od, id_, M) in enumerate(cases):
+        raw = _raw(t, od, id_, seed=420 + i)
+        x = synth.activations(M, id_, seed=430 + i)
+        qa, sc = gpu_quantize(x)
+        prepared.append((t, od, id_, M, raw, x, gpu_pack(t, raw), qa, sc))
+    _sync()
+    streams = [torch.cuda.Stream(dev) for _ in cases]
+    for rep in range(3):
+        outs = []
+        for (t, od, id_, M, raw, x, packed, qa, sc), st in zip(prepared, streams):
+            outs.append(mmq.gemm(t, packed, od, id_, qa, sc, M, stream=st))
+        _sync()
+        for (t, od, id_, M, raw, x, packed, qa, sc), Y in zip(prepared, outs):
+            rows = [0, M - 1]
+            Yo, S = oracle_gemm(t, raw, x[rows])
+            assert_y_close(_rows_of(Y, rows), Yo, S)
