@@ -88,6 +88,18 @@ constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int CONV_WARP0 = 4;
 constexpr int NUM_CONV_WARPS = 8;
 constexpr int PROMO_WARP0 = 12;
+// Register split for q4_K at 49 to 64 tokens (N = 64), whose promotion threads hold 64
+// accumulators and spilled at 128 registers: the control warpgroup gives up registers to
+// the promotion warpgroup out of the launch's 128 x 512 (converters keep 128).  Measured on
+// GB300: q4_K 11008x4096 M = 56 29.1 -> 24.3 us, 4096x4096 15.8 -> 14.2 us; at N = 48 and
+// for q6_K (whose converters keep their spills) it changed nothing or cost 1 %, so those
+// keep the uniform 128.  The host launches a split build only if it compiled to 128
+// registers per thread, the sum the split assumes.
+constexpr int LAUNCH_REGS = 128;
+constexpr int CTRL_REGS = 56;
+constexpr int CONV_REGS = 128;
+constexpr int PROMO_REGS = 200;
+static_assert(4 * 32 * CTRL_REGS + 8 * 32 * CONV_REGS + 4 * 32 * PROMO_REGS == LAUNCH_REGS * 512, "register split");
 constexpr int NUM_PROMO_WARPS = 4;
 constexpr int NUM_ISSUERS = 2;          // warp 3: even stages, warp 1: odd stages
 constexpr int PF_STAGES = 4;            // L2 prefetch distance of the compact codes, stages
@@ -122,6 +134,7 @@ struct Cfg {
     static constexpr int N = 16 * NT;
     static constexpr int TILES = ONE ? 1 : 2;
     static constexpr int ITEMS = items_of(NT);
+    static constexpr bool SPLIT_REGS = TYPE == 12 && NT == 4;
     static constexpr uint32_t ITEM_COLS = item_cols_of(NT);
     static_assert(ITEMS * ITEM_COLS == WBUF_COL0 && 2 * N <= static_cast<int>(ITEM_COLS), "items");
     static_assert(TYPE == 14 || ONE, "q4_K has one tile");
@@ -364,6 +377,8 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     const bool clustered = g.kslices > 1;
 
     if (warp < CONV_WARP0) {
+        if constexpr (C::SPLIT_REGS)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(CTRL_REGS));
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ producer: compact codes, super-block entries
             RingPos<C::RAW_STAGES> rp;
@@ -620,6 +635,8 @@ __device__ __forceinline__ void ft_roles(const FtArgs& g, uint8_t* smem, uint32_
     }
 
     // -------------------------------------------------------- promotion
+    if constexpr (C::SPLIT_REGS)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(PROMO_REGS));
     const int q = warp & 3;                              // TMEM lane quarter
     const int row = q * 32 + lane;                       // weight row of the tile
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -900,6 +917,16 @@ cudaError_t set_smem_attr()
     const uint64_t bit = 1ull << (dev & 63);
     if (attr_set_mask.load() & bit)
         return cudaSuccess;
+    if (Cfg<TYPE, NT, true>::SPLIT_REGS) {
+        // The setmaxnreg split draws on the registers the launch reserved; a build that
+        // compiled to fewer per thread would make the promotion warps wait forever.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, gemm_ft_kernel<TYPE, NT>);
+        if (e != cudaSuccess)
+            return e;
+        if (fa.numRegs < LAUNCH_REGS)
+            return cudaErrorInvalidKernelImage;
+    }
     e = cudaFuncSetAttribute(gemm_ft_kernel<TYPE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_alloc_of<TYPE, NT>());
     if (e != cudaSuccess)
