@@ -1261,3 +1261,25 @@ def test_gemms_on_two_streams_at_once():
             rows = [0, M - 1]
             Yo, S = oracle_gemm(t, raw, x[rows])
             assert_y_close(_rows_of(Y, rows), Yo, S)
+
+
+@pytest.mark.parametrize("selector", [1, 2])
+def test_gemm_min_term_in_two_groups(selector):
+    """id = 65 super-blocks: the q4_K min term of a whole tile takes two TMEM items, 64
+    super-blocks and then 1, on both tile kernels (80 tiles of 128 x 256, none split in
+    K); sampled tokens against the oracle."""
+    M, od, id_ = 130, 10240, 65 * 256
+    raw = synth.q4k_blocks(od, id_, 311)
+    x = synth.activations(M, id_, 312)
+    qa, sc = gpu_quantize(x)
+    packed = gpu_pack("q4_K", raw)
+    mmq.mmq_debug_select_large_m_kernel(selector)
+    try:
+        Y = mmq.gemm("q4_K", packed, od, id_, qa, sc, M)
+        _sync()
+        assert _route_of(mmq.mmq_last_path()) == ("chunk" if selector == 1 else "super-block")
+    finally:
+        mmq.mmq_debug_select_large_m_kernel(0)
+    rows = [0, 77, M - 1]
+    Yo, S = oracle_gemm("q4_K", raw, x[rows])
+    assert_y_close(_rows_of(Y, rows), Yo, S)
