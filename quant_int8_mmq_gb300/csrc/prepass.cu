@@ -17,11 +17,12 @@
 // rows zeroed ("r45 - cp.async for the q6_K A-side staging ...", §1.1 and §2.3;
 // "r56 - q6_K A-side bundle ...", §1).
 //
-// Mapping: one warp per (token row, 256-value super-block); lane l owns values
-// 8l..8l+7 (two 16-byte loads), so four lanes share a 32-value chunk and the amax
-// and ssum reductions run over those four.  A lane's 8 codes are one 16-byte
-// segment of the swizzled operand tile (one store).  Consecutive warps take
-// consecutive token rows of one super-block, so the tile rows and the scale
+// Mapping: one half-warp per (token row, 256-value super-block); lane l of the half owns
+// values 16l..16l+15 (four 16-byte loads), so two lanes share a 32-value chunk and the
+// amax and ssum reductions take one shuffle each, and the per-chunk work (the divisor,
+// its reciprocal, the scale entries) is spread over 16 values per lane.  A lane's 16
+// codes are two 16-byte segments of the swizzled operand tile.  Consecutive half-warps
+// take consecutive token rows of one super-block, so the tile rows and the scale
 // entries they write are contiguous in HBM.
 #include <cuda_fp16.h>
 
@@ -150,146 +151,148 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
     grid_dep_wait();
     grid_dep_launch();
     const int lane = threadIdx.x & 31;
+    const int hl = lane & 15;                 // lane within its half-warp: values 16 hl .. 16 hl + 15
     const int nkb = K / TILE_K;
     const int nchunk = K / CHUNK;
     const int nsb = K / QK_K;
-    // Item w = sb * Mp + t (token row t, super-block sb), grid-stride over warps; the
-    // (t, sb) pair is advanced incrementally (no 64-bit division per item).
-    const int stride = gridDim.x * (blockDim.x >> 5);
-    const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // Item w = sb * Mp + t (token row t, super-block sb), one per half-warp, grid-stride over
+    // half-warps; the (t, sb) pair is advanced incrementally (no 64-bit division per item).
+    const int stride = gridDim.x * (blockDim.x >> 5) * 2;
+    const int w0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 2 + (lane >> 4);
     const int st_t = stride % Mp, st_sb = stride / Mp;
-    int t_cur = w0 % Mp, sb_cur = w0 / Mp;
-    auto advance = [&](int& t, int& sb) {
-        t += st_t;
-        sb += st_sb;
-        if (t >= Mp) {
-            t -= Mp;
-            ++sb;
-        }
-    };
-    // Two items per pass: both loads are in flight before either is reduced.
-    while (sb_cur < nsb) {
-        int ti[2] = {t_cur, t_cur}, si[2] = {sb_cur, sb_cur};
-        advance(ti[1], si[1]);
-        t_cur = ti[1];
-        sb_cur = si[1];
-        advance(t_cur, sb_cur);
-        float vv[2][8];
+    int t = w0 % Mp, sb = w0 / Mp;
+    // Both halves run every pass (the shuffles below span whole warps); a half whose items
+    // are done computes on zeros and stores nothing.
+    while (__any_sync(0xffffffffu, sb < nsb)) {
+        const bool valid = sb < nsb;
+        const int k0 = sb * QK_K + 16 * hl;
+        float v[16];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int t = ti[u];
-            const int k0 = si[u] * QK_K + 8 * lane;
+        for (int i = 0; i < 16; ++i)
+            v[i] = 0.0f;
+        if (valid && t < M) {
+            const float* p = x + static_cast<size_t>(t) * ldx + k0;
+            if (vec4) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                vv[u][i] = 0.0f;
-            if (si[u] < nsb && t < M) {
-                const float* p = x + static_cast<size_t>(t) * ldx + k0;
-                if (vec4) {
-                    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-                    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-                    vv[u][0] = a.x; vv[u][1] = a.y; vv[u][2] = a.z; vv[u][3] = a.w;
-                    vv[u][4] = b.x; vv[u][5] = b.y; vv[u][6] = b.z; vv[u][7] = b.w;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        vv[u][i] = __ldcs(p + i);
+                for (int u = 0; u < 4; ++u) {
+                    const float4 a = __ldcs(reinterpret_cast<const float4*>(p) + u);
+                    v[4 * u] = a.x; v[4 * u + 1] = a.y; v[4 * u + 2] = a.z; v[4 * u + 3] = a.w;
                 }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (si[u] >= nsb)
-                break;
-            const int t = ti[u];
-            const int sb = si[u];
-            const int k0 = sb * QK_K + 8 * lane;
-            const float(&v)[8] = vv[u];
-            float a = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                a = fmaxf(a, fabsf(v[i]));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            const float d = __fdiv_rn(a, 127.0f);
-            const bool shared = (d >= 0x1p-100f && d <= 0x1p100f);
-            const float rd = shared ? __frcp_rn(d) : 0.0f;
-            // codes as integer-valued floats; their chunk sum (|.| <= 4064) is exact in f32
-            // (one branch per lane: the 8 values share d, so the division path is never
-            // evaluated next to the shared-reciprocal one)
-            float q[8];
-            if (shared) {
-                quant8_shared(v, d, rd, q);
-            } else if (d != 0.0f) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    q[i] = quant_one(v[i], d);
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    q[i] = 0.0f;
+                for (int i = 0; i < 16; ++i)
+                    v[i] = __ldcs(p + i);
             }
-            float sf = sum8(q);
-            sf += __shfl_xor_sync(0xffffffffu, sf, 1);
-            sf += __shfl_xor_sync(0xffffffffu, sf, 2);
-            const int s = static_cast<int>(sf);
-
-            const int mt = t / TILE_ROWS, r = t % TILE_ROWS;
-            const int kb = k0 / TILE_K;
-            uint8_t* tile = reinterpret_cast<uint8_t*>(qa) + (static_cast<size_t>(mt) * nkb + kb) * TILE_BYTES;
-            uint32_t h[4];
+        }
+        // the chunk (32 values) is this lane's 16 and its neighbour's (lane ^ 1)
+        float a = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {           // exact: |q| <= 127 is an f16 integer
-                const __half2 p2 = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
-                h[i] = *reinterpret_cast<const uint32_t*>(&p2);
+        for (int i = 0; i < 16; ++i)
+            a = fmaxf(a, fabsf(v[i]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const float d = __fdiv_rn(a, 127.0f);
+        const bool shared = (d >= 0x1p-100f && d <= 0x1p100f);
+        const float rd = shared ? __frcp_rn(d) : 0.0f;
+        // codes as integer-valued floats; their chunk sum (|.| <= 4064) is exact in f32
+        // (one branch per lane: the 16 values share d, so the division path is never
+        // evaluated next to the shared-reciprocal one)
+        float q[2][8];
+        if (shared) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+                quant8_shared(reinterpret_cast<const float(&)[8]>(v[8 * g]), d, rd, q[g]);
+        } else if (d != 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                q[i >> 3][i & 7] = quant_one(v[i], d);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                q[i >> 3][i & 7] = 0.0f;
+        }
+        float sf = __fadd_rn(sum8(q[0]), sum8(q[1]));
+        sf += __shfl_xor_sync(0xffffffffu, sf, 1);
+        const int s = static_cast<int>(sf);
+
+        const int mt = t / TILE_ROWS, r = t % TILE_ROWS;
+        const int kb = k0 / TILE_K;
+        const int kk = k0 % TILE_K;               // 16-value segment inside the k-block
+        uint8_t* tile = reinterpret_cast<uint8_t*>(qa) + (static_cast<size_t>(mt) * nkb + kb) * TILE_BYTES;
+        uint32_t h[2][4];
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {       // exact: |q| <= 127 is an f16 integer
+                const __half2 p2 = __floats2half2_rn(q[g][2 * i], q[g][2 * i + 1]);
+                h[g][i] = *reinterpret_cast<const uint32_t*>(&p2);
             }
-            *reinterpret_cast<uint4*>(tile + tile_byte(r, k0 % TILE_K)) = make_uint4(h[0], h[1], h[2], h[3]);
-            if (tq != nullptr && t < ftn) {
-                // few-token operand: hi and lo tiles of p * d * q for this token row
-                float dm = d;
-                dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 4));
-                dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 8));
-                dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 16));
+        if (valid) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+                *reinterpret_cast<uint4*>(tile + tile_byte(r, kk + 8 * g)) =
+                    make_uint4(h[g][0], h[g][1], h[g][2], h[g][3]);
+        }
+        if (tq != nullptr) {
+            // few-token operand: hi and lo tiles of p * d * q for this token row; p from
+            // the largest chunk scale of the super-block (its 16 lanes)
+            float dm = d;
+            dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 2));
+            dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 4));
+            dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, 8));
+            if (valid && t < ftn) {
                 const uint32_t pf = ft_p_field(dm);
                 const float sv = __fmul_rn(d, __uint_as_float(pf << 23));  // exact: a power of two
                 const __half shh = __float2half_rn(sv);
                 const __half2 s_hi = __half2half2(shh);
                 const __half2 s_lo = __half2half2(__float2half_rn(sv - __half2float(shh)));
-                uint32_t hv[4], lv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    ft_split_pair(h[i], s_hi, s_lo, hv[i], lv[i]);
                 uint8_t* kt = tq + static_cast<size_t>(kb) * (2 * ftn * 128);
-                const int off = tile_byte(t, k0 % TILE_K);
-                *reinterpret_cast<uint4*>(kt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                *reinterpret_cast<uint4*>(kt + ftn * 128 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-                if (lane == 0)
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t hv[4], lv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        ft_split_pair(h[g][i], s_hi, s_lo, hv[i], lv[i]);
+                    const int off = tile_byte(t, kk + 8 * g);
+                    *reinterpret_cast<uint4*>(kt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    *reinterpret_cast<uint4*>(kt + ftn * 128 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+                }
+                if (hl == 0)
                     ip[static_cast<size_t>(sb) * FT_MAX_M + t] = __uint_as_float((254u - pf) << 23);
             }
-            if (qa8 != nullptr && t < M) {
-                // small_pos order inside the 8-value group: values (0,2,4,6) then (1,3,5,7)
+        }
+        if (qa8 != nullptr && valid && t < M) {
+            // small_pos order inside each 8-value group: values (0,2,4,6) then (1,3,5,7)
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
                 int qi[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    qi[i] = static_cast<int>(q[i]);
+                    qi[i] = static_cast<int>(q[g][i]);
                 const uint32_t lo = (qi[0] & 0xFF) | ((qi[2] & 0xFF) << 8) | ((qi[4] & 0xFF) << 16) |
                                     (static_cast<uint32_t>(qi[6] & 0xFF) << 24);
                 const uint32_t hi = (qi[1] & 0xFF) | ((qi[3] & 0xFF) << 8) | ((qi[5] & 0xFF) << 16) |
                                     (static_cast<uint32_t>(qi[7] & 0xFF) << 24);
-                *reinterpret_cast<uint2*>(qa8 + static_cast<size_t>(t) * K + k0) = make_uint2(lo, hi);
+                *reinterpret_cast<uint2*>(qa8 + static_cast<size_t>(t) * K + k0 + 8 * g) = make_uint2(lo, hi);
             }
-            if ((lane & 3) == 0) {
-                const int c = k0 / CHUNK;
-                scales[(static_cast<size_t>(mt) * nchunk + c) * TILE_ROWS + r] =
-                    make_uint2(__float_as_uint(d), static_cast<uint32_t>(s));
-                const float ma = __fmul_rn(d, static_cast<float>(s));
-                const float hi = tf32_rna(ma);
-                const float lo = tf32_rna(__fsub_rn(ma, hi));
-                uint8_t* t0 = am + (static_cast<size_t>(mt) * nsb + sb) * (2 * TF32_TILE_BYTES);
-                *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = hi;
-                *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = lo;
-                if (fm != nullptr && t < ftn)
-                    fm[(static_cast<size_t>(sb) * 8 + (c & 7)) * FT_MAX_M + t] = ma;
-            }
+        }
+        if (valid && (hl & 1) == 0) {
+            const int c = k0 / CHUNK;
+            scales[(static_cast<size_t>(mt) * nchunk + c) * TILE_ROWS + r] =
+                make_uint2(__float_as_uint(d), static_cast<uint32_t>(s));
+            const float ma = __fmul_rn(d, static_cast<float>(s));
+            const float mhi = tf32_rna(ma);
+            const float mlo = tf32_rna(__fsub_rn(ma, mhi));
+            uint8_t* t0 = am + (static_cast<size_t>(mt) * nsb + sb) * (2 * TF32_TILE_BYTES);
+            *reinterpret_cast<float*>(t0 + tf32_tile_byte(r, c & 7)) = mhi;
+            *reinterpret_cast<float*>(t0 + TF32_TILE_BYTES + tf32_tile_byte(r, c & 7)) = mlo;
+            if (fm != nullptr && t < ftn)
+                fm[(static_cast<size_t>(sb) * 8 + (c & 7)) * FT_MAX_M + t] = ma;
+        }
+        t += st_t;
+        sb += st_sb;
+        if (t >= Mp) {
+            t -= Mp;
+            ++sb;
         }
     }
 }
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
 cudaError_t launch_quantize_act(const float* x, int M, int K, int ldx, void* qa, void* scales, cudaStream_t s)
 {
     const int Mp = ceil_div(M, TILE_ROWS) * TILE_ROWS;
-    const long long warps = static_cast<long long>(Mp) * (K / QK_K);
+    const long long warps = (static_cast<long long>(Mp) * (K / QK_K) + 1) / 2;   // one half-warp per item
     int dev = 0, nsm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
