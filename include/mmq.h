@@ -242,8 +242,8 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  * mmq_debug_select_large_m_kernel can force a choice):
  *  - M <= MMQ_SMALL_M (decode and tail shapes), the weight-streaming kernel,
  *    except where the few-token kernel below is faster (measured crossovers,
- *    w = od*id: q4_K with w >= 2^24 and M >= 7, or w >= 2^25 and M >= 6; q6_K
- *    with w >= 2^25 and M >= 6, or w >= 3*2^25 and M >= 5): the
+ *    w = od*id: q4_K with w >= 2^24 and M >= 7, or w >= 2^25 and M >= 5; q6_K
+ *    with w >= 2^25 and M >= 4): the
  *    RAW plane and the int8 activation plane, exact integer dots on the CUDA
  *    cores (dp4a), and the scales applied per chunk in the formula's own order
  *    (q4_K: Y += d_a*(d*sc_c*I) - (d_a*ssum)*(dmin*m_c); q6_K: Y +=

@@ -162,7 +162,8 @@ mmq_status check_weight_shape(mmq_type t, int od, int id)
 // M (its integer dots are issue-bound), unless the weight is large enough that the
 // few-token kernel, whose cost hardly depends on M, is faster.  The crossovers were
 // measured on GB300 over q4_K 4096x4096 / 11008x4096 and q6_K 4096x4096 / 4097x11008 /
-// 32000x4096 at M = 2..8.
+// 32000x4096 at M = 2..8, and retaken at M = 3..6 after the few-token kernel's promotion
+// went to f32x2 pairs (q6_K 4097x11008 M = 4: 17.9 us streaming, 16.8 few-token).
 bool takes_streaming_path(mmq_type t, int od, int id, int M)
 {
     if (M > mmq::SMALL_M)
@@ -170,8 +171,8 @@ bool takes_streaming_path(mmq_type t, int od, int id, int M)
     const long long w = static_cast<long long>(od) * id;
     constexpr long long W24 = 1ll << 24, W25 = 1ll << 25;
     if (t == MMQ_Q4_K)
-        return !(w >= W24 && (M >= 7 || (M >= 6 && w >= W25)));
-    return !((w >= W25 && M >= 6) || (w >= 3 * W25 && M >= 5));
+        return !(w >= W24 && (M >= 7 || (M >= 5 && w >= W25)));
+    return !(w >= W25 && M >= 4);
 }
 
 mmq_status gemm_common(mmq_type t, mmq::GemmMode mode, const void* packed, int od, int id, const void* qa,

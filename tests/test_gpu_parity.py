@@ -885,10 +885,11 @@ def test_gemm_streaming_boundary(M):
 
 
 @pytest.mark.parametrize("typ,od,id_,M,path", [
-    ("q4_K", 11008, 4096, 5, "weight-streaming"), ("q4_K", 11008, 4096, 6, "few-token GEMM"),
+    ("q4_K", 11008, 4096, 4, "weight-streaming"), ("q4_K", 11008, 4096, 5, "few-token GEMM"),
     ("q4_K", 4096, 4096, 6, "weight-streaming"), ("q4_K", 4096, 4096, 7, "few-token GEMM"),
-    ("q6_K", 4097, 11008, 5, "weight-streaming"), ("q6_K", 4097, 11008, 6, "few-token GEMM"),
-    ("q6_K", 32000, 4096, 4, "weight-streaming"), ("q6_K", 32000, 4096, 5, "few-token GEMM")])
+    ("q6_K", 4097, 11008, 3, "weight-streaming"), ("q6_K", 4097, 11008, 4, "few-token GEMM"),
+    ("q6_K", 32000, 4096, 3, "weight-streaming"), ("q6_K", 32000, 4096, 4, "few-token GEMM"),
+    ("q6_K", 4096, 4096, 8, "weight-streaming")])
 def test_gemm_small_m_routing_at_the_crossovers(typ, od, id_, M, path):
     """Up to 8 tokens the weight-streaming kernel runs unless the weight is large enough for
     the few-token kernel to be faster (the header's measured crossovers): either way Y
