@@ -1284,3 +1284,38 @@ def test_gemm_min_term_in_two_groups(selector):
     rows = [0, 77, M - 1]
     Yo, S = oracle_gemm("q4_K", raw, x[rows])
     assert_y_close(_rows_of(Y, rows), Yo, S)
+
+
+def _sweep_cases(n=36, seed=2026):
+    """Seeded shapes across every kernel's regime: M from 1 to 2100, od from 1 to 12 000
+    (ragged), id from 256 to 14 336, both types, q6_K folded and full-range."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        typ = ["q4_K", "q6_K", "q6_K_full"][i % 3]
+        M = int(rng.choice([1, 2, 3, 5, 7, 8, 9, 17, 31, 33, 48, 64, 65, 100, 129, 300, 700, 1300, 2100]))
+        od = int(rng.integers(1, 12000))
+        id_ = 256 * int(rng.choice([1, 2, 3, 8, 16, 43, 56]))
+        while od * id_ > 60_000_000:              # keep the weights and the oracle small
+            od = max(1, od // 2)
+        out.append((typ, M, od, id_))
+    return out
+
+
+@pytest.mark.parametrize("typ,M,od,id_", _sweep_cases())
+def test_gemm_default_choice_sweep(typ, M, od, id_):
+    """The default kernel choice on seeded shapes: whatever kernel it picks (checked to be
+    the one mmq_debug_route names), Y matches the oracle on sampled tokens."""
+    t = "q6_K" if typ.startswith("q6_K") else typ
+    full = typ.endswith("full")
+    raw = _q6_raw(od, id_, od + M, full) if t == "q6_K" else synth.q4k_blocks(od, id_, od + M)
+    x = synth.activations(M, id_, M + 7)
+    Y = _run_gemm(t, raw, x)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    fold = 1
+    if t == "q6_K":
+        fold = 0 if np.abs(raw[:, :, 192:208].view(np.int8)).max() > 64 else 1
+    assert _route_of(mmq.mmq_last_path()) == mmq.mmq_debug_route(t, od, id_, M, fold, nsm)
+    rows = sorted({0, M // 2, M - 1})
+    Yo, S = oracle_gemm(t, raw, x[rows])
+    assert_y_close(_rows_of(Y, rows), Yo, S)
