@@ -611,6 +611,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const GemmArgs g)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + SMEM_TMEMPTR);
+    // A dependent launch: the set-up above overlapped the end of the kernel ahead (the
+    // prepass, or the repack that wrote the flag); nothing global is read before it has
+    // completed, and the next kernel may be scheduled from here on.
+    grid_dep_wait();
+    grid_dep_launch();
 
     if constexpr (TYPE == 14) {
         // q6_K codes hold sc*q in one tile unless some |sc| > 64 (then two exact tiles);
@@ -669,8 +674,7 @@ cudaError_t launch_typed(const GemmArgs& a, int grid, cudaStream_t s)
         attr_set_mask.fetch_or(bit);
     }
     count_launch();
-    gemm_kernel<TYPE, MODE><<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent_smem(gemm_kernel<TYPE, MODE>, dim3(grid), dim3(NUM_THREADS), SMEM_ALLOC, s, a);
 }
 
 }  // namespace

@@ -557,12 +557,19 @@ def test_gemm_third_round_halves_parity(superblock_kernel, typ):
     assert np.array_equal(Y.view(np.uint32), again.view(np.uint32))
 
 
+@pytest.fixture(params=[2, 1], ids=["super-block", "chunk"])
+def tile_kernel(request):
+    mmq.mmq_debug_select_large_m_kernel(request.param)
+    yield "super-block tcgen05 GEMM" if request.param == 2 else "chunk GEMM"
+    mmq.mmq_debug_select_large_m_kernel(0)
+
+
 @pytest.mark.parametrize("typ", ["q4_K", "q6_K"])
-def test_superblock_back_to_back_calls_share_buffers(superblock_kernel, typ):
-    """Prepass and super-block GEMM calls queued on one stream with no synchronisation in
-    between, all through the same activation planes, and the last two GEMMs writing the
-    same Y.  Both are dependent launches: a GEMM's set-up overlaps the prepass ahead of
-    it, a prepass may start while the GEMM ahead still runs.  Each result must still be
+def test_tile_kernel_back_to_back_calls_share_buffers(tile_kernel, typ):
+    """Prepass and tile-GEMM calls (super-block and chunk kernels) queued on one stream with
+    no synchronisation in between, all through the same activation planes, and the last
+    two GEMMs writing the same Y.  Both are dependent launches: a GEMM's set-up overlaps
+    the prepass ahead of it, a prepass may start while the GEMM ahead still runs.  Each result must still be
     the oracle's for its own inputs (no prepass overwrites planes a GEMM still reads, no
     GEMM reads planes before its prepass wrote them, the later Y is the one left).  The
     second weight is packed right before its first GEMM, so the flag and planes a GEMM
@@ -586,7 +593,7 @@ def test_superblock_back_to_back_calls_share_buffers(superblock_kernel, typ):
             packs[i % 2] = gpu_pack(typ, raws[i % 2])
         Y = shared[:M] if i >= len(xd) - 2 else None
         outs.append(mmq.gemm(typ, packs[i % 2], od, id_, qa, sc, M, Y=Y))
-        assert "super-block tcgen05 GEMM" in mmq.mmq_last_path()
+        assert tile_kernel in mmq.mmq_last_path()
     _sync()
     assert mmq.mmq_get_device_error() == 0
     for i, (x, Y) in enumerate(zip(xs, outs)):
