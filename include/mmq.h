@@ -266,16 +266,18 @@ mmq_status mmq_convert_ggml_blocks(mmq_type t, const void* src, size_t nblocks, 
  *    the activation operand p*d_a*q_a as an f16 hi + lo pair
  *    (about 2^-21 relative per value) times the exact f16 CODES (and CODES2 for
  *    two-tile q6_K, a second pair of MMAs into the same accumulator), summed over
- *    a whole super-block in f32, then d and 1/p per super-block.  When the last round of tiles fills at most half the SMs (or
- *    all tiles do), those tiles run as two K-halves added into Y after a zeroing
+ *    a whole super-block in f32, then d and 1/p per super-block.  In both tile
+ *    kernels, when the last round of tiles fills at most half the SMs (or all
+ *    tiles do), those tiles run as two K-halves added into Y after a zeroing
  *    kernel, 0 + a + b, the same in either order;
- *  - otherwise the chunk kernel: the integer dots sum_chunk (sc*q)*q_a run
+ *  - the chunk kernel: the integer dots sum_chunk (sc*q)*q_a run
  *    exactly (codes held as f16 integers, two-tile q6_K as two MMAs per 16
  *    values, every partial sum an integer below 2^24 in the f32 accumulator)
  *    and the f32 scales are applied per chunk (d_a) and per super-block (d).
  * The super-block and chunk kernels compute the q4_K min term sum_c
  * (d_a*ssum)*(dmin*m_c) as a tf32 hi/lo tensor-core contraction (relative error
- * about 2^-21 per product).
+ * about 2^-21 per product), each TMEM accumulator covering at most 64
+ * super-blocks before it is added into Y's f32 sums.
  * Y is deterministic for given inputs and kernel.  Rows t >= M and columns
  * j >= od are never written.  ldy >= od.
  * -------------------------------------------------------------------------- */
