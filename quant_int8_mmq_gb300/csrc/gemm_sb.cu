@@ -825,15 +825,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_sb_kernel(const SbArgs g)
     }
 }
 
+constexpr int ZERO_ROWS = 16;   // rows of Y a zeroing block clears
+
 // Zeroes Y over the 128 x 256 tiles [first, first + count) (rows < M, columns < od).
-__global__ void __launch_bounds__(256) sb_zero_tiles_kernel(float* __restrict__ Y, int ldy, int M, int od,
-                                                            int num_m, int first)
+__global__ void __launch_bounds__(256) sb_zero_tiles_kernel(float* __restrict__ Y, int ldy, int M, int od, int num_m,
+                                                            int first)
 {
+    // Y may still be written by the kernel ahead (a GEMM into the same buffer).
+    grid_dep_wait();
+    grid_dep_launch();
+    // block (tile, row group of ZERO_ROWS rows); consecutive threads take consecutive columns
     const int tile = first + blockIdx.x;
     const int m = tile % num_m, n = tile / num_m;
-    const int r_end = min(BM, M - m * BM), c_end = min(BN, od - n * BN);
-    for (int e = threadIdx.x; e < BM * BN; e += blockDim.x) {
-        const int r = e / BN, c = e % BN;
+    const int r0 = blockIdx.y * ZERO_ROWS;
+    const int r_end = min(r0 + ZERO_ROWS, M - m * BM), c_end = min(BN, od - n * BN);
+    for (int e = threadIdx.x; e < ZERO_ROWS * BN; e += blockDim.x) {
+        const int r = r0 + e / BN, c = e % BN;
         if (r < r_end && c < c_end)
             Y[static_cast<size_t>(m * BM + r) * ldy + n * BN + c] = 0.0f;
     }
@@ -927,8 +934,8 @@ cudaError_t launch_gemm_sb(int type, const void* packed, int od, int id, const v
         a.nsb_half = nsb / 2;
         grid = a.units < nsm ? a.units : nsm;
         count_launch();
-        sb_zero_tiles_kernel<<<split, 256, 0, s>>>(Y, ldy, M, od, a.num_m, a.full_units);
-        e = cudaGetLastError();
+        e = launch_dependent(sb_zero_tiles_kernel, dim3(static_cast<unsigned>(split), BM / ZERO_ROWS), dim3(256), s, Y,
+                             ldy, M, od, a.num_m, a.full_units);
         if (e != cudaSuccess)
             return e;
     }
